@@ -1,0 +1,475 @@
+// C ABI of libmlora.so: the adapter pool (device-resident slot pool with a
+// rank-packed arena) and the entry points declared in include/mlora.h.
+//
+// Host side only: argument checks, the arena allocator, copies into the arena,
+// and launches.  Every step of the forward and of the merge runs in this
+// library's CUDA kernels; there is no CPU fallback.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/mlora.h"
+#include "arena.h"
+#include "internal.h"
+#include "tc.h"
+
+using namespace mlora;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mlora_status fail(mlora_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+mlora_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MLORA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define CU_TRY(expr)                                              \
+    do {                                                          \
+        cudaError_t e_ = (expr);                                  \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #expr);       \
+    } while (0)
+
+// Makes the pool's device current for the scope of one call and restores the caller's.
+struct DeviceGuard {
+    int prev = -1;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) err = cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+struct SlotHost {
+    int rank = 0;
+    int rpad = 0;
+    float scale = 0.f;
+    int unit = -1;
+    uint64_t version = 0;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct mlora_pool {
+    int device = 0;
+    int max_slots = 0, max_rank = 0, din = 0, dout = 0, max_tokens = 0;
+    mlora_dtype dtype = MLORA_BF16;
+    size_t esize = 2;
+    int units = 0;
+    Arena arena{0};
+    std::vector<SlotHost> slots;
+    int loaded = 0;
+
+    // device memory
+    char* arena_base = nullptr;      // Down half [units x din], then Up half [units x dout]
+    char* arena_down = nullptr;
+    char* arena_up = nullptr;
+    size_t arena_bytes = 0;
+    char* table_base = nullptr;      // slot table, then per-slot Up tensor maps
+    SlotRec* d_slots = nullptr;
+    CUtensorMap* d_up_maps = nullptr;
+    size_t table_bytes = 0;
+    char* ws_base = nullptr;
+    size_t ws_bytes = 0;
+    Workspace ws{};
+    PoolDims dims{};
+
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t last_reader = nullptr;
+    bool reader_pending = false;
+};
+
+namespace {
+
+mlora_status wait_readers(mlora_pool* p) {
+    if (p->reader_pending) {
+        CU_TRY(cudaEventSynchronize(p->last_reader));
+        p->reader_pending = false;
+    }
+    return MLORA_OK;
+}
+
+mlora_status push_slot(mlora_pool* p, int slot) {
+    const SlotHost& h = p->slots[slot];
+    SlotRec rec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit};
+    CU_TRY(cudaMemcpyAsync(p->d_slots + slot, &rec, sizeof rec, cudaMemcpyHostToDevice, p->copy_stream));
+    if (p->dtype == MLORA_BF16) {
+        CUtensorMap map;
+        std::memset(&map, 0, sizeof map);
+        if (h.rank > 0) {
+            void* up = p->arena_up + (size_t)h.unit * p->dout * p->esize;
+            if (!tc_encode_up_map(&map, up, h.rpad, p->dout))
+                return fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the Up block of slot %d", slot);
+        }
+        CU_TRY(cudaMemcpyAsync(p->d_up_maps + slot, &map, sizeof map, cudaMemcpyHostToDevice, p->copy_stream));
+    }
+    // the staging objects above live on this stack frame: finish before returning
+    CU_TRY(cudaStreamSynchronize(p->copy_stream));
+    return MLORA_OK;
+}
+
+// Moves `size` units of both arena halves from unit `from` down to unit `to` (to < from),
+// chunk by chunk so that no single copy overlaps itself.
+mlora_status move_units(mlora_pool* p, int from, int to, int size) {
+    const int shift = from - to;
+    for (int off = 0; off < size; off += shift) {
+        const int n = (size - off) < shift ? (size - off) : shift;
+        const size_t drow = (size_t)p->din * p->esize, urow = (size_t)p->dout * p->esize;
+        CU_TRY(cudaMemcpyAsync(p->arena_down + (size_t)(to + off) * drow, p->arena_down + (size_t)(from + off) * drow,
+                               (size_t)n * drow, cudaMemcpyDeviceToDevice, p->copy_stream));
+        CU_TRY(cudaMemcpyAsync(p->arena_up + (size_t)(to + off) * urow, p->arena_up + (size_t)(from + off) * urow,
+                               (size_t)n * urow, cudaMemcpyDeviceToDevice, p->copy_stream));
+    }
+    return MLORA_OK;
+}
+
+bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mlora_status_string(mlora_status s) {
+    switch (s) {
+        case MLORA_OK: return "ok";
+        case MLORA_ERR_INVALID_ARG: return "invalid argument";
+        case MLORA_ERR_BAD_SLOT: return "slot out of range";
+        case MLORA_ERR_RANK: return "rank out of range";
+        case MLORA_ERR_NOT_LOADED: return "slot holds no adapter";
+        case MLORA_ERR_OOM: return "out of memory (rank budget or device)";
+        case MLORA_ERR_CUDA: return "CUDA error";
+        case MLORA_ERR_DEVICE_ROW: return "a row named an invalid or empty slot";
+        case MLORA_ERR_UNSUPPORTED: return "unsupported shape";
+    }
+    return "unknown status";
+}
+
+const char* mlora_last_error(void) { return g_last_error.c_str(); }
+
+mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int din, int dout,
+                               mlora_dtype dtype, int max_tokens, mlora_pool_t* out) {
+    if (!out) return fail(MLORA_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (max_slots < 0 || max_slots > 4096) return fail(MLORA_ERR_INVALID_ARG, "max_slots %d not in [0, 4096]", max_slots);
+    if (rank_budget < 0) return fail(MLORA_ERR_INVALID_ARG, "rank_budget %d < 0", rank_budget);
+    if (max_rank < 1 || max_rank > 256) return fail(MLORA_ERR_INVALID_ARG, "max_rank %d not in [1, 256]", max_rank);
+    if (din < 1 || dout < 1) return fail(MLORA_ERR_INVALID_ARG, "din %d / dout %d must be >= 1", din, dout);
+    if (max_tokens < 1) return fail(MLORA_ERR_INVALID_ARG, "max_tokens %d < 1", max_tokens);
+    if (dtype != MLORA_F32 && dtype != MLORA_BF16) return fail(MLORA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (dtype == MLORA_BF16 && din % 8 != 0)
+        return fail(MLORA_ERR_UNSUPPORTED, "bf16 pools need din %% 8 == 0 (16-byte rows), got %d", din);
+    if ((long long)rank_budget + 8 > (1ll << 30)) return fail(MLORA_ERR_INVALID_ARG, "rank_budget too large");
+
+    mlora_pool* p = new mlora_pool();
+    p->max_slots = max_slots;
+    p->max_rank = max_rank;
+    p->din = din;
+    p->dout = dout;
+    p->max_tokens = max_tokens;
+    p->dtype = dtype;
+    p->esize = dtype == MLORA_BF16 ? 2 : 4;
+    p->units = Arena::round8(rank_budget);
+    p->arena = Arena(p->units);
+    p->slots.assign(max_slots, SlotHost{});
+
+    auto bail = [&](mlora_status s) {
+        mlora_pool_destroy(p);
+        return s;
+    };
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaGetDevice"));
+
+    // arena: Down half then Up half; unit offsets are multiples of 8, so every
+    // Up block starts 16-byte aligned
+    p->arena_bytes = align_up((size_t)p->units * din * p->esize, 256) + (size_t)p->units * dout * p->esize;
+    if (p->arena_bytes > 0) {
+        e = cudaMalloc((void**)&p->arena_base, p->arena_bytes);
+        if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "arena of %zu bytes: %s", p->arena_bytes, cudaGetErrorString(e)));
+        e = cudaMemset(p->arena_base, 0, p->arena_bytes);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemset(arena)"));
+    }
+    p->arena_down = p->arena_base;
+    p->arena_up = p->arena_base + align_up((size_t)p->units * din * p->esize, 256);
+
+    // slot table and per-slot tensor maps (CUtensorMap must be 64-byte aligned)
+    const size_t slots_bytes = align_up(sizeof(SlotRec) * (size_t)(max_slots > 0 ? max_slots : 1), 128);
+    p->table_bytes = slots_bytes + sizeof(CUtensorMap) * (size_t)(max_slots > 0 ? max_slots : 1);
+    e = cudaMalloc((void**)&p->table_base, p->table_bytes);
+    if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "slot table: %s", cudaGetErrorString(e)));
+    e = cudaMemset(p->table_base, 0, p->table_bytes);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemset(slot table)"));
+    p->d_slots = (SlotRec*)p->table_base;
+    p->d_up_maps = (CUtensorMap*)(p->table_base + slots_bytes);
+
+    // workspace
+    PoolDims& d = p->dims;
+    d.S = max_slots;
+    d.din = din;
+    d.dout = dout;
+    d.max_rank = max_rank;
+    d.max_tokens = max_tokens;
+    d.max_chunks = p->units / CHUNK + max_slots + 1;
+    d.tcap = (max_tokens + 15) / 16 * 16;
+    const TcWorkspaceNeeds tcn = tc_workspace_needs(dtype == MLORA_BF16, d);
+    size_t off = 0;
+    auto carve = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    const size_t o_status = carve(4);
+    const size_t o_counts = carve(sizeof(int32_t) * (size_t)(max_slots + 1));
+    const size_t o_offsets = carve(sizeof(int32_t) * (size_t)(max_slots + 1));
+    const size_t o_perm = carve(sizeof(int32_t) * (size_t)max_tokens);
+    const size_t o_meta = carve(sizeof(int32_t) * 8);
+    const size_t o_cslot = carve(sizeof(int32_t) * (size_t)d.max_chunks);
+    const size_t o_ccol = carve(sizeof(int32_t) * (size_t)d.max_chunks);
+    const size_t o_v32 = carve(dtype == MLORA_F32 || tcn.need_v32 ? sizeof(float) * (size_t)max_tokens * max_rank : 0);
+    const size_t o_vt = carve(dtype == MLORA_BF16 ? (size_t)d.max_chunks * d.tcap * CHUNK * 2 : 0);
+    const size_t o_part = carve(tcn.partial_bytes);
+    const size_t o_ctr = carve(tcn.counter_bytes);
+    p->ws_bytes = off;
+    e = cudaMalloc((void**)&p->ws_base, p->ws_bytes);
+    if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "workspace of %zu bytes: %s", p->ws_bytes, cudaGetErrorString(e)));
+    e = cudaMemset(p->ws_base, 0, p->ws_bytes);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemset(workspace)"));
+    Workspace& w = p->ws;
+    w.status = (uint32_t*)(p->ws_base + o_status);
+    w.counts = (int32_t*)(p->ws_base + o_counts);
+    w.offsets = (int32_t*)(p->ws_base + o_offsets);
+    w.perm = (int32_t*)(p->ws_base + o_perm);
+    w.meta = (int32_t*)(p->ws_base + o_meta);
+    w.chunk_slot = (int32_t*)(p->ws_base + o_cslot);
+    w.chunk_col = (int32_t*)(p->ws_base + o_ccol);
+    w.v32 = (float*)(p->ws_base + o_v32);
+    w.vt = (uint16_t*)(p->ws_base + o_vt);
+    w.partials = (float*)(p->ws_base + o_part);
+    w.tile_ctr = (int32_t*)(p->ws_base + o_ctr);
+
+    e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaStreamCreate"));
+    e = cudaEventCreateWithFlags(&p->last_reader, cudaEventDisableTiming);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaDeviceSynchronize"));
+    *out = p;
+    return MLORA_OK;
+}
+
+mlora_status mlora_pool_destroy(mlora_pool_t p) {
+    if (!p) return MLORA_OK;
+    DeviceGuard g(p->device);
+    if (p->last_reader) {
+        if (p->reader_pending) cudaEventSynchronize(p->last_reader);
+        cudaEventDestroy(p->last_reader);
+    }
+    if (p->copy_stream) {
+        cudaStreamSynchronize(p->copy_stream);
+        cudaStreamDestroy(p->copy_stream);
+    }
+    if (p->ws_base) cudaFree(p->ws_base);
+    if (p->table_base) cudaFree(p->table_base);
+    if (p->arena_base) cudaFree(p->arena_base);
+    delete p;
+    return MLORA_OK;
+}
+
+mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const void* down, const void* up, int rank,
+                                float scale) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    if (rank < 1 || rank > p->max_rank) return fail(MLORA_ERR_RANK, "rank %d not in [1, %d]", rank, p->max_rank);
+    if (!down || !up) return fail(MLORA_ERR_INVALID_ARG, "down/up is NULL");
+    SlotHost& h = p->slots[slot];
+    const int need = Arena::round8(rank);
+    const int have = p->arena.free_units() + (h.rank > 0 ? Arena::round8(h.rank) : 0);
+    if (need > have)
+        return fail(MLORA_ERR_OOM, "rank budget: adapter needs %d units, %d free (of %d)", need, have, p->units);
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    mlora_status st = wait_readers(p);
+    if (st != MLORA_OK) return st;
+
+    if (h.rank > 0) {
+        p->arena.release(slot);
+        --p->loaded;
+    }
+    int unit = p->arena.alloc(slot, rank);
+    if (unit < 0) {
+        for (const ArenaMove& m : p->arena.compact()) {
+            st = move_units(p, m.from, m.to, m.size);
+            if (st != MLORA_OK) return st;
+            p->slots[m.id].unit = m.to;
+            st = push_slot(p, m.id);
+            if (st != MLORA_OK) return st;
+        }
+        unit = p->arena.alloc(slot, rank);
+        if (unit < 0) return fail(MLORA_ERR_OOM, "arena placement failed after compaction");
+    }
+    const int rpad = Arena::round8(rank);
+    char* dst_down = p->arena_down + (size_t)unit * p->din * p->esize;
+    char* dst_up = p->arena_up + (size_t)unit * p->dout * p->esize;
+    CU_TRY(cudaMemsetAsync(dst_down, 0, (size_t)rpad * p->din * p->esize, p->copy_stream));
+    CU_TRY(cudaMemsetAsync(dst_up, 0, (size_t)rpad * p->dout * p->esize, p->copy_stream));
+    CU_TRY(cudaMemcpyAsync(dst_down, down, (size_t)rank * p->din * p->esize, cudaMemcpyDefault, p->copy_stream));
+    CU_TRY(cudaMemcpy2DAsync(dst_up, (size_t)rpad * p->esize, up, (size_t)rank * p->esize, (size_t)rank * p->esize,
+                             (size_t)p->dout, cudaMemcpyDefault, p->copy_stream));
+    h.rank = rank;
+    h.rpad = rpad;
+    h.scale = scale;
+    h.unit = unit;
+    h.version += 1;
+    ++p->loaded;
+    return push_slot(p, slot);
+}
+
+mlora_status mlora_unload_adapter(mlora_pool_t p, int slot) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    SlotHost& h = p->slots[slot];
+    if (h.rank <= 0) return fail(MLORA_ERR_NOT_LOADED, "slot %d holds no adapter", slot);
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    mlora_status st = wait_readers(p);
+    if (st != MLORA_OK) return st;
+    p->arena.release(slot);
+    h = SlotHost{0, 0, 0.f, -1, h.version + 1};
+    --p->loaded;
+    return push_slot(p, slot);
+}
+
+mlora_status mlora_adapter_version(mlora_pool_t p, int slot, uint64_t* version) {
+    if (!p || !version) return fail(MLORA_ERR_INVALID_ARG, "pool/version is NULL");
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    *version = p->slots[slot].version;
+    return MLORA_OK;
+}
+
+mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const int32_t* row_adapter, int T,
+                           void* Y, mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
+    if (T == 0) return MLORA_OK;
+    if (!X || !W || !Y) return fail(MLORA_ERR_INVALID_ARG, "X/W/Y is NULL");
+    if (p->dtype == MLORA_BF16 && (!aligned16(X) || !aligned16(W) || !aligned16(Y)))
+        return fail(MLORA_ERR_INVALID_ARG, "bf16 X/W/Y must be 16-byte aligned");
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool lora = row_adapter != nullptr && p->max_slots > 0;
+    const bool bf16 = p->dtype == MLORA_BF16;
+    if (lora) CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
+    if (bf16 && tc_supported(p->dims, T)) {
+        TcForwardArgs a{};
+        a.X = X;
+        a.W = W;
+        a.Y = Y;
+        a.T = T;
+        a.lora = lora;
+        a.row_adapter = row_adapter;
+        a.slots = p->d_slots;
+        a.up_maps = p->d_up_maps;
+        a.arena_down = p->arena_down;
+        a.ws = p->ws;
+        a.dims = p->dims;
+        a.ext_chunk_cap = 0;
+        for (const SlotHost& h : p->slots) a.ext_chunk_cap += h.rank > 0 ? (h.rank + CHUNK - 1) / CHUNK : 0;
+        CU_TRY(tc_forward(a, st));
+    } else {
+        if (lora) CU_TRY(launch_shrink_simt(bf16, X, row_adapter, T, p->d_slots, p->arena_down, p->ws, p->dims, st));
+        CU_TRY(launch_base_expand_simt(bf16, X, W, row_adapter, T, Y, p->d_slots, p->arena_up, p->ws, p->dims, lora, st));
+    }
+    CU_TRY(cudaEventRecord(p->last_reader, st));
+    p->reader_pending = true;
+    return MLORA_OK;
+}
+
+mlora_status mlora_merge(mlora_pool_t p, void* W, int slot, mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (!W) return fail(MLORA_ERR_INVALID_ARG, "W is NULL");
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    if (p->slots[slot].rank <= 0) return fail(MLORA_ERR_NOT_LOADED, "slot %d holds no adapter", slot);
+    if (p->dtype == MLORA_BF16 && !aligned16(W)) return fail(MLORA_ERR_INVALID_ARG, "bf16 W must be 16-byte aligned");
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    CU_TRY(launch_merge_simt(p->dtype == MLORA_BF16, W, p->d_slots, slot, p->arena_down, p->arena_up, p->dims, st));
+    CU_TRY(cudaEventRecord(p->last_reader, st));
+    p->reader_pending = true;
+    return MLORA_OK;
+}
+
+mlora_status mlora_pool_status(mlora_pool_t p, mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    CU_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+    uint32_t word = 0;
+    CU_TRY(cudaMemcpyAsync(&word, p->ws.status, sizeof word, cudaMemcpyDeviceToHost, p->copy_stream));
+    CU_TRY(cudaMemsetAsync(p->ws.status, 0, sizeof word, p->copy_stream));
+    CU_TRY(cudaStreamSynchronize(p->copy_stream));
+    if (word & STATUS_BAD_ROW) return fail(MLORA_ERR_DEVICE_ROW, "a row named an invalid or empty slot");
+    return MLORA_OK;
+}
+
+mlora_status mlora_pool_info(mlora_pool_t p, mlora_pool_info_t* info) {
+    if (!p || !info) return fail(MLORA_ERR_INVALID_ARG, "pool/info is NULL");
+    info->din = p->din;
+    info->dout = p->dout;
+    info->dtype = (int32_t)p->dtype;
+    info->max_slots = p->max_slots;
+    info->max_rank = p->max_rank;
+    info->max_tokens = p->max_tokens;
+    info->rank_units = p->units;
+    info->rank_units_used = p->arena.used();
+    info->loaded = p->loaded;
+    info->device = p->device;
+    info->arena_bytes = p->arena_bytes;
+    info->table_bytes = p->table_bytes;
+    info->workspace_bytes = p->ws_bytes;
+    return MLORA_OK;
+}
+
+mlora_status mlora_debug_segments(mlora_pool_t p, const int32_t* row_adapter, int T, int32_t* perm,
+                                  int32_t* offsets, mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
+    if (!offsets || (T > 0 && !perm)) return fail(MLORA_ERR_INVALID_ARG, "perm/offsets is NULL");
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (!row_adapter || p->max_slots == 0 || T == 0) {
+        if (T > 0) CU_TRY(cudaMemsetAsync(perm, 0xFF, sizeof(int32_t) * (size_t)T, st));
+        CU_TRY(cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(p->max_slots + 1), st));
+        return MLORA_OK;
+    }
+    CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
+    CU_TRY(cudaMemcpyAsync(perm, p->ws.perm, sizeof(int32_t) * (size_t)T, cudaMemcpyDeviceToDevice, st));
+    CU_TRY(cudaMemcpyAsync(offsets, p->ws.offsets, sizeof(int32_t) * (size_t)(p->max_slots + 1),
+                           cudaMemcpyDeviceToDevice, st));
+    CU_TRY(cudaEventRecord(p->last_reader, st));
+    p->reader_pending = true;
+    return MLORA_OK;
+}
+
+}  // extern "C"

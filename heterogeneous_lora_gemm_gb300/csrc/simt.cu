@@ -1,0 +1,192 @@
+// CUDA-core (FMA) kernels of the multi-LoRA layer.
+//
+// These serve the fp32 pools (no TF32 anywhere: the fp32 path keeps full fp32
+// products and sums) and the bf16 shapes the tensor-core kernels do not take.
+//   shrink      v32[t, k] = scale_a * sum_i Down_a[k, i] x_t[i]       (rows of the segments)
+//   base_expand Y[t, o]  = sum_i W[o, i] x_t[i] + sum_k Up_a[o, k] v32[t, k]
+//   merge       W[o, i] += scale * sum_k Up[o, k] Down[k, i]
+// (ai-infra-kb "M031" tutorial §02 and §04.)  The expand reads the row's own
+// adapter and writes Y at the row's own index, so the result is in original row
+// order by construction.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace mlora {
+
+namespace {
+
+template <typename E>
+__device__ __forceinline__ float to_f32(E v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename E>
+__device__ __forceinline__ E from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ bool valid_slot(int a, int S, const SlotRec* slots) {
+    return a >= 0 && a < S && slots[a].rank > 0;
+}
+
+// One block per segment entry i (grid covers T; entries past n_valid exit).
+// Each warp takes rank rows k = warp, warp + nwarps, ... of the row's adapter.
+template <typename E>
+__global__ void shrink_simt_kernel(const E* __restrict__ X, const SlotRec* __restrict__ slots,
+                                   const E* __restrict__ arena_down, Workspace ws, const int32_t* __restrict__ row_adapter,
+                                   int din, int max_rank) {
+    const int i = blockIdx.x;
+    if (i >= ws.meta[0]) return;
+    const int t = ws.perm[i];
+    const int a = row_adapter[t];
+    const SlotRec rec = slots[a];
+    const E* x = X + (size_t)t * din;
+    const E* down = arena_down + (size_t)rec.unit * din;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int k = warp; k < rec.rank; k += nw) {
+        const E* d = down + (size_t)k * din;
+        float acc = 0.f;
+        for (int c = lane; c < din; c += 32) acc = fmaf(to_f32(d[c]), to_f32(x[c]), acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) ws.v32[(size_t)t * max_rank + k] = rec.scale * acc;
+    }
+}
+
+// Tiled FMA GEMM: a 64 (rows t) x 64 (outputs o) tile per block, 256 threads,
+// 4 x 4 outputs per thread, K in steps of 16 through shared memory.  The
+// expand of each output is added to the same fp32 accumulator before the single
+// final rounding.
+constexpr int BT = 64, BO = 64, BK = 16;
+
+template <typename E>
+__global__ void __launch_bounds__(256)
+base_expand_simt_kernel(const E* __restrict__ X, const E* __restrict__ W, const int32_t* __restrict__ row_adapter,
+                        int T, int din, int dout, E* __restrict__ Y, const SlotRec* __restrict__ slots,
+                        const E* __restrict__ arena_up, const float* __restrict__ v32, int S, int max_rank,
+                        int with_lora) {
+    __shared__ float xs[BK][BT + 1];
+    __shared__ float wsm[BK][BO + 1];
+    const int t0 = blockIdx.y * BT, o0 = blockIdx.x * BO;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;   // 16 x 16 threads
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < din; k0 += BK) {
+        for (int idx = threadIdx.x; idx < BK * BT; idx += 256) {
+            const int r = idx / BK, c = idx % BK;
+            const int t = t0 + r, k = k0 + c;
+            xs[c][r] = (t < T && k < din) ? to_f32(X[(size_t)t * din + k]) : 0.f;
+            const int o = o0 + r;
+            wsm[c][r] = (o < dout && k < din) ? to_f32(W[(size_t)o * din + k]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < BK; ++c) {
+            float xv[4], wv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xv[i] = xs[c][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) wv[j] = wsm[c][tx * 4 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+        int a = with_lora ? row_adapter[t] : -1;
+        const bool lora = with_lora && valid_slot(a, S, slots);
+        SlotRec rec{};
+        if (lora) rec = slots[a];
+        const float* v = v32 + (size_t)t * max_rank;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int o = o0 + tx * 4 + j;
+            if (o >= dout) continue;
+            float y = acc[i][j];
+            if (lora) {
+                const E* up = arena_up + (size_t)rec.unit * dout + (size_t)o * rec.rpad;
+                for (int k = 0; k < rec.rank; ++k) y = fmaf(to_f32(up[k]), v[k], y);
+            }
+            Y[(size_t)t * dout + o] = from_f32<E>(y);
+        }
+    }
+}
+
+// W[o, i] += scale * sum_k Up[o, k] Down[k, i]; one block per 4 output rows,
+// threads striding over i (coalesced Down and W accesses).
+template <typename E>
+__global__ void merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot,
+                                  const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din,
+                                  int dout) {
+    const SlotRec rec = slots[slot];
+    const int o = blockIdx.x;
+    if (o >= dout || rec.rank <= 0) return;
+    extern __shared__ float up_row[];
+    const E* up = arena_up + (size_t)rec.unit * dout + (size_t)o * rec.rpad;
+    for (int k = threadIdx.x; k < rec.rank; k += blockDim.x) up_row[k] = to_f32(up[k]);
+    __syncthreads();
+    const E* down = arena_down + (size_t)rec.unit * din;
+    for (int i = threadIdx.x; i < din; i += blockDim.x) {
+        float acc = 0.f;
+        for (int k = 0; k < rec.rank; ++k) acc = fmaf(up_row[k], to_f32(down[(size_t)k * din + i]), acc);
+        E* w = W + (size_t)o * din + i;
+        *w = from_f32<E>(fmaf(rec.scale, acc, to_f32(*w)));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_shrink_simt(bool bf16, const void* X, const int32_t* row_adapter, int T,
+                               const SlotRec* slots, const void* arena_down, const Workspace& ws,
+                               const PoolDims& d, cudaStream_t st) {
+    if (T <= 0) return cudaSuccess;
+    if (bf16)
+        shrink_simt_kernel<__nv_bfloat16><<<T, 128, 0, st>>>(
+            (const __nv_bfloat16*)X, slots, (const __nv_bfloat16*)arena_down, ws, row_adapter, d.din, d.max_rank);
+    else
+        shrink_simt_kernel<float><<<T, 128, 0, st>>>((const float*)X, slots, (const float*)arena_down, ws,
+                                                     row_adapter, d.din, d.max_rank);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_base_expand_simt(bool bf16, const void* X, const void* W,
+                                    const int32_t* row_adapter, int T, void* Y,
+                                    const SlotRec* slots, const void* arena_up, const Workspace& ws,
+                                    const PoolDims& d, bool with_lora, cudaStream_t st) {
+    if (T <= 0) return cudaSuccess;
+    dim3 grid((d.dout + BO - 1) / BO, (T + BT - 1) / BT);
+    if (bf16)
+        base_expand_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            (const __nv_bfloat16*)X, (const __nv_bfloat16*)W, row_adapter, T, d.din, d.dout, (__nv_bfloat16*)Y,
+            slots, (const __nv_bfloat16*)arena_up, ws.v32, d.S, d.max_rank, with_lora ? 1 : 0);
+    else
+        base_expand_simt_kernel<float><<<grid, 256, 0, st>>>((const float*)X, (const float*)W, row_adapter, T,
+                                                            d.din, d.dout, (float*)Y, slots, (const float*)arena_up,
+                                                            ws.v32, d.S, d.max_rank, with_lora ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_simt(bool bf16, void* W, const SlotRec* slots, int slot,
+                              const void* arena_down, const void* arena_up, const PoolDims& d,
+                              cudaStream_t st) {
+    const size_t smem = sizeof(float) * (size_t)d.max_rank;
+    if (bf16)
+        merge_simt_kernel<__nv_bfloat16><<<d.dout, 256, smem, st>>>(
+            (__nv_bfloat16*)W, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din,
+            d.dout);
+    else
+        merge_simt_kernel<float><<<d.dout, 256, smem, st>>>((float*)W, slots, slot, (const float*)arena_down,
+                                                          (const float*)arena_up, d.din, d.dout);
+    return cudaGetLastError();
+}
+
+}  // namespace mlora

@@ -1,0 +1,219 @@
+"""ctypes binding of libmlora.so -- argument marshalling only.
+
+The functions below carry the names and signatures of include/mlora.h; every
+step of the forward, the segment builder and the merge runs in the library's
+CUDA kernels.  ``Pool`` wraps a pool handle for callers that hold torch tensors
+(``tensor.data_ptr()`` and the current torch stream are passed through).
+
+The library must have been built (``__graft_entry__.build()`` or
+``python -m heterogeneous_lora_gemm_gb300.build``); importing a missing library
+raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmlora.so")
+
+MLORA_OK = 0
+MLORA_ERR_INVALID_ARG = 1
+MLORA_ERR_BAD_SLOT = 2
+MLORA_ERR_RANK = 3
+MLORA_ERR_NOT_LOADED = 4
+MLORA_ERR_OOM = 5
+MLORA_ERR_CUDA = 6
+MLORA_ERR_DEVICE_ROW = 7
+MLORA_ERR_UNSUPPORTED = 8
+MLORA_F32 = 0
+MLORA_BF16 = 1
+
+
+class MloraError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {status_string(status)} [{status}] {detail}")
+        self.status = status
+
+
+class PoolInfo(ctypes.Structure):
+    _fields_ = [("din", ctypes.c_int32), ("dout", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("max_slots", ctypes.c_int32), ("max_rank", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("rank_units", ctypes.c_int32), ("rank_units_used", ctypes.c_int32), ("loaded", ctypes.c_int32),
+                ("device", ctypes.c_int32), ("arena_bytes", ctypes.c_uint64), ("table_bytes", ctypes.c_uint64),
+                ("workspace_bytes", ctypes.c_uint64)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+# name -> (restype, argtypes), in header order
+_SIGNATURES = {
+    "mlora_status_string": (ctypes.c_char_p, [_I]),
+    "mlora_last_error": (ctypes.c_char_p, []),
+    "mlora_pool_create": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P)]),
+    "mlora_pool_destroy": (_I, [_P]),
+    "mlora_load_adapter": (_I, [_P, _I, _P, _P, _I, ctypes.c_float]),
+    "mlora_unload_adapter": (_I, [_P, _I]),
+    "mlora_adapter_version": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint64)]),
+    "mlora_forward": (_I, [_P, _P, _P, _P, _I, _P, _P]),
+    "mlora_merge": (_I, [_P, _P, _I, _P]),
+    "mlora_pool_status": (_I, [_P, _P]),
+    "mlora_pool_info": (_I, [_P, ctypes.POINTER(PoolInfo)]),
+    "mlora_debug_segments": (_I, [_P, _P, _I, _P, _P, _P]),
+    "mlora_arena_new": (_P, [_I]),
+    "mlora_arena_delete": (None, [_P]),
+    "mlora_arena_alloc": (_I, [_P, _I, _I]),
+    "mlora_arena_free": (_I, [_P, _I]),
+    "mlora_arena_compact": (_I, [_P, _P, _I]),
+    "mlora_arena_used": (_I, [_P]),
+    "mlora_arena_largest_hole": (_I, [_P]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmlora.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mlora_status_string(status).decode()
+
+
+def last_error() -> str:
+    return lib().mlora_last_error().decode()
+
+
+def check(status: int, where: str) -> None:
+    if status != MLORA_OK:
+        raise MloraError(status, where, last_error())
+
+
+# ---- the C entry points, same names -------------------------------------- #
+def mlora_pool_create(max_slots: int, rank_budget: int, max_rank: int, din: int, dout: int, dtype: int,
+                      max_tokens: int) -> int:
+    h = _P()
+    check(lib().mlora_pool_create(max_slots, rank_budget, max_rank, din, dout, dtype, max_tokens, ctypes.byref(h)),
+          "mlora_pool_create")
+    return h.value
+
+
+def mlora_pool_destroy(pool: int) -> None:
+    check(lib().mlora_pool_destroy(pool), "mlora_pool_destroy")
+
+
+def mlora_load_adapter(pool: int, slot: int, down_ptr: int, up_ptr: int, rank: int, scale: float) -> None:
+    check(lib().mlora_load_adapter(pool, slot, down_ptr, up_ptr, rank, scale), "mlora_load_adapter")
+
+
+def mlora_unload_adapter(pool: int, slot: int) -> None:
+    check(lib().mlora_unload_adapter(pool, slot), "mlora_unload_adapter")
+
+
+def mlora_adapter_version(pool: int, slot: int) -> int:
+    v = ctypes.c_uint64()
+    check(lib().mlora_adapter_version(pool, slot, ctypes.byref(v)), "mlora_adapter_version")
+    return int(v.value)
+
+
+def mlora_forward(pool: int, X_ptr: int, W_ptr: int, row_adapter_ptr: Optional[int], T: int, Y_ptr: int,
+                  stream: int) -> None:
+    check(lib().mlora_forward(pool, X_ptr, W_ptr, row_adapter_ptr or None, T, Y_ptr, stream or None),
+          "mlora_forward")
+
+
+def mlora_merge(pool: int, W_ptr: int, slot: int, stream: int) -> None:
+    check(lib().mlora_merge(pool, W_ptr, slot, stream or None), "mlora_merge")
+
+
+def mlora_pool_status(pool: int, stream: int) -> int:
+    """Returns the status code (MLORA_OK or MLORA_ERR_DEVICE_ROW); raises on CUDA errors."""
+    s = lib().mlora_pool_status(pool, stream or None)
+    if s not in (MLORA_OK, MLORA_ERR_DEVICE_ROW):
+        check(s, "mlora_pool_status")
+    return s
+
+
+def mlora_pool_info(pool: int) -> PoolInfo:
+    info = PoolInfo()
+    check(lib().mlora_pool_info(pool, ctypes.byref(info)), "mlora_pool_info")
+    return info
+
+
+def mlora_debug_segments(pool: int, row_adapter_ptr: Optional[int], T: int, perm_ptr: int, offsets_ptr: int,
+                         stream: int) -> None:
+    check(lib().mlora_debug_segments(pool, row_adapter_ptr or None, T, perm_ptr, offsets_ptr, stream or None),
+          "mlora_debug_segments")
+
+
+# ---- torch-facing convenience ------------------------------------------- #
+def _stream_handle(stream) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+class Pool:
+    """A pool handle driven with torch tensors (device memory and streams only)."""
+
+    def __init__(self, max_slots: int, rank_budget: int, max_rank: int, din: int, dout: int, dtype: str,
+                 max_tokens: int):
+        self.dtype = dtype
+        self.din, self.dout = din, dout
+        self.max_slots = max_slots
+        code = MLORA_BF16 if dtype == "bf16" else MLORA_F32
+        self.handle = mlora_pool_create(max_slots, rank_budget, max_rank, din, dout, code, max_tokens)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            mlora_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def load(self, slot: int, down, up, scale: float) -> None:
+        """down [r x din], up [dout x r]: torch tensors (host or device) of the pool dtype."""
+        down = down.contiguous()
+        up = up.contiguous()
+        mlora_load_adapter(self.handle, slot, down.data_ptr(), up.data_ptr(), int(down.shape[0]), float(scale))
+
+    def unload(self, slot: int) -> None:
+        mlora_unload_adapter(self.handle, slot)
+
+    def version(self, slot: int) -> int:
+        return mlora_adapter_version(self.handle, slot)
+
+    def forward(self, X, W, row_adapter, Y, stream=None) -> None:
+        ra = None if row_adapter is None else row_adapter.data_ptr()
+        mlora_forward(self.handle, X.data_ptr(), W.data_ptr(), ra, int(X.shape[0]), Y.data_ptr(),
+                      _stream_handle(stream))
+
+    def merge(self, W, slot: int, stream=None) -> None:
+        mlora_merge(self.handle, W.data_ptr(), slot, _stream_handle(stream))
+
+    def status(self, stream=None) -> int:
+        return mlora_pool_status(self.handle, _stream_handle(stream))
+
+    def info(self) -> PoolInfo:
+        return mlora_pool_info(self.handle)
+
+    def segments(self, row_adapter, perm, offsets, stream=None) -> None:
+        ra = None if row_adapter is None else row_adapter.data_ptr()
+        mlora_debug_segments(self.handle, ra, int(perm.shape[0]), perm.data_ptr(), offsets.data_ptr(),
+                             _stream_handle(stream))

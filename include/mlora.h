@@ -1,0 +1,210 @@
+/*
+ * mlora.h -- C ABI of the GB300 (sm_103a) multi-LoRA linear layer.
+ *
+ * What the layer computes (ai-infra-kb "M031" multi-LoRA tutorial, §02; airsota
+ * card "multi-LoRA serving vs merging", part 三.1; wiblog "vLLM LoRA adapter
+ * batch scheduling", section on Punica's grouped matmul):
+ *
+ *   for a mixed batch of T rows X[T x din] in which row t names adapter a_t or none,
+ *       Y[t,:] = W X[t,:]  +  scale_a * Up_a (Down_a X[t,:])      (a = a_t)
+ *       Y[t,:] = W X[t,:]                                          (no adapter)
+ *   with W [dout x din], Down_a [r_a x din], Up_a [dout x r_a]; the shared base
+ *   product covers every row in one call, ranks may differ per adapter, and each
+ *   result is written to the row it came from (original row order).
+ *
+ * and, as a separate call (M031 §04), the static merge W <- W + scale_a Up_a Down_a.
+ *
+ * Conventions for every call below
+ *   - Matrices are dense and row-major: X [T x din], W [dout x din] (the layout of
+ *     a torch Linear weight), Y [T x dout], Down [r x din], Up [dout x r].
+ *   - Element type is the pool's dtype (MLORA_BF16: bf16 in, fp32 accumulate, bf16
+ *     out with one final rounding; MLORA_F32: fp32 throughout, CUDA-core FMA only).
+ *   - X, W, Y, row_adapter, perm and offsets are DEVICE pointers on the pool's
+ *     device; for MLORA_BF16 X, W and Y must be 16-byte aligned.  The caller owns
+ *     them.  Adapter sources given to mlora_load_adapter may be host or device
+ *     memory and may be freed as soon as that call returns.
+ *   - Calls taking a stream only enqueue work on it and return; errors of
+ *     arguments are returned before anything is enqueued.  A pool serves one
+ *     stream at a time: its forward and merge calls share the pool's workspace,
+ *     so calls on one pool that overlap on the GPU race.  Calls on one pool must
+ *     not be made from several host threads at once.
+ *   - No call traps or asserts on the device.  A row that names a slot outside
+ *     [0, max_slots) or an empty slot is treated as a row without adapter and
+ *     raises a device status bit, read by mlora_pool_status.
+ */
+#ifndef MLORA_H
+#define MLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mlora_pool* mlora_pool_t;
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* mlora_stream_t;
+
+typedef enum mlora_status {
+    MLORA_OK = 0,
+    MLORA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, T > max_tokens */
+    MLORA_ERR_BAD_SLOT = 2,      /* slot outside [0, max_slots) */
+    MLORA_ERR_RANK = 3,          /* rank < 1 or rank > max_rank */
+    MLORA_ERR_NOT_LOADED = 4,    /* the slot holds no adapter */
+    MLORA_ERR_OOM = 5,           /* rank budget exhausted, or a device allocation failed */
+    MLORA_ERR_CUDA = 6,          /* a CUDA runtime call failed (no device, launch failure, ...) */
+    MLORA_ERR_DEVICE_ROW = 7,    /* (mlora_pool_status) a row named an invalid or empty slot */
+    MLORA_ERR_UNSUPPORTED = 8    /* shape outside what the kernels handle (see mlora_pool_create) */
+} mlora_status;
+
+typedef enum mlora_dtype { MLORA_F32 = 0, MLORA_BF16 = 1 } mlora_dtype;
+
+typedef struct mlora_pool_info_s {
+    int32_t din, dout, dtype, max_slots, max_rank, max_tokens;
+    int32_t rank_units;          /* capacity of the adapter arena, in rank units */
+    int32_t rank_units_used;     /* units held by loaded adapters (rank rounded up to 8 each) */
+    int32_t loaded;              /* number of loaded slots */
+    int32_t device;              /* CUDA device the pool lives on */
+    uint64_t arena_bytes;        /* device bytes of the adapter arena (Down and Up) */
+    uint64_t table_bytes;        /* device bytes of the slot table and per-slot descriptors */
+    uint64_t workspace_bytes;    /* device bytes of the per-forward workspace */
+} mlora_pool_info_t;
+
+/* Text for a status code (static storage). */
+const char* mlora_status_string(mlora_status s);
+
+/* Detail of the most recent failure in the calling thread ("" if none). */
+const char* mlora_last_error(void);
+
+/*
+ * Creates an adapter pool on the current CUDA device: the device-resident slot
+ * pool that M031 §06 and the wiblog section on max_loras describe (slots fixed
+ * up front), sized by a total rank budget instead of max_slots x max_rank so that
+ * one high-rank adapter does not inflate every slot (wiblog failure mode
+ * "max_lora_rank set too large").
+ *
+ *   max_slots   number of adapter slots (ids 0..max_slots-1), 0..4096; 0 makes a
+ *               pool whose forward is the plain base projection
+ *   rank_budget total rank resident at once; an adapter of rank r holds
+ *               roundup(r, 8) units of it; rounded up to a multiple of 8
+ *   max_rank    largest rank one adapter may have, 1..256
+ *   din, dout   layer shape, >= 1; MLORA_BF16 needs din % 8 == 0
+ *   dtype       element type of X, W, Y, Down and Up
+ *   max_tokens  largest T a forward may pass, >= 1
+ *   out         receives the pool handle (NULL on failure)
+ *
+ * All device memory the pool uses is allocated here (arena, slot table,
+ * workspace); forward, merge, load and unload allocate nothing.
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA.  Argument checks run before any
+ * CUDA call.
+ */
+mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int din, int dout,
+                               mlora_dtype dtype, int max_tokens, mlora_pool_t* out);
+
+/* Waits for the pool's outstanding work and frees all its device memory. NULL is a no-op. */
+mlora_status mlora_pool_destroy(mlora_pool_t pool);
+
+/*
+ * Copies an adapter into a slot (M031 §06: weights must be in place before a
+ * forward uses them; the slot is overwritten only after its last reader).
+ *
+ *   slot   0..max_slots-1; an adapter already in the slot is replaced
+ *   down   Down [rank x din], row-major, pool dtype, host or device memory
+ *   up     Up [dout x rank], row-major, pool dtype, host or device memory
+ *   rank   1..max_rank
+ *   scale  the adapter's scale (alpha / r in the airsota card's notation)
+ *
+ * Blocks the calling thread until the pool's last enqueued forward or merge has
+ * finished, then copies, updates the device slot table and bumps the slot's
+ * version; returns when the copy is complete.  If the rank budget has no room
+ * left, live adapters are compacted first; OOM if it still does not fit.
+ * Errors: INVALID_ARG, BAD_SLOT, RANK, OOM, CUDA.  On error the slot is unchanged.
+ */
+mlora_status mlora_load_adapter(mlora_pool_t pool, int slot, const void* down, const void* up,
+                                int rank, float scale);
+
+/* Empties a slot after its last reader (same waiting rule as load); bumps its version.
+ * Errors: BAD_SLOT, NOT_LOADED, CUDA. */
+mlora_status mlora_unload_adapter(mlora_pool_t pool, int slot);
+
+/* Version counter of a slot: 0 before the first load, +1 at every load and unload
+ * (the immutable compute identity of M031 §07). Errors: BAD_SLOT, INVALID_ARG. */
+mlora_status mlora_adapter_version(mlora_pool_t pool, int slot, uint64_t* version);
+
+/*
+ * The multi-LoRA forward (M031 §02): Y = X W^T for all T rows, plus
+ * scale_a Up_a (Down_a x) on every row x whose adapter is a, in original row
+ * order.  Segment build, shrink, base projection and expand all run in this
+ * library's kernels on `stream`.
+ *
+ *   X            device [T x din], pool dtype
+ *   W            device [dout x din], pool dtype
+ *   row_adapter  device int32 [T]: slot id per row, -1 = no adapter; NULL = all -1
+ *   T            0..max_tokens; T == 0 enqueues nothing and returns OK
+ *   Y            device [T x dout], pool dtype, overwritten; must not overlap X or W
+ *   stream       CUDA stream
+ *
+ * Rows naming an invalid or empty slot get no delta and set the status bit
+ * reported by mlora_pool_status.  Errors: INVALID_ARG, CUDA.
+ */
+mlora_status mlora_forward(mlora_pool_t pool, const void* X, const void* W,
+                           const int32_t* row_adapter, int T, void* Y, mlora_stream_t stream);
+
+/*
+ * Static merge of one adapter into a base weight, in place (M031 §04):
+ *   W[o,i] <- W[o,i] + scale * sum_k Up[o,k] Down[k,i]      (fp32 sum, one rounding)
+ * The merged weight is valid for rows of this adapter only.  Keep the original
+ * W if the merge may need to be undone: it is not reversible exactly.
+ *   W      device [dout x din], pool dtype
+ *   slot   a loaded slot
+ * Errors: INVALID_ARG, BAD_SLOT, NOT_LOADED, CUDA.
+ */
+mlora_status mlora_merge(mlora_pool_t pool, void* W, int slot, mlora_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the pool's device status word.
+ * Returns MLORA_OK, MLORA_ERR_DEVICE_ROW (a forward since the last call saw a row
+ * naming an invalid or empty slot) or MLORA_ERR_CUDA (the stream reported an error).
+ */
+mlora_status mlora_pool_status(mlora_pool_t pool, mlora_stream_t stream);
+
+/* Fills `info` with the pool's configuration and memory split. Errors: INVALID_ARG. */
+mlora_status mlora_pool_info(mlora_pool_t pool, mlora_pool_info_t* info);
+
+/*
+ * Runs only the segment builder of mlora_forward (M031 §03: rows grouped by
+ * adapter, original order kept inside a group, groups in ascending slot id) and
+ * copies its result to the caller's device buffers:
+ *   perm     device int32 [T]: original row indices in segment order; entries past
+ *            the number of rows with a valid adapter are set to -1
+ *   offsets  device int32 [max_slots + 1]: offsets[s]..offsets[s+1] is slot s's range
+ * Errors: INVALID_ARG, CUDA.
+ */
+mlora_status mlora_debug_segments(mlora_pool_t pool, const int32_t* row_adapter, int T,
+                                  int32_t* perm, int32_t* offsets, mlora_stream_t stream);
+
+/*
+ * Host-only view of the arena allocator the pool uses (no CUDA calls), for tests
+ * of the placement logic.  An arena has `units` rank units; an allocation of
+ * `n` units is placed first-fit at a multiple of 8.  mlora_arena_compact slides
+ * every live block toward offset 0, keeping their order, and reports the moves.
+ */
+typedef struct mlora_arena* mlora_arena_t;
+mlora_arena_t mlora_arena_new(int units);
+void mlora_arena_delete(mlora_arena_t arena);
+/* Returns the unit offset of the new block of `id`, or -1 if no hole fits. */
+int mlora_arena_alloc(mlora_arena_t arena, int id, int n);
+/* Frees the block of `id`; returns 0, or -1 if `id` holds no block. */
+int mlora_arena_free(mlora_arena_t arena, int id);
+/* Compacts; writes up to `cap` moves as (id, old_offset, new_offset) triples; returns the count. */
+int mlora_arena_compact(mlora_arena_t arena, int32_t* moves, int cap);
+/* Units in use and largest free hole. */
+int mlora_arena_used(mlora_arena_t arena);
+int mlora_arena_largest_hole(mlora_arena_t arena);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLORA_H */

@@ -1,0 +1,274 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Values: |gpu - oracle| <= 1e-2 (1 + |oracle|) for bf16, 1e-5 (1 + |oracle|) for fp32.
+Indices (perm, offsets): bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from tests.tolerance import assert_within, within
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():   # pragma: no cover - CPU machine
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+from heterogeneous_lora_gemm_gb300 import mlora  # noqa: E402
+from tests.gpu_harness import make_pool, run_layer, to_device, to_f64, upload  # noqa: E402
+
+
+def ora_adapters(layer):
+    return [None if a is None else oracle.OracleAdapter(a.down_f64, a.up_f64, a.scale) for a in layer.slot_list()]
+
+
+def want_of(layer, rows=None, row_adapter=None):
+    ra = layer.row_adapter if row_adapter is None else row_adapter
+    return oracle.forward(layer.X_f64, layer.W_f64, ra, ora_adapters(layer), rows=rows)
+
+
+def gpu_segments(layer, pool, row_adapter=None):
+    ra = torch.from_numpy((layer.row_adapter if row_adapter is None else row_adapter).astype(np.int32)).cuda()
+    T = ra.shape[0]
+    perm = torch.full((max(T, 1),), -7, dtype=torch.int32, device="cuda")
+    offs = torch.full((layer.max_slots + 1,), -7, dtype=torch.int32, device="cuda")
+    pool.segments(ra, perm[:T], offs)
+    torch.cuda.synchronize()
+    return perm[:T].cpu().numpy(), offs.cpu().numpy()
+
+
+def check_segments(layer, pool, row_adapter=None):
+    ra = layer.row_adapter if row_adapter is None else row_adapter
+    perm, offs = gpu_segments(layer, pool, ra)
+    counts, w_offs, w_perm, _ = oracle.segments(ra, oracle.slot_ranks(ora_adapters(layer)), layer.max_slots)
+    assert np.array_equal(offs, w_offs), (offs, w_offs)
+    n = w_perm.size
+    assert np.array_equal(perm[:n], w_perm)
+    assert np.all(perm[n:] == -1)
+
+
+# --------------------------------------------------------------------------- #
+def test_worked_example_fp32():
+    layer = wl.worked_example(0)
+    Y = run_layer(layer)
+    assert_within(Y, want_of(layer), "f32", "worked example")
+    pool = make_pool(layer)
+    check_segments(layer, pool)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode_step(seed):
+    layer = wl.decode_step(seed)
+    assert_within(run_layer(layer), want_of(layer), "bf16", "decode_step")
+
+
+def test_fragmented_decode():
+    layer = wl.fragmented_decode(0)
+    pool = make_pool(layer)
+    check_segments(layer, pool)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "fragmented_decode")
+
+
+def prefill_sample_rows(seed):
+    lengths = wl.prefill_lengths(seed)
+    starts = np.concatenate([[0], np.cumsum(lengths)[:-1]])
+    rng = np.random.default_rng(1000 + seed)
+    rows = []
+    for s, n in zip(starts, lengths):
+        rows += [s, s + n - 1] + list(s + rng.choice(n, size=8, replace=False))
+    return np.array(sorted(set(int(r) for r in rows)), np.int64)
+
+
+def test_prefill_sampled_rows():
+    layer = wl.prefill(0)
+    pool = make_pool(layer)
+    check_segments(layer, pool)
+    Y = run_layer(layer, pool)
+    rows = prefill_sample_rows(0)
+    assert_within(Y[rows], want_of(layer, rows=rows), "bf16", "prefill")
+    assert np.isfinite(Y).all()
+
+
+@pytest.mark.parametrize("module", ["q", "k", "v", "down", "gate"])
+def test_stack7b_projection(module):
+    layer = wl.stack7b_projection(0, 0 if module in "qkv" else 17, module)
+    Y = run_layer(layer)
+    rows = None if module in ("q", "k", "v") else np.arange(0, 128, 9)
+    want = want_of(layer, rows=rows)
+    assert_within(Y if rows is None else Y[rows], want, "bf16", f"stack7b {module}")
+
+
+# --------------------------------------------------------------------------- #
+# edge cases
+@pytest.mark.parametrize("T,din,dout,ranks", [
+    (1, 64, 64, [16]),
+    (37, 72, 200, [8, 0, 24, 64, 1]),
+    (300, 128, 136, [16, 8, 64]),
+    (129, 4096, 256, [16, 64, 8]),
+    (5, 8, 8, [3, 5]),
+])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_ragged_shapes(T, din, dout, ranks, dtype):
+    layer = wl.random_layer(T * 7 + din, T=T, din=din, dout=dout, ranks=ranks, dtype=dtype)
+    pool = make_pool(layer)
+    check_segments(layer, pool)
+    assert_within(run_layer(layer, pool), want_of(layer), dtype, f"ragged {T}x{din}x{dout}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_all_rows_without_adapter_and_null_map(dtype):
+    layer = wl.random_layer(3, T=33, din=64, dout=48, ranks=[16, 8], dtype=dtype,
+                            row_adapter=np.full(33, -1, np.int32))
+    pool = make_pool(layer)
+    assert_within(run_layer(layer, pool), want_of(layer), dtype, "all -1")
+    assert_within(run_layer(layer, pool, with_row_adapter=False), want_of(layer), dtype, "NULL map")
+    check_segments(layer, pool)
+
+
+def test_all_rows_one_adapter_equals_merged():
+    layer = wl.random_layer(4, T=64, din=256, dout=128, ranks=[0, 32], row_adapter=np.full(64, 1, np.int32))
+    Y = run_layer(layer)
+    a = layer.slot_list()[1]
+    Wm = layer.W_f64 + a.scale * (a.up_f64 @ a.down_f64)
+    assert_within(Y, layer.X_f64 @ Wm.T, "bf16", "single adapter")
+
+
+def test_invalid_ids_set_status_and_act_as_none():
+    ra = np.array([0, 5, 1, -3, 2, 0, 9, -1], np.int32)   # 5, 9 out of range, -3 bad, slot 1 empty
+    layer = wl.random_layer(5, T=8, din=64, dout=32, ranks=[8, 0, 16], row_adapter=ra)
+    pool = make_pool(layer)
+    assert pool.status() == mlora.MLORA_OK
+    Y = run_layer(layer, pool)
+    assert pool.status() == mlora.MLORA_ERR_DEVICE_ROW
+    assert pool.status() == mlora.MLORA_OK           # read-and-clear
+    assert_within(Y, want_of(layer), "bf16", "invalid ids")
+    base = layer.X_f64 @ layer.W_f64.T
+    assert_within(Y[[1, 2, 3, 6, 7]], base[[1, 2, 3, 6, 7]], "bf16", "invalid rows keep base")
+    check_segments(layer, pool)
+
+
+def test_zero_rows_is_noop():
+    layer = wl.random_layer(6, T=4, din=64, dout=32, ranks=[8])
+    pool = make_pool(layer)
+    X, W, ra, Y = upload(layer)
+    mlora.mlora_forward(pool.handle, X.data_ptr(), W.data_ptr(), ra.data_ptr(), 0, Y.data_ptr(), 0)
+    torch.cuda.synchronize()
+    assert torch.isnan(Y.float()).all()
+
+
+def test_max_tokens_boundary_and_errors():
+    layer = wl.random_layer(7, T=48, din=64, dout=64, ranks=[16, 16])
+    pool = make_pool(layer, max_tokens=48)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "T = max_tokens")
+    X, W, ra, Y = upload(layer)
+    with pytest.raises(mlora.MloraError) as e:
+        mlora.mlora_forward(pool.handle, X.data_ptr(), W.data_ptr(), ra.data_ptr(), 49, Y.data_ptr(), 0)
+    assert e.value.status == mlora.MLORA_ERR_INVALID_ARG
+    with pytest.raises(mlora.MloraError) as e:
+        mlora.mlora_forward(pool.handle, X.data_ptr() + 2, W.data_ptr(), ra.data_ptr(), 4, Y.data_ptr(), 0)
+    assert e.value.status == mlora.MLORA_ERR_INVALID_ARG
+    with pytest.raises(mlora.MloraError) as e:
+        pool.load(0, to_device(layer.adapters[0].down, "bf16")[:0], to_device(layer.adapters[0].up, "bf16"), 1.0)
+    assert e.value.status == mlora.MLORA_ERR_RANK
+
+
+# --------------------------------------------------------------------------- #
+# merge (M031 §04)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_merge_matches_oracle(dtype):
+    layer = wl.random_layer(8, T=1, din=512, dout=384, ranks=[16, 64], dtype=dtype)
+    pool = make_pool(layer)
+    for slot in (0, 1):
+        W = to_device(layer.W, dtype)
+        pool.merge(W, slot)
+        torch.cuda.synchronize()
+        a = ora_adapters(layer)[slot]
+        assert_within(to_f64(W), oracle.merge(layer.W_f64, a), dtype, f"merge slot {slot}")
+
+
+def test_merged_weight_serves_only_its_adapter():
+    layer = wl.decode_step(0)
+    pool = make_pool(layer)
+    W = to_device(layer.W, "bf16")
+    pool.merge(W, 0)
+    X, _, ra, Y = upload(layer)
+    pool.forward(X, W, None, Y)        # merged weight, no branch
+    torch.cuda.synchronize()
+    Ym = to_f64(Y)
+    want = want_of(layer)
+    rows_a = layer.row_adapter == 0
+    assert_within(Ym[rows_a], want[rows_a], "bf16", "merged A on A rows")
+    assert not within(Ym[layer.row_adapter == 1], want[layer.row_adapter == 1], "bf16").all()
+
+
+# --------------------------------------------------------------------------- #
+# pool lifecycle (M031 §06/§07)
+def test_load_waits_for_last_reader_and_versions():
+    layer = wl.random_layer(9, T=256, din=1024, dout=1024, ranks=[16, 16], p_none=0.0)
+    other = wl.random_layer(10, T=256, din=1024, dout=1024, ranks=[16, 16], p_none=0.0)
+    pool = make_pool(layer)
+    assert pool.version(0) == 1
+    X, W, ra, Y = upload(layer)
+    pool.forward(X, W, ra, Y)                       # enqueued, not waited for
+    b = other.adapters[0]
+    pool.load(0, to_device(b.down, "bf16"), to_device(b.up, "bf16"), b.scale)   # replaces slot 0
+    assert pool.version(0) == 2
+    torch.cuda.synchronize()
+    assert_within(to_f64(Y), want_of(layer), "bf16", "forward before the load keeps old weights")
+    Y2 = torch.empty_like(Y)
+    pool.forward(X, W, ra, Y2)
+    torch.cuda.synchronize()
+    swapped = [oracle.OracleAdapter(b.down_f64, b.up_f64, b.scale), ora_adapters(layer)[1]]
+    assert_within(to_f64(Y2), oracle.forward(layer.X_f64, layer.W_f64, layer.row_adapter, swapped), "bf16",
+                  "forward after the load uses new weights")
+    pool.unload(1)
+    assert pool.version(1) == 2
+    with pytest.raises(mlora.MloraError) as e:
+        pool.unload(1)
+    assert e.value.status == mlora.MLORA_ERR_NOT_LOADED
+
+
+def test_arena_compaction_keeps_adapters_correct():
+    ranks = [16, 64, 8, 24, 16, 8]
+    layer = wl.random_layer(11, T=96, din=256, dout=192, ranks=ranks, p_none=0.1)
+    budget = sum((r + 7) // 8 * 8 for r in ranks)
+    pool = make_pool(layer, rank_budget=budget, max_rank=64)
+    info = pool.info()
+    assert info.rank_units == budget and info.rank_units_used == budget
+    pool.unload(0)
+    pool.unload(2)
+    pool.unload(4)           # holes of 16, 8, 16 units: 40 free, largest hole 16
+    big = wl.random_layer(12, T=1, din=256, dout=192, ranks=[40])
+    a = big.adapters[0]
+    pool.load(0, to_device(a.down, "bf16"), to_device(a.up, "bf16"), a.scale)    # needs compaction
+    assert pool.info().rank_units_used == budget
+    slots = ora_adapters(layer)
+    slots[0] = oracle.OracleAdapter(a.down_f64, a.up_f64, a.scale)
+    slots[2] = slots[4] = None
+    ra = layer.row_adapter.copy()
+    ra[(ra == 2) | (ra == 4)] = -1
+    lay2 = wl.LayerData(layer.name, "bf16", layer.din, layer.dout, layer.X, layer.W, ra, layer.max_slots, [])
+    Y = run_layer(lay2, pool)
+    assert_within(Y, oracle.forward(layer.X_f64, layer.W_f64, ra, slots), "bf16", "after compaction")
+    with pytest.raises(mlora.MloraError) as e:
+        pool.load(2, to_device(a.down, "bf16"), to_device(a.up, "bf16"), a.scale)
+    assert e.value.status == mlora.MLORA_ERR_OOM
+
+
+def test_host_sources_for_load():
+    layer = wl.random_layer(13, T=20, din=128, dout=96, ranks=[8, 16])
+    pool = make_pool(layer, host_sources=True)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "host sources")
+
+
+# --------------------------------------------------------------------------- #
+# the checker catches wrong routings on real GPU output (M031 §03)
+def test_wrong_routing_is_detected_on_gpu_output():
+    layer = wl.decode_step(0)
+    Y = run_layer(layer)
+    ads = ora_adapters(layer)
+    swapped = oracle.forward(layer.X_f64, layer.W_f64, layer.row_adapter, [ads[1], ads[0], ads[2]])
+    assert not within(Y, swapped, "bf16").all()
+    assert within(Y, want_of(layer), "bf16").all()
