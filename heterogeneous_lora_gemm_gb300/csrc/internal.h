@@ -16,7 +16,7 @@ struct SlotRec {
 };
 
 // Bits of the device status word.
-enum : uint32_t { STATUS_BAD_ROW = 1u };
+enum : uint32_t { STATUS_BAD_ROW = 1u, STATUS_TIMEOUT = 2u };
 
 // Width of one K-extension chunk of the low-rank intermediate (one bf16 MMA K step).
 constexpr int CHUNK = 16;
@@ -41,6 +41,7 @@ struct PoolDims {
 };
 
 // ---- launchers (each returns the launch's cudaError_t) ----
+cudaError_t seg_init();   // raises the segment builder's shared memory cap (outside capture)
 cudaError_t launch_seg_build(const int32_t* row_adapter, int T, const SlotRec* slots,
                              const Workspace& ws, const PoolDims& d, cudaStream_t st);
 

@@ -97,11 +97,21 @@ struct mlora_pool {
     cudaStream_t copy_stream = nullptr;
     cudaEvent_t last_reader = nullptr;
     bool reader_pending = false;
+    bool captured = false;           // a forward or merge was captured into a graph
+
+    std::vector<cudaEvent_t> prof_start, prof_stop;
+    size_t prof_next = 0;
 };
 
 namespace {
 
 mlora_status wait_readers(mlora_pool* p) {
+    if (p->captured) {
+        // graph replays of captured calls are invisible to the pool: wait for the device
+        CU_TRY(cudaDeviceSynchronize());
+        p->reader_pending = false;
+        return MLORA_OK;
+    }
     if (p->reader_pending) {
         CU_TRY(cudaEventSynchronize(p->last_reader));
         p->reader_pending = false;
@@ -145,6 +155,20 @@ mlora_status move_units(mlora_pool* p, int from, int to, int size) {
 
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
+// Records the pool's last-reader event after a forward/merge, or notes that the
+// call went into a graph under capture (then later loads wait for the device).
+mlora_status note_reader(mlora_pool* p, cudaStream_t st) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CU_TRY(cudaStreamIsCapturing(st, &cs));
+    if (cs != cudaStreamCaptureStatusNone) {
+        p->captured = true;
+        return MLORA_OK;
+    }
+    CU_TRY(cudaEventRecord(p->last_reader, st));
+    p->reader_pending = true;
+    return MLORA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -160,6 +184,7 @@ const char* mlora_status_string(mlora_status s) {
         case MLORA_ERR_CUDA: return "CUDA error";
         case MLORA_ERR_DEVICE_ROW: return "a row named an invalid or empty slot";
         case MLORA_ERR_UNSUPPORTED: return "unsupported shape";
+        case MLORA_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait gave up";
     }
     return "unknown status";
 }
@@ -266,6 +291,10 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     w.partials = (float*)(p->ws_base + o_part);
     w.tile_ctr = (int32_t*)(p->ws_base + o_ctr);
 
+    e = seg_init();
+    if (e != cudaSuccess) return bail(cuda_fail(e, "seg_init"));
+    e = tc_init();
+    if (e != cudaSuccess) return bail(cuda_fail(e, "tc_init"));
     e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaStreamCreate"));
     e = cudaEventCreateWithFlags(&p->last_reader, cudaEventDisableTiming);
@@ -379,6 +408,12 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
     const bool lora = row_adapter != nullptr && p->max_slots > 0;
     const bool bf16 = p->dtype == MLORA_BF16;
     if (lora) CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
+    cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+    if (!p->prof_start.empty()) {
+        const size_t k = p->prof_next++ % p->prof_start.size();
+        ev_start = p->prof_start[k];
+        ev_stop = p->prof_stop[k];
+    }
     if (bf16 && tc_supported(p->dims, T)) {
         TcForwardArgs a{};
         a.X = X;
@@ -394,14 +429,16 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
         a.dims = p->dims;
         a.ext_chunk_cap = 0;
         for (const SlotHost& h : p->slots) a.ext_chunk_cap += h.rank > 0 ? (h.rank + CHUNK - 1) / CHUNK : 0;
+        a.ev_start = ev_start;
+        a.ev_stop = ev_stop;
         CU_TRY(tc_forward(a, st));
     } else {
         if (lora) CU_TRY(launch_shrink_simt(bf16, X, row_adapter, T, p->d_slots, p->arena_down, p->ws, p->dims, st));
+        if (ev_start) CU_TRY(record_profile(ev_start, st));
         CU_TRY(launch_base_expand_simt(bf16, X, W, row_adapter, T, Y, p->d_slots, p->arena_up, p->ws, p->dims, lora, st));
+        if (ev_stop) CU_TRY(record_profile(ev_stop, st));
     }
-    CU_TRY(cudaEventRecord(p->last_reader, st));
-    p->reader_pending = true;
-    return MLORA_OK;
+    return note_reader(p, st);
 }
 
 mlora_status mlora_merge(mlora_pool_t p, void* W, int slot, mlora_stream_t stream) {
@@ -414,9 +451,7 @@ mlora_status mlora_merge(mlora_pool_t p, void* W, int slot, mlora_stream_t strea
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t st = (cudaStream_t)stream;
     CU_TRY(launch_merge_simt(p->dtype == MLORA_BF16, W, p->d_slots, slot, p->arena_down, p->arena_up, p->dims, st));
-    CU_TRY(cudaEventRecord(p->last_reader, st));
-    p->reader_pending = true;
-    return MLORA_OK;
+    return note_reader(p, st);
 }
 
 mlora_status mlora_pool_status(mlora_pool_t p, mlora_stream_t stream) {
@@ -428,6 +463,7 @@ mlora_status mlora_pool_status(mlora_pool_t p, mlora_stream_t stream) {
     CU_TRY(cudaMemcpyAsync(&word, p->ws.status, sizeof word, cudaMemcpyDeviceToHost, p->copy_stream));
     CU_TRY(cudaMemsetAsync(p->ws.status, 0, sizeof word, p->copy_stream));
     CU_TRY(cudaStreamSynchronize(p->copy_stream));
+    if (word & STATUS_TIMEOUT) return fail(MLORA_ERR_DEVICE_TIMEOUT, "a kernel pipeline wait gave up");
     if (word & STATUS_BAD_ROW) return fail(MLORA_ERR_DEVICE_ROW, "a row named an invalid or empty slot");
     return MLORA_OK;
 }
@@ -467,8 +503,19 @@ mlora_status mlora_debug_segments(mlora_pool_t p, const int32_t* row_adapter, in
     CU_TRY(cudaMemcpyAsync(perm, p->ws.perm, sizeof(int32_t) * (size_t)T, cudaMemcpyDeviceToDevice, st));
     CU_TRY(cudaMemcpyAsync(offsets, p->ws.offsets, sizeof(int32_t) * (size_t)(p->max_slots + 1),
                            cudaMemcpyDeviceToDevice, st));
-    CU_TRY(cudaEventRecord(p->last_reader, st));
-    p->reader_pending = true;
+    return note_reader(p, st);
+}
+
+mlora_status mlora_profile_events(mlora_pool_t p, void* const* starts, void* const* stops, int n) {
+    if (!p || n < 0 || (n > 0 && (!starts || !stops))) return fail(MLORA_ERR_INVALID_ARG, "bad profiling events");
+    p->prof_start.clear();
+    p->prof_stop.clear();
+    for (int i = 0; i < n; ++i) {
+        if (!starts[i] || !stops[i]) return fail(MLORA_ERR_INVALID_ARG, "event %d is NULL", i);
+        p->prof_start.push_back((cudaEvent_t)starts[i]);
+        p->prof_stop.push_back((cudaEvent_t)stops[i]);
+    }
+    p->prof_next = 0;
     return MLORA_OK;
 }
 

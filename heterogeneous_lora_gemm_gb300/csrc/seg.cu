@@ -195,17 +195,20 @@ seg_build_kernel(const int32_t* __restrict__ row_adapter, int T, const SlotRec* 
 
 }  // namespace
 
+cudaError_t seg_init() {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(seg_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    return e;
+}
+
 cudaError_t launch_seg_build(const int32_t* row_adapter, int T, const SlotRec* slots,
                              const Workspace& ws, const PoolDims& d, cudaStream_t st) {
     const int S = d.S;
     int P = S > 0 ? 10240 / S : SEG_WARPS;
     P = P < 1 ? 1 : (P > SEG_WARPS ? SEG_WARPS : P);
     const size_t smem = sizeof(int) * ((size_t)2 * S + (size_t)P * S);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(seg_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-    }
     seg_build_kernel<<<1, SEG_THREADS, smem, st>>>(row_adapter, T, slots, ws, S, P, d.max_chunks);
     return cudaGetLastError();
 }

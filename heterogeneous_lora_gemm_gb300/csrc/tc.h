@@ -19,6 +19,9 @@ TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d);
 // columns past rpad read as zero.
 bool tc_encode_up_map(CUtensorMap* map, void* up_block, int rpad, int dout);
 
+// Raises the dynamic shared memory cap of the tensor-core kernels (call outside capture).
+cudaError_t tc_init();
+
 // Whether the tensor-core forward takes this pool shape and batch size.
 bool tc_supported(const PoolDims& d, int T);
 
@@ -35,7 +38,12 @@ struct TcForwardArgs {
     Workspace ws;
     PoolDims dims;
     int ext_chunk_cap;      // upper bound of K-extension chunks (sum over loaded slots)
+    cudaEvent_t ev_start;   // optional profiling events around the projection kernel
+    cudaEvent_t ev_stop;
 };
+
+// Records a profiling event; inside stream capture it becomes an event-record node.
+cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st);
 cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st);
 
 }  // namespace mlora

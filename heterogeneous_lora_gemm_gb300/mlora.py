@@ -27,6 +27,7 @@ MLORA_ERR_OOM = 5
 MLORA_ERR_CUDA = 6
 MLORA_ERR_DEVICE_ROW = 7
 MLORA_ERR_UNSUPPORTED = 8
+MLORA_ERR_DEVICE_TIMEOUT = 9
 MLORA_F32 = 0
 MLORA_BF16 = 1
 
@@ -63,6 +64,7 @@ _SIGNATURES = {
     "mlora_pool_status": (_I, [_P, _P]),
     "mlora_pool_info": (_I, [_P, ctypes.POINTER(PoolInfo)]),
     "mlora_debug_segments": (_I, [_P, _P, _I, _P, _P, _P]),
+    "mlora_profile_events": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I]),
     "mlora_arena_new": (_P, [_I]),
     "mlora_arena_delete": (None, [_P]),
     "mlora_arena_alloc": (_I, [_P, _I, _I]),
@@ -139,9 +141,9 @@ def mlora_merge(pool: int, W_ptr: int, slot: int, stream: int) -> None:
 
 
 def mlora_pool_status(pool: int, stream: int) -> int:
-    """Returns the status code (MLORA_OK or MLORA_ERR_DEVICE_ROW); raises on CUDA errors."""
+    """Returns MLORA_OK, MLORA_ERR_DEVICE_ROW or MLORA_ERR_DEVICE_TIMEOUT; raises on CUDA errors."""
     s = lib().mlora_pool_status(pool, stream or None)
-    if s not in (MLORA_OK, MLORA_ERR_DEVICE_ROW):
+    if s not in (MLORA_OK, MLORA_ERR_DEVICE_ROW, MLORA_ERR_DEVICE_TIMEOUT):
         check(s, "mlora_pool_status")
     return s
 
@@ -156,6 +158,14 @@ def mlora_debug_segments(pool: int, row_adapter_ptr: Optional[int], T: int, perm
                          stream: int) -> None:
     check(lib().mlora_debug_segments(pool, row_adapter_ptr or None, T, perm_ptr, offsets_ptr, stream or None),
           "mlora_debug_segments")
+
+
+def mlora_profile_events(pool: int, starts, stops) -> None:
+    """starts/stops: sequences of cudaEvent_t handles (ints); empty turns recording off."""
+    n = len(starts)
+    a = (_P * max(n, 1))(*[int(x) for x in starts])
+    b = (_P * max(n, 1))(*[int(x) for x in stops])
+    check(lib().mlora_profile_events(pool, a, b, n), "mlora_profile_events")
 
 
 # ---- torch-facing convenience ------------------------------------------- #
@@ -212,6 +222,10 @@ class Pool:
 
     def info(self) -> PoolInfo:
         return mlora_pool_info(self.handle)
+
+    def profile_events(self, starts, stops) -> None:
+        """torch.cuda.Event objects (created with enable_timing=True); [] turns recording off."""
+        mlora_profile_events(self.handle, [e.cuda_event for e in starts], [e.cuda_event for e in stops])
 
     def segments(self, row_adapter, perm, offsets, stream=None) -> None:
         ra = None if row_adapter is None else row_adapter.data_ptr()

@@ -55,7 +55,8 @@ typedef enum mlora_status {
     MLORA_ERR_OOM = 5,           /* rank budget exhausted, or a device allocation failed */
     MLORA_ERR_CUDA = 6,          /* a CUDA runtime call failed (no device, launch failure, ...) */
     MLORA_ERR_DEVICE_ROW = 7,    /* (mlora_pool_status) a row named an invalid or empty slot */
-    MLORA_ERR_UNSUPPORTED = 8    /* shape outside what the kernels handle (see mlora_pool_create) */
+    MLORA_ERR_UNSUPPORTED = 8,   /* shape outside what the kernels handle (see mlora_pool_create) */
+    MLORA_ERR_DEVICE_TIMEOUT = 9 /* (mlora_pool_status) a kernel pipeline wait gave up after its limit */
 } mlora_status;
 
 typedef enum mlora_dtype { MLORA_F32 = 0, MLORA_BF16 = 1 } mlora_dtype;
@@ -165,7 +166,9 @@ mlora_status mlora_merge(mlora_pool_t pool, void* W, int slot, mlora_stream_t st
 /*
  * Synchronizes `stream`, then reads and clears the pool's device status word.
  * Returns MLORA_OK, MLORA_ERR_DEVICE_ROW (a forward since the last call saw a row
- * naming an invalid or empty slot) or MLORA_ERR_CUDA (the stream reported an error).
+ * naming an invalid or empty slot), MLORA_ERR_DEVICE_TIMEOUT (a pipeline wait in a
+ * kernel gave up after its bounded limit; that call's output is not valid) or
+ * MLORA_ERR_CUDA (the stream reported an error).
  */
 mlora_status mlora_pool_status(mlora_pool_t pool, mlora_stream_t stream);
 
@@ -183,6 +186,16 @@ mlora_status mlora_pool_info(mlora_pool_t pool, mlora_pool_info_t* info);
  */
 mlora_status mlora_debug_segments(mlora_pool_t pool, const int32_t* row_adapter, int T,
                                   int32_t* perm, int32_t* offsets, mlora_stream_t stream);
+
+/*
+ * Profiling hook for timing the projection kernel with CUDA events (no work is
+ * skipped or changed).  With n > 0, the k-th later forward call of this pool
+ * records starts[k % n] and stops[k % n] (cudaEvent_t handles owned by the
+ * caller) on its stream immediately before and after launching its base +
+ * expand projection kernel; inside stream capture they become event-record
+ * nodes of the graph.  n == 0 turns recording off.  Errors: INVALID_ARG.
+ */
+mlora_status mlora_profile_events(mlora_pool_t pool, void* const* starts, void* const* stops, int n);
 
 /*
  * Host-only view of the arena allocator the pool uses (no CUDA calls), for tests

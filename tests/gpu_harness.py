@@ -54,15 +54,20 @@ def upload(layer: wl.LayerData):
     return X, W, ra, Y
 
 
-def run_layer(layer: wl.LayerData, pool=None, with_row_adapter: bool = True) -> np.ndarray:
-    """Y of one forward, as fp64 numpy."""
+def run_layer(layer: wl.LayerData, pool=None, with_row_adapter: bool = True,
+              check_status: bool = True) -> np.ndarray:
+    """Y of one forward, as fp64 numpy; by default also requires a clean device status."""
     import torch
+    from heterogeneous_lora_gemm_gb300 import mlora
     own = pool is None
     if own:
         pool = make_pool(layer)
     X, W, ra, Y = upload(layer)
     pool.forward(X, W, ra if with_row_adapter else None, Y)
     torch.cuda.synchronize()
+    if check_status:
+        st = pool.status()
+        assert st == mlora.MLORA_OK, f"device status {st}: {mlora.status_string(st)}"
     out = to_f64(Y)
     if own:
         pool.close()

@@ -43,7 +43,7 @@ def test_library_has_no_libcuda_link_dependency(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         assert lib.status_string(code)
     assert lib.status_string(0) == "ok"
 
