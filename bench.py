@@ -306,6 +306,8 @@ def run_ours(args, dist, rank, local):
     prof_pairs = []
     for it in items:
         s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)   # torch creates the CUDA event lazily, at its first record
+        e_ev.record(stream)
         it["pool"].profile_events([s_ev], [e_ev])
         prof_pairs.append((s_ev, e_ev))
     pgraph = torch.cuda.CUDAGraph()
