@@ -30,8 +30,11 @@
 #include <cstring>
 
 #include "tc.h"
+#include "tc_ptx.cuh"
 
 namespace mlora {
+
+using namespace ptx;
 
 namespace {
 
@@ -77,112 +80,9 @@ constexpr int EXT_SUB = 4;         // K-extension chunks per pipeline step
 constexpr int A_BYTES = BM * BK * 2;            // 16 KiB: W tile, or 4 Up chunk tiles
 constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int MAX_N = 256;
-constexpr long long WAIT_LIMIT = 4000000000ll;  // clock cycles (~2 s) before a wait gives up
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
-
-// ---------------------------------------------------------------- device helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: gives up after WAIT_LIMIT cycles or when another role gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > WAIT_LIMIT) {
-            *abort_flag = 1;
-            atomicOr(status, STATUS_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
-        "[%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
-        "%5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
-    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
-}
-
-// tcgen05 shared-memory matrix descriptor (K-major operand).
-//   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4 (unused when swizzled)
-//   bits 32-45 stride byte offset >> 4 (distance between 8-row groups)
-//   bits 46-47 descriptor version (1)  bits 61-63 swizzle: 2 = 128B, 6 = 32B
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo, uint32_t swz) {
-    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-    d |= (uint64_t)1u << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1u << 46;
-    d |= (uint64_t)swz << 61;
-    return d;
-}
-constexpr uint32_t SW128 = 2, SW32 = 6;
-
-// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
-            tmem_d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 struct DecodeParams {
     const CUtensorMap* up_maps;   // per-slot Up descriptors (global memory)
@@ -505,12 +405,13 @@ cudaError_t tc_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(decode_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess) e = prefill_init();
     return e;
 }
 
 TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d) {
     TcWorkspaceNeeds n{};
-    n.need_v32 = !bf16 || true;   // the FMA path still serves T > 256 (and din % 64 tails)
+    n.need_v32 = !bf16;   // fp32 pools use the FMA path
     if (bf16) {
         const int tiles = (d.dout + BM - 1) / BM;
         const int ncap = d.max_tokens < MAX_N ? (d.max_tokens + 15) / 16 * 16 : MAX_N;
@@ -531,13 +432,14 @@ bool tc_encode_up_map(CUtensorMap* map, void* up_block, int rpad, int dout) {
 
 bool tc_supported(const PoolDims& d, int T) {
     (void)d;
-    return T >= 1 && T <= MAX_N;
+    return T >= 1;
 }
 
 cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const PoolDims& d = a.dims;
     const int T = a.T;
-    const int N = (T + 15) / 16 * 16;
+    const bool decode = T <= MAX_N;
+    const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
     const int tiles = (d.dout + BM - 1) / BM;
     const int kb_total = (d.din + BK - 1) / BK;
     const int ext_chunks = a.lora ? a.ext_chunk_cap : 0;
@@ -547,7 +449,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)d.dout};
         cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
-        cuuint32_t box[2] = {BK, BM};
+        cuuint32_t box[2] = {BK, decode ? (cuuint32_t)BM : 256u};
         if (!encode(&tmW, a.W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
@@ -563,13 +465,20 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         if (!encode(&tmV, a.ws.vt, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
     }
 
+    cudaError_t e;
     if (a.lora && ext_chunks > 0) {
         dim3 grid(ext_chunks, (T + SHRINK_ROWS - 1) / SHRINK_ROWS);
         shrink_chunks_kernel<<<grid, 256, 0, st>>>(
             (const __nv_bfloat16*)a.X, a.row_adapter, a.slots, (const __nv_bfloat16*)a.arena_down,
             a.ws.chunk_slot, a.ws.chunk_col, a.ws.meta, (__nv_bfloat16*)a.ws.vt, T, d.din, d.S, d.tcap);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+
+    if (!decode) {
+        if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
+        if ((e = launch_prefill(a, tmX, tmW, tmV, sm_count(), st)) != cudaSuccess) return e;
+        if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
+        return cudaSuccess;
     }
 
     DecodeParams p{};
@@ -590,7 +499,6 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.stages = decode_stages(N);
     const size_t smem = 1024 + (size_t)p.stages * stage_bytes(N) + (size_t)(2 * p.stages + 1) * 8 +
                         (size_t)p.stages * 4 + 16;
-    cudaError_t e;
     dim3 grid(tiles, p.splits);
     if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
     decode_gemm_kernel<<<grid, NUM_THREADS, smem, st>>>(tmW, tmX, tmV, p);

@@ -44,6 +44,11 @@ struct TcForwardArgs {
 
 // Records a profiling event; inside stream capture it becomes an event-record node.
 cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st);
+
+// Prefill-shaped projection (T > 256), tc_prefill.cu.
+cudaError_t prefill_init();
+cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                           const CUtensorMap& tmV, int num_sms, cudaStream_t st);
 cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st);
 
 }  // namespace mlora

@@ -1,0 +1,276 @@
+// Prefill-shaped batches (T > 256): persistent tcgen05 GEMM with the fused expand.
+//
+// Tiles are 128 tokens x 256 output features (one tcgen05.mma.cta_group::1 of
+// M = 128, N = 256, K = 16 per 32 bytes of K).  One CTA per SM walks its share of
+// the tiles in a grouped raster order (8 token tiles share each weight tile, so
+// the weight tiles in flight stay in L2).  Warp 0 issues TMA loads into a 4-stage
+// ring, warp 1 issues the MMAs into one of two TMEM accumulators (2 x 256
+// columns), and warps 2-5 drain the other accumulator to bf16 Y while the next
+// tile is being multiplied.  As in the decode kernel, the K loop of every tile is
+// din columns of X W^T followed by the K-extension over the touched adapters'
+// chunks (ai-infra-kb "M031" §02), so each row's delta is added to its own output
+// row before the single rounding.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "tc.h"
+#include "tc_ptx.cuh"
+
+namespace mlora {
+
+using namespace ptx;
+
+namespace {
+
+constexpr int PM = 128;                         // tokens per tile
+constexpr int PN = 256;                         // output features per tile
+constexpr int PK = 64;                          // K per pipeline step
+constexpr int PA_BYTES = PM * PK * 2;           // 16 KiB
+constexpr int PB_BYTES = PN * PK * 2;           // 32 KiB
+constexpr int PSTAGE = PA_BYTES + PB_BYTES;     // 48 KiB
+constexpr int PSTAGES = 4;
+constexpr int P_THREADS = 192;
+constexpr int GROUP_M = 8;
+constexpr int EXT_SUB = 4;
+
+struct PrefillParams {
+    const CUtensorMap* up_maps;
+    const int32_t* chunk_slot;
+    const int32_t* chunk_col;
+    const int32_t* meta;
+    __nv_bfloat16* Y;
+    uint32_t* status;
+    int T, dout, kb_total, m_tiles, n_tiles, lora, vec_store;
+};
+
+__device__ __forceinline__ void tile_coords(int i, int m_tiles, int n_tiles, int& m, int& n) {
+    const int per_group = GROUP_M * n_tiles;
+    const int first_m = (i / per_group) * GROUP_M;
+    const int gm = min(m_tiles - first_m, GROUP_M);
+    const int r = i % per_group;
+    m = first_m + r % gm;
+    n = r / gm;
+}
+
+__global__ void __launch_bounds__(P_THREADS, 1)
+prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmV, PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* full = (uint64_t*)(smem + (size_t)PSTAGES * PSTAGE);
+    uint64_t* empty = full + PSTAGES;
+    uint64_t* tfull = empty + PSTAGES;     // [2] accumulator ready
+    uint64_t* tempty = tfull + 2;          // [2] accumulator drained
+    uint64_t* drain = tempty + 2;          // MMA completion on the give-up path
+    int* stage_kind = (int*)(drain + 1);   // -1 = din step, else valid chunks
+    uint32_t* tmem_slot = (uint32_t*)(stage_kind + PSTAGES);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.m_tiles * p.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int n_chunks = p.lora ? p.meta[1] : 0;
+    const int ext_steps = (n_chunks + EXT_SUB - 1) / EXT_SUB;
+    const int steps = p.kb_total + ext_steps;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- producer
+        int s = 0;
+        uint32_t ph = 0;
+        int armed[PSTAGES] = {0, 0, 0, 0};
+        for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+            int m, n;
+            tile_coords(tile, p.m_tiles, p.n_tiles, m, n);
+            for (int i = 0; i < steps; ++i) {
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
+                ++armed[s];
+                uint8_t* a = smem + (size_t)s * PSTAGE;
+                uint8_t* b = a + PA_BYTES;
+                if (i < p.kb_total) {
+                    stage_kind[s] = -1;
+                    mbar_expect_tx(&full[s], PSTAGE);
+                    tma_2d(a, &tmX, &full[s], i * PK, m * PM);
+                    tma_2d(b, &tmW, &full[s], i * PK, n * PN);
+                } else {
+                    const int c0 = (i - p.kb_total) * EXT_SUB;
+                    const int nv = min(EXT_SUB, n_chunks - c0);
+                    stage_kind[s] = nv;
+                    mbar_expect_tx(&full[s], (uint32_t)(PA_BYTES + nv * (PN * 32)));
+                    tma_3d(a, &tmV, &full[s], 0, m * PM, c0);
+                    for (int j = 0; j < nv; ++j) {
+                        const CUtensorMap* um = p.up_maps + p.chunk_slot[c0 + j];
+                        tensormap_acquire(um);
+                        const int col = p.chunk_col[c0 + j];
+                        tma_2d(b + j * (PN * 32), um, &full[s], col, n * PN);
+                        tma_2d(b + j * (PN * 32) + PM * 32, um, &full[s], col, n * PN + 128);
+                    }
+                }
+                if (++s == PSTAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
+        if (*abort_flag) {
+            for (int j = 0; j < PSTAGES; ++j) {
+                if (armed[j] == 0) continue;
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&full[j], (uint32_t)((armed[j] - 1) & 1)) && clock64() - t0 < 200000000ll) {
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        const uint32_t idesc = idesc_bf16(PM, PN);
+        int s = 0;
+        uint32_t ph = 0;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x, ++local) {
+            const int buf = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            if (!mbar_wait(&tempty[buf], (use & 1) ^ 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(buf * PN);
+            uint32_t acc = 0;
+            for (int i = 0; i < steps; ++i) {
+                if (!mbar_wait(&full[s], ph, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t a = smem_u32(smem + (size_t)s * PSTAGE);
+                const uint32_t b = a + PA_BYTES;
+                const int kind = stage_kind[s];
+                if (kind < 0) {
+#pragma unroll
+                    for (int k = 0; k < PK / 16; ++k) {
+                        mma_bf16(d, sdesc(a + k * 32, 1024, SW128), sdesc(b + k * 32, 1024, SW128), idesc, acc);
+                        acc = 1;
+                    }
+                } else {
+                    for (int j = 0; j < kind; ++j) {
+                        mma_bf16(d, sdesc(a + j * (PM * 32), 256, SW32), sdesc(b + j * (PN * 32), 256, SW32), idesc,
+                                 acc);
+                        acc = 1;
+                    }
+                }
+                mma_commit(&empty[s]);
+                if (++s == PSTAGES) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            mma_commit(&tfull[buf]);
+        }
+        if (*abort_flag) {   // MMAs already issued must finish before TMEM is released
+            mma_commit(drain);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(drain, 0) && clock64() - t0 < 200000000ll) {
+            }
+        }
+    } else if (warp >= 2) {
+        // ---------------- epilogue
+        const int q = warp & 3;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
+            int m, n;
+            tile_coords(tile, p.m_tiles, p.n_tiles, m, n);
+            const int buf = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            if (!mbar_wait(&tfull[buf], use & 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            const int t = m * PM + q * 32 + lane;
+            const uint32_t taddr = tmem + (uint32_t)(buf * PN) + ((uint32_t)(q * 32) << 16);
+            __nv_bfloat16* yrow = p.Y + (size_t)t * p.dout;
+            for (int c0 = 0; c0 < PN; c0 += 16) {
+                float v[16];
+                tmem_ld16(taddr + c0, v);
+                const int o = n * PN + c0;
+                if (t < p.T) {
+                    if (p.vec_store && o + 16 <= p.dout) {
+                        uint4 w[2];
+                        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(w);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+                        *reinterpret_cast<uint4*>(yrow + o) = w[0];
+                        *reinterpret_cast<uint4*>(yrow + o + 8) = w[1];
+                    } else {
+                        for (int j = 0; j < 16; ++j)
+                            if (o + j < p.dout) yrow[o + j] = __float2bfloat16_rn(v[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty[buf])) : "memory");
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+    }
+}
+
+}  // namespace
+
+cudaError_t prefill_init() {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, prefill_gemm_kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - (int)fa.sharedSizeBytes);
+    return e;
+}
+
+cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                           const CUtensorMap& tmV, int num_sms, cudaStream_t st) {
+    const PoolDims& d = a.dims;
+    PrefillParams p{};
+    p.up_maps = a.up_maps;
+    p.chunk_slot = a.ws.chunk_slot;
+    p.chunk_col = a.ws.chunk_col;
+    p.meta = a.ws.meta;
+    p.Y = (__nv_bfloat16*)a.Y;
+    p.status = a.ws.status;
+    p.T = a.T;
+    p.dout = d.dout;
+    p.kb_total = (d.din + PK - 1) / PK;
+    p.m_tiles = (a.T + PM - 1) / PM;
+    p.n_tiles = (d.dout + PN - 1) / PN;
+    p.lora = a.lora ? 1 : 0;
+    p.vec_store = (d.dout % 8 == 0) ? 1 : 0;
+    const int total = p.m_tiles * p.n_tiles;
+    const int grid = total < num_sms ? total : num_sms;
+    const size_t smem = 1024 + (size_t)PSTAGES * PSTAGE + (2 * PSTAGES + 5) * 8 + PSTAGES * 4 + 16;
+    prefill_gemm_kernel<<<grid, P_THREADS, smem, st>>>(tmX, tmW, tmV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace mlora
