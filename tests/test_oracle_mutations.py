@@ -1,0 +1,89 @@
+"""Plants plausible mistakes in a copy of the oracle (on the CPU) and checks that
+the pins of tests/test_oracle_pins.py catch every one of them.
+
+Each mutant is the oracle's C source with one edit (a dropped term, a wrong
+sign or index, a transposed operand, an unstable group order), compiled into a
+temporary library and swapped in for the duration of the pin run.
+"""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "mlora_oracle.c")
+
+MUTANTS = {
+    "scale dropped": ("y[o] += scales[a] * acc;", "y[o] += acc;"),
+    "delta sign flipped": ("y[o] += scales[a] * acc;", "y[o] -= scales[a] * acc;"),
+    "Up transposed": ("acc += u[k] * v[k];", "acc += up[(int64_t)k * dout + o] * v[k];"),
+    "Down row stride": ("const double* d = down + (int64_t)k * din;", "const double* d = down + k;"),
+    "base uses W transposed": ("const double* w = W + o * din;", "const double* w = W + o;"),
+    "groups not stable": ("if (a->row != b->row) return a->row < b->row ? -1 : 1;",
+                          "if (a->row != b->row) return a->row > b->row ? -1 : 1;"),
+    "merge drops scale": ("W_out[o * din + i] = W[o * din + i] + scale * acc;",
+                          "W_out[o * din + i] = W[o * din + i] + acc;"),
+    "merge transposed": ("acc += up[o * rank + k] * down[(int64_t)k * din + i];",
+                         "acc += up[o * rank + k] * down[(int64_t)k + i * rank];"),
+    "flops count din only": ("e += 2 * (int64_t)ranks[a] * (din + dout);", "e += 2 * (int64_t)ranks[a] * din;"),
+    "padded budget uses valid rows": ("*padded = 2 * T * (int64_t)r_max * (din + dout);",
+                                      "*padded = e / (r_max > 0 ? 1 : 1);"),
+}
+
+PIN_TESTS = [
+    pins.test_worked_example_group_order,
+    pins.test_worked_example_flops,
+    pins.test_worked_example_writeback_rows,
+    pins.test_worked_example_brute_force_exact,
+    pins.test_rows_without_adapter_equal_library_matmul,
+    lambda: pins.test_single_adapter_batch_equals_merged_weight(2),
+    pins.test_merge_matches_library,
+    pins.test_rank_padding_leaves_output_unchanged,
+    pins.test_rank1_unit_adapter_closed_form,
+    pins.test_segments_match_sorted_definition,
+]
+
+
+def _build_mutant(name, tmpdir):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site of {name!r} not found exactly once"
+    path = os.path.join(tmpdir, "mutant.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = os.path.join(tmpdir, "libmutant.so")
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", lib, path])
+    return lib
+
+
+def _run_pins_with(lib_path):
+    saved_lib, saved_path = oracle._lib, oracle._LIB_PATH
+    oracle._lib = None
+    oracle._LIB_PATH = lib_path
+    try:
+        failures = 0
+        for t in PIN_TESTS:
+            try:
+                t()
+            except AssertionError:
+                failures += 1
+        return failures
+    finally:
+        oracle._lib = saved_lib
+        oracle._LIB_PATH = saved_path
+
+
+def test_pins_pass_on_the_real_oracle():
+    assert _run_pins_with(oracle.build()) == 0
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_every_planted_mistake_is_caught(name, monkeypatch):
+    monkeypatch.setattr(oracle, "build", lambda force=False: oracle._LIB_PATH)
+    with tempfile.TemporaryDirectory() as d:
+        lib = _build_mutant(name, d)
+        assert _run_pins_with(lib) > 0, f"no pin caught the mutant {name!r}"
