@@ -85,9 +85,10 @@ struct mlora_pool {
     char* arena_down = nullptr;
     char* arena_up = nullptr;
     size_t arena_bytes = 0;
-    char* table_base = nullptr;      // slot table, then per-slot Up tensor maps
+    char* table_base = nullptr;      // slot table, then per-slot Up and Down tensor maps
     SlotRec* d_slots = nullptr;
     CUtensorMap* d_up_maps = nullptr;
+    CUtensorMap* d_down_maps = nullptr;
     size_t table_bytes = 0;
     char* ws_base = nullptr;
     size_t ws_bytes = 0;
@@ -124,14 +125,18 @@ mlora_status push_slot(mlora_pool* p, int slot) {
     SlotRec rec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit};
     CU_TRY(cudaMemcpyAsync(p->d_slots + slot, &rec, sizeof rec, cudaMemcpyHostToDevice, p->copy_stream));
     if (p->dtype == MLORA_BF16) {
-        CUtensorMap map;
-        std::memset(&map, 0, sizeof map);
+        CUtensorMap maps[2];
+        std::memset(maps, 0, sizeof maps);
         if (h.rank > 0) {
             void* up = p->arena_up + (size_t)h.unit * p->dout * p->esize;
-            if (!tc_encode_up_map(&map, up, h.rpad, p->dout))
-                return fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the Up block of slot %d", slot);
+            void* down = p->arena_down + (size_t)h.unit * p->din * p->esize;
+            if (!tc_encode_up_map(&maps[0], up, h.rpad, p->dout) || !tc_encode_down_map(&maps[1], down, h.rank, p->din))
+                return fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the adapter of slot %d", slot);
         }
-        CU_TRY(cudaMemcpyAsync(p->d_up_maps + slot, &map, sizeof map, cudaMemcpyHostToDevice, p->copy_stream));
+        CU_TRY(cudaMemcpyAsync(p->d_up_maps + slot, &maps[0], sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                               p->copy_stream));
+        CU_TRY(cudaMemcpyAsync(p->d_down_maps + slot, &maps[1], sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                               p->copy_stream));
     }
     // the staging objects above live on this stack frame: finish before returning
     CU_TRY(cudaStreamSynchronize(p->copy_stream));
@@ -238,13 +243,15 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
 
     // slot table and per-slot tensor maps (CUtensorMap must be 64-byte aligned)
     const size_t slots_bytes = align_up(sizeof(SlotRec) * (size_t)(max_slots > 0 ? max_slots : 1), 128);
-    p->table_bytes = slots_bytes + sizeof(CUtensorMap) * (size_t)(max_slots > 0 ? max_slots : 1);
+    const size_t maps_bytes = sizeof(CUtensorMap) * (size_t)(max_slots > 0 ? max_slots : 1);
+    p->table_bytes = slots_bytes + 2 * maps_bytes;
     e = cudaMalloc((void**)&p->table_base, p->table_bytes);
     if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "slot table: %s", cudaGetErrorString(e)));
     e = cudaMemset(p->table_base, 0, p->table_bytes);
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemset(slot table)"));
     p->d_slots = (SlotRec*)p->table_base;
     p->d_up_maps = (CUtensorMap*)(p->table_base + slots_bytes);
+    p->d_down_maps = (CUtensorMap*)(p->table_base + slots_bytes + maps_bytes);
 
     // workspace
     PoolDims& d = p->dims;
@@ -424,6 +431,7 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
         a.row_adapter = row_adapter;
         a.slots = p->d_slots;
         a.up_maps = p->d_up_maps;
+        a.down_maps = p->d_down_maps;
         a.arena_down = p->arena_down;
         a.ws = p->ws;
         a.dims = p->dims;

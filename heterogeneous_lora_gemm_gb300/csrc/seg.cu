@@ -83,6 +83,8 @@ seg_build_kernel(const int32_t* __restrict__ row_adapter, int T, const SlotRec* 
     __shared__ int bad_row;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the shrink that follows may launch now; it reads this kernel's output only after its wait
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int s = tid; s < S; s += SEG_THREADS) {
         rank_s[s] = slots[s].rank;
         scan[s] = 0;

@@ -1,32 +1,40 @@
 // Tensor-core path of the bf16 forward: tcgen05 MMA with TMEM accumulators, TMA
 // loads into 128B/32B-swizzled shared memory, warp-specialised pipeline.
 //
-// Decode-shaped batches (T <= 256) use one kernel, "swap-AB": the weight is the M
-// operand (128 output features per tile) and the tokens are the N operand
-// (N = T rounded up to 16), so W streams through the tensor cores exactly once
-// however few rows the batch has.  The K loop of every tile is the din columns of
-// W followed by a K-extension over the touched adapters (ai-infra-kb "M031" §02:
-// each row adds scale_a Up_a (Down_a x)):
+// "swap-AB" GEMM kernel, in two modes.  The weight-like operand is the MMA's M
+// side (128 rows per tile) and the tokens are the N side (N = up to 256 tokens,
+// a multiple of 16), so the weight streams through the tensor cores once however
+// few rows the batch has.
+//
+// Projection (T <= 256): rows = output features.  The K loop of a tile is the din
+// columns of W followed by a K-extension over the touched adapters (ai-infra-kb
+// "M031" §02: each row adds scale_a Up_a (Down_a x)):
 //
 //     Y^T[o, t] = sum_i W[o, i] X[t, i]  +  sum_c Up_{a(c)}[o, col(c) + j] Vt[c][t][j]
 //
 // where chunk c holds 16 rank columns of one touched adapter and Vt[c][t][:] is
-// scale_a Down_a x_t for rows t of that adapter and zero for every other row.
-// The delta therefore lands in the same fp32 accumulator as the base product,
-// on the row's own column, and the output is rounded once.  Up is read from the
-// adapter arena once per output tile, through per-slot TMA descriptors whose
-// out-of-range columns read as zero (ranks that are not a multiple of 16).
+// scale_a Down_a x_t for rows t of that adapter and zero for every other row.  The
+// delta therefore lands in the same fp32 accumulator as the base product, on the
+// row's own column, and the output is rounded once.  Up is read once per output
+// tile through per-slot TMA descriptors whose out-of-range columns read as zero.
 //
-// Work split: a grid of (output tile, K split).  Split s takes a contiguous
-// share of the din steps and of the K-extension steps of its tile.  Each split
-// writes an fp32 partial tile; the last split to arrive (atomic counter, no
-// waiting) adds all partials in split order and writes bf16 Y, so the result
-// does not depend on arrival order.
+// Shrink (any T; token tiles of 256 along grid z): rows = 8 chunks of 16 rank rows
+// of the touched adapters' Down (per-slot descriptors; rows past the rank read as
+// zero), K = din, giving Down_c X^T for every token.  The epilogue keeps the
+// entry of a token only if the token belongs to the chunk's adapter, scales it,
+// rounds it to bf16 and writes Vt; every other entry is written as zero, so Vt
+// needs no clearing.
+//
+// Work split: a grid of (row tile, K split, token tile).  Split s takes a
+// contiguous share of the K steps.  Each split writes an fp32 partial tile; the
+// last split to arrive (atomic counter, no waiting) adds all partials in split
+// order and writes the result, so it does not depend on arrival order.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <cstring>
 
 #include "tc.h"
@@ -74,32 +82,39 @@ int sm_count() {
 }
 
 // ---------------------------------------------------------------- constants
-constexpr int BM = 128;            // output features per tile (MMA M)
-constexpr int BK = 64;             // din columns per pipeline step (128 bytes of bf16)
+constexpr int BM = 128;            // rows per tile (MMA M)
+constexpr int BK = 64;             // K per pipeline step (128 bytes of bf16)
 constexpr int EXT_SUB = 4;         // K-extension chunks per pipeline step
-constexpr int A_BYTES = BM * BK * 2;            // 16 KiB: W tile, or 4 Up chunk tiles
+constexpr int A_BYTES = BM * BK * 2;            // 16 KiB: W tile, 4 Up chunk tiles or 8 Down chunk tiles
 constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int MAX_N = 256;
+constexpr int CHUNKS_PER_TILE = BM / CHUNK;     // shrink: 8 chunks of 16 rank rows
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
 
-struct DecodeParams {
-    const CUtensorMap* up_maps;   // per-slot Up descriptors (global memory)
+struct GemmParams {
+    const CUtensorMap* up_maps;     // per-slot Up descriptors (projection K-extension)
+    const CUtensorMap* down_maps;   // per-slot Down descriptors (shrink rows)
     const int32_t* chunk_slot;
     const int32_t* chunk_col;
-    const int32_t* meta;          // meta[1] = number of K-extension chunks
-    __nv_bfloat16* Y;
-    float* partials;
-    int32_t* tile_ctr;
+    const int32_t* meta;            // meta[1] = number of chunks of the touched slots
+    const int32_t* row_adapter;     // shrink: slot id per token
+    const SlotRec* slots;
+    __nv_bfloat16* Y;               // projection output [T x dout]
+    __nv_bfloat16* vt;              // shrink output [max_chunks][tcap][16]
+    float* partials;                // [tile][z][split][BM][N]
+    int32_t* tile_ctr;              // [tile][z] arrival counters
     uint32_t* status;
-    int T, dout, N, kb_total, ext_units, splits, stages;
+    int T, dout, N, kb_total, ext_units, splits, stages, tcap;
+    int pdl;    // launched while an earlier kernel may still run: wait before reading its outputs
 };
 
-// ---------------------------------------------------------------- decode kernel
+// ---------------------------------------------------------------- the GEMM kernel
+template <bool SHRINK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ CUtensorMap tmV, DecodeParams p) {
+swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const __grid_constant__ CUtensorMap tmV, GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int NS = p.stages;
@@ -113,11 +128,22 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int* flags = (int*)(tmem_slot + 2);              // [0] issued-any, [1] last-arrival
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x, split = blockIdx.y;
+    const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
+    const int tok0 = ztile * MAX_N;                  // first token of this token tile
+    const int T = min(p.T - tok0, p.N);              // tokens in this tile
+
+    int tile_chunks = 0;
+    if (SHRINK) {
+        pdl_trigger();   // the projection may launch and stream W meanwhile
+        pdl_wait();      // the segment builder's chunk table must be complete
+        tile_chunks = min(CHUNKS_PER_TILE, p.meta[1] - tile * CHUNKS_PER_TILE);
+        if (tile_chunks <= 0) return;                // uniform for the whole CTA (and all its splits)
+    }
+
     const int kb0 = (int)((long long)split * p.kb_total / p.splits);
     const int kb1 = (int)((long long)(split + 1) * p.kb_total / p.splits);
-    const int eu0 = (int)((long long)split * p.ext_units / p.splits);
-    const int eu1 = (int)((long long)(split + 1) * p.ext_units / p.splits);
+    const int eu0 = SHRINK ? 0 : (int)((long long)split * p.ext_units / p.splits);
+    const int eu1 = SHRINK ? 0 : (int)((long long)(split + 1) * p.ext_units / p.splits);
     const int n_steps = (kb1 - kb0) + (eu1 - eu0);
     const uint32_t ncols = p.N <= 32 ? 32 : (p.N <= 64 ? 64 : (p.N <= 128 ? 128 : 256));
 
@@ -131,7 +157,7 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         flags[0] = 0;
         flags[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+        if (!SHRINK) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
     }
     if (warp == 1) {
@@ -157,13 +183,26 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             uint8_t* a = smem + (size_t)s * SB;
             uint8_t* b = a + A_BYTES;
             const int kb = kb0 + i;
-            if (kb < kb1) {
+            if (SHRINK) {
+                stage_kind[s] = -1;
+                mbar_expect_tx(&full[s], (uint32_t)(tile_chunks * CHUNK * BK * 2 + b_bytes(p.N)));
+                for (int j = 0; j < tile_chunks; ++j) {
+                    const int c = tile * CHUNKS_PER_TILE + j;
+                    const CUtensorMap* dm = p.down_maps + p.chunk_slot[c];
+                    tensormap_acquire(dm);
+                    tma_2d(a + j * (CHUNK * BK * 2), dm, &full[s], kb * BK, p.chunk_col[c]);
+                }
+                tma_2d(b, &tmX, &full[s], kb * BK, tok0);
+            } else if (kb < kb1) {
                 stage_kind[s] = -1;
                 mbar_expect_tx(&full[s], (uint32_t)SB);
                 tma_2d(a, &tmW, &full[s], kb * BK, tile * BM);
                 tma_2d(b, &tmX, &full[s], kb * BK, 0);
             } else {
-                if (n_chunks < 0) n_chunks = p.meta[1];
+                if (n_chunks < 0) {
+                    if (p.pdl) pdl_wait();   // chunk table and Vt come from the kernels before
+                    n_chunks = p.meta[1];
+                }
                 const int u = eu0 + (kb - kb1);
                 const int c0 = u * EXT_SUB;
                 int nv = n_chunks - c0;
@@ -234,59 +273,96 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
         }
     } else if (warp >= 2) {
-        // ---------------- epilogue: TMEM -> partial tile or bf16 Y
+        // ---------------- epilogue: TMEM -> partial tile, or the final values
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;          // row of the tile = output feature
-        const int o = tile * BM + row;
+        const int row = q * 32 + lane;          // row of the tile
         const bool ok = mbar_wait(acc_full, 0, abort_flag, p.status);
         tc_fence_after();
         const bool have = ok && flags[0] != 0;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-        const int T = p.T;
+
+        // final write of 16 consecutive tokens t0..t0+15 of this row
+        int c_slot = -1, c_idx = 0;
+        float c_scale = 0.f;
+        if (SHRINK && (row / CHUNK) < tile_chunks) {
+            c_idx = tile * CHUNKS_PER_TILE + row / CHUNK;
+            c_slot = p.chunk_slot[c_idx];
+            c_scale = p.slots[c_slot].scale;
+        }
+        const int o = tile * BM + row;
+        auto emit = [&](int t0, const float* v) {
+            if (SHRINK) {
+                if (c_slot < 0) return;
+                __nv_bfloat16* dst = p.vt + ((size_t)c_idx * p.tcap + tok0) * CHUNK + (row % CHUNK);
+                for (int j = 0; j < 16 && t0 + j < T; ++j) {
+                    const bool mine = p.row_adapter[tok0 + t0 + j] == c_slot;
+                    dst[(size_t)(t0 + j) * CHUNK] = __float2bfloat16_rn(mine ? c_scale * v[j] : 0.f);
+                }
+            } else if (o < p.dout) {
+                for (int j = 0; j < 16 && t0 + j < T; ++j)
+                    p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
+            }
+        };
+
+        const int ctr = tile * gridDim.z + ztile;
         if (p.splits == 1) {
             for (int t0 = 0; t0 < T; t0 += 16) {
                 float v[16];
                 if (have) tmem_ld16(tbase + t0, v);
                 else
                     for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                if (o < p.dout)
-                    for (int j = 0; j < 16 && t0 + j < T; ++j)
-                        p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
+                emit(t0, v);
             }
         } else {
-            float* mine = p.partials + ((size_t)(tile * p.splits + split) * p.N) * BM;
+            // partial tile layout [row][N] fp32: each thread stores and reloads its own
+            // contiguous row of N values with 16-byte accesses
+            const size_t tile_base = (size_t)ctr * p.splits * BM * p.N;
+            float* mine = p.partials + tile_base + ((size_t)split * BM + row) * p.N;
             for (int t0 = 0; t0 < T; t0 += 16) {
                 float v[16];
                 if (have) tmem_ld16(tbase + t0, v);
                 else
                     for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                for (int j = 0; j < 16 && t0 + j < T; ++j) mine[(size_t)(t0 + j) * BM + row] = v[j];
+                float4* dst = reinterpret_cast<float4*>(mine + t0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
             __threadfence();
             epi_bar();
             if (threadIdx.x == 64) {
-                const int prev = atomicAdd(&p.tile_ctr[tile], 1);
+                const int prev = atomicAdd(&p.tile_ctr[ctr], 1);
                 const int last = prev == p.splits - 1;
                 if (last) {
-                    p.tile_ctr[tile] = 0;
+                    p.tile_ctr[ctr] = 0;
                     __threadfence();
                 }
                 flags[1] = last;
             }
             epi_bar();
             if (flags[1]) {
-                const float* base = p.partials + (size_t)tile * p.splits * p.N * BM;
+                // last split of the tile: sum the partials in split order (independent of
+                // arrival order), the loads of several splits in flight together
+                const float* base = p.partials + tile_base + (size_t)row * p.N;
+                const size_t sstride = (size_t)BM * p.N;
                 for (int t0 = 0; t0 < T; t0 += 16) {
-                    float v[16];
-                    if (have) tmem_ld16(tbase + t0, v);
-                    else
-                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                    for (int j = 0; j < 16 && t0 + j < T; ++j) {
-                        float sum = 0.f;
-                        for (int sp = 0; sp < p.splits; ++sp)
-                            sum += (sp == split) ? v[j] : __ldcg(base + ((size_t)sp * p.N + t0 + j) * BM + row);
-                        if (o < p.dout) p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(sum);
+                    float acc[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+#pragma unroll 4
+                    for (int sp = 0; sp < p.splits; ++sp) {
+                        const float4* src = reinterpret_cast<const float4*>(base + sp * sstride + t0);
+                        float4 q4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) q4[j] = __ldcg(src + j);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc[4 * j] += q4[j].x;
+                            acc[4 * j + 1] += q4[j].y;
+                            acc[4 * j + 2] += q4[j].z;
+                            acc[4 * j + 3] += q4[j].w;
+                        }
                     }
+                    emit(t0, acc);
                 }
             }
         }
@@ -296,73 +372,6 @@ decode_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
-    }
-}
-
-// ---------------------------------------------------------------- shrink into chunks
-// Vt[c][t][j] = bf16(scale_a * sum_i Down_a[col(c) + j, i] x_t[i]) if row t belongs to
-// the chunk's adapter a and col(c) + j < rank_a, else 0.  One warp per (chunk, row).
-constexpr int SHRINK_ROWS = 32;   // rows per block (8 warps x 4 rows)
-
-__global__ void __launch_bounds__(256)
-shrink_chunks_kernel(const __nv_bfloat16* __restrict__ X, const int32_t* __restrict__ row_adapter,
-                     const SlotRec* __restrict__ slots, const __nv_bfloat16* __restrict__ arena_down,
-                     const int32_t* __restrict__ chunk_slot, const int32_t* __restrict__ chunk_col,
-                     const int32_t* __restrict__ meta, __nv_bfloat16* __restrict__ vt, int T, int din, int S,
-                     int tcap) {
-    const int c = blockIdx.x;
-    if (c >= meta[1]) return;
-    const int slot = chunk_slot[c], col0 = chunk_col[c];
-    const SlotRec rec = slots[slot];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kmax = min(CHUNK, rec.rank - col0);
-    const __nv_bfloat16* down = arena_down + ((size_t)rec.unit + col0) * din;
-    for (int r = warp; r < SHRINK_ROWS; r += 8) {
-        const int t = blockIdx.y * SHRINK_ROWS + r;
-        if (t >= T) break;
-        const int a = row_adapter[t];
-        float acc[CHUNK];
-#pragma unroll
-        for (int j = 0; j < CHUNK; ++j) acc[j] = 0.f;
-        if (a == slot) {
-            const __nv_bfloat16* x = X + (size_t)t * din;
-            for (int i = lane * 8; i < din; i += 32 * 8) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(x + i);
-                const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&xv);
-                float xf[8];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float2 f = __bfloat1622float2(x2[h]);
-                    xf[2 * h] = f.x;
-                    xf[2 * h + 1] = f.y;
-                }
-#pragma unroll
-                for (int j = 0; j < CHUNK; ++j) {
-                    if (j < kmax) {
-                        const uint4 dv = *reinterpret_cast<const uint4*>(down + (size_t)j * din + i);
-                        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            const float2 f = __bfloat1622float2(d2[h]);
-                            acc[j] = fmaf(f.x, xf[2 * h], acc[j]);
-                            acc[j] = fmaf(f.y, xf[2 * h + 1], acc[j]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < CHUNK; ++j)
-#pragma unroll
-                for (int d = 16; d > 0; d >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], d);
-        }
-        // lane j < 16 writes element j of the row's 32-byte chunk entry
-        if (lane < CHUNK) {
-            float v = 0.f;
-#pragma unroll
-            for (int j = 0; j < CHUNK; ++j)
-                if (j == lane) v = acc[j];
-            vt[((size_t)c * tcap + t) * CHUNK + lane] = __float2bfloat16_rn(a == slot ? rec.scale * v : 0.f);
-        }
     }
 }
 
@@ -377,22 +386,38 @@ cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st) {
                                              : cudaEventRecord(ev, st);
 }
 
-static int decode_splits(int tiles, int kb_total, int ext_units) {
-    const int slots = 2 * sm_count();
-    int s = slots / (tiles > 0 ? tiles : 1);
-    if (s < 1) s = 1;
-    if (s > 16) s = 16;
-    if (s > kb_total) s = kb_total;
-    (void)ext_units;
-    return s;
-}
+namespace {
 
-static int decode_stages(int N) {
-    int ns = (100 * 1024) / stage_bytes(N);
+// Shared-memory budgets: the projection and the shrink that precedes it may share
+// an SM while both run, so their rings together stay inside one SM's 228 KiB.
+constexpr int PROJ_SMEM_BUDGET = 136 * 1024;
+constexpr int SHRINK_SMEM_BUDGET = 84 * 1024;
+
+int ring_stages(int N, int budget) {
+    int ns = budget / stage_bytes(N);
     if (ns < 2) ns = 2;
     if (ns > 8) ns = 8;
     return ns;
 }
+
+// K splits so that row tiles x token tiles x splits fill the SMs once.
+int k_splits(int tiles, int kb_total) {
+    int s = sm_count() / (tiles > 0 ? tiles : 1);
+    if (s < 1) s = 1;
+    if (s > 16) s = 16;
+    if (s > kb_total) s = kb_total;
+    return s;
+}
+
+size_t smem_bytes(int stages, int N) {
+    return 1024 + (size_t)stages * stage_bytes(N) + (size_t)(2 * stages + 1) * 8 + (size_t)stages * 4 + 16;
+}
+
+int proj_tiles(const PoolDims& d) { return (d.dout + BM - 1) / BM; }
+int shrink_tiles(const PoolDims& d) { return (d.max_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE; }
+int token_tiles(int T) { return (T + MAX_N - 1) / MAX_N; }
+
+}  // namespace
 
 cudaError_t tc_init() {
     // the cap on dynamic shared memory is raised once, outside any stream capture
@@ -400,10 +425,14 @@ cudaError_t tc_init() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     cudaFuncAttributes fa;
-    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_gemm_kernel);
     // static shared memory counts against the same per-block limit
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, swapab_gemm_kernel<false>);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(decode_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(swapab_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, swapab_gemm_kernel<true>);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(swapab_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin - (int)fa.sharedSizeBytes);
     if (e == cudaSuccess) e = prefill_init();
     return e;
@@ -413,12 +442,13 @@ TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d) {
     TcWorkspaceNeeds n{};
     n.need_v32 = !bf16;   // fp32 pools use the FMA path
     if (bf16) {
-        const int tiles = (d.dout + BM - 1) / BM;
+        // partial tiles exist only when a split count > 1, i.e. tiles x token tiles x
+        // splits <= SMs; each of the two kernels gets its own region
         const int ncap = d.max_tokens < MAX_N ? (d.max_tokens + 15) / 16 * 16 : MAX_N;
-        const int kb_total = (d.din + BK - 1) / BK;
-        const int splits = decode_splits(tiles, kb_total, 0);
-        n.partial_bytes = (size_t)tiles * splits * ncap * BM * sizeof(float);
-        n.counter_bytes = (size_t)tiles * sizeof(int32_t);
+        const size_t region = (size_t)sm_count() * BM * ncap * sizeof(float);
+        n.partial_bytes = 2 * region;
+        n.counter_bytes =
+            sizeof(int32_t) * ((size_t)proj_tiles(d) + (size_t)shrink_tiles(d) * token_tiles(d.max_tokens));
     }
     return n;
 }
@@ -430,6 +460,13 @@ bool tc_encode_up_map(CUtensorMap* map, void* up_block, int rpad, int dout) {
     return encode(map, up_block, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
+bool tc_encode_down_map(CUtensorMap* map, void* down_block, int rank, int din) {
+    cuuint64_t dims[2] = {(cuuint64_t)din, (cuuint64_t)rank};
+    cuuint64_t strides[1] = {(cuuint64_t)din * 2};
+    cuuint32_t box[2] = {BK, (cuuint32_t)CHUNK};
+    return encode(map, down_block, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool tc_supported(const PoolDims& d, int T) {
     (void)d;
     return T >= 1;
@@ -439,12 +476,48 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const PoolDims& d = a.dims;
     const int T = a.T;
     const bool decode = T <= MAX_N;
-    const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
-    const int tiles = (d.dout + BM - 1) / BM;
     const int kb_total = (d.din + BK - 1) / BK;
     const int ext_chunks = a.lora ? a.ext_chunk_cap : 0;
-    const int ext_units = (ext_chunks + EXT_SUB - 1) / EXT_SUB;
+    const bool shrink = a.lora && ext_chunks > 0;
+    const size_t region_floats =
+        (size_t)sm_count() * BM * (d.max_tokens < MAX_N ? (d.max_tokens + 15) / 16 * 16 : MAX_N);
+    cudaError_t e;
 
+    // ---- shrink: Vt = masked scale * Down_chunks X^T, all tokens, every chunk of the touched slots
+    if (shrink) {
+        const int Ns = decode ? (T + 15) / 16 * 16 : MAX_N;
+        CUtensorMap tmXs, tmNone;
+        std::memset(&tmNone, 0, sizeof tmNone);
+        cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)T};
+        cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
+        cuuint32_t box[2] = {BK, (cuuint32_t)Ns};
+        if (!encode(&tmXs, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        const int tiles = (ext_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
+        const int ztiles = token_tiles(T);
+        GemmParams g{};
+        g.down_maps = a.down_maps;
+        g.chunk_slot = a.ws.chunk_slot;
+        g.chunk_col = a.ws.chunk_col;
+        g.meta = a.ws.meta;
+        g.row_adapter = a.row_adapter;
+        g.slots = a.slots;
+        g.vt = (__nv_bfloat16*)a.ws.vt;
+        g.partials = a.ws.partials + region_floats;
+        g.tile_ctr = a.ws.tile_ctr + proj_tiles(d);
+        g.status = a.ws.status;
+        g.T = T;
+        g.N = Ns;
+        g.kb_total = kb_total;
+        g.splits = k_splits(tiles * ztiles, kb_total);
+        g.stages = ring_stages(Ns, SHRINK_SMEM_BUDGET);
+        g.tcap = d.tcap;
+        g.pdl = 1;
+        e = launch_k(swapab_gemm_kernel<true>, dim3(tiles, g.splits, ztiles), dim3(NUM_THREADS),
+                     smem_bytes(g.stages, Ns), st, true, tmNone, tmXs, tmNone, g);
+        if (e != cudaSuccess) return e;
+    }
+
+    const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
     CUtensorMap tmW, tmX, tmV;
     {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)d.dout};
@@ -465,23 +538,15 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         if (!encode(&tmV, a.ws.vt, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
     }
 
-    cudaError_t e;
-    if (a.lora && ext_chunks > 0) {
-        dim3 grid(ext_chunks, (T + SHRINK_ROWS - 1) / SHRINK_ROWS);
-        shrink_chunks_kernel<<<grid, 256, 0, st>>>(
-            (const __nv_bfloat16*)a.X, a.row_adapter, a.slots, (const __nv_bfloat16*)a.arena_down,
-            a.ws.chunk_slot, a.ws.chunk_col, a.ws.meta, (__nv_bfloat16*)a.ws.vt, T, d.din, d.S, d.tcap);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-
     if (!decode) {
         if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
-        if ((e = launch_prefill(a, tmX, tmW, tmV, sm_count(), st)) != cudaSuccess) return e;
+        if ((e = launch_prefill(a, tmX, tmW, tmV, sm_count(), shrink, st)) != cudaSuccess) return e;
         if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
         return cudaSuccess;
     }
 
-    DecodeParams p{};
+    const int tiles = proj_tiles(d);
+    GemmParams p{};
     p.up_maps = a.up_maps;
     p.chunk_slot = a.ws.chunk_slot;
     p.chunk_col = a.ws.chunk_col;
@@ -494,15 +559,15 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.dout = d.dout;
     p.N = N;
     p.kb_total = kb_total;
-    p.ext_units = ext_units;
-    p.splits = decode_splits(tiles, kb_total, ext_units);
-    p.stages = decode_stages(N);
-    const size_t smem = 1024 + (size_t)p.stages * stage_bytes(N) + (size_t)(2 * p.stages + 1) * 8 +
-                        (size_t)p.stages * 4 + 16;
-    dim3 grid(tiles, p.splits);
+    p.ext_units = (ext_chunks + EXT_SUB - 1) / EXT_SUB;
+    p.splits = k_splits(tiles, kb_total);
+    p.stages = ring_stages(N, PROJ_SMEM_BUDGET);
+    p.tcap = d.tcap;
+    p.pdl = shrink ? 1 : 0;
     if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
-    decode_gemm_kernel<<<grid, NUM_THREADS, smem, st>>>(tmW, tmX, tmV, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p.stages, N), st,
+                 shrink && !a.ev_start, tmW, tmX, tmV, p);
+    if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
     return cudaSuccess;
 }

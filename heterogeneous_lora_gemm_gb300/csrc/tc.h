@@ -19,6 +19,11 @@ TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d);
 // columns past rpad read as zero.
 bool tc_encode_up_map(CUtensorMap* map, void* up_block, int rpad, int dout);
 
+// Encodes the TMA descriptor of one adapter's Down block [rank x din] (bf16,
+// row-major): boxes of 64 din columns x 16 rank rows, 128-byte swizzle, rows past
+// the rank read as zero.
+bool tc_encode_down_map(CUtensorMap* map, void* down_block, int rank, int din);
+
 // Raises the dynamic shared memory cap of the tensor-core kernels (call outside capture).
 cudaError_t tc_init();
 
@@ -34,6 +39,7 @@ struct TcForwardArgs {
     const int32_t* row_adapter;
     const SlotRec* slots;
     const CUtensorMap* up_maps;
+    const CUtensorMap* down_maps;
     const void* arena_down;
     Workspace ws;
     PoolDims dims;
@@ -48,7 +54,7 @@ cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st);
 // Prefill-shaped projection (T > 256), tc_prefill.cu.
 cudaError_t prefill_init();
 cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                           const CUtensorMap& tmV, int num_sms, cudaStream_t st);
+                           const CUtensorMap& tmV, int num_sms, bool after_shrink, cudaStream_t st);
 cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st);
 
 }  // namespace mlora

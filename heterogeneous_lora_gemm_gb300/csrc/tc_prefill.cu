@@ -42,6 +42,7 @@ struct PrefillParams {
     __nv_bfloat16* Y;
     uint32_t* status;
     int T, dout, kb_total, m_tiles, n_tiles, lora, vec_store;
+    int pdl;    // launched while the shrink may still run: wait before reading its outputs
 };
 
 __device__ __forceinline__ void tile_coords(int i, int m_tiles, int n_tiles, int& m, int& n) {
@@ -95,9 +96,17 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int n_chunks = p.lora ? p.meta[1] : 0;
-    const int ext_steps = (n_chunks + EXT_SUB - 1) / EXT_SUB;
-    const int steps = p.kb_total + ext_steps;
+    // The number of K-extension steps comes from the segment builder; the producer
+    // and the MMA issuer read it only after their first tile's din steps (and,
+    // when launched early, after waiting for the kernels before).
+    int n_chunks = -1;
+    auto ext_steps_known = [&]() {
+        if (n_chunks < 0) {
+            if (p.pdl) pdl_wait();
+            n_chunks = p.lora ? p.meta[1] : 0;
+        }
+        return (n_chunks + EXT_SUB - 1) / EXT_SUB;
+    };
 
     if (warp == 0 && lane == 0) {
         // ---------------- producer
@@ -107,7 +116,9 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
             int m, n;
             tile_coords(tile, p.m_tiles, p.n_tiles, m, n);
+            int steps = p.kb_total;
             for (int i = 0; i < steps; ++i) {
+                if (i == p.kb_total - 1) steps = p.kb_total + ext_steps_known();
                 if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
                 ++armed[s];
                 uint8_t* a = smem + (size_t)s * PSTAGE;
@@ -158,7 +169,9 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(buf * PN);
             uint32_t acc = 0;
+            int steps = p.kb_total;
             for (int i = 0; i < steps; ++i) {
+                if (i == p.kb_total - 1) steps = p.kb_total + ext_steps_known();
                 if (!mbar_wait(&full[s], ph, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t a = smem_u32(smem + (size_t)s * PSTAGE);
@@ -250,7 +263,7 @@ cudaError_t prefill_init() {
 }
 
 cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                           const CUtensorMap& tmV, int num_sms, cudaStream_t st) {
+                           const CUtensorMap& tmV, int num_sms, bool after_shrink, cudaStream_t st) {
     const PoolDims& d = a.dims;
     PrefillParams p{};
     p.up_maps = a.up_maps;
@@ -266,11 +279,12 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
     p.n_tiles = (d.dout + PN - 1) / PN;
     p.lora = a.lora ? 1 : 0;
     p.vec_store = (d.dout % 8 == 0) ? 1 : 0;
+    p.pdl = after_shrink ? 1 : 0;
     const int total = p.m_tiles * p.n_tiles;
     const int grid = total < num_sms ? total : num_sms;
     const size_t smem = 1024 + (size_t)PSTAGES * PSTAGE + (2 * PSTAGES + 5) * 8 + PSTAGES * 4 + 16;
-    prefill_gemm_kernel<<<grid, P_THREADS, smem, st>>>(tmX, tmW, tmV, p);
-    return cudaGetLastError();
+    return launch_k(prefill_gemm_kernel, dim3(grid), dim3(P_THREADS), smem, st, after_shrink && !a.ev_start, tmX,
+                    tmW, tmV, p);
 }
 
 }  // namespace mlora
