@@ -121,25 +121,50 @@ base_expand_simt_kernel(const E* __restrict__ X, const E* __restrict__ W, const 
     }
 }
 
-// W[o, i] += scale * sum_k Up[o, k] Down[k, i]; one block per 4 output rows,
-// threads striding over i (coalesced Down and W accesses).
+// W[o, i] += scale * sum_k Up[o, k] Down[k, i] (M031 §04), fp32 sum, one rounding.
+// A block owns a tile of MERGE_ROWS rows x MERGE_COLS columns of W: the Down slab
+// [k-chunk x MERGE_COLS] and the Up slab [MERGE_ROWS x k-chunk] sit in shared
+// memory, each thread keeps MERGE_ROWS accumulators for one column, so every
+// Down element is read from memory once per row tile and W is read and written
+// exactly once, with coalesced accesses.
+constexpr int MERGE_ROWS = 32, MERGE_COLS = 256, MERGE_KC = 32;
+
 template <typename E>
-__global__ void merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot,
-                                  const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din,
-                                  int dout) {
+__global__ void __launch_bounds__(MERGE_COLS)
+merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot,
+                  const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout) {
+    __shared__ float down_s[MERGE_KC][MERGE_COLS];
+    __shared__ float up_s[MERGE_ROWS][MERGE_KC + 1];
     const SlotRec rec = slots[slot];
-    const int o = blockIdx.x;
-    if (o >= dout || rec.rank <= 0) return;
-    extern __shared__ float up_row[];
-    const E* up = arena_up + (size_t)rec.unit * dout + (size_t)o * rec.rpad;
-    for (int k = threadIdx.x; k < rec.rank; k += blockDim.x) up_row[k] = to_f32(up[k]);
-    __syncthreads();
+    if (rec.rank <= 0) return;
+    const int o0 = blockIdx.y * MERGE_ROWS, i0 = blockIdx.x * MERGE_COLS;
+    const int i = i0 + threadIdx.x;
     const E* down = arena_down + (size_t)rec.unit * din;
-    for (int i = threadIdx.x; i < din; i += blockDim.x) {
-        float acc = 0.f;
-        for (int k = 0; k < rec.rank; ++k) acc = fmaf(up_row[k], to_f32(down[(size_t)k * din + i]), acc);
-        E* w = W + (size_t)o * din + i;
-        *w = from_f32<E>(fmaf(rec.scale, acc, to_f32(*w)));
+    const E* up = arena_up + (size_t)rec.unit * dout;
+    float acc[MERGE_ROWS];
+#pragma unroll
+    for (int r = 0; r < MERGE_ROWS; ++r) acc[r] = 0.f;
+    for (int k0 = 0; k0 < rec.rank; k0 += MERGE_KC) {
+        const int kn = min(MERGE_KC, rec.rank - k0);
+        __syncthreads();
+        for (int k = 0; k < kn; ++k) down_s[k][threadIdx.x] = i < din ? to_f32(down[(size_t)(k0 + k) * din + i]) : 0.f;
+        for (int idx = threadIdx.x; idx < MERGE_ROWS * MERGE_KC; idx += MERGE_COLS) {
+            const int r = idx / MERGE_KC, k = idx % MERGE_KC;
+            up_s[r][k] = (o0 + r < dout && k < kn) ? to_f32(up[(size_t)(o0 + r) * rec.rpad + k0 + k]) : 0.f;
+        }
+        __syncthreads();
+        for (int k = 0; k < kn; ++k) {
+            const float d = down_s[k][threadIdx.x];
+#pragma unroll
+            for (int r = 0; r < MERGE_ROWS; ++r) acc[r] = fmaf(up_s[r][k], d, acc[r]);
+        }
+    }
+    if (i >= din) return;
+#pragma unroll
+    for (int r = 0; r < MERGE_ROWS; ++r) {
+        if (o0 + r >= dout) break;
+        E* w = W + (size_t)(o0 + r) * din + i;
+        *w = from_f32<E>(fmaf(rec.scale, acc[r], to_f32(*w)));
     }
 }
 
@@ -178,13 +203,13 @@ cudaError_t launch_base_expand_simt(bool bf16, const void* X, const void* W,
 cudaError_t launch_merge_simt(bool bf16, void* W, const SlotRec* slots, int slot,
                               const void* arena_down, const void* arena_up, const PoolDims& d,
                               cudaStream_t st) {
-    const size_t smem = sizeof(float) * (size_t)d.max_rank;
+    const dim3 grid((d.din + MERGE_COLS - 1) / MERGE_COLS, (d.dout + MERGE_ROWS - 1) / MERGE_ROWS);
     if (bf16)
-        merge_simt_kernel<__nv_bfloat16><<<d.dout, 256, smem, st>>>(
+        merge_simt_kernel<__nv_bfloat16><<<grid, MERGE_COLS, 0, st>>>(
             (__nv_bfloat16*)W, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din,
             d.dout);
     else
-        merge_simt_kernel<float><<<d.dout, 256, smem, st>>>((float*)W, slots, slot, (const float*)arena_down,
+        merge_simt_kernel<float><<<grid, MERGE_COLS, 0, st>>>((float*)W, slots, slot, (const float*)arena_down,
                                                           (const float*)arena_up, d.din, d.dout);
     return cudaGetLastError();
 }
