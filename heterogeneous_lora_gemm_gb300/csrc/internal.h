@@ -10,10 +10,19 @@ namespace mlora {
 // Device slot table entry (one per adapter slot).
 struct SlotRec {
     int32_t rank;    // 0 = empty slot
-    int32_t rpad;    // roundup(rank, 8): row length of the stored Up block [dout x rpad]
+    int32_t rpad;    // roundup(rank, 8): rank units the adapter holds
     float scale;
-    int32_t unit;    // unit offset in the arena: Down at unit*din, Up at unit*dout elements
+    int32_t unit;    // first rank unit in the arena (a multiple of 8)
 };
+
+// Arena layout, per rank unit u (one rank row of one adapter):
+//   Down half: row u = [din] elements at u*din   (Down_a row k is unit u_a + k)
+//   Up half:   units come in blocks of 8; block b = [dout x 8] row-major at b*8*dout,
+//              so Up_a[o][k] sits at ((u_a + k) / 8 * dout + o) * 8 + (u_a + k) % 8.
+__host__ __device__ inline size_t up_index(int unit, int k, int o, int dout) {
+    const int u = unit + k;
+    return ((size_t)(u >> 3) * dout + o) * 8 + (u & 7);
+}
 
 // Bits of the device status word.
 enum : uint32_t { STATUS_BAD_ROW = 1u, STATUS_TIMEOUT = 2u };
@@ -29,7 +38,8 @@ struct Workspace {
     int32_t* perm;         // [max_tokens] rows in segment order, -1 past n_valid
     int32_t* meta;         // [8]     0: n_valid, 1: n_chunks, 2: n_touched
     int32_t* chunk_slot;   // [max_chunks] slot of each K-extension chunk (touched slots ascending)
-    int32_t* chunk_col;    // [max_chunks] first rank column of the chunk inside its adapter
+    int32_t* chunk_unit;   // [max_chunks] arena rank unit of the chunk's first rank column
+    int32_t* chunk_kval;   // [max_chunks] valid rank columns of the chunk (<= CHUNK)
     float* v32;            // [max_tokens x max_rank] scale * Down x per row (SIMT path)
     uint16_t* vt;          // [max_chunks x tcap x CHUNK] bf16 scale * Down x, chunked (tensor path)
     float* partials;       // split-K partial tiles
@@ -42,6 +52,9 @@ struct PoolDims {
 
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t seg_init();   // raises the segment builder's shared memory cap (outside capture)
+// Row ranges (warps) the segment builder can use with `scratch_ints_avail` ints of
+// shared memory, at most `warps`; 0 if even one does not fit.
+int seg_warps_for(int S, int warps, int scratch_ints_avail, int max_chunks);
 cudaError_t launch_seg_build(const int32_t* row_adapter, int T, const SlotRec* slots,
                              const Workspace& ws, const PoolDims& d, cudaStream_t st);
 

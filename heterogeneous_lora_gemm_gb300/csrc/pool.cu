@@ -85,10 +85,9 @@ struct mlora_pool {
     char* arena_down = nullptr;
     char* arena_up = nullptr;
     size_t arena_bytes = 0;
-    char* table_base = nullptr;      // slot table, then per-slot Up and Down tensor maps
+    char* table_base = nullptr;      // slot table
     SlotRec* d_slots = nullptr;
-    CUtensorMap* d_up_maps = nullptr;
-    CUtensorMap* d_down_maps = nullptr;
+    TcArenaMaps maps{};              // TMA descriptors of the whole arena (bf16 pools)
     size_t table_bytes = 0;
     char* ws_base = nullptr;
     size_t ws_bytes = 0;
@@ -124,21 +123,7 @@ mlora_status push_slot(mlora_pool* p, int slot) {
     const SlotHost& h = p->slots[slot];
     SlotRec rec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit};
     CU_TRY(cudaMemcpyAsync(p->d_slots + slot, &rec, sizeof rec, cudaMemcpyHostToDevice, p->copy_stream));
-    if (p->dtype == MLORA_BF16) {
-        CUtensorMap maps[2];
-        std::memset(maps, 0, sizeof maps);
-        if (h.rank > 0) {
-            void* up = p->arena_up + (size_t)h.unit * p->dout * p->esize;
-            void* down = p->arena_down + (size_t)h.unit * p->din * p->esize;
-            if (!tc_encode_up_map(&maps[0], up, h.rpad, p->dout) || !tc_encode_down_map(&maps[1], down, h.rank, p->din))
-                return fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the adapter of slot %d", slot);
-        }
-        CU_TRY(cudaMemcpyAsync(p->d_up_maps + slot, &maps[0], sizeof(CUtensorMap), cudaMemcpyHostToDevice,
-                               p->copy_stream));
-        CU_TRY(cudaMemcpyAsync(p->d_down_maps + slot, &maps[1], sizeof(CUtensorMap), cudaMemcpyHostToDevice,
-                               p->copy_stream));
-    }
-    // the staging objects above live on this stack frame: finish before returning
+    // the staging object above lives on this stack frame: finish before returning
     CU_TRY(cudaStreamSynchronize(p->copy_stream));
     return MLORA_OK;
 }
@@ -243,15 +228,15 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
 
     // slot table and per-slot tensor maps (CUtensorMap must be 64-byte aligned)
     const size_t slots_bytes = align_up(sizeof(SlotRec) * (size_t)(max_slots > 0 ? max_slots : 1), 128);
-    const size_t maps_bytes = sizeof(CUtensorMap) * (size_t)(max_slots > 0 ? max_slots : 1);
-    p->table_bytes = slots_bytes + 2 * maps_bytes;
+    p->table_bytes = slots_bytes;
     e = cudaMalloc((void**)&p->table_base, p->table_bytes);
     if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "slot table: %s", cudaGetErrorString(e)));
     e = cudaMemset(p->table_base, 0, p->table_bytes);
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemset(slot table)"));
     p->d_slots = (SlotRec*)p->table_base;
-    p->d_up_maps = (CUtensorMap*)(p->table_base + slots_bytes);
-    p->d_down_maps = (CUtensorMap*)(p->table_base + slots_bytes + maps_bytes);
+    if (dtype == MLORA_BF16 && p->units > 0 &&
+        !tc_encode_arena_maps(&p->maps, p->arena_down, p->arena_up, p->units, din, dout))
+        return bail(fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the adapter arena"));
 
     // workspace
     PoolDims& d = p->dims;
@@ -275,7 +260,8 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     const size_t o_perm = carve(sizeof(int32_t) * (size_t)max_tokens);
     const size_t o_meta = carve(sizeof(int32_t) * 8);
     const size_t o_cslot = carve(sizeof(int32_t) * (size_t)d.max_chunks);
-    const size_t o_ccol = carve(sizeof(int32_t) * (size_t)d.max_chunks);
+    const size_t o_cunit = carve(sizeof(int32_t) * (size_t)d.max_chunks);
+    const size_t o_ckval = carve(sizeof(int32_t) * (size_t)d.max_chunks);
     const size_t o_v32 = carve(dtype == MLORA_F32 || tcn.need_v32 ? sizeof(float) * (size_t)max_tokens * max_rank : 0);
     const size_t o_vt = carve(dtype == MLORA_BF16 ? (size_t)d.max_chunks * d.tcap * CHUNK * 2 : 0);
     const size_t o_part = carve(tcn.partial_bytes);
@@ -292,7 +278,8 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     w.perm = (int32_t*)(p->ws_base + o_perm);
     w.meta = (int32_t*)(p->ws_base + o_meta);
     w.chunk_slot = (int32_t*)(p->ws_base + o_cslot);
-    w.chunk_col = (int32_t*)(p->ws_base + o_ccol);
+    w.chunk_unit = (int32_t*)(p->ws_base + o_cunit);
+    w.chunk_kval = (int32_t*)(p->ws_base + o_ckval);
     w.v32 = (float*)(p->ws_base + o_v32);
     w.vt = (uint16_t*)(p->ws_base + o_vt);
     w.partials = (float*)(p->ws_base + o_part);
@@ -368,8 +355,13 @@ mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const void* down, cons
     CU_TRY(cudaMemsetAsync(dst_down, 0, (size_t)rpad * p->din * p->esize, p->copy_stream));
     CU_TRY(cudaMemsetAsync(dst_up, 0, (size_t)rpad * p->dout * p->esize, p->copy_stream));
     CU_TRY(cudaMemcpyAsync(dst_down, down, (size_t)rank * p->din * p->esize, cudaMemcpyDefault, p->copy_stream));
-    CU_TRY(cudaMemcpy2DAsync(dst_up, (size_t)rpad * p->esize, up, (size_t)rank * p->esize, (size_t)rank * p->esize,
-                             (size_t)p->dout, cudaMemcpyDefault, p->copy_stream));
+    // Up [dout x rank] goes in blocks of 8 rank columns, each [dout x 8] row-major
+    for (int g = 0; g * 8 < rank; ++g) {
+        const int w = (rank - 8 * g) < 8 ? (rank - 8 * g) : 8;
+        CU_TRY(cudaMemcpy2DAsync(dst_up + (size_t)g * p->dout * 8 * p->esize, 8 * p->esize,
+                                 (const char*)up + (size_t)8 * g * p->esize, (size_t)rank * p->esize,
+                                 (size_t)w * p->esize, (size_t)p->dout, cudaMemcpyDefault, p->copy_stream));
+    }
     h.rank = rank;
     h.rpad = rpad;
     h.scale = scale;
@@ -414,14 +406,19 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
     cudaStream_t st = (cudaStream_t)stream;
     const bool lora = row_adapter != nullptr && p->max_slots > 0;
     const bool bf16 = p->dtype == MLORA_BF16;
-    if (lora) CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
+    int ext_chunk_cap = 0;
+    for (const SlotHost& h : p->slots) ext_chunk_cap += h.rank > 0 ? (h.rank + CHUNK - 1) / CHUNK : 0;
+    const bool tc = bf16 && tc_supported(p->dims, T);
+    // the tensor-core shrink builds the segments in its own prologue; otherwise a
+    // separate segment kernel runs (fp32 path, or nothing loaded: only the status bit)
+    if (lora && (!tc || ext_chunk_cap == 0)) CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
     cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
     if (!p->prof_start.empty()) {
         const size_t k = p->prof_next++ % p->prof_start.size();
         ev_start = p->prof_start[k];
         ev_stop = p->prof_stop[k];
     }
-    if (bf16 && tc_supported(p->dims, T)) {
+    if (tc) {
         TcForwardArgs a{};
         a.X = X;
         a.W = W;
@@ -430,13 +427,11 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
         a.lora = lora;
         a.row_adapter = row_adapter;
         a.slots = p->d_slots;
-        a.up_maps = p->d_up_maps;
-        a.down_maps = p->d_down_maps;
+        a.maps = p->maps;
         a.arena_down = p->arena_down;
         a.ws = p->ws;
         a.dims = p->dims;
-        a.ext_chunk_cap = 0;
-        for (const SlotHost& h : p->slots) a.ext_chunk_cap += h.rank > 0 ? (h.rank + CHUNK - 1) / CHUNK : 0;
+        a.ext_chunk_cap = ext_chunk_cap;
         a.ev_start = ev_start;
         a.ev_stop = ev_stop;
         CU_TRY(tc_forward(a, st));

@@ -1,0 +1,243 @@
+// Row -> adapter segment builder as a block-wide device function (ai-infra-kb "M031"
+// tutorial §02/§03; wiblog section on Punica's grouped matmul): group the rows of
+// a mixed batch by adapter slot, keep the original order inside each group (P, R
+// before Q in the page's example) and order groups by ascending slot id.
+//
+// Produced, bit-exactly:
+//   counts[S]      rows per slot
+//   offsets[S+1]   exclusive prefix sum of counts
+//   perm[T]        original row indices in segment order, -1 past the valid rows
+//   chunk table    the touched slots (count > 0) in ascending order, each split into
+//                  ceil(rank/16) chunks of 16 rank columns: the K-extension layout of
+//                  the tensor-core shrink and expand.  Per chunk: slot, absolute
+//                  rank-unit index in the arena (unit of the slot + first column)
+//                  and the number of valid rank columns (<= 16).
+//
+// Stable scatter without a sort: the rows are split into P contiguous ranges, one
+// per warp.  Pass 1 counts rows per (warp, slot) with __match_any_sync (one
+// leader per group of equal ids in each 32-row step).  The counts become
+// per-(warp, slot) cursors: offsets[s] + rows of slot s in earlier warps.  Pass 2
+// walks the same ranges again; a row's position is its warp's cursor for its
+// slot plus the number of lower lanes with the same id in that step.  Ranges and
+// steps are in row order, so the result is the stable order.
+//
+// Everything is built in shared memory by one CTA; no CTA ever waits on another.
+// Used by the standalone segment kernel (seg.cu) and, redundantly in each CTA, by
+// the prologue of the tensor-core shrink (tc.cu), whose CTA (0,0,0) publishes.
+#pragma once
+#include "internal.h"
+
+namespace mlora {
+namespace seg {
+
+struct Scratch {
+    int* rank_s;     // [S]
+    int* unit_s;     // [S]
+    int* scan;       // [S]
+    int* cur;        // [P*S]
+    int* c_slot;     // [max_chunks]
+    int* c_unit;     // [max_chunks]
+    int* c_kval;     // [max_chunks]
+    int* misc;       // [40]: warp_tmp[0..32], [33] bad row, [34] n_valid, [35] n_chunks, [36] touched
+};
+
+__host__ __device__ inline int scratch_ints(int S, int P, int max_chunks) {
+    return 3 * S + P * S + 3 * max_chunks + 40;
+}
+
+__device__ inline Scratch carve(int* base, int S, int P, int max_chunks) {
+    Scratch s;
+    s.rank_s = base;
+    s.unit_s = s.rank_s + S;
+    s.scan = s.unit_s + S;
+    s.cur = s.scan + S;
+    s.c_slot = s.cur + P * S;
+    s.c_unit = s.c_slot + max_chunks;
+    s.c_kval = s.c_unit + max_chunks;
+    s.misc = s.c_kval + max_chunks;
+    return s;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exclusive scan of n ints in shared memory, in place, by the whole block
+// (blockDim.x a multiple of 32, at most 1024).  Returns the total.
+__device__ inline int block_exclusive_scan(int* a, int n, int* warp_tmp) {
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+    const int per = (n + nt - 1) / nt;
+    const int lo = min(n, tid * per), hi = min(n, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += a[i];
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) warp_tmp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < nwarps ? warp_tmp[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, d);
+            if (lane >= d) wi += v;
+        }
+        if (lane < nwarps) warp_tmp[lane] = wi - w;
+        if (lane == 31) warp_tmp[32] = wi;
+    }
+    __syncthreads();
+    int run = warp_tmp[warp] + incl - local;
+    for (int i = lo; i < hi; ++i) {
+        const int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    const int total = warp_tmp[32];
+    __syncthreads();
+    return total;
+}
+
+// Builds the segments of row_adapter[0..T) over S slots in shared memory.  Every
+// thread of the block must call it.  With `publish`, also writes counts, offsets,
+// perm, the chunk table, meta and the bad-row status bit to the workspace.
+// Returns the number of chunks; the chunk table stays in sc.c_* (shared memory).
+__device__ inline int build(const int32_t* __restrict__ row_adapter, int T, const SlotRec* __restrict__ slots,
+                            int S, int P, int max_chunks, const Scratch& sc, bool publish, const Workspace& ws) {
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int* warp_tmp = sc.misc;
+    for (int s = tid; s < S; s += nt) {
+        const SlotRec r = slots[s];
+        sc.rank_s[s] = r.rank;
+        sc.unit_s[s] = r.unit;
+    }
+    for (int i = tid; i < P * S; i += nt) sc.cur[i] = 0;
+    if (tid == 0) sc.misc[33] = 0;
+    __syncthreads();
+
+    // ---- pass 1: per (warp, slot) counts
+    const int t_lo = (int)((long long)warp * T / P);
+    const int t_hi = (int)((long long)(warp + 1) * T / P);
+    if (warp < P) {
+        for (int base = t_lo; base < t_hi; base += 32) {
+            const int t = base + lane;
+            int a = -1;
+            if (t < t_hi) {
+                a = row_adapter[t];
+                if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) {
+                    if (a != -1) sc.misc[33] = 1;
+                    a = -1;
+                }
+            }
+            const unsigned grp = __match_any_sync(0xffffffffu, a);
+            if (a >= 0 && (grp & lanemask_lt()) == 0) sc.cur[warp * S + a] += __popc(grp);
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    // ---- totals, offsets and per-warp cursors
+    for (int s = tid; s < S; s += nt) {
+        int tot = 0;
+        for (int w = 0; w < P; ++w) tot += sc.cur[w * S + s];
+        sc.scan[s] = tot;
+        if (publish) ws.counts[s] = tot;
+    }
+    __syncthreads();
+    const int n_valid = block_exclusive_scan(sc.scan, S, warp_tmp);
+    for (int s = tid; s < S; s += nt) {
+        const int off = sc.scan[s];
+        if (publish) ws.offsets[s] = off;
+        int run = off;
+        for (int w = 0; w < P; ++w) {
+            const int c = sc.cur[w * S + s];
+            sc.cur[w * S + s] = run;
+            run += c;
+        }
+    }
+    if (publish && tid == 0) ws.offsets[S] = n_valid;
+    __syncthreads();
+
+    // ---- pass 2: stable scatter (only the publishing CTA needs the permutation)
+    if (publish) {
+        if (warp < P) {
+            for (int base = t_lo; base < t_hi; base += 32) {
+                const int t = base + lane;
+                int a = -1;
+                if (t < t_hi) {
+                    a = row_adapter[t];
+                    if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) a = -1;
+                }
+                const unsigned grp = __match_any_sync(0xffffffffu, a);
+                int pos = 0;
+                if (a >= 0) pos = sc.cur[warp * S + a] + __popc(grp & lanemask_lt());
+                __syncwarp();
+                if (a >= 0) {
+                    ws.perm[pos] = t;
+                    if ((grp & lanemask_lt()) == 0) sc.cur[warp * S + a] += __popc(grp);
+                }
+                __syncwarp();
+            }
+        }
+        for (int i = n_valid + tid; i < T; i += nt) ws.perm[i] = -1;
+    }
+    __syncthreads();
+
+    // ---- chunks of the touched slots (non-empty segments: offsets[s+1] > offsets[s]),
+    // ascending slot id; cur[0..S) is reused for the per-slot chunk counts
+    for (int s = tid; s < S; s += nt) {
+        const int off = sc.scan[s];
+        const int nxt = (s + 1 < S) ? sc.scan[s + 1] : n_valid;
+        sc.cur[s] = (nxt > off) ? (sc.rank_s[s] + CHUNK - 1) / CHUNK : 0;
+    }
+    __syncthreads();
+    const int n_chunks_raw = block_exclusive_scan(sc.cur, S, warp_tmp);
+    const int n_chunks = min(n_chunks_raw, max_chunks);
+    int touched = 0;
+    for (int s = tid; s < S; s += nt) {
+        const int off = sc.scan[s];
+        const int nxt = (s + 1 < S) ? sc.scan[s + 1] : n_valid;
+        if (nxt > off) {
+            ++touched;
+            const int nc = (sc.rank_s[s] + CHUNK - 1) / CHUNK;
+            for (int j = 0; j < nc; ++j) {
+                const int c = sc.cur[s] + j;
+                if (c < max_chunks) {
+                    sc.c_slot[c] = s;
+                    sc.c_unit[c] = sc.unit_s[s] + j * CHUNK;
+                    sc.c_kval[c] = min(CHUNK, sc.rank_s[s] - j * CHUNK);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) touched += __shfl_xor_sync(0xffffffffu, touched, d);
+    __syncthreads();   // warp_tmp reuse below
+    if (lane == 0) warp_tmp[warp] = touched;
+    __syncthreads();
+    if (publish) {
+        for (int c = tid; c < n_chunks; c += nt) {
+            ws.chunk_slot[c] = sc.c_slot[c];
+            ws.chunk_unit[c] = sc.c_unit[c];
+            ws.chunk_kval[c] = sc.c_kval[c];
+        }
+        if (tid == 0) {
+            int tt = 0;
+            for (int w = 0; w < (nt >> 5); ++w) tt += warp_tmp[w];
+            ws.meta[0] = n_valid;
+            ws.meta[1] = n_chunks;
+            ws.meta[2] = tt;
+            if (sc.misc[33]) atomicOr(ws.status, STATUS_BAD_ROW);
+        }
+    }
+    __syncthreads();
+    return n_chunks;
+}
+
+}  // namespace seg
+}  // namespace mlora

@@ -112,10 +112,8 @@ base_expand_simt_kernel(const E* __restrict__ X, const E* __restrict__ W, const 
             const int o = o0 + tx * 4 + j;
             if (o >= dout) continue;
             float y = acc[i][j];
-            if (lora) {
-                const E* up = arena_up + (size_t)rec.unit * dout + (size_t)o * rec.rpad;
-                for (int k = 0; k < rec.rank; ++k) y = fmaf(to_f32(up[k]), v[k], y);
-            }
+            if (lora)
+                for (int k = 0; k < rec.rank; ++k) y = fmaf(to_f32(arena_up[up_index(rec.unit, k, o, dout)]), v[k], y);
             Y[(size_t)t * dout + o] = from_f32<E>(y);
         }
     }
@@ -140,7 +138,6 @@ merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot
     const int o0 = blockIdx.y * MERGE_ROWS, i0 = blockIdx.x * MERGE_COLS;
     const int i = i0 + threadIdx.x;
     const E* down = arena_down + (size_t)rec.unit * din;
-    const E* up = arena_up + (size_t)rec.unit * dout;
     float acc[MERGE_ROWS];
 #pragma unroll
     for (int r = 0; r < MERGE_ROWS; ++r) acc[r] = 0.f;
@@ -150,7 +147,7 @@ merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot
         for (int k = 0; k < kn; ++k) down_s[k][threadIdx.x] = i < din ? to_f32(down[(size_t)(k0 + k) * din + i]) : 0.f;
         for (int idx = threadIdx.x; idx < MERGE_ROWS * MERGE_KC; idx += MERGE_COLS) {
             const int r = idx / MERGE_KC, k = idx % MERGE_KC;
-            up_s[r][k] = (o0 + r < dout && k < kn) ? to_f32(up[(size_t)(o0 + r) * rec.rpad + k0 + k]) : 0.f;
+            up_s[r][k] = (o0 + r < dout && k < kn) ? to_f32(arena_up[up_index(rec.unit, k0 + k, o0 + r, dout)]) : 0.f;
         }
         __syncthreads();
         for (int k = 0; k < kn; ++k) {

@@ -37,6 +37,7 @@
 #include <cstdlib>
 #include <cstring>
 
+#include "seg.cuh"
 #include "tc.h"
 #include "tc_ptx.cuh"
 
@@ -60,8 +61,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-            const cuuint32_t* box, CUtensorMapSwizzle sw) {
+}  // namespace
+
+bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box, CUtensorMapSwizzle sw) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint32_t estr[3] = {1, 1, 1};
@@ -70,6 +73,8 @@ bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 int sm_count() {
     static int n = 0;
@@ -94,10 +99,8 @@ __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
 
 struct GemmParams {
-    const CUtensorMap* up_maps;     // per-slot Up descriptors (projection K-extension)
-    const CUtensorMap* down_maps;   // per-slot Down descriptors (shrink rows)
-    const int32_t* chunk_slot;
-    const int32_t* chunk_col;
+    const int32_t* chunk_slot;      // projection: chunk table of the touched slots (from the shrink)
+    const int32_t* chunk_unit;
     const int32_t* meta;            // meta[1] = number of chunks of the touched slots
     const int32_t* row_adapter;     // shrink: slot id per token
     const SlotRec* slots;
@@ -108,24 +111,31 @@ struct GemmParams {
     uint32_t* status;
     int T, dout, N, kb_total, ext_units, splits, stages, tcap;
     int pdl;    // launched while an earlier kernel may still run: wait before reading its outputs
+    // shrink prologue: segment builder over S slots with segP row ranges, in
+    // scratch_bytes at the start of shared memory (the ring region is at least that large)
+    int S, segP, max_chunks, scratch_bytes;
+    Workspace ws;
 };
 
 // ---------------------------------------------------------------- the GEMM kernel
 template <bool SHRINK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ CUtensorMap tmV, GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmArena,
+                   GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int NS = p.stages;
     const int SB = stage_bytes(p.N);
-    uint64_t* full = (uint64_t*)(smem + (size_t)NS * SB);
+    const int ring = max(NS * SB, SHRINK ? p.scratch_bytes : 0);
+    uint64_t* full = (uint64_t*)(smem + ring);
     uint64_t* empty = full + NS;
     uint64_t* acc_full = empty + NS;
     int* stage_kind = (int*)(acc_full + 1);          // -1 = din step, else number of valid chunks
     uint32_t* tmem_slot = (uint32_t*)(stage_kind + NS);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     int* flags = (int*)(tmem_slot + 2);              // [0] issued-any, [1] last-arrival
+    int* my_chunk = flags + 2;                       // shrink: [3][8] slot, unit, valid columns
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
@@ -135,8 +145,20 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     int tile_chunks = 0;
     if (SHRINK) {
         pdl_trigger();   // the projection may launch and stream W meanwhile
-        pdl_wait();      // the segment builder's chunk table must be complete
-        tile_chunks = min(CHUNKS_PER_TILE, p.meta[1] - tile * CHUNKS_PER_TILE);
+        // Segment build (M031 §02/§03) in the stage memory, before any load uses it.
+        // Every CTA builds the same table; CTA (0,0,0) publishes it (perm, offsets,
+        // chunk table, meta) for the projection and for the caller.
+        const seg::Scratch sc = seg::carve(reinterpret_cast<int*>(smem), p.S, p.segP, p.max_chunks);
+        const bool publish = (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
+        const int n_chunks = seg::build(p.row_adapter, p.T, p.slots, p.S, p.segP, p.max_chunks, sc, publish, p.ws);
+        tile_chunks = min(CHUNKS_PER_TILE, n_chunks - tile * CHUNKS_PER_TILE);
+        if (threadIdx.x < CHUNKS_PER_TILE && (int)threadIdx.x < tile_chunks) {
+            const int c = tile * CHUNKS_PER_TILE + threadIdx.x;
+            my_chunk[threadIdx.x] = sc.c_slot[c];
+            my_chunk[CHUNKS_PER_TILE + threadIdx.x] = sc.c_unit[c];
+            my_chunk[2 * CHUNKS_PER_TILE + threadIdx.x] = sc.c_kval[c];
+        }
+        __syncthreads();
         if (tile_chunks <= 0) return;                // uniform for the whole CTA (and all its splits)
     }
 
@@ -186,12 +208,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (SHRINK) {
                 stage_kind[s] = -1;
                 mbar_expect_tx(&full[s], (uint32_t)(tile_chunks * CHUNK * BK * 2 + b_bytes(p.N)));
-                for (int j = 0; j < tile_chunks; ++j) {
-                    const int c = tile * CHUNKS_PER_TILE + j;
-                    const CUtensorMap* dm = p.down_maps + p.chunk_slot[c];
-                    tensormap_acquire(dm);
-                    tma_2d(a + j * (CHUNK * BK * 2), dm, &full[s], kb * BK, p.chunk_col[c]);
-                }
+                for (int j = 0; j < tile_chunks; ++j)
+                    tma_2d(a + j * (CHUNK * BK * 2), &tmArena, &full[s], kb * BK, my_chunk[CHUNKS_PER_TILE + j]);
                 tma_2d(b, &tmX, &full[s], kb * BK, tok0);
             } else if (kb < kb1) {
                 stage_kind[s] = -1;
@@ -213,11 +231,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 } else {
                     mbar_expect_tx(&full[s], (uint32_t)(nv * (BM * 32) + b_bytes(p.N)));
                     tma_3d(b, &tmV, &full[s], 0, 0, c0);
-                    for (int j = 0; j < nv; ++j) {
-                        const CUtensorMap* um = p.up_maps + p.chunk_slot[c0 + j];
-                        tensormap_acquire(um);
-                        tma_2d(a + j * (BM * 32), um, &full[s], p.chunk_col[c0 + j], tile * BM);
-                    }
+                    for (int j = 0; j < nv; ++j)   // two blocks of 8 rank columns x 128 rows
+                        tma_3d(a + j * (BM * 32), &tmArena, &full[s], 0, tile * BM, p.chunk_unit[c0 + j] >> 3);
                 }
             }
             if (++s == NS) {
@@ -253,9 +268,11 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     acc = 1;
                 }
             } else {
+                // Up chunk: [2 blocks of 8 columns][128 rows][16 B], no swizzle (K-direction core
+                // matrices BM*16 bytes apart, M-direction 128 bytes); Vt chunk: 32-byte swizzle
                 for (int j = 0; j < kind; ++j) {
-                    mma_bf16(tmem, sdesc(a + j * (BM * 32), 256, SW32), sdesc(b + j * (p.N * 32), 256, SW32), idesc,
-                             acc);
+                    mma_bf16(tmem, sdesc_lbo(a + j * (BM * 32), BM * 16, 128, SW_NONE),
+                             sdesc(b + j * (p.N * 32), 256, SW32), idesc, acc);
                     acc = 1;
                 }
             }
@@ -286,8 +303,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         float c_scale = 0.f;
         if (SHRINK && (row / CHUNK) < tile_chunks) {
             c_idx = tile * CHUNKS_PER_TILE + row / CHUNK;
-            c_slot = p.chunk_slot[c_idx];
-            c_scale = p.slots[c_slot].scale;
+            c_slot = my_chunk[row / CHUNK];
+            // rank columns past the adapter's rank belong to the next adapter in the arena
+            c_scale = (row % CHUNK) < my_chunk[2 * CHUNKS_PER_TILE + row / CHUNK] ? p.slots[c_slot].scale : 0.f;
         }
         const int o = tile * BM + row;
         auto emit = [&](int t0, const float* v) {
@@ -409,8 +427,12 @@ int k_splits(int tiles, int kb_total) {
     return s;
 }
 
-size_t smem_bytes(int stages, int N) {
-    return 1024 + (size_t)stages * stage_bytes(N) + (size_t)(2 * stages + 1) * 8 + (size_t)stages * 4 + 16;
+// dynamic shared memory of one CTA: alignment slack, the ring (or the segment
+// scratch, if larger), barriers, stage kinds, TMEM slot / flags, chunk info
+size_t smem_bytes(int stages, int N, int scratch_bytes = 0) {
+    size_t ring = (size_t)stages * stage_bytes(N);
+    if ((size_t)scratch_bytes > ring) ring = (size_t)scratch_bytes;
+    return 1024 + ring + (size_t)(2 * stages + 1) * 8 + (size_t)stages * 4 + 16 + 3 * CHUNKS_PER_TILE * 4;
 }
 
 int proj_tiles(const PoolDims& d) { return (d.dout + BM - 1) / BM; }
@@ -453,18 +475,19 @@ TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d) {
     return n;
 }
 
-bool tc_encode_up_map(CUtensorMap* map, void* up_block, int rpad, int dout) {
-    cuuint64_t dims[2] = {(cuuint64_t)rpad, (cuuint64_t)dout};
-    cuuint64_t strides[1] = {(cuuint64_t)rpad * 2};
-    cuuint32_t box[2] = {16, (cuuint32_t)BM};
-    return encode(map, up_block, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B);
-}
-
-bool tc_encode_down_map(CUtensorMap* map, void* down_block, int rank, int din) {
-    cuuint64_t dims[2] = {(cuuint64_t)din, (cuuint64_t)rank};
-    cuuint64_t strides[1] = {(cuuint64_t)din * 2};
-    cuuint32_t box[2] = {BK, (cuuint32_t)CHUNK};
-    return encode(map, down_block, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+bool tc_encode_arena_maps(TcArenaMaps* m, void* arena_down, void* arena_up, int units, int din, int dout) {
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)din, (cuuint64_t)units};
+        cuuint64_t strides[1] = {(cuuint64_t)din * 2};
+        cuuint32_t box[2] = {BK, (cuuint32_t)CHUNK};
+        if (!tc_encode(&m->down, arena_down, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return false;
+    }
+    cuuint64_t dims[3] = {8, (cuuint64_t)dout, (cuuint64_t)(units / 8)};
+    cuuint64_t strides[2] = {16, (cuuint64_t)dout * 16};
+    cuuint32_t box128[3] = {8, 128, 2};
+    cuuint32_t box256[3] = {8, 256, 2};
+    return tc_encode(&m->up128, arena_up, 3, dims, strides, box128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           tc_encode(&m->up256, arena_up, 3, dims, strides, box256, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool tc_supported(const PoolDims& d, int T) {
@@ -491,13 +514,10 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)T};
         cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
         cuuint32_t box[2] = {BK, (cuuint32_t)Ns};
-        if (!encode(&tmXs, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!tc_encode(&tmXs, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         const int tiles = (ext_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
         const int ztiles = token_tiles(T);
         GemmParams g{};
-        g.down_maps = a.down_maps;
-        g.chunk_slot = a.ws.chunk_slot;
-        g.chunk_col = a.ws.chunk_col;
         g.meta = a.ws.meta;
         g.row_adapter = a.row_adapter;
         g.slots = a.slots;
@@ -511,9 +531,19 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         g.splits = k_splits(tiles * ztiles, kb_total);
         g.stages = ring_stages(Ns, SHRINK_SMEM_BUDGET);
         g.tcap = d.tcap;
-        g.pdl = 1;
+        g.pdl = 0;
+        g.S = d.S;
+        g.max_chunks = d.max_chunks;
+        g.ws = a.ws;
+        // segment scratch in the ring memory: as many row ranges as fit (at most one per warp)
+        const int ring_ints = g.stages * stage_bytes(Ns) / 4;
+        g.segP = seg_warps_for(d.S, NUM_THREADS / 32, ring_ints, d.max_chunks);
+        if (g.segP < 1) g.segP = 1;   // the ring grows to the scratch (large slot counts)
+        g.scratch_bytes = 4 * seg::scratch_ints(d.S, g.segP, d.max_chunks);
+        // first kernel of the forward: an ordinary launch (it may overwrite the workspace
+        // the previous forward's kernels read)
         e = launch_k(swapab_gemm_kernel<true>, dim3(tiles, g.splits, ztiles), dim3(NUM_THREADS),
-                     smem_bytes(g.stages, Ns), st, true, tmNone, tmXs, tmNone, g);
+                     smem_bytes(g.stages, Ns, g.scratch_bytes), st, false, tmNone, tmXs, tmNone, a.maps.down, g);
         if (e != cudaSuccess) return e;
     }
 
@@ -523,19 +553,19 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)d.dout};
         cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
         cuuint32_t box[2] = {BK, decode ? (cuuint32_t)BM : 256u};
-        if (!encode(&tmW, a.W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!tc_encode(&tmW, a.W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)T};
         cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
         cuuint32_t box[2] = {BK, (cuuint32_t)N};
-        if (!encode(&tmX, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!tc_encode(&tmX, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[3] = {(cuuint64_t)CHUNK, (cuuint64_t)d.tcap, (cuuint64_t)d.max_chunks};
         cuuint64_t strides[2] = {(cuuint64_t)CHUNK * 2, (cuuint64_t)d.tcap * CHUNK * 2};
         cuuint32_t box[3] = {CHUNK, (cuuint32_t)N, EXT_SUB};
-        if (!encode(&tmV, a.ws.vt, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
+        if (!tc_encode(&tmV, a.ws.vt, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
     }
 
     if (!decode) {
@@ -547,9 +577,8 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
 
     const int tiles = proj_tiles(d);
     GemmParams p{};
-    p.up_maps = a.up_maps;
     p.chunk_slot = a.ws.chunk_slot;
-    p.chunk_col = a.ws.chunk_col;
+    p.chunk_unit = a.ws.chunk_unit;
     p.meta = a.ws.meta;
     p.Y = (__nv_bfloat16*)a.Y;
     p.partials = a.ws.partials;
@@ -566,7 +595,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.pdl = shrink ? 1 : 0;
     if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
     e = launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p.stages, N), st,
-                 shrink && !a.ev_start, tmW, tmX, tmV, p);
+                 shrink && !a.ev_start, tmW, tmX, tmV, a.maps.up128, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
     return cudaSuccess;

@@ -14,15 +14,14 @@ struct TcWorkspaceNeeds {
 };
 TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d);
 
-// Encodes the TMA descriptor of one adapter's Up block [dout x rpad] (bf16,
-// row-major): boxes of 16 rank columns x 128 output rows, 32-byte swizzle,
-// columns past rpad read as zero.
-bool tc_encode_up_map(CUtensorMap* map, void* up_block, int rpad, int dout);
-
-// Encodes the TMA descriptor of one adapter's Down block [rank x din] (bf16,
-// row-major): boxes of 64 din columns x 16 rank rows, 128-byte swizzle, rows past
-// the rank read as zero.
-bool tc_encode_down_map(CUtensorMap* map, void* down_block, int rank, int din);
+// TMA descriptors of the whole adapter arena (bf16), encoded once per pool:
+//   down   : 2D {din, units}, boxes of 64 din columns x 16 rank rows, 128-byte swizzle
+//   up128  : 3D {8, dout, units/8}, boxes of 8 rank columns x 128 rows x 2 blocks, no swizzle
+//   up256  : the same with 256 rows per box (prefill tiles)
+struct TcArenaMaps {
+    CUtensorMap down, up128, up256;
+};
+bool tc_encode_arena_maps(TcArenaMaps* maps, void* arena_down, void* arena_up, int units, int din, int dout);
 
 // Raises the dynamic shared memory cap of the tensor-core kernels (call outside capture).
 cudaError_t tc_init();
@@ -38,8 +37,7 @@ struct TcForwardArgs {
     bool lora;
     const int32_t* row_adapter;
     const SlotRec* slots;
-    const CUtensorMap* up_maps;
-    const CUtensorMap* down_maps;
+    TcArenaMaps maps;
     const void* arena_down;
     Workspace ws;
     PoolDims dims;
@@ -55,6 +53,10 @@ cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st);
 cudaError_t prefill_init();
 cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
                            const CUtensorMap& tmV, int num_sms, bool after_shrink, cudaStream_t st);
+
+// Encodes a bf16 tensor map (used by both tensor-core translation units).
+bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box, CUtensorMapSwizzle sw);
 cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st);
 
 }  // namespace mlora

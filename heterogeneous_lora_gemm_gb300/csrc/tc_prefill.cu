@@ -35,9 +35,7 @@ constexpr int GROUP_M = 8;
 constexpr int EXT_SUB = 4;
 
 struct PrefillParams {
-    const CUtensorMap* up_maps;
-    const int32_t* chunk_slot;
-    const int32_t* chunk_col;
+    const int32_t* chunk_unit;
     const int32_t* meta;
     __nv_bfloat16* Y;
     uint32_t* status;
@@ -56,7 +54,8 @@ __device__ __forceinline__ void tile_coords(int i, int m_tiles, int n_tiles, int
 
 __global__ void __launch_bounds__(P_THREADS, 1)
 prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                    const __grid_constant__ CUtensorMap tmV, PrefillParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmUp,
+                    PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* full = (uint64_t*)(smem + (size_t)PSTAGES * PSTAGE);
@@ -134,13 +133,8 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     stage_kind[s] = nv;
                     mbar_expect_tx(&full[s], (uint32_t)(PA_BYTES + nv * (PN * 32)));
                     tma_3d(a, &tmV, &full[s], 0, m * PM, c0);
-                    for (int j = 0; j < nv; ++j) {
-                        const CUtensorMap* um = p.up_maps + p.chunk_slot[c0 + j];
-                        tensormap_acquire(um);
-                        const int col = p.chunk_col[c0 + j];
-                        tma_2d(b + j * (PN * 32), um, &full[s], col, n * PN);
-                        tma_2d(b + j * (PN * 32) + PM * 32, um, &full[s], col, n * PN + 128);
-                    }
+                    for (int j = 0; j < nv; ++j)   // two blocks of 8 rank columns x 256 rows
+                        tma_3d(b + j * (PN * 32), &tmUp, &full[s], 0, n * PN, p.chunk_unit[c0 + j] >> 3);
                 }
                 if (++s == PSTAGES) {
                     s = 0;
@@ -184,9 +178,11 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         acc = 1;
                     }
                 } else {
+                    // Vt chunk: 32-byte swizzle; Up chunk: [2 blocks of 8 columns][256 rows][16 B],
+                    // no swizzle (K-direction core matrices PN*16 bytes apart, N-direction 128)
                     for (int j = 0; j < kind; ++j) {
-                        mma_bf16(d, sdesc(a + j * (PM * 32), 256, SW32), sdesc(b + j * (PN * 32), 256, SW32), idesc,
-                                 acc);
+                        mma_bf16(d, sdesc(a + j * (PM * 32), 256, SW32), sdesc_lbo(b + j * (PN * 32), PN * 16, 128, SW_NONE),
+                                 idesc, acc);
                         acc = 1;
                     }
                 }
@@ -266,9 +262,7 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
                            const CUtensorMap& tmV, int num_sms, bool after_shrink, cudaStream_t st) {
     const PoolDims& d = a.dims;
     PrefillParams p{};
-    p.up_maps = a.up_maps;
-    p.chunk_slot = a.ws.chunk_slot;
-    p.chunk_col = a.ws.chunk_col;
+    p.chunk_unit = a.ws.chunk_unit;
     p.meta = a.ws.meta;
     p.Y = (__nv_bfloat16*)a.Y;
     p.status = a.ws.status;
@@ -284,7 +278,7 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
     const int grid = total < num_sms ? total : num_sms;
     const size_t smem = 1024 + (size_t)PSTAGES * PSTAGE + (2 * PSTAGES + 5) * 8 + PSTAGES * 4 + 16;
     return launch_k(prefill_gemm_kernel, dim3(grid), dim3(P_THREADS), smem, st, after_shrink && !a.ev_start, tmX,
-                    tmW, tmV, p);
+                    tmW, tmV, a.maps.up256, p);
 }
 
 }  // namespace mlora

@@ -80,7 +80,19 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t sbo, uint32_t
     d |= (uint64_t)swz << 61;
     return d;
 }
-constexpr uint32_t SW128 = 2, SW32 = 6;
+constexpr uint32_t SW_NONE = 0, SW128 = 2, SW32 = 6;
+
+// Descriptor with an explicit leading byte offset: for the K-major layout without
+// swizzle, lbo is the distance between core matrices (8 rows x 16 bytes) adjacent
+// in K and sbo the distance between core matrices adjacent in M/N.
+__device__ __forceinline__ uint64_t sdesc_lbo(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+    uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)swz << 61;
+    return d;
+}
 
 // Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
