@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <string>
 
 namespace mlora {
 
@@ -49,6 +50,9 @@ struct Workspace {
 struct PoolDims {
     int S, din, dout, max_rank, max_tokens, max_chunks, tcap;
 };
+
+// Sets the text returned by mlora_last_error() in the calling thread.
+void set_last_error(const std::string& msg);
 
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t seg_init();   // raises the segment builder's shared memory cap (outside capture)

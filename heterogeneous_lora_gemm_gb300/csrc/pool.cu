@@ -70,6 +70,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
 
+void mlora::set_last_error(const std::string& msg) { g_last_error = msg; }
+
 struct mlora_pool {
     int device = 0;
     int max_slots = 0, max_rank = 0, din = 0, dout = 0, max_tokens = 0;

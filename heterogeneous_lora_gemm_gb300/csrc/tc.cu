@@ -601,4 +601,48 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     return cudaSuccess;
 }
 
+cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din, int dout, void* Y,
+                                   float* partials, size_t partial_bytes, int32_t* counters, int max_tiles,
+                                   uint32_t* status, cudaStream_t st) {
+    if (T < 1 || T > MAX_N) return cudaErrorInvalidValue;
+    const int N = (T + 15) / 16 * 16;
+    const int tiles = (dout + BM - 1) / BM;
+    const int kb_total = (din + BK - 1) / BK;
+    if (tiles > max_tiles) return cudaErrorInvalidValue;
+    CUtensorMap tmW, tmX, tmNone;
+    std::memset(&tmNone, 0, sizeof tmNone);
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)din, (cuuint64_t)dout};
+        cuuint64_t strides[1] = {(cuuint64_t)din * 2};
+        cuuint32_t box[2] = {BK, (cuuint32_t)BM};
+        if (!tc_encode(&tmW, W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)din, (cuuint64_t)T};
+        cuuint64_t strides[1] = {(cuuint64_t)din * 2};
+        cuuint32_t box[2] = {BK, (cuuint32_t)N};
+        if (!tc_encode(&tmX, X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
+    GemmParams p{};
+    p.Y = (__nv_bfloat16*)Y;
+    p.partials = partials;
+    p.tile_ctr = counters;
+    p.status = status;
+    p.T = T;
+    p.dout = dout;
+    p.N = N;
+    p.kb_total = kb_total;
+    p.ext_units = 0;
+    // as many K splits as fill the SMs and whose partial tiles fit the scratch
+    int splits = k_splits(tiles, kb_total);
+    const size_t per_split = (size_t)tiles * BM * N * sizeof(float);
+    while (splits > 1 && (size_t)splits * per_split > partial_bytes) --splits;
+    p.splits = splits;
+    p.stages = ring_stages(N, PROJ_SMEM_BUDGET);
+    p.tcap = 0;
+    p.pdl = 0;
+    return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p.stages, N),
+                    st, false, tmW, tmX, tmNone, tmNone, p);
+}
+
 }  // namespace mlora

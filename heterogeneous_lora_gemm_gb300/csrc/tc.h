@@ -54,6 +54,13 @@ cudaError_t prefill_init();
 cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
                            const CUtensorMap& tmV, int num_sms, bool after_shrink, cudaStream_t st);
 
+// Base projection Y = X W^T (T <= 256, bf16) on the decode kernel with caller-given
+// scratch: `partials` (partial_bytes of fp32 partial tiles) and `counters`
+// (max_tiles zeroed ints, one per 128 output features), `status` one word.
+cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din, int dout, void* Y,
+                                   float* partials, size_t partial_bytes, int32_t* counters, int max_tiles,
+                                   uint32_t* status, cudaStream_t st);
+
 // Encodes a bf16 tensor map (used by both tensor-core translation units).
 bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                const cuuint32_t* box, CUtensorMapSwizzle sw);

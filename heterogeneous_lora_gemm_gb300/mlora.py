@@ -65,6 +65,7 @@ _SIGNATURES = {
     "mlora_pool_info": (_I, [_P, ctypes.POINTER(PoolInfo)]),
     "mlora_debug_segments": (_I, [_P, _P, _I, _P, _P, _P]),
     "mlora_profile_events": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I]),
+    "mlora_project_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "mlora_arena_new": (_P, [_I]),
     "mlora_arena_delete": (None, [_P]),
     "mlora_arena_alloc": (_I, [_P, _I, _I]),
@@ -166,6 +167,11 @@ def mlora_profile_events(pool: int, starts, stops) -> None:
     a = (_P * max(n, 1))(*[int(x) for x in starts])
     b = (_P * max(n, 1))(*[int(x) for x in stops])
     check(lib().mlora_profile_events(pool, a, b, n), "mlora_profile_events")
+
+
+def mlora_project_noalloc(X_ptr: int, W_ptr: int, T: int, din: int, dout: int, Y_ptr: int, stream: int) -> None:
+    """Y = X W^T (bf16, T <= 256) without any device allocation; see include/mlora.h."""
+    check(lib().mlora_project_noalloc(X_ptr, W_ptr, T, din, dout, Y_ptr, stream or None), "mlora_project_noalloc")
 
 
 # ---- torch-facing convenience ------------------------------------------- #

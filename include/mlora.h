@@ -198,6 +198,37 @@ mlora_status mlora_debug_segments(mlora_pool_t pool, const int32_t* row_adapter,
 mlora_status mlora_profile_events(mlora_pool_t pool, void* const* starts, void* const* stops, int n);
 
 /*
+ * Base projection Y = X W^T for a decode-sized batch that allocates nothing.
+ * The pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory when they need the projection -- code running inside a
+ * CUDA stream capture (cudaMalloc/cudaFree cannot be captured), plugins whose
+ * host runtime owns the device-memory budget and forbids allocations after
+ * start-up, and latency-critical loops that cannot take the device-wide
+ * synchronisation an allocation may cause.  Such callers cannot create a pool,
+ * whose workspace comes from cudaMalloc.
+ *
+ *   X   device [T x din] bf16, W device [dout x din] bf16, Y device [T x dout] bf16,
+ *       all 16-byte aligned, owned by the caller; Y is overwritten
+ *   T   0..256 (T == 0 enqueues nothing); din a positive multiple of 8;
+ *       dout 1..262144
+ *
+ * It runs the split-K tensor-core projection of mlora_forward (no adapters) on
+ * `stream`, with that kernel's scratch (fp32 partial tiles, arrival counters and
+ * a status word) in one fixed device array of about 8 MiB that every GPU loading
+ * this library holds until the process exits; larger shapes are rejected with
+ * MLORA_ERR_UNSUPPORTED, never served from anywhere else.  No cudaMalloc, cudaFree
+ * or allocating library routine is called.  The first call on a device looks up
+ * the array's device address and raises the kernel's shared-memory cap; make
+ * that first call outside any stream capture.  All calls share the one array
+ * (it keeps what the last call left; the counters are cleared on every call), so
+ * calls whose work overlaps on the GPU -- on different streams, or from several
+ * host threads -- race and must be ordered by the caller.
+ * Errors: INVALID_ARG (NULL or misaligned pointer), UNSUPPORTED, CUDA.
+ */
+mlora_status mlora_project_noalloc(const void* X, const void* W, int T, int din, int dout, void* Y,
+                                   mlora_stream_t stream);
+
+/*
  * Host-only view of the arena allocator the pool uses (no CUDA calls), for tests
  * of the placement logic.  An arena has `units` rank units; an allocation of
  * `n` units is placed first-fit at a multiple of 8.  mlora_arena_compact slides
