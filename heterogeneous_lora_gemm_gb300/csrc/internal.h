@@ -58,7 +58,7 @@ void set_last_error(const std::string& msg);
 cudaError_t seg_init();   // raises the segment builder's shared memory cap (outside capture)
 // Row ranges (warps) the segment builder can use with `scratch_ints_avail` ints of
 // shared memory, at most `warps`; 0 if even one does not fit.
-int seg_warps_for(int S, int warps, int scratch_ints_avail, int max_chunks);
+int seg_warps_for(int S, int warps, int scratch_ints_avail, int max_chunks, int T);
 cudaError_t launch_seg_build(const int32_t* row_adapter, int T, const SlotRec* slots,
                              const Workspace& ws, const PoolDims& d, cudaStream_t st);
 

@@ -20,11 +20,11 @@ seg_build_kernel(const int32_t* __restrict__ row_adapter, int T, const SlotRec* 
 
 }  // namespace
 
-int seg_warps_for(int S, int warps, int scratch_ints_avail, int max_chunks) {
+int seg_warps_for(int S, int warps, int scratch_ints_avail, int max_chunks, int T) {
     // as many row ranges as fit the scratch (per-(warp, slot) counters), at most one per warp
     int P = warps;
-    while (P > 1 && seg::scratch_ints(S, P, max_chunks) > scratch_ints_avail) --P;
-    return seg::scratch_ints(S, P, max_chunks) <= scratch_ints_avail ? P : 0;
+    while (P > 1 && seg::scratch_ints(S, P, max_chunks, T) > scratch_ints_avail) --P;
+    return seg::scratch_ints(S, P, max_chunks, T) <= scratch_ints_avail ? P : 0;
 }
 
 cudaError_t seg_init() {
@@ -42,9 +42,9 @@ cudaError_t seg_init() {
 
 cudaError_t launch_seg_build(const int32_t* row_adapter, int T, const SlotRec* slots, const Workspace& ws,
                              const PoolDims& d, cudaStream_t st) {
-    const int P = seg_warps_for(d.S, SEG_THREADS / 32, (160 * 1024) / 4, d.max_chunks);
+    const int P = seg_warps_for(d.S, SEG_THREADS / 32, (200 * 1024) / 4, d.max_chunks, T);
     if (P < 1) return cudaErrorInvalidConfiguration;
-    const size_t smem = sizeof(int) * (size_t)seg::scratch_ints(d.S, P, d.max_chunks);
+    const size_t smem = sizeof(int) * (size_t)seg::scratch_ints(d.S, P, d.max_chunks, T);
     seg_build_kernel<<<1, SEG_THREADS, smem, st>>>(row_adapter, T, slots, ws, d.S, P, d.max_chunks);
     return cudaGetLastError();
 }

@@ -38,11 +38,12 @@ struct Scratch {
     int* c_slot;     // [max_chunks]
     int* c_unit;     // [max_chunks]
     int* c_kval;     // [max_chunks]
-    int* misc;       // [40]: warp_tmp[0..32], [33] bad row, [34] n_valid, [35] n_chunks, [36] touched
+    int* misc;       // [40]: warp_tmp[0..32], [33] bad row
+    int* ra_s;       // [T] the row map, staged once
 };
 
-__host__ __device__ inline int scratch_ints(int S, int P, int max_chunks) {
-    return 3 * S + P * S + 3 * max_chunks + 40;
+__host__ __device__ inline int scratch_ints(int S, int P, int max_chunks, int T) {
+    return 3 * S + P * S + 3 * max_chunks + 40 + T;
 }
 
 __device__ inline Scratch carve(int* base, int S, int P, int max_chunks) {
@@ -55,6 +56,7 @@ __device__ inline Scratch carve(int* base, int S, int P, int max_chunks) {
     s.c_unit = s.c_slot + max_chunks;
     s.c_kval = s.c_unit + max_chunks;
     s.misc = s.c_kval + max_chunks;
+    s.ra_s = s.misc + 40;
     return s;
 }
 
@@ -111,6 +113,8 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
                             int S, int P, int max_chunks, const Scratch& sc, bool publish, const Workspace& ws) {
     const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int* warp_tmp = sc.misc;
+    // all global reads of the builder are issued here, together
+    for (int t = tid; t < T; t += nt) sc.ra_s[t] = row_adapter[t];
     for (int s = tid; s < S; s += nt) {
         const SlotRec r = slots[s];
         sc.rank_s[s] = r.rank;
@@ -128,7 +132,7 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
             const int t = base + lane;
             int a = -1;
             if (t < t_hi) {
-                a = row_adapter[t];
+                a = sc.ra_s[t];
                 if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) {
                     if (a != -1) sc.misc[33] = 1;
                     a = -1;
@@ -170,7 +174,7 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
                 const int t = base + lane;
                 int a = -1;
                 if (t < t_hi) {
-                    a = row_adapter[t];
+                    a = sc.ra_s[t];
                     if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) a = -1;
                 }
                 const unsigned grp = __match_any_sync(0xffffffffu, a);

@@ -183,6 +183,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
     }
     if (warp == 1) {
+        __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(ncols)
                      : "memory");
@@ -294,8 +295,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;          // row of the tile
         const bool ok = mbar_wait(acc_full, 0, abort_flag, p.status);
+        __syncwarp();   // reconverge: lanes may leave the wait loop apart; tcgen05.ld is warp-collective
         tc_fence_after();
-        const bool have = ok && flags[0] != 0;
+        const bool have = __all_sync(0xffffffffu, ok) && flags[0] != 0;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
 
         // final write of 16 consecutive tokens t0..t0+15 of this row
@@ -388,6 +390,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();   // reconverge: lane 0 ran the MMA loop alone, dealloc is warp-collective
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
     }
@@ -537,9 +540,9 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         g.ws = a.ws;
         // segment scratch in the ring memory: as many row ranges as fit (at most one per warp)
         const int ring_ints = g.stages * stage_bytes(Ns) / 4;
-        g.segP = seg_warps_for(d.S, NUM_THREADS / 32, ring_ints, d.max_chunks);
-        if (g.segP < 1) g.segP = 1;   // the ring grows to the scratch (large slot counts)
-        g.scratch_bytes = 4 * seg::scratch_ints(d.S, g.segP, d.max_chunks);
+        g.segP = seg_warps_for(d.S, NUM_THREADS / 32, ring_ints, d.max_chunks, T);
+        if (g.segP < 1) g.segP = 1;   // the ring grows to the scratch (many slots, long batches)
+        g.scratch_bytes = 4 * seg::scratch_ints(d.S, g.segP, d.max_chunks, T);
         // first kernel of the forward: an ordinary launch (it may overwrite the workspace
         // the previous forward's kernels read)
         e = launch_k(swapab_gemm_kernel<true>, dim3(tiles, g.splits, ztiles), dim3(NUM_THREADS),

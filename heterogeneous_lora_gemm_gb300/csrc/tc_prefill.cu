@@ -86,6 +86,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
     }
     if (warp == 1) {
+        __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(512)
                      : "memory");
@@ -209,7 +210,9 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             tile_coords(tile, p.m_tiles, p.n_tiles, m, n);
             const int buf = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
-            if (!mbar_wait(&tfull[buf], use & 1, abort_flag, p.status)) break;
+            const bool got = mbar_wait(&tfull[buf], use & 1, abort_flag, p.status);
+            __syncwarp();   // reconverge: lanes may leave the wait loop apart; tcgen05.ld is warp-collective
+            if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             const int t = m * PM + q * 32 + lane;
             const uint32_t taddr = tmem + (uint32_t)(buf * PN) + ((uint32_t)(q * 32) << 16);
@@ -239,6 +242,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
+        __syncwarp();   // reconverge: lane 0 ran the MMA loop alone, dealloc is warp-collective
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
     }
