@@ -15,7 +15,7 @@ seg_build_kernel(const int32_t* __restrict__ row_adapter, int T, const SlotRec* 
                  int S, int P, int max_chunks) {
     extern __shared__ int smem[];
     const seg::Scratch sc = seg::carve(smem, S, P, max_chunks);
-    seg::build(row_adapter, T, slots, S, P, max_chunks, sc, true, ws);
+    seg::build<false>(row_adapter, T, slots, S, P, max_chunks, sc, true, ws);
 }
 
 }  // namespace

@@ -66,10 +66,22 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-// Exclusive scan of n ints in shared memory, in place, by the whole block
-// (blockDim.x a multiple of 32, at most 1024).  Returns the total.
-__device__ inline int block_exclusive_scan(int* a, int n, int* warp_tmp) {
-    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+// The builder runs either on the whole block (WARP = false; blockDim.x a multiple
+// of 32, at most 1024) or on one warp alone (WARP = true), which needs no block
+// barrier and lets the other warps of the CTA do their own set-up meanwhile.
+template <bool WARP>
+__device__ __forceinline__ void group_sync() {
+    if (WARP)
+        __syncwarp();
+    else
+        __syncthreads();
+}
+
+// Exclusive scan of n ints in shared memory, in place, by the group.  Returns the total.
+template <bool WARP>
+__device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
+    const int nt = WARP ? 32 : blockDim.x, lane = threadIdx.x & 31;
+    const int tid = WARP ? lane : threadIdx.x, warp = WARP ? 0 : threadIdx.x >> 5, nwarps = nt >> 5;
     const int per = (n + nt - 1) / nt;
     const int lo = min(n, tid * per), hi = min(n, lo + per);
     int local = 0;
@@ -81,7 +93,7 @@ __device__ inline int block_exclusive_scan(int* a, int n, int* warp_tmp) {
         if (lane >= d) incl += v;
     }
     if (lane == 31) warp_tmp[warp] = incl;
-    __syncthreads();
+    group_sync<WARP>();
     if (warp == 0) {
         const int w = lane < nwarps ? warp_tmp[lane] : 0;
         int wi = w;
@@ -93,7 +105,7 @@ __device__ inline int block_exclusive_scan(int* a, int n, int* warp_tmp) {
         if (lane < nwarps) warp_tmp[lane] = wi - w;
         if (lane == 31) warp_tmp[32] = wi;
     }
-    __syncthreads();
+    group_sync<WARP>();
     int run = warp_tmp[warp] + incl - local;
     for (int i = lo; i < hi; ++i) {
         const int v = a[i];
@@ -101,17 +113,19 @@ __device__ inline int block_exclusive_scan(int* a, int n, int* warp_tmp) {
         run += v;
     }
     const int total = warp_tmp[32];
-    __syncthreads();
+    group_sync<WARP>();
     return total;
 }
 
 // Builds the segments of row_adapter[0..T) over S slots in shared memory.  Every
-// thread of the block must call it.  With `publish`, also writes counts, offsets,
-// perm, the chunk table, meta and the bad-row status bit to the workspace.
-// Returns the number of chunks; the chunk table stays in sc.c_* (shared memory).
+// thread of the group must call it (P = 1 for a single warp).  With `publish`, also
+// writes counts, offsets, perm, the chunk table, meta and the bad-row status bit to
+// the workspace.  Returns the number of chunks; the chunk table stays in sc.c_*.
+template <bool WARP>
 __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, const SlotRec* __restrict__ slots,
                             int S, int P, int max_chunks, const Scratch& sc, bool publish, const Workspace& ws) {
-    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nt = WARP ? 32 : blockDim.x, lane = threadIdx.x & 31;
+    const int tid = WARP ? lane : threadIdx.x, warp = WARP ? 0 : threadIdx.x >> 5;
     int* warp_tmp = sc.misc;
     // all global reads of the builder are issued here, together
     for (int t = tid; t < T; t += nt) sc.ra_s[t] = row_adapter[t];
@@ -122,7 +136,7 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
     }
     for (int i = tid; i < P * S; i += nt) sc.cur[i] = 0;
     if (tid == 0) sc.misc[33] = 0;
-    __syncthreads();
+    group_sync<WARP>();
 
     // ---- pass 1: per (warp, slot) counts
     const int t_lo = (int)((long long)warp * T / P);
@@ -143,7 +157,7 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
             __syncwarp();
         }
     }
-    __syncthreads();
+    group_sync<WARP>();
 
     // ---- totals, offsets and per-warp cursors
     for (int s = tid; s < S; s += nt) {
@@ -152,8 +166,8 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
         sc.scan[s] = tot;
         if (publish) ws.counts[s] = tot;
     }
-    __syncthreads();
-    const int n_valid = block_exclusive_scan(sc.scan, S, warp_tmp);
+    group_sync<WARP>();
+    const int n_valid = group_exclusive_scan<WARP>(sc.scan, S, warp_tmp);
     for (int s = tid; s < S; s += nt) {
         const int off = sc.scan[s];
         if (publish) ws.offsets[s] = off;
@@ -165,7 +179,7 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
         }
     }
     if (publish && tid == 0) ws.offsets[S] = n_valid;
-    __syncthreads();
+    group_sync<WARP>();
 
     // ---- pass 2: stable scatter (only the publishing CTA needs the permutation)
     if (publish) {
@@ -190,7 +204,7 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
         }
         for (int i = n_valid + tid; i < T; i += nt) ws.perm[i] = -1;
     }
-    __syncthreads();
+    group_sync<WARP>();
 
     // ---- chunks of the touched slots (non-empty segments: offsets[s+1] > offsets[s]),
     // ascending slot id; cur[0..S) is reused for the per-slot chunk counts
@@ -199,8 +213,8 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
         const int nxt = (s + 1 < S) ? sc.scan[s + 1] : n_valid;
         sc.cur[s] = (nxt > off) ? (sc.rank_s[s] + CHUNK - 1) / CHUNK : 0;
     }
-    __syncthreads();
-    const int n_chunks_raw = block_exclusive_scan(sc.cur, S, warp_tmp);
+    group_sync<WARP>();
+    const int n_chunks_raw = group_exclusive_scan<WARP>(sc.cur, S, warp_tmp);
     const int n_chunks = min(n_chunks_raw, max_chunks);
     int touched = 0;
     for (int s = tid; s < S; s += nt) {
@@ -221,9 +235,9 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) touched += __shfl_xor_sync(0xffffffffu, touched, d);
-    __syncthreads();   // warp_tmp reuse below
+    group_sync<WARP>();   // warp_tmp reuse below
     if (lane == 0) warp_tmp[warp] = touched;
-    __syncthreads();
+    group_sync<WARP>();
     if (publish) {
         for (int c = tid; c < n_chunks; c += nt) {
             ws.chunk_slot[c] = sc.c_slot[c];
@@ -239,7 +253,7 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
             if (sc.misc[33]) atomicOr(ws.status, STATUS_BAD_ROW);
         }
     }
-    __syncthreads();
+    group_sync<WARP>();
     return n_chunks;
 }
 

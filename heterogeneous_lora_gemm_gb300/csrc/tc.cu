@@ -94,6 +94,8 @@ constexpr int A_BYTES = BM * BK * 2;            // 16 KiB: W tile, 4 Up chunk ti
 constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int MAX_N = 256;
 constexpr int CHUNKS_PER_TILE = BM / CHUNK;     // shrink: 8 chunks of 16 rank rows
+constexpr int MAX_SPLITS = 16;     // K splits per tile at most
+constexpr int MAX_CLUSTER = 8;     // K splits of a tile reduced inside one (portable) cluster
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
@@ -112,8 +114,11 @@ struct GemmParams {
     int T, dout, N, kb_total, ext_units, splits, stages, tcap;
     int pdl;    // launched while an earlier kernel may still run: wait before reading its outputs
     // shrink prologue: segment builder over S slots with segP row ranges, in
-    // scratch_bytes at the start of shared memory (the ring region is at least that large)
-    int S, segP, max_chunks, scratch_bytes;
+    // scratch_bytes at the start of shared memory (the ring region is at least that
+    // large); seg_warp: one warp builds it (segP = 1)
+    int S, segP, max_chunks, scratch_bytes, seg_warp;
+    // the K splits of a tile form a cluster and reduce through distributed shared memory
+    int cluster;
     Workspace ws;
 };
 
@@ -135,31 +140,41 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     uint32_t* tmem_slot = (uint32_t*)(stage_kind + NS);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     int* flags = (int*)(tmem_slot + 2);              // [0] issued-any, [1] last-arrival
-    int* my_chunk = flags + 2;                       // shrink: [3][8] slot, unit, valid columns
+    int* my_chunk = flags + 2;                       // shrink: [4][8] slot, unit, valid columns, scale
+    int* tile_ra = my_chunk + 4 * CHUNKS_PER_TILE;   // shrink: slot of each token of this token tile
+    int* tile_chunks_s = tile_ra + MAX_N;            // shrink: chunks of this row tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
     const int tok0 = ztile * MAX_N;                  // first token of this token tile
     const int T = min(p.T - tok0, p.N);              // tokens in this tile
 
-    int tile_chunks = 0;
     if (SHRINK) {
         pdl_trigger();   // the projection may launch and stream W meanwhile
         // Segment build (M031 §02/§03) in the stage memory, before any load uses it.
         // Every CTA builds the same table; CTA (0,0,0) publishes it (perm, offsets,
-        // chunk table, meta) for the projection and for the caller.
-        const seg::Scratch sc = seg::carve(reinterpret_cast<int*>(smem), p.S, p.segP, p.max_chunks);
-        const bool publish = (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
-        const int n_chunks = seg::build(p.row_adapter, p.T, p.slots, p.S, p.segP, p.max_chunks, sc, publish, p.ws);
-        tile_chunks = min(CHUNKS_PER_TILE, n_chunks - tile * CHUNKS_PER_TILE);
-        if (threadIdx.x < CHUNKS_PER_TILE && (int)threadIdx.x < tile_chunks) {
-            const int c = tile * CHUNKS_PER_TILE + threadIdx.x;
-            my_chunk[threadIdx.x] = sc.c_slot[c];
-            my_chunk[CHUNKS_PER_TILE + threadIdx.x] = sc.c_unit[c];
-            my_chunk[2 * CHUNKS_PER_TILE + threadIdx.x] = sc.c_kval[c];
+        // chunk table, meta) for the projection and for the caller.  Small batches
+        // are built by warp 2 alone while warps 0 and 1 set up barriers and TMEM.
+        if (!p.seg_warp || warp == 2) {
+            const seg::Scratch sc = seg::carve(reinterpret_cast<int*>(smem), p.S, p.segP, p.max_chunks);
+            const bool publish = (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
+            const int n_chunks =
+                p.seg_warp ? seg::build<true>(p.row_adapter, p.T, p.slots, p.S, 1, p.max_chunks, sc, publish, p.ws)
+                           : seg::build<false>(p.row_adapter, p.T, p.slots, p.S, p.segP, p.max_chunks, sc, publish,
+                                               p.ws);
+            const int gt = p.seg_warp ? lane : (int)threadIdx.x, gn = p.seg_warp ? 32 : (int)blockDim.x;
+            const int tc = min(CHUNKS_PER_TILE, n_chunks - tile * CHUNKS_PER_TILE);
+            if (gt == 0) *tile_chunks_s = tc;
+            if (gt < CHUNKS_PER_TILE && gt < tc) {
+                const int c = tile * CHUNKS_PER_TILE + gt;
+                my_chunk[gt] = sc.c_slot[c];
+                my_chunk[CHUNKS_PER_TILE + gt] = sc.c_unit[c];
+                my_chunk[2 * CHUNKS_PER_TILE + gt] = sc.c_kval[c];
+                my_chunk[3 * CHUNKS_PER_TILE + gt] = __float_as_int(p.slots[sc.c_slot[c]].scale);
+            }
+            // the epilogue masks tokens by their slot: keep this token tile's row map at hand
+            for (int t = gt; t < T; t += gn) tile_ra[t] = sc.ra_s[tok0 + t];
         }
-        __syncthreads();
-        if (tile_chunks <= 0) return;                // uniform for the whole CTA (and all its splits)
     }
 
     const int kb0 = (int)((long long)split * p.kb_total / p.splits);
@@ -189,10 +204,22 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // A block barrier needs converged warps: lanes that skipped a one-thread branch
+    // above (barrier set-up, the TMA and MMA roles) wait here for it first.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int tile_chunks = SHRINK ? *tile_chunks_s : 0;
+    if (SHRINK && tile_chunks <= 0) {   // no chunk of the touched slots falls in this row tile
+        if (warp == 1) {
+            __syncwarp();
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+        }
+        return;
+    }
 
     if (warp == 0 && lane == 0) {
         // ---------------- producer: TMA loads into the stage ring
@@ -307,7 +334,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             c_idx = tile * CHUNKS_PER_TILE + row / CHUNK;
             c_slot = my_chunk[row / CHUNK];
             // rank columns past the adapter's rank belong to the next adapter in the arena
-            c_scale = (row % CHUNK) < my_chunk[2 * CHUNKS_PER_TILE + row / CHUNK] ? p.slots[c_slot].scale : 0.f;
+            c_scale = (row % CHUNK) < my_chunk[2 * CHUNKS_PER_TILE + row / CHUNK]
+                          ? __int_as_float(my_chunk[3 * CHUNKS_PER_TILE + row / CHUNK])
+                          : 0.f;
         }
         const int o = tile * BM + row;
         auto emit = [&](int t0, const float* v) {
@@ -315,12 +344,46 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 if (c_slot < 0) return;
                 __nv_bfloat16* dst = p.vt + ((size_t)c_idx * p.tcap + tok0) * CHUNK + (row % CHUNK);
                 for (int j = 0; j < 16 && t0 + j < T; ++j) {
-                    const bool mine = p.row_adapter[tok0 + t0 + j] == c_slot;
+                    const bool mine = tile_ra[t0 + j] == c_slot;
                     dst[(size_t)(t0 + j) * CHUNK] = __float2bfloat16_rn(mine ? c_scale * v[j] : 0.f);
                 }
             } else if (o < p.dout) {
                 for (int j = 0; j < 16 && t0 + j < T; ++j)
                     p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
+            }
+        };
+
+        // final write of rows r0..r0+3 (a multiple of 4) of token t
+        auto emit4 = [&](int t, int r0, const float4& v) {
+            if (SHRINK) {
+                const int ci = r0 / CHUNK;
+                if (ci >= tile_chunks) return;
+                const int slot = my_chunk[ci];
+                const int kval = my_chunk[2 * CHUNKS_PER_TILE + ci];
+                const int k0 = r0 % CHUNK;
+                const bool mine = tile_ra[t] == slot;
+                const float sc = mine ? __int_as_float(my_chunk[3 * CHUNKS_PER_TILE + ci]) : 0.f;
+                __nv_bfloat162 lo = __floats2bfloat162_rn(k0 < kval ? sc * v.x : 0.f, k0 + 1 < kval ? sc * v.y : 0.f);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(k0 + 2 < kval ? sc * v.z : 0.f, k0 + 3 < kval ? sc * v.w : 0.f);
+                uint2 w;
+                w.x = *reinterpret_cast<uint32_t*>(&lo);
+                w.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(p.vt + ((size_t)(tile * CHUNKS_PER_TILE + ci) * p.tcap + tok0 + t) * CHUNK + k0) = w;
+            } else {
+                const int o0 = tile * BM + r0;
+                __nv_bfloat16* y = p.Y + (size_t)t * p.dout + o0;
+                if (p.dout % 4 == 0 && o0 + 4 <= p.dout) {
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+                    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+                    uint2 w;
+                    w.x = *reinterpret_cast<uint32_t*>(&lo);
+                    w.y = *reinterpret_cast<uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(y) = w;
+                } else {
+                    const float vv[4] = {v.x, v.y, v.z, v.w};
+                    for (int j = 0; j < 4; ++j)
+                        if (o0 + j < p.dout) y[j] = __float2bfloat16_rn(vv[j]);
+                }
             }
         };
 
@@ -333,19 +396,59 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     for (int j = 0; j < 16; ++j) v[j] = 0.f;
                 emit(t0, v);
             }
-        } else {
-            // partial tile layout [row][N] fp32: each thread stores and reloads its own
-            // contiguous row of N values with 16-byte accesses
-            const size_t tile_base = (size_t)ctr * p.splits * BM * p.N;
-            float* mine = p.partials + tile_base + ((size_t)split * BM + row) * p.N;
+        } else if (p.cluster) {
+            // Stage this split's partial tile [token][row] in its own shared memory (the
+            // ring is idle: every load has been consumed by the finished MMAs), then,
+            // after a cluster barrier, reduce one slice of tokens over the shared
+            // memory of all splits, summed in split order, and write it.
+            float* part_s = reinterpret_cast<float*>(smem);
             for (int t0 = 0; t0 < T; t0 += 16) {
                 float v[16];
                 if (have) tmem_ld16(tbase + t0, v);
                 else
                     for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                float4* dst = reinterpret_cast<float4*>(mine + t0);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                for (int j = 0; j < 16; ++j) part_s[(t0 + j) * BM + row] = v[j];
+            }
+            __syncwarp();
+            cluster_sync();
+            const int ts = (T + p.splits - 1) / p.splits;
+            const int t_lo = (int)cluster_rank() * ts;
+            const int t_hi = min(T, t_lo + ts);
+            const uint32_t part_a = smem_u32(part_s);
+            for (int g = threadIdx.x - 64; g < (t_hi - t_lo) * (BM / 4); g += 128) {
+                const int t = t_lo + g / (BM / 4), r0 = (g % (BM / 4)) * 4;
+                const uint32_t off = part_a + (uint32_t)((t * BM + r0) * 4);
+                float4 q4[MAX_CLUSTER];
+#pragma unroll
+                for (int sp = 0; sp < MAX_CLUSTER; ++sp)
+                    if (sp < p.splits) q4[sp] = ld_cluster_f4(map_cluster(off, (uint32_t)sp));
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sp = 0; sp < MAX_CLUSTER; ++sp)
+                    if (sp < p.splits) {
+                        acc.x += q4[sp].x;
+                        acc.y += q4[sp].y;
+                        acc.z += q4[sp].z;
+                        acc.w += q4[sp].w;
+                    }
+                emit4(t, r0, acc);
+            }
+            __syncwarp();
+            cluster_sync();   // no CTA leaves while the others still read its shared memory
+        } else {
+            // partial tile layout [split][token][row] fp32: for a fixed token the 128 rows
+            // of a tile are contiguous, so both the stores below and the reduction's
+            // loads are coalesced
+            const size_t tile_base = (size_t)ctr * p.splits * p.N * BM;
+            float* mine = p.partials + tile_base + (size_t)split * p.N * BM + row;
+            for (int t0 = 0; t0 < T; t0 += 16) {
+                float v[16];
+                if (have) tmem_ld16(tbase + t0, v);
+                else
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) mine[(size_t)(t0 + j) * BM] = v[j];
             }
             __threadfence();
             epi_bar();
@@ -361,32 +464,39 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             epi_bar();
             if (flags[1]) {
                 // last split of the tile: sum the partials in split order (independent of
-                // arrival order), the loads of several splits in flight together
-                const float* base = p.partials + tile_base + (size_t)row * p.N;
-                const size_t sstride = (size_t)BM * p.N;
-                for (int t0 = 0; t0 < T; t0 += 16) {
-                    float acc[16];
+                // arrival order).  The 128 epilogue threads sweep the tile as float4
+                // groups of 4 rows of one token; the loads of all splits are independent.
+                const float4* base = reinterpret_cast<const float4*>(p.partials + tile_base);
+                const int groups = T * (BM / 4);
+                const size_t sstride4 = (size_t)p.N * (BM / 4);
+                const int et = threadIdx.x - 64;
+                for (int g = et; g < groups; g += 128) {
+                    float4 q4[MAX_SPLITS];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-#pragma unroll 4
-                    for (int sp = 0; sp < p.splits; ++sp) {
-                        const float4* src = reinterpret_cast<const float4*>(base + sp * sstride + t0);
-                        float4 q4[4];
+                    for (int sp = 0; sp < MAX_SPLITS; ++sp)
+                        if (sp < p.splits) q4[sp] = __ldcg(base + sp * sstride4 + g);
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) q4[j] = __ldcg(src + j);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            acc[4 * j] += q4[j].x;
-                            acc[4 * j + 1] += q4[j].y;
-                            acc[4 * j + 2] += q4[j].z;
-                            acc[4 * j + 3] += q4[j].w;
+                    for (int sp = 0; sp < MAX_SPLITS; ++sp)
+                        if (sp < p.splits) {
+                            acc.x += q4[sp].x;
+                            acc.y += q4[sp].y;
+                            acc.z += q4[sp].z;
+                            acc.w += q4[sp].w;
                         }
-                    }
-                    emit(t0, acc);
+                    emit4(g / (BM / 4), (g % (BM / 4)) * 4, acc);
                 }
             }
         }
     }
+    if (warp < 2 && p.cluster && p.splits > 1) {   // the epilogue warps' two cluster barriers
+        __syncwarp();
+        cluster_sync();
+        cluster_sync();
+    }
+    // A block barrier needs converged warps: lanes that skipped a one-thread branch
+    // above (barrier set-up, the TMA and MMA roles) wait here for it first.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -421,12 +531,15 @@ int ring_stages(int N, int budget) {
     return ns;
 }
 
-// K splits so that row tiles x token tiles x splits fill the SMs once.
-int k_splits(int tiles, int kb_total) {
+// K splits so that row tiles x token tiles x splits fill the SMs once, with the
+// partial tiles the last split reads back (splits x N x 128 floats) bounded.
+int k_splits(int tiles, int kb_total, int N) {
     int s = sm_count() / (tiles > 0 ? tiles : 1);
-    if (s < 1) s = 1;
-    if (s > 16) s = 16;
+    const int cap = 1024 / (N > 0 ? N : 1);
+    if (s > cap) s = cap;
+    if (s > MAX_SPLITS) s = MAX_SPLITS;
     if (s > kb_total) s = kb_total;
+    if (s < 1) s = 1;
     return s;
 }
 
@@ -435,7 +548,8 @@ int k_splits(int tiles, int kb_total) {
 size_t smem_bytes(int stages, int N, int scratch_bytes = 0) {
     size_t ring = (size_t)stages * stage_bytes(N);
     if ((size_t)scratch_bytes > ring) ring = (size_t)scratch_bytes;
-    return 1024 + ring + (size_t)(2 * stages + 1) * 8 + (size_t)stages * 4 + 16 + 3 * CHUNKS_PER_TILE * 4;
+    return 1024 + ring + (size_t)(2 * stages + 1) * 8 + (size_t)stages * 4 + 16 + 4 * CHUNKS_PER_TILE * 4 +
+           MAX_N * 4 + 16;
 }
 
 int proj_tiles(const PoolDims& d) { return (d.dout + BM - 1) / BM; }
@@ -459,6 +573,12 @@ cudaError_t tc_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(swapab_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin - (int)fa.sharedSizeBytes);
+    // the same (largest) shared-memory carve-out for every kernel of a forward, so that
+    // consecutive kernels can share an SM without reconfiguring it
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(swapab_gemm_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(swapab_gemm_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess) e = prefill_init();
     return e;
 }
@@ -531,7 +651,8 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         g.T = T;
         g.N = Ns;
         g.kb_total = kb_total;
-        g.splits = k_splits(tiles * ztiles, kb_total);
+        g.splits = k_splits(tiles * ztiles, kb_total, Ns);
+        if (g.splits > 8) g.splits = 8;   // the shrink's K loop is short: fewer, longer splits
         g.stages = ring_stages(Ns, SHRINK_SMEM_BUDGET);
         g.tcap = d.tcap;
         g.pdl = 0;
@@ -540,13 +661,15 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         g.ws = a.ws;
         // segment scratch in the ring memory: as many row ranges as fit (at most one per warp)
         const int ring_ints = g.stages * stage_bytes(Ns) / 4;
-        g.segP = seg_warps_for(d.S, NUM_THREADS / 32, ring_ints, d.max_chunks, T);
+        g.seg_warp = T <= MAX_N && d.S <= 1024;   // decode-sized: one warp builds the segments
+        g.segP = g.seg_warp ? 1 : seg_warps_for(d.S, NUM_THREADS / 32, ring_ints, d.max_chunks, T);
         if (g.segP < 1) g.segP = 1;   // the ring grows to the scratch (many slots, long batches)
         g.scratch_bytes = 4 * seg::scratch_ints(d.S, g.segP, d.max_chunks, T);
         // first kernel of the forward: an ordinary launch (it may overwrite the workspace
         // the previous forward's kernels read)
+        g.cluster = g.splits > 1 && g.splits <= MAX_CLUSTER && Ns * BM * 4 <= g.stages * stage_bytes(Ns);
         e = launch_k(swapab_gemm_kernel<true>, dim3(tiles, g.splits, ztiles), dim3(NUM_THREADS),
-                     smem_bytes(g.stages, Ns, g.scratch_bytes), st, false, tmNone, tmXs, tmNone, a.maps.down, g);
+                     smem_bytes(g.stages, Ns, g.scratch_bytes), st, false, g.cluster ? g.splits : 1, tmNone, tmXs, tmNone, a.maps.down, g);
         if (e != cudaSuccess) return e;
     }
 
@@ -592,13 +715,15 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.N = N;
     p.kb_total = kb_total;
     p.ext_units = (ext_chunks + EXT_SUB - 1) / EXT_SUB;
-    p.splits = k_splits(tiles, kb_total);
+    p.splits = k_splits(tiles, kb_total, N);
     p.stages = ring_stages(N, PROJ_SMEM_BUDGET);
     p.tcap = d.tcap;
     p.pdl = shrink ? 1 : 0;
     if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
+    if (p.splits > MAX_CLUSTER && N * BM * 4 <= p.stages * stage_bytes(N)) p.splits = MAX_CLUSTER;
+    p.cluster = p.splits > 1 && N * BM * 4 <= p.stages * stage_bytes(N);
     e = launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p.stages, N), st,
-                 shrink && !a.ev_start, tmW, tmX, tmV, a.maps.up128, p);
+                 shrink && !a.ev_start, p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -637,15 +762,16 @@ cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din
     p.kb_total = kb_total;
     p.ext_units = 0;
     // as many K splits as fill the SMs and whose partial tiles fit the scratch
-    int splits = k_splits(tiles, kb_total);
+    int splits = k_splits(tiles, kb_total, N);
     const size_t per_split = (size_t)tiles * BM * N * sizeof(float);
     while (splits > 1 && (size_t)splits * per_split > partial_bytes) --splits;
     p.splits = splits;
     p.stages = ring_stages(N, PROJ_SMEM_BUDGET);
     p.tcap = 0;
     p.pdl = 0;
+    p.cluster = 0;   // the K splits meet through the given scratch
     return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p.stages, N),
-                    st, false, tmW, tmX, tmNone, tmNone, p);
+                    st, false, 1, tmW, tmX, tmNone, tmNone, p);
 }
 
 }  // namespace mlora

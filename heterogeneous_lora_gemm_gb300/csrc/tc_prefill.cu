@@ -92,6 +92,9 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // A block barrier needs converged warps: lanes that skipped a one-thread branch
+    // above (barrier set-up, the TMA and MMA roles) wait here for it first.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -239,6 +242,9 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tempty[buf])) : "memory");
         }
     }
+    // A block barrier needs converged warps: lanes that skipped a one-thread branch
+    // above (barrier set-up, the TMA and MMA roles) wait here for it first.
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -259,6 +265,8 @@ cudaError_t prefill_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     return e;
 }
 
@@ -281,7 +289,7 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
     const int total = p.m_tiles * p.n_tiles;
     const int grid = total < num_sms ? total : num_sms;
     const size_t smem = 1024 + (size_t)PSTAGES * PSTAGE + (2 * PSTAGES + 5) * 8 + PSTAGES * 4 + 16;
-    return launch_k(prefill_gemm_kernel, dim3(grid), dim3(P_THREADS), smem, st, after_shrink && !a.ev_start, tmX,
+    return launch_k(prefill_gemm_kernel, dim3(grid), dim3(P_THREADS), smem, st, after_shrink && !a.ev_start, 1, tmX,
                     tmW, tmV, a.maps.up256, p);
 }
 
