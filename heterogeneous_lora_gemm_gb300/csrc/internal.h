@@ -25,6 +25,17 @@ __host__ __device__ inline size_t up_index(int unit, int k, int o, int dout) {
     return ((size_t)(u >> 3) * dout + o) * 8 + (u & 7);
 }
 
+// One K-extension chunk of a loaded adapter: 16 rank columns (fewer in the last
+// chunk of a rank that is not a multiple of 16).  The pool keeps the chunks of all
+// loaded slots, in ascending slot order, in a device table that changes only on
+// load, unload and compaction.
+struct ChunkRec {
+    int32_t slot;
+    int32_t unit;    // arena rank unit of the chunk's first column (a multiple of 8)
+    int32_t kval;    // valid rank columns, 1..16
+    float scale;
+};
+
 // Bits of the device status word.
 enum : uint32_t { STATUS_BAD_ROW = 1u, STATUS_TIMEOUT = 2u };
 
@@ -42,9 +53,12 @@ struct Workspace {
     int32_t* chunk_unit;   // [max_chunks] arena rank unit of the chunk's first rank column
     int32_t* chunk_kval;   // [max_chunks] valid rank columns of the chunk (<= CHUNK)
     float* v32;            // [max_tokens x max_rank] scale * Down x per row (SIMT path)
-    uint16_t* vt;          // [max_chunks x tcap x CHUNK] bf16 scale * Down x, chunked (tensor path)
+    uint16_t* vt;          // [max_chunks x tcap x CHUNK] bf16 scale * Down x per loaded chunk (tensor path);
+                           // written for the (chunk, token tile) pairs tmask marks, read only there
     float* partials;       // split-K partial tiles
     int32_t* tile_ctr;     // split-K arrival counters (zero between forwards)
+    const ChunkRec* chunks;   // [max_chunks] chunks of the loaded slots (pool state, not per forward)
+    uint8_t* tmask;        // [token tiles of 256][max_chunks] 1 = a row of the token tile uses the chunk's slot
 };
 
 struct PoolDims {
@@ -56,9 +70,15 @@ void set_last_error(const std::string& msg);
 
 // ---- launchers (each returns the launch's cudaError_t) ----
 cudaError_t seg_init();   // raises the segment builder's shared memory cap (outside capture)
-// Row ranges (warps) the segment builder can use with `scratch_ints_avail` ints of
-// shared memory, at most `warps`; 0 if even one does not fit.
-int seg_warps_for(int S, int warps, int scratch_ints_avail, int max_chunks, int T);
+// Row ranges (warps, at most `warps`) the segment builder can use with
+// `scratch_ints_avail` ints of shared memory, and whether the row map is staged
+// there too; P = 0 if even one range does not fit.
+struct SegPlan {
+    int P;
+    bool stage_rows;
+    int ints;
+};
+SegPlan seg_plan(int S, int warps, int scratch_ints_avail, int T);
 cudaError_t launch_seg_build(const int32_t* row_adapter, int T, const SlotRec* slots,
                              const Workspace& ws, const PoolDims& d, cudaStream_t st);
 

@@ -87,8 +87,10 @@ struct mlora_pool {
     char* arena_down = nullptr;
     char* arena_up = nullptr;
     size_t arena_bytes = 0;
-    char* table_base = nullptr;      // slot table
+    char* table_base = nullptr;      // slot table, then the chunk table
     SlotRec* d_slots = nullptr;
+    ChunkRec* d_chunks = nullptr;    // chunks of the loaded slots, ascending slot (tensor path)
+    int n_chunks = 0;
     TcArenaMaps maps{};              // TMA descriptors of the whole arena (bf16 pools)
     size_t table_bytes = 0;
     char* ws_base = nullptr;
@@ -127,6 +129,30 @@ mlora_status push_slot(mlora_pool* p, int slot) {
     CU_TRY(cudaMemcpyAsync(p->d_slots + slot, &rec, sizeof rec, cudaMemcpyHostToDevice, p->copy_stream));
     // the staging object above lives on this stack frame: finish before returning
     CU_TRY(cudaStreamSynchronize(p->copy_stream));
+    return MLORA_OK;
+}
+
+// Rewrites the chunk table of the loaded slots after a load, unload or move (no
+// forward reads it meanwhile: every caller waited for the pool's last reader).
+mlora_status push_chunks(mlora_pool* p) {
+    std::vector<ChunkRec> host;
+    for (int s = 0; s < p->max_slots; ++s) {
+        const SlotHost& h = p->slots[s];
+        if (h.rank <= 0) continue;
+        for (int j = 0; j * CHUNK < h.rank; ++j) {
+            const int kv = h.rank - j * CHUNK;
+            host.push_back(ChunkRec{s, h.unit + j * CHUNK, kv < CHUNK ? kv : CHUNK, h.scale});
+        }
+    }
+    if ((int)host.size() > p->dims.max_chunks)
+        return fail(MLORA_ERR_CUDA, "chunk table overflow: %zu > %d", host.size(), p->dims.max_chunks);
+    p->n_chunks = (int)host.size();
+    if (!host.empty()) {
+        CU_TRY(cudaMemcpyAsync(p->d_chunks, host.data(), sizeof(ChunkRec) * host.size(), cudaMemcpyHostToDevice,
+                               p->copy_stream));
+        // the staging vector lives on this stack frame: finish before returning
+        CU_TRY(cudaStreamSynchronize(p->copy_stream));
+    }
     return MLORA_OK;
 }
 
@@ -228,14 +254,17 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     p->arena_down = p->arena_base;
     p->arena_up = p->arena_base + align_up((size_t)p->units * din * p->esize, 256);
 
-    // slot table and per-slot tensor maps (CUtensorMap must be 64-byte aligned)
+    // chunks of 16 rank columns: each slot's last chunk may be partial
+    const int max_chunks = p->units / CHUNK + max_slots + 1;
+    // slot table and chunk table
     const size_t slots_bytes = align_up(sizeof(SlotRec) * (size_t)(max_slots > 0 ? max_slots : 1), 128);
-    p->table_bytes = slots_bytes;
+    p->table_bytes = slots_bytes + align_up(sizeof(ChunkRec) * (size_t)max_chunks, 128);
     e = cudaMalloc((void**)&p->table_base, p->table_bytes);
     if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "slot table: %s", cudaGetErrorString(e)));
     e = cudaMemset(p->table_base, 0, p->table_bytes);
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemset(slot table)"));
     p->d_slots = (SlotRec*)p->table_base;
+    p->d_chunks = (ChunkRec*)(p->table_base + slots_bytes);
     if (dtype == MLORA_BF16 && p->units > 0 &&
         !tc_encode_arena_maps(&p->maps, p->arena_down, p->arena_up, p->units, din, dout))
         return bail(fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the adapter arena"));
@@ -247,7 +276,7 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     d.dout = dout;
     d.max_rank = max_rank;
     d.max_tokens = max_tokens;
-    d.max_chunks = p->units / CHUNK + max_slots + 1;
+    d.max_chunks = max_chunks;
     d.tcap = (max_tokens + 15) / 16 * 16;
     const TcWorkspaceNeeds tcn = tc_workspace_needs(dtype == MLORA_BF16, d);
     size_t off = 0;
@@ -268,6 +297,7 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     const size_t o_vt = carve(dtype == MLORA_BF16 ? (size_t)d.max_chunks * d.tcap * CHUNK * 2 : 0);
     const size_t o_part = carve(tcn.partial_bytes);
     const size_t o_ctr = carve(tcn.counter_bytes);
+    const size_t o_tmask = carve(tcn.tmask_bytes);
     p->ws_bytes = off;
     e = cudaMalloc((void**)&p->ws_base, p->ws_bytes);
     if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "workspace of %zu bytes: %s", p->ws_bytes, cudaGetErrorString(e)));
@@ -286,6 +316,8 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     w.vt = (uint16_t*)(p->ws_base + o_vt);
     w.partials = (float*)(p->ws_base + o_part);
     w.tile_ctr = (int32_t*)(p->ws_base + o_ctr);
+    w.chunks = p->d_chunks;
+    w.tmask = (uint8_t*)(p->ws_base + o_tmask);
 
     e = seg_init();
     if (e != cudaSuccess) return bail(cuda_fail(e, "seg_init"));
@@ -348,6 +380,8 @@ mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const void* down, cons
             st = push_slot(p, m.id);
             if (st != MLORA_OK) return st;
         }
+        st = push_chunks(p);
+        if (st != MLORA_OK) return st;
         unit = p->arena.alloc(slot, rank);
         if (unit < 0) return fail(MLORA_ERR_OOM, "arena placement failed after compaction");
     }
@@ -370,7 +404,9 @@ mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const void* down, cons
     h.unit = unit;
     h.version += 1;
     ++p->loaded;
-    return push_slot(p, slot);
+    st = push_slot(p, slot);
+    if (st != MLORA_OK) return st;
+    return push_chunks(p);
 }
 
 mlora_status mlora_unload_adapter(mlora_pool_t p, int slot) {
@@ -385,7 +421,9 @@ mlora_status mlora_unload_adapter(mlora_pool_t p, int slot) {
     p->arena.release(slot);
     h = SlotHost{0, 0, 0.f, -1, h.version + 1};
     --p->loaded;
-    return push_slot(p, slot);
+    st = push_slot(p, slot);
+    if (st != MLORA_OK) return st;
+    return push_chunks(p);
 }
 
 mlora_status mlora_adapter_version(mlora_pool_t p, int slot, uint64_t* version) {
@@ -408,12 +446,10 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
     cudaStream_t st = (cudaStream_t)stream;
     const bool lora = row_adapter != nullptr && p->max_slots > 0;
     const bool bf16 = p->dtype == MLORA_BF16;
-    int ext_chunk_cap = 0;
-    for (const SlotHost& h : p->slots) ext_chunk_cap += h.rank > 0 ? (h.rank + CHUNK - 1) / CHUNK : 0;
     const bool tc = bf16 && tc_supported(p->dims, T);
-    // the tensor-core shrink builds the segments in its own prologue; otherwise a
-    // separate segment kernel runs (fp32 path, or nothing loaded: only the status bit)
-    if (lora && (!tc || ext_chunk_cap == 0)) CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
+    // the tensor-core shrink builds the segments itself; otherwise a separate segment
+    // kernel runs (fp32 path, or nothing loaded: only the status bit)
+    if (lora && (!tc || p->n_chunks == 0)) CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
     cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
     if (!p->prof_start.empty()) {
         const size_t k = p->prof_next++ % p->prof_start.size();
@@ -433,7 +469,7 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
         a.arena_down = p->arena_down;
         a.ws = p->ws;
         a.dims = p->dims;
-        a.ext_chunk_cap = ext_chunk_cap;
+        a.n_chunks = p->n_chunks;
         a.ev_start = ev_start;
         a.ev_stop = ev_stop;
         CU_TRY(tc_forward(a, st));

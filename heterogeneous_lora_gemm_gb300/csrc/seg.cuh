@@ -1,17 +1,19 @@
-// Row -> adapter segment builder as a block-wide device function (ai-infra-kb "M031"
-// tutorial §02/§03; wiblog section on Punica's grouped matmul): group the rows of
-// a mixed batch by adapter slot, keep the original order inside each group (P, R
-// before Q in the page's example) and order groups by ascending slot id.
+// Row -> adapter segment builder as a device function over a group of threads
+// (ai-infra-kb "M031" tutorial §02/§03; wiblog section on Punica's grouped
+// matmul): group the rows of a mixed batch by adapter slot, keep the original
+// order inside each group (P, R before Q in the page's example) and order groups
+// by ascending slot id.
 //
-// Produced, bit-exactly:
+// Published to the workspace, bit-exactly:
 //   counts[S]      rows per slot
 //   offsets[S+1]   exclusive prefix sum of counts
 //   perm[T]        original row indices in segment order, -1 past the valid rows
 //   chunk table    the touched slots (count > 0) in ascending order, each split into
-//                  ceil(rank/16) chunks of 16 rank columns: the K-extension layout of
-//                  the tensor-core shrink and expand.  Per chunk: slot, absolute
-//                  rank-unit index in the arena (unit of the slot + first column)
-//                  and the number of valid rank columns (<= 16).
+//                  ceil(rank/16) chunks of 16 rank columns.  Per chunk: slot,
+//                  absolute rank-unit index in the arena (unit of the slot + first
+//                  column) and the number of valid rank columns (<= 16).
+//   meta           [0] valid rows, [1] chunks of the touched slots, [2] touched slots
+//   status         STATUS_BAD_ROW if a row names an invalid or empty slot
 //
 // Stable scatter without a sort: the rows are split into P contiguous ranges, one
 // per warp.  Pass 1 counts rows per (warp, slot) with __match_any_sync (one
@@ -21,42 +23,39 @@
 // slot plus the number of lower lanes with the same id in that step.  Ranges and
 // steps are in row order, so the result is the stable order.
 //
-// Everything is built in shared memory by one CTA; no CTA ever waits on another.
-// Used by the standalone segment kernel (seg.cu) and, redundantly in each CTA, by
-// the prologue of the tensor-core shrink (tc.cu), whose CTA (0,0,0) publishes.
+// The builder runs on one of three thread groups, all inside one CTA (no CTA
+// ever waits on another):
+//   GROUP_WARP   one warp; no block barrier
+//   GROUP_BLOCK  the whole block; __syncthreads
+//   GROUP_EPI    warps 2..5 of a 192-thread CTA; named barrier 2, so the
+//                tensor-core shrink runs it beside its TMA and MMA warps
 #pragma once
 #include "internal.h"
 
 namespace mlora {
 namespace seg {
 
+enum { GROUP_WARP = 0, GROUP_BLOCK = 1, GROUP_EPI = 2 };
+
 struct Scratch {
     int* rank_s;     // [S]
     int* unit_s;     // [S]
     int* scan;       // [S]
     int* cur;        // [P*S]
-    int* c_slot;     // [max_chunks]
-    int* c_unit;     // [max_chunks]
-    int* c_kval;     // [max_chunks]
     int* misc;       // [40]: warp_tmp[0..32], [33] bad row
-    int* ra_s;       // [T] the row map, staged once
+    int* ra_s;       // [T] the row map staged once, or nullptr (read from global memory)
 };
 
-__host__ __device__ inline int scratch_ints(int S, int P, int max_chunks, int T) {
-    return 3 * S + P * S + 3 * max_chunks + 40 + T;
-}
+__host__ __device__ inline int scratch_ints(int S, int P, int T_staged) { return 3 * S + P * S + 40 + T_staged; }
 
-__device__ inline Scratch carve(int* base, int S, int P, int max_chunks) {
+__device__ inline Scratch carve(int* base, int S, int P, bool stage_rows) {
     Scratch s;
     s.rank_s = base;
     s.unit_s = s.rank_s + S;
     s.scan = s.unit_s + S;
     s.cur = s.scan + S;
-    s.c_slot = s.cur + P * S;
-    s.c_unit = s.c_slot + max_chunks;
-    s.c_kval = s.c_unit + max_chunks;
-    s.misc = s.c_kval + max_chunks;
-    s.ra_s = s.misc + 40;
+    s.misc = s.cur + P * S;
+    s.ra_s = stage_rows ? s.misc + 40 : nullptr;
     return s;
 }
 
@@ -66,22 +65,29 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-// The builder runs either on the whole block (WARP = false; blockDim.x a multiple
-// of 32, at most 1024) or on one warp alone (WARP = true), which needs no block
-// barrier and lets the other warps of the CTA do their own set-up meanwhile.
-template <bool WARP>
-__device__ __forceinline__ void group_sync() {
-    if (WARP)
-        __syncwarp();
-    else
-        __syncthreads();
-}
+template <int G>
+struct Group {
+    __device__ static int size() { return G == GROUP_WARP ? 32 : (G == GROUP_EPI ? 128 : (int)blockDim.x); }
+    __device__ static int tid() {
+        return G == GROUP_WARP ? (int)(threadIdx.x & 31) : (G == GROUP_EPI ? (int)threadIdx.x - 64 : (int)threadIdx.x);
+    }
+    __device__ static int warp() { return tid() >> 5; }
+    __device__ static void sync() {
+        if (G == GROUP_WARP)
+            __syncwarp();
+        else if (G == GROUP_EPI)
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+        else
+            __syncthreads();
+    }
+};
 
 // Exclusive scan of n ints in shared memory, in place, by the group.  Returns the total.
-template <bool WARP>
+template <int G>
 __device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
-    const int nt = WARP ? 32 : blockDim.x, lane = threadIdx.x & 31;
-    const int tid = WARP ? lane : threadIdx.x, warp = WARP ? 0 : threadIdx.x >> 5, nwarps = nt >> 5;
+    using Gr = Group<G>;
+    const int nt = Gr::size(), lane = threadIdx.x & 31;
+    const int tid = Gr::tid(), warp = Gr::warp(), nwarps = nt >> 5;
     const int per = (n + nt - 1) / nt;
     const int lo = min(n, tid * per), hi = min(n, lo + per);
     int local = 0;
@@ -93,7 +99,7 @@ __device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
         if (lane >= d) incl += v;
     }
     if (lane == 31) warp_tmp[warp] = incl;
-    group_sync<WARP>();
+    Gr::sync();
     if (warp == 0) {
         const int w = lane < nwarps ? warp_tmp[lane] : 0;
         int wi = w;
@@ -105,7 +111,7 @@ __device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
         if (lane < nwarps) warp_tmp[lane] = wi - w;
         if (lane == 31) warp_tmp[32] = wi;
     }
-    group_sync<WARP>();
+    Gr::sync();
     int run = warp_tmp[warp] + incl - local;
     for (int i = lo; i < hi; ++i) {
         const int v = a[i];
@@ -113,22 +119,23 @@ __device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
         run += v;
     }
     const int total = warp_tmp[32];
-    group_sync<WARP>();
+    Gr::sync();
     return total;
 }
 
-// Builds the segments of row_adapter[0..T) over S slots in shared memory.  Every
-// thread of the group must call it (P = 1 for a single warp).  With `publish`, also
-// writes counts, offsets, perm, the chunk table, meta and the bad-row status bit to
-// the workspace.  Returns the number of chunks; the chunk table stays in sc.c_*.
-template <bool WARP>
-__device__ inline int build(const int32_t* __restrict__ row_adapter, int T, const SlotRec* __restrict__ slots,
-                            int S, int P, int max_chunks, const Scratch& sc, bool publish, const Workspace& ws) {
-    const int nt = WARP ? 32 : blockDim.x, lane = threadIdx.x & 31;
-    const int tid = WARP ? lane : threadIdx.x, warp = WARP ? 0 : threadIdx.x >> 5;
+// Builds the segments of row_adapter[0..T) over S slots in shared memory, with P
+// row ranges (at most the group's warps; warps past P only help with the scans),
+// and publishes them to the workspace.  Every thread of the group must call it.
+template <int G>
+__device__ inline void build(const int32_t* __restrict__ row_adapter, int T, const SlotRec* __restrict__ slots,
+                             int S, int P, int max_chunks, const Scratch& sc, const Workspace& ws) {
+    using Gr = Group<G>;
+    const int nt = Gr::size(), lane = threadIdx.x & 31;
+    const int tid = Gr::tid(), warp = Gr::warp();
     int* warp_tmp = sc.misc;
     // all global reads of the builder are issued here, together
-    for (int t = tid; t < T; t += nt) sc.ra_s[t] = row_adapter[t];
+    if (sc.ra_s)
+        for (int t = tid; t < T; t += nt) sc.ra_s[t] = row_adapter[t];
     for (int s = tid; s < S; s += nt) {
         const SlotRec r = slots[s];
         sc.rank_s[s] = r.rank;
@@ -136,41 +143,40 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
     }
     for (int i = tid; i < P * S; i += nt) sc.cur[i] = 0;
     if (tid == 0) sc.misc[33] = 0;
-    group_sync<WARP>();
+    Gr::sync();
+    const int32_t* ra = sc.ra_s ? sc.ra_s : row_adapter;
 
     // ---- pass 1: per (warp, slot) counts
-    const int t_lo = (int)((long long)warp * T / P);
-    const int t_hi = (int)((long long)(warp + 1) * T / P);
-    if (warp < P) {
-        for (int base = t_lo; base < t_hi; base += 32) {
-            const int t = base + lane;
-            int a = -1;
-            if (t < t_hi) {
-                a = sc.ra_s[t];
-                if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) {
-                    if (a != -1) sc.misc[33] = 1;
-                    a = -1;
-                }
+    const int t_lo = warp < P ? (int)((long long)warp * T / P) : 0;
+    const int t_hi = warp < P ? (int)((long long)(warp + 1) * T / P) : 0;
+    for (int base = t_lo; base < t_hi; base += 32) {
+        const int t = base + lane;
+        int a = -1;
+        if (t < t_hi) {
+            a = ra[t];
+            if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) {
+                if (a != -1) sc.misc[33] = 1;
+                a = -1;
             }
-            const unsigned grp = __match_any_sync(0xffffffffu, a);
-            if (a >= 0 && (grp & lanemask_lt()) == 0) sc.cur[warp * S + a] += __popc(grp);
-            __syncwarp();
         }
+        const unsigned grp = __match_any_sync(0xffffffffu, a);
+        if (a >= 0 && (grp & lanemask_lt()) == 0) sc.cur[warp * S + a] += __popc(grp);
+        __syncwarp();
     }
-    group_sync<WARP>();
+    Gr::sync();
 
     // ---- totals, offsets and per-warp cursors
     for (int s = tid; s < S; s += nt) {
         int tot = 0;
         for (int w = 0; w < P; ++w) tot += sc.cur[w * S + s];
         sc.scan[s] = tot;
-        if (publish) ws.counts[s] = tot;
+        ws.counts[s] = tot;
     }
-    group_sync<WARP>();
-    const int n_valid = group_exclusive_scan<WARP>(sc.scan, S, warp_tmp);
+    Gr::sync();
+    const int n_valid = group_exclusive_scan<G>(sc.scan, S, warp_tmp);
     for (int s = tid; s < S; s += nt) {
         const int off = sc.scan[s];
-        if (publish) ws.offsets[s] = off;
+        ws.offsets[s] = off;
         int run = off;
         for (int w = 0; w < P; ++w) {
             const int c = sc.cur[w * S + s];
@@ -178,43 +184,39 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
             run += c;
         }
     }
-    if (publish && tid == 0) ws.offsets[S] = n_valid;
-    group_sync<WARP>();
+    if (tid == 0) ws.offsets[S] = n_valid;
+    Gr::sync();
 
-    // ---- pass 2: stable scatter (only the publishing CTA needs the permutation)
-    if (publish) {
-        if (warp < P) {
-            for (int base = t_lo; base < t_hi; base += 32) {
-                const int t = base + lane;
-                int a = -1;
-                if (t < t_hi) {
-                    a = sc.ra_s[t];
-                    if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) a = -1;
-                }
-                const unsigned grp = __match_any_sync(0xffffffffu, a);
-                int pos = 0;
-                if (a >= 0) pos = sc.cur[warp * S + a] + __popc(grp & lanemask_lt());
-                __syncwarp();
-                if (a >= 0) {
-                    ws.perm[pos] = t;
-                    if ((grp & lanemask_lt()) == 0) sc.cur[warp * S + a] += __popc(grp);
-                }
-                __syncwarp();
-            }
+    // ---- pass 2: stable scatter
+    for (int base = t_lo; base < t_hi; base += 32) {
+        const int t = base + lane;
+        int a = -1;
+        if (t < t_hi) {
+            a = ra[t];
+            if (!(a >= 0 && a < S && sc.rank_s[a] > 0)) a = -1;
         }
-        for (int i = n_valid + tid; i < T; i += nt) ws.perm[i] = -1;
+        const unsigned grp = __match_any_sync(0xffffffffu, a);
+        int pos = 0;
+        if (a >= 0) pos = sc.cur[warp * S + a] + __popc(grp & lanemask_lt());
+        __syncwarp();
+        if (a >= 0) {
+            ws.perm[pos] = t;
+            if ((grp & lanemask_lt()) == 0) sc.cur[warp * S + a] += __popc(grp);
+        }
+        __syncwarp();
     }
-    group_sync<WARP>();
+    for (int i = n_valid + tid; i < T; i += nt) ws.perm[i] = -1;
+    Gr::sync();
 
-    // ---- chunks of the touched slots (non-empty segments: offsets[s+1] > offsets[s]),
-    // ascending slot id; cur[0..S) is reused for the per-slot chunk counts
+    // ---- chunks of the touched slots (non-empty segments), ascending slot id;
+    // cur[0..S) is reused for the per-slot chunk counts
     for (int s = tid; s < S; s += nt) {
         const int off = sc.scan[s];
         const int nxt = (s + 1 < S) ? sc.scan[s + 1] : n_valid;
         sc.cur[s] = (nxt > off) ? (sc.rank_s[s] + CHUNK - 1) / CHUNK : 0;
     }
-    group_sync<WARP>();
-    const int n_chunks_raw = group_exclusive_scan<WARP>(sc.cur, S, warp_tmp);
+    Gr::sync();
+    const int n_chunks_raw = group_exclusive_scan<G>(sc.cur, S, warp_tmp);
     const int n_chunks = min(n_chunks_raw, max_chunks);
     int touched = 0;
     for (int s = tid; s < S; s += nt) {
@@ -226,35 +228,27 @@ __device__ inline int build(const int32_t* __restrict__ row_adapter, int T, cons
             for (int j = 0; j < nc; ++j) {
                 const int c = sc.cur[s] + j;
                 if (c < max_chunks) {
-                    sc.c_slot[c] = s;
-                    sc.c_unit[c] = sc.unit_s[s] + j * CHUNK;
-                    sc.c_kval[c] = min(CHUNK, sc.rank_s[s] - j * CHUNK);
+                    ws.chunk_slot[c] = s;
+                    ws.chunk_unit[c] = sc.unit_s[s] + j * CHUNK;
+                    ws.chunk_kval[c] = min(CHUNK, sc.rank_s[s] - j * CHUNK);
                 }
             }
         }
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) touched += __shfl_xor_sync(0xffffffffu, touched, d);
-    group_sync<WARP>();   // warp_tmp reuse below
+    Gr::sync();   // warp_tmp reuse below
     if (lane == 0) warp_tmp[warp] = touched;
-    group_sync<WARP>();
-    if (publish) {
-        for (int c = tid; c < n_chunks; c += nt) {
-            ws.chunk_slot[c] = sc.c_slot[c];
-            ws.chunk_unit[c] = sc.c_unit[c];
-            ws.chunk_kval[c] = sc.c_kval[c];
-        }
-        if (tid == 0) {
-            int tt = 0;
-            for (int w = 0; w < (nt >> 5); ++w) tt += warp_tmp[w];
-            ws.meta[0] = n_valid;
-            ws.meta[1] = n_chunks;
-            ws.meta[2] = tt;
-            if (sc.misc[33]) atomicOr(ws.status, STATUS_BAD_ROW);
-        }
+    Gr::sync();
+    if (tid == 0) {
+        int tt = 0;
+        for (int w = 0; w < (nt >> 5); ++w) tt += warp_tmp[w];
+        ws.meta[0] = n_valid;
+        ws.meta[1] = n_chunks;
+        ws.meta[2] = tt;
+        if (sc.misc[33]) atomicOr(ws.status, STATUS_BAD_ROW);
     }
-    group_sync<WARP>();
-    return n_chunks;
+    Gr::sync();
 }
 
 }  // namespace seg

@@ -11,6 +11,7 @@ struct TcWorkspaceNeeds {
     bool need_v32;          // the SIMT shrink/expand path is still reachable for this pool
     size_t partial_bytes;   // split-K partial tiles
     size_t counter_bytes;   // split-K arrival counters
+    size_t tmask_bytes;     // per token tile of 256, one byte per chunk: the shrink computed it
 };
 TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d);
 
@@ -41,7 +42,7 @@ struct TcForwardArgs {
     const void* arena_down;
     Workspace ws;
     PoolDims dims;
-    int ext_chunk_cap;      // upper bound of K-extension chunks (sum over loaded slots)
+    int n_chunks;           // chunks of the loaded slots (entries of ws.chunks)
     cudaEvent_t ev_start;   // optional profiling events around the projection kernel
     cudaEvent_t ev_stop;
 };

@@ -7,9 +7,10 @@
 // ring, warp 1 issues the MMAs into one of two TMEM accumulators (2 x 256
 // columns), and warps 2-5 drain the other accumulator to bf16 Y while the next
 // tile is being multiplied.  As in the decode kernel, the K loop of every tile is
-// din columns of X W^T followed by the K-extension over the touched adapters'
+// din columns of X W^T followed by the K-extension over the loaded adapters'
 // chunks (ai-infra-kb "M031" §02), so each row's delta is added to its own output
-// row before the single rounding.
+// row before the single rounding.  A tile multiplies only the chunks the shrink
+// marked as used by its token tile (tmask); the others' Up tiles are not loaded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -35,11 +36,13 @@ constexpr int GROUP_M = 8;
 constexpr int EXT_SUB = 4;
 
 struct PrefillParams {
-    const int32_t* chunk_unit;
-    const int32_t* meta;
+    const ChunkRec* chunks;     // chunk table of the loaded slots
+    const uint8_t* tmask;       // [token tile of 256][max_chunks], from the shrink
     __nv_bfloat16* Y;
     uint32_t* status;
-    int T, dout, kb_total, m_tiles, n_tiles, lora, vec_store;
+    int T, dout, kb_total, m_tiles, n_tiles, vec_store;
+    int n_chunks, max_chunks;
+    int ext_steps;              // K-extension steps per tile (EXT_SUB chunks each), 0 without adapters
     int pdl;    // launched while the shrink may still run: wait before reading its outputs
 };
 
@@ -63,7 +66,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     uint64_t* tfull = empty + PSTAGES;     // [2] accumulator ready
     uint64_t* tempty = tfull + 2;          // [2] accumulator drained
     uint64_t* drain = tempty + 2;          // MMA completion on the give-up path
-    int* stage_kind = (int*)(drain + 1);   // -1 = din step, else valid chunks
+    int* stage_kind = (int*)(drain + 1);   // -1 = din step, else bit mask of the chunks loaded
     uint32_t* tmem_slot = (uint32_t*)(stage_kind + PSTAGES);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
@@ -99,29 +102,18 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // The number of K-extension steps comes from the segment builder; the producer
-    // and the MMA issuer read it only after their first tile's din steps (and,
-    // when launched early, after waiting for the kernels before).
-    int n_chunks = -1;
-    auto ext_steps_known = [&]() {
-        if (n_chunks < 0) {
-            if (p.pdl) pdl_wait();
-            n_chunks = p.lora ? p.meta[1] : 0;
-        }
-        return (n_chunks + EXT_SUB - 1) / EXT_SUB;
-    };
+    const int steps = p.kb_total + p.ext_steps;
 
     if (warp == 0 && lane == 0) {
         // ---------------- producer
         int s = 0;
         uint32_t ph = 0;
+        bool waited = false;
         int armed[PSTAGES] = {0, 0, 0, 0};
         for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
             int m, n;
             tile_coords(tile, p.m_tiles, p.n_tiles, m, n);
-            int steps = p.kb_total;
             for (int i = 0; i < steps; ++i) {
-                if (i == p.kb_total - 1) steps = p.kb_total + ext_steps_known();
                 if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
                 ++armed[s];
                 uint8_t* a = smem + (size_t)s * PSTAGE;
@@ -132,13 +124,33 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                     tma_2d(a, &tmX, &full[s], i * PK, m * PM);
                     tma_2d(b, &tmW, &full[s], i * PK, n * PN);
                 } else {
+                    if (!waited) {   // tmask and Vt come from the shrink
+                        if (p.pdl) pdl_wait();
+                        waited = true;
+                    }
                     const int c0 = (i - p.kb_total) * EXT_SUB;
-                    const int nv = min(EXT_SUB, n_chunks - c0);
-                    stage_kind[s] = nv;
-                    mbar_expect_tx(&full[s], (uint32_t)(PA_BYTES + nv * (PN * 32)));
-                    tma_3d(a, &tmV, &full[s], 0, m * PM, c0);
-                    for (int j = 0; j < nv; ++j)   // two blocks of 8 rank columns x 256 rows
-                        tma_3d(b + j * (PN * 32), &tmUp, &full[s], 0, n * PN, p.chunk_unit[c0 + j] >> 3);
+                    const uint8_t* tm = p.tmask + (size_t)(m * PM / 256) * p.max_chunks;
+                    int used[EXT_SUB], un[EXT_SUB];
+#pragma unroll
+                    for (int j = 0; j < EXT_SUB; ++j) {   // independent loads, then the mask
+                        const bool in = c0 + j < p.n_chunks;
+                        used[j] = in ? tm[c0 + j] : 0;
+                        un[j] = in ? p.chunks[c0 + j].unit : 0;
+                    }
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int j = 0; j < EXT_SUB; ++j)
+                        if (used[j]) mask |= 1u << j;
+                    stage_kind[s] = (int)mask;
+                    if (mask == 0) {
+                        mbar_expect_tx(&full[s], 0);
+                    } else {
+                        mbar_expect_tx(&full[s], (uint32_t)(PA_BYTES + __popc(mask) * (PN * 32)));
+                        tma_3d(a, &tmV, &full[s], 0, m * PM, c0);
+#pragma unroll
+                        for (int j = 0; j < EXT_SUB; ++j)   // two blocks of 8 rank columns x 256 rows
+                            if ((mask >> j) & 1u) tma_3d(b + j * (PN * 32), &tmUp, &full[s], 0, n * PN, un[j] >> 3);
+                    }
                 }
                 if (++s == PSTAGES) {
                     s = 0;
@@ -167,9 +179,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(buf * PN);
             uint32_t acc = 0;
-            int steps = p.kb_total;
             for (int i = 0; i < steps; ++i) {
-                if (i == p.kb_total - 1) steps = p.kb_total + ext_steps_known();
                 if (!mbar_wait(&full[s], ph, abort_flag, p.status)) break;
                 tc_fence_after();
                 const uint32_t a = smem_u32(smem + (size_t)s * PSTAGE);
@@ -184,11 +194,13 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                 } else {
                     // Vt chunk: 32-byte swizzle; Up chunk: [2 blocks of 8 columns][256 rows][16 B],
                     // no swizzle (K-direction core matrices PN*16 bytes apart, N-direction 128)
-                    for (int j = 0; j < kind; ++j) {
-                        mma_bf16(d, sdesc(a + j * (PM * 32), 256, SW32), sdesc_lbo(b + j * (PN * 32), PN * 16, 128, SW_NONE),
-                                 idesc, acc);
-                        acc = 1;
-                    }
+#pragma unroll
+                    for (int j = 0; j < EXT_SUB; ++j)
+                        if ((kind >> j) & 1) {
+                            mma_bf16(d, sdesc(a + j * (PM * 32), 256, SW32),
+                                     sdesc_lbo(b + j * (PN * 32), PN * 16, 128, SW_NONE), idesc, acc);
+                            acc = 1;
+                        }
                 }
                 mma_commit(&empty[s]);
                 if (++s == PSTAGES) {
@@ -274,8 +286,8 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
                            const CUtensorMap& tmV, int num_sms, bool after_shrink, cudaStream_t st) {
     const PoolDims& d = a.dims;
     PrefillParams p{};
-    p.chunk_unit = a.ws.chunk_unit;
-    p.meta = a.ws.meta;
+    p.chunks = a.ws.chunks;
+    p.tmask = a.ws.tmask;
     p.Y = (__nv_bfloat16*)a.Y;
     p.status = a.ws.status;
     p.T = a.T;
@@ -283,7 +295,9 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
     p.kb_total = (d.din + PK - 1) / PK;
     p.m_tiles = (a.T + PM - 1) / PM;
     p.n_tiles = (d.dout + PN - 1) / PN;
-    p.lora = a.lora ? 1 : 0;
+    p.n_chunks = a.lora ? a.n_chunks : 0;
+    p.max_chunks = d.max_chunks;
+    p.ext_steps = after_shrink ? (p.n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
     p.vec_store = (d.dout % 8 == 0) ? 1 : 0;
     p.pdl = after_shrink ? 1 : 0;
     const int total = p.m_tiles * p.n_tiles;

@@ -117,6 +117,29 @@ def test_ragged_shapes(T, din, dout, ranks, dtype):
     assert_within(run_layer(layer, pool), want_of(layer), dtype, f"ragged {T}x{din}x{dout}")
 
 
+def test_many_loaded_slots_few_used():
+    """300 loaded rank-16 slots, a batch that uses three of them: the shrink and the
+    expand skip the unused chunks, and one projection CTA holds more chunks (300,
+    din = 64 gives a single K split) than it keeps in shared memory."""
+    ra = np.random.default_rng(11).choice(np.array([3, 150, 299, -1], np.int32), size=64).astype(np.int32)
+    layer = wl.random_layer(11, T=64, din=64, dout=256, ranks=[16] * 300, row_adapter=ra)
+    pool = make_pool(layer)
+    check_segments(layer, pool)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "300 slots, 3 used")
+
+
+def test_prefill_runs_with_multichunk_ranks():
+    """Request-ordered runs over slots whose ranks span 1..4 chunks: every 256-token
+    tile of the shrink, and every 128-token tile of the projection, uses its own
+    subset of the chunks."""
+    runs = [(0, 180), (2, 90), (-1, 40), (4, 300), (1, 70), (3, 120), (0, 30)]
+    ra = np.concatenate([np.full(n, s, np.int32) for s, n in runs])
+    layer = wl.random_layer(12, T=int(ra.shape[0]), din=256, dout=512, ranks=[64, 8, 40, 16, 1], row_adapter=ra)
+    pool = make_pool(layer)
+    check_segments(layer, pool)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "prefill runs")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_all_rows_without_adapter_and_null_map(dtype):
     layer = wl.random_layer(3, T=33, din=64, dout=48, ranks=[16, 8], dtype=dtype,
