@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -91,6 +92,7 @@ struct mlora_pool {
     SlotRec* d_slots = nullptr;
     ChunkRec* d_chunks = nullptr;    // chunks of the loaded slots, ascending slot (tensor path)
     int n_chunks = 0;
+    int tile_span = 0;               // largest arena span of 8 consecutive chunks of the table
     TcArenaMaps maps{};              // TMA descriptors of the whole arena (bf16 pools)
     size_t table_bytes = 0;
     char* ws_base = nullptr;
@@ -134,6 +136,8 @@ mlora_status push_slot(mlora_pool* p, int slot) {
 
 // Rewrites the chunk table of the loaded slots after a load, unload or move (no
 // forward reads it meanwhile: every caller waited for the pool's last reader).
+// The table is in arena order, so that 8 consecutive chunks (one row tile of the
+// tensor-core shrink) usually lie in one window of at most 128 arena rows.
 mlora_status push_chunks(mlora_pool* p) {
     std::vector<ChunkRec> host;
     for (int s = 0; s < p->max_slots; ++s) {
@@ -144,9 +148,16 @@ mlora_status push_chunks(mlora_pool* p) {
             host.push_back(ChunkRec{s, h.unit + j * CHUNK, kv < CHUNK ? kv : CHUNK, h.scale});
         }
     }
+    std::sort(host.begin(), host.end(), [](const ChunkRec& x, const ChunkRec& y) { return x.unit < y.unit; });
     if ((int)host.size() > p->dims.max_chunks)
         return fail(MLORA_ERR_CUDA, "chunk table overflow: %zu > %d", host.size(), p->dims.max_chunks);
     p->n_chunks = (int)host.size();
+    p->tile_span = 0;
+    for (size_t t0 = 0; t0 < host.size(); t0 += 8) {
+        const size_t t1 = (t0 + 8 < host.size() ? t0 + 8 : host.size()) - 1;
+        const int span = host[t1].unit + CHUNK - host[t0].unit;
+        if (span > p->tile_span) p->tile_span = span;
+    }
     if (!host.empty()) {
         CU_TRY(cudaMemcpyAsync(p->d_chunks, host.data(), sizeof(ChunkRec) * host.size(), cudaMemcpyHostToDevice,
                                p->copy_stream));
@@ -470,6 +481,8 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
         a.ws = p->ws;
         a.dims = p->dims;
         a.n_chunks = p->n_chunks;
+        a.tile_span = p->tile_span;
+        a.units = p->units;
         a.ev_start = ev_start;
         a.ev_stop = ev_stop;
         CU_TRY(tc_forward(a, st));

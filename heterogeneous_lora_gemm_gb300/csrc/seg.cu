@@ -1,7 +1,7 @@
 // Standalone segment-builder kernel (one CTA of 1024 threads), used by
 // mlora_debug_segments, by the fp32 forward and by a bf16 forward with no adapter
-// loaded.  The bf16 forward otherwise runs the same builder (seg.cuh) inside its
-// tensor-core shrink.
+// loaded.  The bf16 forward otherwise runs the same builder (seg.cuh) in a CTA of
+// its tensor-core shrink's grid.
 #include "internal.h"
 #include "seg.cuh"
 
@@ -16,7 +16,7 @@ seg_build_kernel(const int32_t* __restrict__ row_adapter, int T, const SlotRec* 
                  int S, int P, int max_chunks, int stage_rows) {
     extern __shared__ int smem[];
     const seg::Scratch sc = seg::carve(smem, S, P, stage_rows != 0);
-    seg::build<seg::GROUP_BLOCK>(row_adapter, T, slots, S, P, max_chunks, sc, ws);
+    seg::build(row_adapter, T, slots, S, P, max_chunks, sc, ws);
 }
 
 }  // namespace

@@ -23,19 +23,13 @@
 // slot plus the number of lower lanes with the same id in that step.  Ranges and
 // steps are in row order, so the result is the stable order.
 //
-// The builder runs on one of three thread groups, all inside one CTA (no CTA
-// ever waits on another):
-//   GROUP_WARP   one warp; no block barrier
-//   GROUP_BLOCK  the whole block; __syncthreads
-//   GROUP_EPI    warps 2..5 of a 192-thread CTA; named barrier 2, so the
-//                tensor-core shrink runs it beside its TMA and MMA warps
+// The whole block of one CTA runs it (no CTA ever waits on another): the
+// standalone segment kernel, or a CTA of its own in the tensor-core shrink's grid.
 #pragma once
 #include "internal.h"
 
 namespace mlora {
 namespace seg {
-
-enum { GROUP_WARP = 0, GROUP_BLOCK = 1, GROUP_EPI = 2 };
 
 struct Scratch {
     int* rank_s;     // [S]
@@ -65,29 +59,10 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
-template <int G>
-struct Group {
-    __device__ static int size() { return G == GROUP_WARP ? 32 : (G == GROUP_EPI ? 128 : (int)blockDim.x); }
-    __device__ static int tid() {
-        return G == GROUP_WARP ? (int)(threadIdx.x & 31) : (G == GROUP_EPI ? (int)threadIdx.x - 64 : (int)threadIdx.x);
-    }
-    __device__ static int warp() { return tid() >> 5; }
-    __device__ static void sync() {
-        if (G == GROUP_WARP)
-            __syncwarp();
-        else if (G == GROUP_EPI)
-            asm volatile("bar.sync 2, 128;" ::: "memory");
-        else
-            __syncthreads();
-    }
-};
-
-// Exclusive scan of n ints in shared memory, in place, by the group.  Returns the total.
-template <int G>
-__device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
-    using Gr = Group<G>;
-    const int nt = Gr::size(), lane = threadIdx.x & 31;
-    const int tid = Gr::tid(), warp = Gr::warp(), nwarps = nt >> 5;
+// Exclusive scan of n ints in shared memory, in place, by the block.  Returns the total.
+__device__ inline int block_exclusive_scan(int* a, int n, int* warp_tmp) {
+    const int nt = blockDim.x, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = threadIdx.x >> 5, nwarps = nt >> 5;
     const int per = (n + nt - 1) / nt;
     const int lo = min(n, tid * per), hi = min(n, lo + per);
     int local = 0;
@@ -99,7 +74,7 @@ __device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
         if (lane >= d) incl += v;
     }
     if (lane == 31) warp_tmp[warp] = incl;
-    Gr::sync();
+    __syncthreads();
     if (warp == 0) {
         const int w = lane < nwarps ? warp_tmp[lane] : 0;
         int wi = w;
@@ -111,7 +86,7 @@ __device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
         if (lane < nwarps) warp_tmp[lane] = wi - w;
         if (lane == 31) warp_tmp[32] = wi;
     }
-    Gr::sync();
+    __syncthreads();
     int run = warp_tmp[warp] + incl - local;
     for (int i = lo; i < hi; ++i) {
         const int v = a[i];
@@ -119,19 +94,17 @@ __device__ inline int group_exclusive_scan(int* a, int n, int* warp_tmp) {
         run += v;
     }
     const int total = warp_tmp[32];
-    Gr::sync();
+    __syncthreads();
     return total;
 }
 
 // Builds the segments of row_adapter[0..T) over S slots in shared memory, with P
-// row ranges (at most the group's warps; warps past P only help with the scans),
-// and publishes them to the workspace.  Every thread of the group must call it.
-template <int G>
+// row ranges (at most the block's warps; warps past P only help with the scans),
+// and publishes them to the workspace.  Every thread of the block must call it.
 __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, const SlotRec* __restrict__ slots,
                              int S, int P, int max_chunks, const Scratch& sc, const Workspace& ws) {
-    using Gr = Group<G>;
-    const int nt = Gr::size(), lane = threadIdx.x & 31;
-    const int tid = Gr::tid(), warp = Gr::warp();
+    const int nt = blockDim.x, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = threadIdx.x >> 5;
     int* warp_tmp = sc.misc;
     // all global reads of the builder are issued here, together
     if (sc.ra_s)
@@ -143,7 +116,7 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
     }
     for (int i = tid; i < P * S; i += nt) sc.cur[i] = 0;
     if (tid == 0) sc.misc[33] = 0;
-    Gr::sync();
+    __syncthreads();
     const int32_t* ra = sc.ra_s ? sc.ra_s : row_adapter;
 
     // ---- pass 1: per (warp, slot) counts
@@ -163,7 +136,7 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
         if (a >= 0 && (grp & lanemask_lt()) == 0) sc.cur[warp * S + a] += __popc(grp);
         __syncwarp();
     }
-    Gr::sync();
+    __syncthreads();
 
     // ---- totals, offsets and per-warp cursors
     for (int s = tid; s < S; s += nt) {
@@ -172,8 +145,8 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
         sc.scan[s] = tot;
         ws.counts[s] = tot;
     }
-    Gr::sync();
-    const int n_valid = group_exclusive_scan<G>(sc.scan, S, warp_tmp);
+    __syncthreads();
+    const int n_valid = block_exclusive_scan(sc.scan, S, warp_tmp);
     for (int s = tid; s < S; s += nt) {
         const int off = sc.scan[s];
         ws.offsets[s] = off;
@@ -185,7 +158,7 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
         }
     }
     if (tid == 0) ws.offsets[S] = n_valid;
-    Gr::sync();
+    __syncthreads();
 
     // ---- pass 2: stable scatter
     for (int base = t_lo; base < t_hi; base += 32) {
@@ -206,7 +179,7 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
         __syncwarp();
     }
     for (int i = n_valid + tid; i < T; i += nt) ws.perm[i] = -1;
-    Gr::sync();
+    __syncthreads();
 
     // ---- chunks of the touched slots (non-empty segments), ascending slot id;
     // cur[0..S) is reused for the per-slot chunk counts
@@ -215,8 +188,8 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
         const int nxt = (s + 1 < S) ? sc.scan[s + 1] : n_valid;
         sc.cur[s] = (nxt > off) ? (sc.rank_s[s] + CHUNK - 1) / CHUNK : 0;
     }
-    Gr::sync();
-    const int n_chunks_raw = group_exclusive_scan<G>(sc.cur, S, warp_tmp);
+    __syncthreads();
+    const int n_chunks_raw = block_exclusive_scan(sc.cur, S, warp_tmp);
     const int n_chunks = min(n_chunks_raw, max_chunks);
     int touched = 0;
     for (int s = tid; s < S; s += nt) {
@@ -237,9 +210,9 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) touched += __shfl_xor_sync(0xffffffffu, touched, d);
-    Gr::sync();   // warp_tmp reuse below
+    __syncthreads();   // warp_tmp reuse below
     if (lane == 0) warp_tmp[warp] = touched;
-    Gr::sync();
+    __syncthreads();
     if (tid == 0) {
         int tt = 0;
         for (int w = 0; w < (nt >> 5); ++w) tt += warp_tmp[w];
@@ -248,7 +221,7 @@ __device__ inline void build(const int32_t* __restrict__ row_adapter, int T, con
         ws.meta[2] = tt;
         if (sc.misc[33]) atomicOr(ws.status, STATUS_BAD_ROW);
     }
-    Gr::sync();
+    __syncthreads();
 }
 
 }  // namespace seg

@@ -12,9 +12,9 @@
 // some token of its token tile uses, and marks them in tmask; Vt entries of the
 // other (chunk, token tile) pairs are never read.  The epilogue keeps the entry
 // of a token only if the token belongs to the chunk's adapter, scales it, rounds
-// it to bf16 and writes Vt[c][t][:], zero for every other token.  CTA (0,0,0)
-// also runs the segment builder (seg.cuh), in its epilogue warps while its MMAs
-// run, and publishes the segments.
+// it to bf16 and writes Vt[c][t][:], zero for every other token.  One more grid
+// column holds the segment builder (seg.cuh): its first CTA builds and publishes
+// the segments while the others multiply.
 //
 // Projection (T <= 256): rows = output features.  The K loop of a tile is the din
 // columns of W followed by a K-extension over the loaded adapters' chunks
@@ -108,9 +108,6 @@ constexpr int MAX_STAGES = 8;
 constexpr int EXT_CAP = 256;       // projection: K-extension chunks of a CTA kept in shared memory
 constexpr int MAX_SLOT_WORDS = 4096 / 32;
 
-// where the publishing shrink CTA builds the segments
-enum { SEG_NONE = 0, SEG_BEFORE = 1, SEG_BESIDE = 2 };
-
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
 
@@ -119,14 +116,17 @@ struct Tail {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
     uint64_t acc_full;
+    uint64_t info_ready;              // projection: the K-extension chunk info is in place
     int stage_kind[MAX_STAGES];       // -1 = din step, else bit mask of the K-extension chunks loaded
     uint32_t tmem_slot;
     int abort_flag;
     int flags[2];                     // [0] an MMA was issued, [1] last arrival (global reduction)
     int tile_chunks;                  // shrink: chunks of this row tile some token uses
+    int win_u0;                       // shrink: arena unit of the window's first row
     int my_c[CHUNKS_PER_TILE];        // shrink, per compacted chunk: index in the chunk table,
-    int my_slot[CHUNKS_PER_TILE];     //   slot, arena unit, valid rank columns, scale
+    int my_slot[CHUNKS_PER_TILE];     //   slot, arena unit,
     int my_unit[CHUNKS_PER_TILE];
+    int my_off[CHUNKS_PER_TILE];      //   first accumulator row, valid rank columns, scale
     int my_kval[CHUNKS_PER_TILE];
     float my_scale[CHUNKS_PER_TILE];
     int tile_ra[MAX_N];               // shrink: slot id of each token of the token tile
@@ -136,7 +136,7 @@ struct Tail {
 };
 
 struct GemmParams {
-    const ChunkRec* chunks;         // chunk table of the loaded slots
+    const ChunkRec* chunks;         // chunk table of the loaded slots (ascending arena unit)
     const int32_t* row_adapter;     // slot id per token
     const SlotRec* slots;           // shrink: slot table (segment builder)
     __nv_bfloat16* Y;               // projection output [T x dout]
@@ -145,22 +145,69 @@ struct GemmParams {
     float* partials;                // global reduction: [tile][split][N][BM]
     int32_t* tile_ctr;              // global reduction: [tile] arrival counters
     uint32_t* status;
-    int T, dout, N, kb_total, splits, stages, tcap;
+    int T, dout, N, splits, stages, tcap;
+    int kc;                         // K chunks of 64 columns per pipeline step
+    int ksteps;                     // pipeline steps over din (ceil(din / (64 kc)))
+    int a_sub;                      // bytes of the A operand per K chunk
+    int window;                     // shrink: A is one window of win_rows arena rows per K chunk
+    int win_rows;
     int n_chunks;                   // chunks in the table
     int ext_units;                  // projection: K-extension steps (EXT_SUB chunks each)
-    int a_bytes;                    // bytes of the A operand in a stage
-    int ring_bytes;                 // the stage ring; also the cluster reduction's staging space
+    int ring_bytes;                 // the stage ring; also the staging space of the reduction
     int tail_off;                   // offset of the Tail
-    int pdl;                        // launched while the shrink may still run: wait before reading Vt
+    int pdl;                        // projection: launched while the shrink may still run
     int cluster;                    // the K splits of a tile form a cluster (else: global reduction)
     int S, max_chunks;
-    int seg_mode, seg_P, seg_stage_rows, scratch_off;   // shrink: segment builder of CTA (0,0,0)
+    int seg_tile, seg_P, seg_stage_rows;   // shrink: grid column of the segment builder, its plan
     Workspace ws;
 };
 
+// Sum of one slice of the staged partial tiles: groups g in [et, ng) step 128 of 4
+// rows x 1 token, gpt groups per token, group i of a token at staged row row_of(i),
+// loaded from the shared memory of all NSP CTAs of the cluster (or, NSP = 1, of this
+// CTA), 8 float4 loads in flight per thread, summed in split order.
+template <int NSP, typename RowOf, typename Emit>
+__device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng, int gpt, int et, RowOf&& row_of,
+                                              Emit&& emit) {
+    constexpr int U = NSP >= 8 ? 1 : 8 / NSP;
+    for (int g0 = et; g0 < ng; g0 += 128 * U) {
+        float4 q[U][NSP];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int g = g0 + 128 * u;
+            if (g < ng) {
+                const int t = t_lo + g / gpt;
+                const uint32_t off = part_a + (uint32_t)((t * BM + row_of(g % gpt)) * 4);
+                if (NSP == 1) {
+                    q[u][0] = ld_shared_f4(off);
+                } else {
+#pragma unroll
+                    for (int sp = 0; sp < NSP; ++sp) q[u][sp] = ld_cluster_f4(map_cluster(off, (uint32_t)sp));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int g = g0 + 128 * u;
+            if (g < ng) {
+                float4 acc = q[u][0];
+#pragma unroll
+                for (int sp = 1; sp < NSP; ++sp) {
+                    acc.x += q[u][sp].x;
+                    acc.y += q[u][sp].y;
+                    acc.z += q[u][sp].z;
+                    acc.w += q[u][sp].w;
+                }
+                emit(t_lo + g / gpt, g % gpt, acc);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- the GEMM kernel
+// Two CTAs per SM: a shrink CTA and a projection CTA launched behind it share an SM.
 template <bool SHRINK>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 2)
 swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmArena,
                    GemmParams p) {
@@ -169,26 +216,31 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     Tail& tl = *reinterpret_cast<Tail*>(smem + p.tail_off);
     volatile int* abort_flag = &tl.abort_flag;
     const int NS = p.stages;
-    const int SB = p.a_bytes + b_bytes(p.N);
+    const int B_SUB = b_bytes(p.N);                  // bytes of the B operand per K chunk
+    const int A_STAGE = p.kc * p.a_sub;
+    const int SB = A_STAGE + p.kc * B_SUB;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
     const int tok0 = ztile * MAX_N;                  // first token of this token tile
     const int T = min(p.T - tok0, p.N);              // tokens in this tile
-    const bool publisher = SHRINK && (blockIdx.x | blockIdx.y | blockIdx.z) == 0;
 
     if (SHRINK) {
-        pdl_trigger();   // the projection may launch and stream W meanwhile
-        if (publisher && p.seg_mode == SEG_BEFORE) {
-            // too many slots or rows for scratch beside the ring: the whole CTA builds
-            // the segments in the ring memory before any load
-            const seg::Scratch sc = seg::carve(reinterpret_cast<int*>(smem), p.S, p.seg_P, p.seg_stage_rows != 0);
-            seg::build<seg::GROUP_BLOCK>(p.row_adapter, p.T, p.slots, p.S, p.seg_P, p.max_chunks, sc, p.ws);
+        if (tile == p.seg_tile) {
+            // the segment builder's column: its first CTA builds and publishes the
+            // segments (and the bad-row status), the others have nothing to do
+            pdl_wait();
+            pdl_trigger();
+            if (split == 0 && ztile == 0) {
+                const seg::Scratch sc = seg::carve(reinterpret_cast<int*>(smem), p.S, p.seg_P, p.seg_stage_rows != 0);
+                seg::build(p.row_adapter, p.T, p.slots, p.S, p.seg_P, p.max_chunks, sc, p.ws);
+            }
+            return;
         }
     }
 
-    const int kb0 = (int)((long long)split * p.kb_total / p.splits);
-    const int kb1 = (int)((long long)(split + 1) * p.kb_total / p.splits);
+    const int kb0 = (int)((long long)split * p.ksteps / p.splits);
+    const int kb1 = (int)((long long)(split + 1) * p.ksteps / p.splits);
     const int eu0 = SHRINK ? 0 : (int)((long long)split * p.ext_units / p.splits);
     const int eu1 = SHRINK ? 0 : (int)((long long)(split + 1) * p.ext_units / p.splits);
     const int n_steps = (kb1 - kb0) + (eu1 - eu0);
@@ -200,6 +252,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             mbar_init(&tl.empty[s], 1);
         }
         mbar_init(&tl.acc_full, 1);
+        mbar_init(&tl.info_ready, 1);
         tl.abort_flag = 0;
         tl.flags[0] = 0;
         tl.flags[1] = 0;
@@ -215,6 +268,15 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (SHRINK) {
+        // Launched while the stream's previous kernel may still run (it may produce X
+        // or the row map, or read the Vt this kernel overwrites): wait for it here,
+        // after the set-up, then let the projection launch and stream W meanwhile.
+        pdl_wait();
+        pdl_trigger();
+    } else {
+        pdl_trigger();   // the next forward's shrink may get resident and set up meanwhile
+    }
     if (warp == 2 && SHRINK) {
         // Which of this row tile's chunks does some token of the token tile use?  The
         // row ids and the chunk entries are read together; a chunk is needed if a
@@ -228,6 +290,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         ChunkRec cr{-2, 0, 0, 0.f};
         if (lane < CHUNKS_PER_TILE && cb + lane < p.n_chunks) cr = p.chunks[cb + lane];
+        // the table is in arena order: the window of the tile starts at its first chunk
+        const int u0 = __shfl_sync(0xffffffffu, cr.unit, 0);
         uint32_t m = 0;
 #pragma unroll
         for (int j = 0; j < CHUNKS_PER_TILE; ++j) {
@@ -247,16 +311,39 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             tl.my_c[k] = cb + lane;
             tl.my_slot[k] = cr.slot;
             tl.my_unit[k] = cr.unit;
+            tl.my_off[k] = p.window ? cr.unit - u0 : k * CHUNK;   // first accumulator row of the chunk
             tl.my_kval[k] = cr.kval;
             tl.my_scale[k] = cr.scale;
         }
-        if (lane == 0) tl.tile_chunks = __popc(m);
+        if (lane == 0) {
+            tl.tile_chunks = __popc(m);
+            tl.win_u0 = u0;
+        }
         if (split == 0 && lane < CHUNKS_PER_TILE && cb + lane < p.n_chunks)
             p.tmask[(size_t)ztile * p.max_chunks + cb + lane] = (uint8_t)((m >> lane) & 1u);
     }
+    // A block barrier needs converged warps: lanes that skipped a one-thread branch
+    // above (barrier set-up, the TMA and MMA roles) wait here for it first.
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tl.tmem_slot;
+    const int tile_chunks = SHRINK ? tl.tile_chunks : 0;
+    if (SHRINK && tile_chunks <= 0) {   // no token of the token tile uses a chunk of this row tile
+        if (warp == 1) {
+            __syncwarp();
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+        }
+        return;
+    }
+
     if (warp == 2 && !SHRINK && eu1 > eu0) {
-        // The slots the batch uses, then this CTA's K-extension chunks: the arena unit
-        // of each chunk whose slot is used, -1 for the others (never loaded).
+        // While the producer streams W: the slots the batch uses, then this CTA's
+        // K-extension chunks, the arena unit of each chunk whose slot is used and -1
+        // for the others (never loaded).  The producer waits for it at its first
+        // K-extension step.
         int av[MAX_N / 32];
 #pragma unroll
         for (int i = 0; i < MAX_N / 32; ++i) {
@@ -286,29 +373,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const int sl = tl.ext_slot[k];
             if (sl < 0 || !((tl.slot_bits[sl >> 5] >> (sl & 31)) & 1u)) tl.ext_unit[k] = -1;
         }
-    }
-    // A block barrier needs converged warps: lanes that skipped a one-thread branch
-    // above (barrier set-up, the TMA and MMA roles) wait here for it first.
-    __syncwarp();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tl.tmem_slot;
-    const int tile_chunks = SHRINK ? tl.tile_chunks : 0;
-    const bool seg_here = publisher && p.seg_mode == SEG_BESIDE;
-    auto run_seg = [&]() {   // warps 2..5 of the publishing CTA, beside the TMA and MMA warps
-        const seg::Scratch sc =
-            seg::carve(reinterpret_cast<int*>(smem + p.scratch_off), p.S, p.seg_P, p.seg_stage_rows != 0);
-        seg::build<seg::GROUP_EPI>(p.row_adapter, p.T, p.slots, p.S, p.seg_P, p.max_chunks, sc, p.ws);
-    };
-    if (SHRINK && tile_chunks <= 0) {   // no token of the token tile uses a chunk of this row tile
-        if (seg_here && warp >= 2) run_seg();
-        if (warp == 1) {
-            __syncwarp();
-            tc_fence_after();
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
-        }
-        return;
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(&tl.info_ready, 0);
     }
 
     if (warp == 0 && lane == 0) {
@@ -316,19 +382,26 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         int s = 0;
         uint32_t ph = 0;
         bool waited = false;
-        int armed[MAX_STAGES] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int i = 0; i < n_steps; ++i) {
+        int issued = 0;   // steps whose loads went out
+        for (; issued < n_steps; ++issued) {
+            const int i = issued;
             if (!mbar_wait(&tl.empty[s], ph ^ 1, abort_flag, p.status)) break;
-            ++armed[s];
             uint8_t* a = smem + (size_t)s * SB;
-            uint8_t* b = a + p.a_bytes;
+            uint8_t* b = a + A_STAGE;
             const int kb = kb0 + i;
             if (SHRINK) {
                 tl.stage_kind[s] = -1;
-                mbar_expect_tx(&tl.full[s], (uint32_t)(tile_chunks * CHUNK_BYTES + b_bytes(p.N)));
-                for (int j = 0; j < tile_chunks; ++j)
-                    tma_2d(a + j * CHUNK_BYTES, &tmArena, &tl.full[s], kb * BK, tl.my_unit[j]);
-                tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
+                if (p.window) {
+                    // one box each: win_rows arena rows x kc K chunks of Down, N tokens x kc K chunks of X
+                    mbar_expect_tx(&tl.full[s], (uint32_t)SB);
+                    tma_3d(a, &tmArena, &tl.full[s], 0, tl.win_u0, kb * p.kc);
+                    tma_3d(b, &tmX, &tl.full[s], 0, tok0, kb * p.kc);
+                } else {
+                    mbar_expect_tx(&tl.full[s], (uint32_t)(tile_chunks * CHUNK_BYTES + B_SUB));
+                    for (int j = 0; j < tile_chunks; ++j)
+                        tma_2d(a + j * CHUNK_BYTES, &tmArena, &tl.full[s], kb * BK, tl.my_unit[j]);
+                    tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
+                }
             } else if (kb < kb1) {
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)SB);
@@ -337,6 +410,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             } else {
                 const int u = eu0 + (kb - kb1);
                 const int kx = (u - eu0) * EXT_SUB;
+                if (u == eu0 && !mbar_wait(&tl.info_ready, 0, abort_flag, p.status)) break;
                 int un[EXT_SUB];
                 uint32_t mask = 0;
 #pragma unroll
@@ -366,10 +440,10 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         if ((mask >> j) & 1u)
                             tma_3d(a + j * (BM * 32), &tmArena, &tl.full[s], 0, tile * BM, un[j] >> 3);
                     if (!waited) {
-                        if (p.pdl) pdl_wait();
+                        if (p.pdl) pdl_wait();   // Vt comes from the shrink
                         waited = true;
                     }
-                    mbar_expect_tx(&tl.full[s], (uint32_t)b_bytes(p.N));
+                    mbar_expect_tx(&tl.full[s], (uint32_t)B_SUB);
                     tma_3d(b, &tmV, &tl.full[s], 0, 0, u * EXT_SUB);
                 }
             }
@@ -379,11 +453,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
         }
         if (*abort_flag) {
-            // let loads already issued land before the CTA's shared memory goes away
-            for (int j = 0; j < NS; ++j) {
-                if (armed[j] == 0) continue;
+            // let loads already issued land before the CTA's shared memory goes away:
+            // step i filled stage i % NS in its phase (i / NS) & 1
+            for (int j = 0; j < NS && j < issued; ++j) {
+                const int fills = (issued - 1 - j) / NS + 1;
                 const long long t0 = clock64();
-                while (!mbar_try_wait(&tl.full[j], (uint32_t)((armed[j] - 1) & 1)) && clock64() - t0 < 200000000ll) {
+                while (!mbar_try_wait(&tl.full[j], (uint32_t)((fills - 1) & 1)) && clock64() - t0 < 200000000ll) {
                 }
             }
         }
@@ -397,15 +472,19 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (!mbar_wait(&tl.full[s], ph, abort_flag, p.status)) break;
             tc_fence_after();
             const uint32_t a = smem_u32(smem + (size_t)s * SB);
-            const uint32_t b = a + p.a_bytes;
+            const uint32_t b = a + A_STAGE;
             const int kind = tl.stage_kind[s];
             if (kind < 0) {
-                // A spans 128 rows (16 KiB) from a; in the shrink, rows past the loaded
-                // chunks hold whatever lies there and give accumulator rows nobody reads
+                // each K chunk: A spans 128 rows (16 KiB) from its sub-block; in the shrink,
+                // rows past the loaded ones hold whatever lies there and give accumulator
+                // rows nobody reads
+                for (int kc = 0; kc < p.kc; ++kc) {
+                    const uint32_t ak = a + kc * p.a_sub, bk = b + kc * B_SUB;
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    mma_bf16(tmem, sdesc(a + k * 32, 1024, SW128), sdesc(b + k * 32, 1024, SW128), idesc, acc);
-                    acc = 1;
+                    for (int k = 0; k < BK / 16; ++k) {
+                        mma_bf16(tmem, sdesc(ak + k * 32, 1024, SW128), sdesc(bk + k * 32, 1024, SW128), idesc, acc);
+                        acc = 1;
+                    }
                 }
             } else {
                 // Up chunk: [2 blocks of 8 columns][128 rows][16 B], no swizzle (K-direction core
@@ -432,7 +511,6 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
         }
     } else if (warp >= 2) {
-        if (seg_here) run_seg();   // the segment build overlaps this CTA's loads and MMAs
         // ---------------- epilogue: TMEM -> partial tile, or the final values
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;          // row of the tile
@@ -442,117 +520,36 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const bool have = __all_sync(0xffffffffu, ok) && tl.flags[0] != 0;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
 
-        // final write of 16 consecutive tokens t0..t0+15 of this row
-        int c_slot = -1, c_idx = 0;
-        float c_scale = 0.f;
-        if (SHRINK && (row / CHUNK) < tile_chunks) {
-            const int k = row / CHUNK;
-            c_idx = tl.my_c[k];
-            c_slot = tl.my_slot[k];
-            // rank columns past the adapter's rank belong to the next adapter in the arena
-            c_scale = (row % CHUNK) < tl.my_kval[k] ? tl.my_scale[k] : 0.f;
-        }
-        const int o = tile * BM + row;
-        auto emit = [&](int t0, const float* v) {
-            if (SHRINK) {
-                if (c_slot < 0) return;
-                __nv_bfloat16* dst = p.vt + ((size_t)c_idx * p.tcap + tok0) * CHUNK + (row % CHUNK);
-                for (int j = 0; j < 16 && t0 + j < T; ++j) {
-                    const bool mine = tl.tile_ra[t0 + j] == c_slot;
-                    dst[(size_t)(t0 + j) * CHUNK] = __float2bfloat16_rn(mine ? c_scale * v[j] : 0.f);
-                }
-            } else if (o < p.dout) {
-                for (int j = 0; j < 16 && t0 + j < T; ++j)
-                    p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
-            }
-        };
-
-        // final write of rows r0..r0+3 (a multiple of 4) of token t
+        // projection: final write of rows r0..r0+3 (a multiple of 4) of token t
         auto emit4 = [&](int t, int r0, const float4& v) {
-            if (SHRINK) {
-                const int k = r0 / CHUNK;
-                if (k >= tile_chunks) return;
-                const int kval = tl.my_kval[k];
-                const int k0 = r0 % CHUNK;
-                const float sc = tl.tile_ra[t] == tl.my_slot[k] ? tl.my_scale[k] : 0.f;
-                __nv_bfloat162 lo = __floats2bfloat162_rn(k0 < kval ? sc * v.x : 0.f, k0 + 1 < kval ? sc * v.y : 0.f);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(k0 + 2 < kval ? sc * v.z : 0.f, k0 + 3 < kval ? sc * v.w : 0.f);
+            const int o0 = tile * BM + r0;
+            __nv_bfloat16* y = p.Y + (size_t)t * p.dout + o0;
+            if (p.dout % 4 == 0 && o0 + 4 <= p.dout) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
                 uint2 w;
                 w.x = *reinterpret_cast<uint32_t*>(&lo);
                 w.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(p.vt + ((size_t)tl.my_c[k] * p.tcap + tok0 + t) * CHUNK + k0) = w;
+                *reinterpret_cast<uint2*>(y) = w;
             } else {
-                const int o0 = tile * BM + r0;
-                __nv_bfloat16* y = p.Y + (size_t)t * p.dout + o0;
-                if (p.dout % 4 == 0 && o0 + 4 <= p.dout) {
-                    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-                    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-                    uint2 w;
-                    w.x = *reinterpret_cast<uint32_t*>(&lo);
-                    w.y = *reinterpret_cast<uint32_t*>(&hi);
-                    *reinterpret_cast<uint2*>(y) = w;
-                } else {
-                    const float vv[4] = {v.x, v.y, v.z, v.w};
-                    for (int j = 0; j < 4; ++j)
-                        if (o0 + j < p.dout) y[j] = __float2bfloat16_rn(vv[j]);
-                }
+                const float vv[4] = {v.x, v.y, v.z, v.w};
+                for (int j = 0; j < 4; ++j)
+                    if (o0 + j < p.dout) y[j] = __float2bfloat16_rn(vv[j]);
             }
         };
 
-        if (p.splits == 1) {
+        if (!SHRINK && p.splits == 1) {
+            const int o = tile * BM + row;
             for (int t0 = 0; t0 < T; t0 += 16) {
                 float v[16];
                 if (have) tmem_ld16(tbase + t0, v);
                 else
                     for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                emit(t0, v);
+                if (o < p.dout)
+                    for (int j = 0; j < 16 && t0 + j < T; ++j)
+                        p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
             }
-        } else if (p.cluster) {
-            // Stage this split's partial tile [token][row] in its own shared memory (the
-            // ring is idle: every load has been consumed by the finished MMAs), then,
-            // after a cluster barrier, reduce one slice of tokens over the shared
-            // memory of all splits, summed in split order, and write it.  Passes of
-            // tp tokens when the whole tile does not fit the ring.
-            float* part_s = reinterpret_cast<float*>(smem);
-            const uint32_t part_a = smem_u32(part_s);
-            const int tp = min(p.N, (p.ring_bytes / (BM * 4)) & ~15);
-            for (int p0 = 0; p0 < T; p0 += tp) {
-                const int pt = min(tp, T - p0);
-                for (int t0 = 0; t0 < pt; t0 += 16) {
-                    float v[16];
-                    if (have) tmem_ld16(tbase + p0 + t0, v);
-                    else
-                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) part_s[(t0 + j) * BM + row] = v[j];
-                }
-                __syncwarp();
-                cluster_sync();
-                const int ts = (pt + p.splits - 1) / p.splits;
-                const int t_lo = (int)cluster_rank() * ts;
-                const int t_hi = min(pt, t_lo + ts);
-                for (int g = threadIdx.x - 64; g < (t_hi - t_lo) * (BM / 4); g += 128) {
-                    const int t = t_lo + g / (BM / 4), r0 = (g % (BM / 4)) * 4;
-                    const uint32_t off = part_a + (uint32_t)((t * BM + r0) * 4);
-                    float4 q4[MAX_CLUSTER];
-#pragma unroll
-                    for (int sp = 0; sp < MAX_CLUSTER; ++sp)
-                        if (sp < p.splits) q4[sp] = ld_cluster_f4(map_cluster(off, (uint32_t)sp));
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int sp = 0; sp < MAX_CLUSTER; ++sp)
-                        if (sp < p.splits) {
-                            acc.x += q4[sp].x;
-                            acc.y += q4[sp].y;
-                            acc.z += q4[sp].z;
-                            acc.w += q4[sp].w;
-                        }
-                    emit4(p0 + t, r0, acc);
-                }
-                __syncwarp();
-                cluster_sync();   // no CTA refills or leaves while the others still read its shared memory
-            }
-        } else {
+        } else if (!SHRINK && !p.cluster) {
             // partial tile layout [split][token][row] fp32: for a fixed token the 128 rows
             // of a tile are contiguous, so both the stores below and the reduction's
             // loads are coalesced
@@ -604,6 +601,68 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     emit4(g / (BM / 4), (g % (BM / 4)) * 4, acc);
                 }
             }
+        } else {
+            // Staged reduction: each split stages its partial tile [token][row] in its
+            // own shared memory (the ring is idle: every load has been consumed by the
+            // finished MMAs), then, after a barrier (over the cluster when the splits
+            // form one), sums one slice of tokens over the shared memory of all splits,
+            // in split order, and writes it.  Passes of tp tokens when the whole tile
+            // does not fit the ring.  The shrink stages only the rows of its window
+            // (or of its chunks) and writes each used chunk's 16 columns of Vt, in
+            // groups of 4: the row's value for this chunk's own rank columns (scaled,
+            // for the tokens of the chunk's adapter), zero elsewhere.
+            float* part_s = reinterpret_cast<float*>(smem);
+            const uint32_t part_a = smem_u32(part_s);
+            const bool multi = p.splits > 1;
+            const int tp = min(p.N, (p.ring_bytes / (BM * 4)) & ~15);
+            const int rows = SHRINK ? (p.window ? p.win_rows : tile_chunks * CHUNK) : BM;
+            const int gpt = SHRINK ? tile_chunks * 4 : BM / 4;   // groups of 4 rows per token
+            auto row_of = [&](int gi) { return SHRINK ? tl.my_off[gi >> 2] + (gi & 3) * 4 : gi * 4; };
+            for (int p0 = 0; p0 < T; p0 += tp) {
+                const int pt = min(tp, T - p0);
+                if (q * 32 < rows)
+                    for (int t0 = 0; t0 < pt; t0 += 16) {
+                        float v[16];
+                        if (have) tmem_ld16(tbase + p0 + t0, v);
+                        else
+                            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) part_s[(t0 + j) * BM + row] = v[j];
+                    }
+                __syncwarp();
+                if (multi) cluster_sync();
+                else epi_bar();
+                const int ts = (pt + p.splits - 1) / p.splits;
+                const int t_lo = multi ? (int)cluster_rank() * ts : 0;
+                const int t_hi = min(pt, t_lo + ts);
+                const int ng = t_hi > t_lo ? (t_hi - t_lo) * gpt : 0;
+                auto emit_g = [&](int t, int gi, const float4& v) {
+                    if (SHRINK) {
+                        const int k = gi >> 2, j0 = (gi & 3) * 4;
+                        const int kval = tl.my_kval[k];
+                        const float sc = tl.tile_ra[p0 + t] == tl.my_slot[k] ? tl.my_scale[k] : 0.f;
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(j0 < kval ? sc * v.x : 0.f,
+                                                                  j0 + 1 < kval ? sc * v.y : 0.f);
+                        __nv_bfloat162 hi = __floats2bfloat162_rn(j0 + 2 < kval ? sc * v.z : 0.f,
+                                                                  j0 + 3 < kval ? sc * v.w : 0.f);
+                        uint2 w;
+                        w.x = *reinterpret_cast<uint32_t*>(&lo);
+                        w.y = *reinterpret_cast<uint32_t*>(&hi);
+                        *reinterpret_cast<uint2*>(p.vt + ((size_t)tl.my_c[k] * p.tcap + tok0 + p0 + t) * CHUNK + j0) = w;
+                    } else {
+                        emit4(p0 + t, gi * 4, v);
+                    }
+                };
+                const int et = threadIdx.x - 64;
+                if (p.splits == 1) staged_reduce<1>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
+                else if (p.splits == 2) staged_reduce<2>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
+                else if (p.splits == 4) staged_reduce<4>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
+                else staged_reduce<8>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
+                __syncwarp();
+                // no CTA refills or leaves while the others still read its shared memory
+                if (multi) cluster_sync();
+                else epi_bar();
+            }
         }
     }
     if (warp < 2 && p.cluster && p.splits > 1) {   // the epilogue warps' cluster barriers, two per pass
@@ -653,12 +712,12 @@ int cluster_splits(int s) {
     return c;
 }
 
-// K splits so that row tiles x token tiles x splits fill the SMs once, with the
-// partial tiles of a tile (splits x N x 128 floats) bounded.
-int k_splits(int tiles, int kb_total, int N) {
+// K splits so that row tiles x token tiles x splits fill the SMs once; through
+// global memory, with the partial tiles of a tile (splits x N x 128 floats) bounded.
+int k_splits(int tiles, int kb_total, int N, bool global_reduction) {
     int s = sm_count() / (tiles > 0 ? tiles : 1);
     const int cap = 1024 / (N > 0 ? N : 1);
-    if (s > cap) s = cap;
+    if (global_reduction && s > cap) s = cap;
     if (s > MAX_SPLITS) s = MAX_SPLITS;
     if (s > kb_total) s = kb_total;
     if (s < 1) s = 1;
@@ -757,12 +816,8 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     // ---- shrink: Vt = masked scale * Down_chunks X^T, per token tile, the used chunks
     if (shrink) {
         const int Ns = decode ? (T + 15) / 16 * 16 : MAX_N;
-        CUtensorMap tmXs, tmNone;
+        CUtensorMap tmXs, tmNone, tmDown;
         std::memset(&tmNone, 0, sizeof tmNone);
-        cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)T};
-        cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
-        cuuint32_t box[2] = {BK, (cuuint32_t)Ns};
-        if (!tc_encode(&tmXs, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         const int tiles = (n_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
         const int ztiles = token_tiles(T);
         GemmParams g{};
@@ -776,42 +831,71 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         g.status = a.ws.status;
         g.T = T;
         g.N = Ns;
-        g.kb_total = kb_total;
         g.tcap = d.tcap;
         g.n_chunks = n_chunks;
         g.S = d.S;
         g.max_chunks = d.max_chunks;
         g.ws = a.ws;
-        // A holds the chunks of one row tile: fewer than 8 when fewer are loaded
-        g.a_bytes = (n_chunks < CHUNKS_PER_TILE ? n_chunks : CHUNKS_PER_TILE) * CHUNK_BYTES;
-        const int sb = g.a_bytes + b_bytes(Ns);
-        g.splits = cluster_splits(k_splits(tiles * ztiles, kb_total, Ns));
-        g.stages = clamp_stages(SHRINK_SMEM_BUDGET / sb);
-        // the MMA reads 128 rows of A from every stage: slack after the last one
-        g.ring_bytes = g.stages * sb + (A_BYTES - g.a_bytes);
-        // segment builder of CTA (0,0,0): scratch beside the ring, built by the epilogue
-        // warps while the loads run, if it fits; else by the whole CTA before its loads
-        const int room = max_dyn_smem() - 1024 - (int)sizeof(Tail) - 16 - g.ring_bytes;
-        SegPlan sp = seg_plan(d.S, 4, room > 0 ? room / 4 : 0, T);
-        size_t scratch = 0;
-        if (sp.P >= 1) {
-            g.seg_mode = SEG_BESIDE;
-            scratch = align16((size_t)sp.ints * 4);
+        // Window mode: the chunks of a row tile (8 consecutive entries of the table, in
+        // arena order) lie within win_rows <= 128 arena rows, so one box of win_rows
+        // rows x kc K chunks loads them all; X comes as one box of Ns tokens x kc K
+        // chunks.  Both views need din % 64 == 0.  Otherwise every chunk is a box of
+        // its own, one K chunk per step.
+        g.window = (d.din % BK == 0 && a.tile_span <= BM) ? 1 : 0;
+        if (g.window) {
+            int R = 16;
+            while (R < a.tile_span) R *= 2;
+            g.win_rows = R;
+            g.a_sub = R * BK * 2;
+            const int per = g.a_sub + b_bytes(Ns);
+            g.kc = SHRINK_SMEM_BUDGET / (2 * per);
+            g.kc = g.kc < 1 ? 1 : (g.kc > 4 ? 4 : g.kc);
+            cuuint64_t dims[3] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)kb_total};
+            cuuint64_t strides[2] = {(cuuint64_t)d.din * 2, (cuuint64_t)BK * 2};
+            cuuint32_t box[3] = {BK, (cuuint32_t)Ns, (cuuint32_t)g.kc};
+            if (!tc_encode(&tmXs, a.X, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+            cuuint64_t ddims[3] = {(cuuint64_t)BK, (cuuint64_t)a.units, (cuuint64_t)kb_total};
+            cuuint32_t dbox[3] = {BK, (cuuint32_t)R, (cuuint32_t)g.kc};
+            if (!tc_encode(&tmDown, a.arena_down, 3, ddims, strides, dbox, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
         } else {
-            sp = seg_plan(d.S, NUM_THREADS / 32, (max_dyn_smem() - 1024 - (int)sizeof(Tail) - 16) / 4, T);
-            if (sp.P < 1) return cudaErrorInvalidConfiguration;
-            g.seg_mode = SEG_BEFORE;
-            if ((size_t)g.ring_bytes < (size_t)sp.ints * 4) g.ring_bytes = (int)align16((size_t)sp.ints * 4);
+            g.kc = 1;
+            // A holds the chunks of one row tile: fewer than 8 when fewer are loaded
+            g.a_sub = (n_chunks < CHUNKS_PER_TILE ? n_chunks : CHUNKS_PER_TILE) * CHUNK_BYTES;
+            cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)T};
+            cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
+            cuuint32_t box[2] = {BK, (cuuint32_t)Ns};
+            if (!tc_encode(&tmXs, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+            tmDown = a.maps.down;
         }
+        g.ksteps = (kb_total + g.kc - 1) / g.kc;
+        const int sb = g.kc * (g.a_sub + b_bytes(Ns));
+        g.splits = cluster_splits(k_splits(tiles * ztiles, g.ksteps, Ns, false));
+        g.stages = clamp_stages(SHRINK_SMEM_BUDGET / sb);
+        // the MMA reads 128 rows of A from each K chunk's sub-block: slack after the ring
+        const int slack = A_BYTES - g.a_sub - b_bytes(Ns) * g.kc;
+        g.ring_bytes = g.stages * sb + (slack > 0 ? slack : 0);
+        g.tail_off = g.ring_bytes;
+        // the segment builder's CTA (grid column `tiles`) uses the same shared memory:
+        // as many row ranges as fit it, or more memory for every CTA if none does
+        const int have_ints = (int)((size_t)g.ring_bytes + sizeof(Tail)) / 4;
+        SegPlan sp = seg_plan(d.S, NUM_THREADS / 32, have_ints, T);
+        if (sp.P < 1) {
+            sp = seg_plan(d.S, NUM_THREADS / 32, (max_dyn_smem() - 1024) / 4, T);
+            if (sp.P < 1) return cudaErrorInvalidConfiguration;
+            g.ring_bytes = (int)align16((size_t)sp.ints * 4);
+            g.tail_off = g.ring_bytes;
+        }
+        g.seg_tile = tiles;
         g.seg_P = sp.P;
         g.seg_stage_rows = sp.stage_rows ? 1 : 0;
-        g.scratch_off = g.ring_bytes;
-        g.tail_off = (int)align16((size_t)g.ring_bytes + scratch);
         g.cluster = g.splits > 1 ? 1 : 0;
-        // first kernel of the forward: an ordinary launch (it overwrites the Vt the
-        // previous forward's projection read)
-        e = launch_k(swapab_gemm_kernel<true>, dim3(tiles, g.splits, ztiles), dim3(NUM_THREADS), smem_bytes(g), st,
-                     false, g.cluster ? g.splits : 1, tmNone, tmXs, tmNone, a.maps.down, g);
+        // first kernel of the forward: it may launch while the stream's previous kernel
+        // runs, and waits for it before reading X or the row map
+        e = launch_k(swapab_gemm_kernel<true>, dim3(tiles + 1, g.splits, ztiles), dim3(NUM_THREADS), smem_bytes(g),
+                     st, true, g.cluster ? g.splits : 1, tmNone, tmXs, tmNone, tmDown, g);
         if (e != cudaSuccess) return e;
     }
 
@@ -854,12 +938,13 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.T = T;
     p.dout = d.dout;
     p.N = N;
-    p.kb_total = kb_total;
+    p.kc = 1;
+    p.ksteps = kb_total;
     p.n_chunks = n_chunks;
     p.ext_units = shrink ? (n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
-    p.splits = cluster_splits(k_splits(tiles, kb_total, N));
+    p.splits = cluster_splits(k_splits(tiles, kb_total, N, false));
     p.stages = clamp_stages(PROJ_SMEM_BUDGET / stage_bytes(N));
-    p.a_bytes = A_BYTES;
+    p.a_sub = A_BYTES;
     p.ring_bytes = p.stages * stage_bytes(N);
     p.tail_off = p.ring_bytes;
     p.tcap = d.tcap;
@@ -905,15 +990,16 @@ cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din
     p.T = T;
     p.dout = dout;
     p.N = N;
-    p.kb_total = kb_total;
+    p.kc = 1;
+    p.ksteps = kb_total;
     p.ext_units = 0;
     // as many K splits as fill the SMs and whose partial tiles fit the scratch
-    int splits = k_splits(tiles, kb_total, N);
+    int splits = k_splits(tiles, kb_total, N, true);
     const size_t per_split = (size_t)tiles * BM * N * sizeof(float);
     while (splits > 1 && (size_t)splits * per_split > partial_bytes) --splits;
     p.splits = splits;
     p.stages = clamp_stages(PROJ_SMEM_BUDGET / stage_bytes(N));
-    p.a_bytes = A_BYTES;
+    p.a_sub = A_BYTES;
     p.ring_bytes = p.stages * stage_bytes(N);
     p.tail_off = p.ring_bytes;
     p.tcap = 0;

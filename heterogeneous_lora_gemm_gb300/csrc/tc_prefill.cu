@@ -103,6 +103,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int steps = p.kb_total + p.ext_steps;
+    pdl_trigger();   // the next forward's shrink may get resident and set up meanwhile
 
     if (warp == 0 && lane == 0) {
         // ---------------- producer

@@ -128,6 +128,17 @@ def test_many_loaded_slots_few_used():
     assert_within(run_layer(layer, pool), want_of(layer), "bf16", "300 slots, 3 used")
 
 
+def test_arena_holes_use_one_box_per_chunk():
+    """Slots 1..8 unloaded leave a hole of 128 rank rows between slots 0 and 9: their
+    chunks no longer fit one 128-row window, so the shrink loads each chunk alone."""
+    ra = np.random.default_rng(13).choice(np.array([0, 9, -1], np.int32), size=48).astype(np.int32)
+    layer = wl.random_layer(13, T=48, din=256, dout=192, ranks=[16] * 10, row_adapter=ra)
+    pool = make_pool(layer)
+    for slot in range(1, 9):
+        pool.unload(slot)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "arena holes")
+
+
 def test_prefill_runs_with_multichunk_ranks():
     """Request-ordered runs over slots whose ranks span 1..4 chunks: every 256-token
     tile of the shrink, and every 128-token tile of the projection, uses its own
