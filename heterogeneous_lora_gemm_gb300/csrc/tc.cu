@@ -107,6 +107,8 @@ constexpr int MAX_CLUSTER = 8;     // K splits of a tile reduced inside one (por
 constexpr int MAX_STAGES = 8;
 constexpr int EXT_CAP = 256;       // projection: K-extension chunks of a CTA kept in shared memory
 constexpr int MAX_SLOT_WORDS = 4096 / 32;
+constexpr int EXT_LEAD = 3;        // projection: K-extension steps go in this many steps before the end
+constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
@@ -117,6 +119,7 @@ struct Tail {
     uint64_t empty[MAX_STAGES];
     uint64_t acc_full;
     uint64_t info_ready;              // projection: the K-extension chunk info is in place
+    uint64_t rx_bar;                  // projection, push reduction: all splits' slices have landed
     int stage_kind[MAX_STAGES];       // -1 = din step, else bit mask of the K-extension chunks loaded
     uint32_t tmem_slot;
     int abort_flag;
@@ -157,6 +160,8 @@ struct GemmParams {
     int tail_off;                   // offset of the Tail
     int pdl;                        // projection: launched while the shrink may still run
     int cluster;                    // the K splits of a tile form a cluster (else: global reduction)
+    int push;                       // projection: the splits push their partial slices (st.async)
+    int rx_off;                     // push: offset of the receive buffer [split][BM][N / splits] fp32
     int S, max_chunks;
     int seg_tile, seg_P, seg_stage_rows;   // shrink: grid column of the segment builder, its plan
     Workspace ws;
@@ -253,10 +258,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         mbar_init(&tl.acc_full, 1);
         mbar_init(&tl.info_ready, 1);
+        mbar_init(&tl.rx_bar, 1);
         tl.abort_flag = 0;
         tl.flags[0] = 0;
         tl.flags[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!SHRINK && p.push) mbar_expect_tx(&tl.rx_bar, (uint32_t)(BM * p.N * 4));   // every split's slice
         if (!SHRINK) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
         if (SHRINK || p.ext_units > 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmArena) : "memory");
@@ -330,6 +337,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = tl.tmem_slot;
     const int tile_chunks = SHRINK ? tl.tile_chunks : 0;
+    // push reduction: this CTA's receive barrier is set up (the epilogues wait for all;
+    // the mbarrier-init fence above orders it)
+    if (!SHRINK && p.push) cluster_arrive_relaxed();
     if (SHRINK && tile_chunks <= 0) {   // no token of the token tile uses a chunk of this row tile
         if (warp == 1) {
             __syncwarp();
@@ -388,7 +398,11 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (!mbar_wait(&tl.empty[s], ph ^ 1, abort_flag, p.status)) break;
             uint8_t* a = smem + (size_t)s * SB;
             uint8_t* b = a + A_STAGE;
-            const int kb = kb0 + i;
+            // din steps, with the K-extension steps placed EXT_LEAD steps before the end
+            // so that their Vt loads overlap the last W tiles
+            const int ne = eu1 - eu0, ins = max(0, (kb1 - kb0) - EXT_LEAD);
+            const bool ext = i >= ins && i < ins + ne;
+            const int kb = kb0 + (i < ins ? i : i - ne);
             if (SHRINK) {
                 tl.stage_kind[s] = -1;
                 if (p.window) {
@@ -402,13 +416,13 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         tma_2d(a + j * CHUNK_BYTES, &tmArena, &tl.full[s], kb * BK, tl.my_unit[j]);
                     tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
                 }
-            } else if (kb < kb1) {
+            } else if (!ext) {
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)SB);
                 tma_2d(a, &tmW, &tl.full[s], kb * BK, tile * BM);
                 tma_2d(b, &tmX, &tl.full[s], kb * BK, 0);
             } else {
-                const int u = eu0 + (kb - kb1);
+                const int u = eu0 + (i - ins);
                 const int kx = (u - eu0) * EXT_SUB;
                 if (u == eu0 && !mbar_wait(&tl.info_ready, 0, abort_flag, p.status)) break;
                 int un[EXT_SUB];
@@ -549,6 +563,52 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     for (int j = 0; j < 16 && t0 + j < T; ++j)
                         p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
             }
+        } else if (!SHRINK && p.push) {
+            // Push reduction.  Stage this split's partial tile [token][row] in its idle
+            // ring: the tokens of split j's slice are then one contiguous block, which
+            // one bulk copy sends into CTA j's receive buffer [src][token][row],
+            // signalling j's receive barrier.  Each CTA then sums its own slice over the
+            // sources in split order and writes it.  A second cluster barrier keeps
+            // every CTA alive until all the copies out of its shared memory have landed.
+            const int ts = p.N / p.splits;
+            const uint32_t me = cluster_rank();
+            float* part_s = reinterpret_cast<float*>(smem);
+            for (int t0 = 0; t0 < p.N; t0 += 16) {
+                float v[16];
+                if (have) tmem_ld16(tbase + t0, v);
+                else
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) part_s[(t0 + j) * BM + row] = v[j];
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            epi_bar();
+            cluster_wait();   // every CTA of the cluster has set up its receive barrier
+            const uint32_t rx_a = smem_u32(smem + p.rx_off);
+            const uint32_t slice = (uint32_t)(ts * BM * 4);
+            if (threadIdx.x == 64)
+                for (int j = 0; j < p.splits; ++j)
+                    bulk_s2s(map_cluster(rx_a + me * slice, (uint32_t)j), smem_u32(part_s) + (uint32_t)j * slice, slice,
+                             map_cluster(smem_u32(&tl.rx_bar), (uint32_t)j));
+            mbar_wait(&tl.rx_bar, 0, abort_flag, p.status);
+            __syncwarp();
+            cluster_arrive();   // every copy into this CTA has landed
+            const int et = threadIdx.x - 64;
+            for (int g = et; g < ts * (BM / 4); g += 128) {
+                const int t = g / (BM / 4), r0 = (g % (BM / 4)) * 4;
+                float4 acc = ld_shared_f4(rx_a + (uint32_t)((t * BM + r0) * 4));
+                for (int src = 1; src < p.splits; ++src) {
+                    const float4 q4 = ld_shared_f4(rx_a + src * slice + (uint32_t)((t * BM + r0) * 4));
+                    acc.x += q4.x;
+                    acc.y += q4.y;
+                    acc.z += q4.z;
+                    acc.w += q4.w;
+                }
+                if ((int)me * ts + t < T) emit4((int)me * ts + t, r0, acc);
+            }
+            __syncwarp();
+            cluster_wait();   // ... and into every other CTA: the copies out of this one are done
         } else if (!SHRINK && !p.cluster) {
             // partial tile layout [split][token][row] fp32: for a fixed token the 128 rows
             // of a tile are contiguous, so both the stores below and the reduction's
@@ -665,7 +725,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
         }
     }
-    if (warp < 2 && p.cluster && p.splits > 1) {   // the epilogue warps' cluster barriers, two per pass
+    if (warp < 2 && !SHRINK && p.push) {   // the epilogue warps' two split cluster barriers
+        __syncwarp();
+        cluster_wait();
+        cluster_arrive();
+        cluster_wait();
+    } else if (warp < 2 && p.cluster && p.splits > 1) {   // the epilogue warps' cluster barriers, two per pass
         __syncwarp();
         const int tp = min(p.N, (p.ring_bytes / (BM * 4)) & ~15);
         for (int p0 = 0; p0 < T; p0 += tp) {
@@ -943,10 +1008,14 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.n_chunks = n_chunks;
     p.ext_units = shrink ? (n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
     p.splits = cluster_splits(k_splits(tiles, kb_total, N, false));
-    p.stages = clamp_stages(PROJ_SMEM_BUDGET / stage_bytes(N));
+    // small batches: the splits push their partial slices into a receive buffer
+    p.push = (p.splits > 1 && N <= PUSH_MAX_N && N % p.splits == 0) ? 1 : 0;
+    const int rx_bytes = p.push ? BM * N * 4 : 0;
+    p.stages = clamp_stages((PROJ_SMEM_BUDGET - rx_bytes) / stage_bytes(N));
     p.a_sub = A_BYTES;
     p.ring_bytes = p.stages * stage_bytes(N);
-    p.tail_off = p.ring_bytes;
+    p.rx_off = p.ring_bytes;
+    p.tail_off = p.ring_bytes + rx_bytes;
     p.tcap = d.tcap;
     p.pdl = shrink ? 1 : 0;
     p.cluster = p.splits > 1 ? 1 : 0;

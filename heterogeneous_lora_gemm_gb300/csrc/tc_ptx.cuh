@@ -162,6 +162,25 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
     return v;
 }
 
+// Split cluster barrier: arrive early, wait where the other CTAs' state is needed.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory into
+// another CTA's, signalling the transaction bytes on the destination's mbarrier.
+// Shared-memory writes of the generic proxy must be fenced (fence_proxy_async_smem)
+// before the copy reads them.
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_caddr, uint32_t src_saddr, uint32_t bytes, uint32_t cbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_caddr),
+                 "r"(src_saddr), "r"(bytes), "r"(cbar)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t saddr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
