@@ -275,11 +275,15 @@ def run_ours(args, dist, rank, local):
         for i in range(max(args.warmup, 3) * per_step_items):
             fwd(items[i % n_items])
     torch.cuda.synchronize(dev)
+    # at least 256 forwards per replay, so that the gap between two graph launches
+    # is spread over many steps
+    passes = max(1, -(-256 // n_items))
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        for it in items:
-            fwd(it)
-    steps_per_replay = n_items // per_step_items
+        for _ in range(passes):
+            for it in items:
+                fwd(it)
+    steps_per_replay = passes * n_items // per_step_items
     replays, rest = divmod(args.steps, steps_per_replay)
     with torch.cuda.stream(stream):      # a graph replays on the current stream
         graph.replay()
@@ -294,18 +298,16 @@ def run_ours(args, dist, rank, local):
             for _ in range(replays):
                 graph.replay()
             for i in range(rest * per_step_items):
-                fwd(items[i])
+                fwd(items[i % n_items])
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         barrier(dist)
         elapsed = ev0.elapsed_time(ev1) / 1e3
         clocks = clk.summary(elapsed)
-    launches_per_item = 0
-    for it in items[:1]:
-        L = it["layer"]
-        lora = L.max_slots > 0
-        launches_per_item = (1 if lora else 0) + (1 if lora else 0) + 1
-    gpu_launches = args.steps * per_step_items * launches_per_item
+    # a forward is one projection launch, plus the shrink (which also builds the
+    # segments) when its pool has adapter slots (every workload here loads them all)
+    launches = [2 if it["layer"].max_slots > 0 else 1 for it in items]
+    gpu_launches = args.steps * sum(launches[:per_step_items])
     tokens_rank = args.steps * tokens_per_item[0]
     job_elapsed, job_tokens = reduce_job(dist, elapsed, tokens_rank)
 
@@ -351,12 +353,14 @@ def run_ours(args, dist, rank, local):
         torch.cuda.synchronize(dev)
         barrier(dist)
         torch.cuda.synchronize(dev)
+        # this graph holds one pass over the copies
+        e_replays, e_rest = divmod(args.steps, n_items // per_step_items)
         ev0.record(stream)
         with torch.cuda.stream(stream):
-            for _ in range(replays):
+            for _ in range(e_replays):
                 egraph.replay()
-            for i in range(rest * per_step_items):
-                it, h = items[i], hosts[i]
+            for i in range(e_rest * per_step_items):
+                it, h = items[i % n_items], hosts[i % n_items]
                 it["X"].copy_(h["X"], non_blocking=True)
                 it["ra"].copy_(h["ra"], non_blocking=True)
                 fwd(it)
@@ -420,7 +424,7 @@ def run_ours(args, dist, rank, local):
         "config": {"workload": args.workload, "T": L0.T, "din": L0.din, "dout": L0.dout,
                    "adapters_touched": w0["touched"], "rank_touched_sum": w0["r_touched"],
                    "l2": f"inputs rotate over {copies} device copies (working set > 2x L2 of {l2 >> 20} MiB), no flush",
-                   "replay": f"CUDA graph of {n_items} forwards", "parallelism": f"replicas x{args.gpus}",
+                   "replay": f"CUDA graph of {passes * n_items} forwards", "parallelism": f"replicas x{args.gpus}",
                    "seed": args.seed},
         "roofline": roof,
         "step_roofline": {"frac": step_roof_s / step_s, "bytes": int(layer_step_bytes), "flops": int(layer_flops)},
