@@ -107,8 +107,9 @@ constexpr int MAX_CLUSTER = 8;     // K splits of a tile reduced inside one (por
 constexpr int MAX_STAGES = 8;
 constexpr int EXT_CAP = 256;       // projection: K-extension chunks of a CTA kept in shared memory
 constexpr int MAX_SLOT_WORDS = 4096 / 32;
-constexpr int EXT_LEAD = 3;        // projection: K-extension steps go in this many steps before the end
+constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
 constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
+constexpr int PROJ_KC = 2;         // projection: K chunks of 64 per pipeline step (one 3D box each for W and X)
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
@@ -160,7 +161,10 @@ struct GemmParams {
     int tail_off;                   // offset of the Tail
     int pdl;                        // projection: launched while the shrink may still run
     int cluster;                    // the K splits of a tile form a cluster (else: global reduction)
-    int push;                       // projection: the splits push their partial slices (st.async)
+    int push;                       // projection: the splits push their partial slices (bulk copies)
+    int ext_lead;                   // projection: pipeline steps after the K-extension steps
+    int xwait;                      // projection without shrink: launched early, griddepcontrol.wait
+                                    // before reading X (W of the first stages goes out before)
     int rx_off;                     // push: offset of the receive buffer [split][BM][N / splits] fp32
     int S, max_chunks;
     int seg_tile, seg_P, seg_stage_rows;   // shrink: grid column of the segment builder, its plan
@@ -393,6 +397,28 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         uint32_t ph = 0;
         bool waited = false;
         int issued = 0;   // steps whose loads went out
+        if (!SHRINK && p.xwait) {
+            // Launched while the kernel before may still run (it may produce X): the W
+            // tiles of the first stages go out now, their X tiles once it has completed.
+            const int pre = min(NS, max(0, (kb1 - kb0) - p.ext_lead));
+            for (int i = 0; i < pre; ++i) {
+                uint8_t* a = smem + (size_t)i * SB;
+                tl.stage_kind[i] = -1;
+                mbar_expect_tx_only(&tl.full[i], (uint32_t)A_STAGE);
+                if (p.kc > 1) tma_3d(a, &tmW, &tl.full[i], 0, tile * BM, (kb0 + i) * p.kc);
+                else tma_2d(a, &tmW, &tl.full[i], (kb0 + i) * BK, tile * BM);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i) {
+                uint8_t* b = smem + (size_t)i * SB + A_STAGE;
+                mbar_expect_tx(&tl.full[i], (uint32_t)(p.kc * B_SUB));
+                if (p.kc > 1) tma_3d(b, &tmX, &tl.full[i], 0, 0, (kb0 + i) * p.kc);
+                else tma_2d(b, &tmX, &tl.full[i], (kb0 + i) * BK, 0);
+            }
+            issued = pre;
+            s = pre % NS;
+            ph = pre == NS ? 1u : 0u;
+        }
         for (; issued < n_steps; ++issued) {
             const int i = issued;
             if (!mbar_wait(&tl.empty[s], ph ^ 1, abort_flag, p.status)) break;
@@ -400,7 +426,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             uint8_t* b = a + A_STAGE;
             // din steps, with the K-extension steps placed EXT_LEAD steps before the end
             // so that their Vt loads overlap the last W tiles
-            const int ne = eu1 - eu0, ins = max(0, (kb1 - kb0) - EXT_LEAD);
+            const int ne = eu1 - eu0, ins = max(0, (kb1 - kb0) - p.ext_lead);
             const bool ext = i >= ins && i < ins + ne;
             const int kb = kb0 + (i < ins ? i : i - ne);
             if (SHRINK) {
@@ -419,8 +445,13 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             } else if (!ext) {
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)SB);
-                tma_2d(a, &tmW, &tl.full[s], kb * BK, tile * BM);
-                tma_2d(b, &tmX, &tl.full[s], kb * BK, 0);
+                if (p.kc > 1) {   // kc K chunks of W (128 rows) and of X (N tokens), one box each
+                    tma_3d(a, &tmW, &tl.full[s], 0, tile * BM, kb * p.kc);
+                    tma_3d(b, &tmX, &tl.full[s], 0, 0, kb * p.kc);
+                } else {
+                    tma_2d(a, &tmW, &tl.full[s], kb * BK, tile * BM);
+                    tma_2d(b, &tmX, &tl.full[s], kb * BK, 0);
+                }
             } else {
                 const int u = eu0 + (i - ins);
                 const int kx = (u - eu0) * EXT_SUB;
@@ -992,6 +1023,20 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         return cudaSuccess;
     }
 
+    // decode: W and X as 3D views {64, rows, K chunks}, so that one box carries
+    // PROJ_KC K chunks (needs din % 64 == 0)
+    // (at most as many as let two stages fit the budget)
+    int pkc = d.din % BK == 0 ? PROJ_KC : 1;
+    while (pkc > 1 && 2 * pkc * stage_bytes(N) > PROJ_SMEM_BUDGET - (N <= PUSH_MAX_N ? BM * N * 4 : 0)) --pkc;
+    if (pkc > 1) {
+        cuuint64_t wdims[3] = {(cuuint64_t)BK, (cuuint64_t)d.dout, (cuuint64_t)kb_total};
+        cuuint64_t strides[2] = {(cuuint64_t)d.din * 2, (cuuint64_t)BK * 2};
+        cuuint32_t wbox[3] = {BK, (cuuint32_t)BM, (cuuint32_t)pkc};
+        if (!tc_encode(&tmW, a.W, 3, wdims, strides, wbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        cuuint64_t xdims[3] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)kb_total};
+        cuuint32_t xbox[3] = {BK, (cuuint32_t)N, (cuuint32_t)pkc};
+        if (!tc_encode(&tmX, a.X, 3, xdims, strides, xbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    }
     const int tiles = proj_tiles(d);
     GemmParams p{};
     p.chunks = a.ws.chunks;
@@ -1003,27 +1048,33 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.T = T;
     p.dout = d.dout;
     p.N = N;
-    p.kc = 1;
-    p.ksteps = kb_total;
+    p.kc = pkc;
+    p.ksteps = (kb_total + pkc - 1) / pkc;
     p.n_chunks = n_chunks;
     p.ext_units = shrink ? (n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
-    p.splits = cluster_splits(k_splits(tiles, kb_total, N, false));
+    p.splits = cluster_splits(k_splits(tiles, p.ksteps, N, false));
     // small batches: the splits push their partial slices into a receive buffer
     p.push = (p.splits > 1 && N <= PUSH_MAX_N && N % p.splits == 0) ? 1 : 0;
+    p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
     const int rx_bytes = p.push ? BM * N * 4 : 0;
-    p.stages = clamp_stages((PROJ_SMEM_BUDGET - rx_bytes) / stage_bytes(N));
+    p.stages = clamp_stages((PROJ_SMEM_BUDGET - rx_bytes) / (pkc * stage_bytes(N)));
     p.a_sub = A_BYTES;
-    p.ring_bytes = p.stages * stage_bytes(N);
+    p.ring_bytes = p.stages * pkc * stage_bytes(N);
     p.rx_off = p.ring_bytes;
     p.tail_off = p.ring_bytes + rx_bytes;
     p.tcap = d.tcap;
     p.pdl = shrink ? 1 : 0;
+    // Without a shrink the projection is the forward's first kernel: launched while the
+    // kernel before it may run, its W goes out at once and its X after that kernel
+    // has completed.  After a shrink it launches once the shrink has seen the kernel
+    // before the forward complete, so X may be read at once.
+    p.xwait = (!shrink && !a.ev_start) ? 1 : 0;
     p.cluster = p.splits > 1 ? 1 : 0;
     p.S = d.S;
     p.max_chunks = d.max_chunks;
     if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
     e = launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p), st,
-                 shrink && !a.ev_start, p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
+                 !a.ev_start, p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
     if (e != cudaSuccess) return e;
     if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
     return cudaSuccess;

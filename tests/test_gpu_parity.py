@@ -128,6 +128,35 @@ def test_many_loaded_slots_few_used():
     assert_within(run_layer(layer, pool), want_of(layer), "bf16", "300 slots, 3 used")
 
 
+def test_chained_forwards_read_the_previous_output():
+    """Each forward's X is the previous forward's Y, enqueued back to back on one
+    stream: the kernels of a forward start while the previous forward's kernels may
+    still run, and must read X only once it is written.  The kernels are
+    deterministic (fixed split order), so the chain must equal, bit for bit, the same
+    chain with a device synchronisation after every forward."""
+    layer = wl.random_layer(14, T=32, din=1024, dout=1024, ranks=[16, 8])
+    pool = make_pool(layer)
+    X0, W, ra, _ = upload(layer)
+    for row_map in (ra, None):
+        synced, x = [], X0
+        for _ in range(4):
+            y = torch.empty_like(x)
+            pool.forward(x, W, row_map, y)
+            torch.cuda.synchronize()
+            synced.append(y.clone())
+            x = y
+        chained, x = [], X0
+        ys = [torch.empty_like(X0) for _ in range(4)]
+        for y in ys:
+            pool.forward(x, W, row_map, y)
+            chained.append(y)
+            x = y
+        torch.cuda.synchronize()
+        for k, (a, b) in enumerate(zip(synced, chained)):
+            assert torch.equal(a, b), f"forward {k} of the chain (row map {'on' if row_map is not None else 'off'})"
+    assert pool.status() == mlora.MLORA_OK
+
+
 def test_arena_holes_use_one_box_per_chunk():
     """Slots 1..8 unloaded leave a hole of 128 rank rows between slots 0 and 9: their
     chunks no longer fit one 128-row window, so the shrink loads each chunk alone."""
