@@ -391,6 +391,32 @@ def run_ours(args, dist, rank, local):
         from tests.tolerance import within
         spot = bool(within(got[rows], want, L.dtype).all())
 
+    # ---- merge (W <- W + s Up Down) of the first adapter, on scratch copies of W: one
+    # launch per merge, read + write of W plus the adapter's Up and Down
+    merge = None
+    L0m = items[0]["layer"]
+    if L0m.max_slots > 0 and L0m.dtype == "bf16" and args.workload != "stack7b":
+        a0 = layers[0].adapters[0]
+        Wm = [torch.empty_like(items[i % n_items]["W"]).copy_(items[i % n_items]["W"]) for i in range(max(2, copies))]
+        pool0 = items[0]["pool"]
+        for w in Wm:
+            pool0.merge(w, a0.slot, stream=stream)
+        torch.cuda.synchronize(dev)
+        mreps = 20
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(mreps):
+            for w in Wm:
+                pool0.merge(w, a0.slot, stream=stream)
+        m1.record(stream)
+        torch.cuda.synchronize(dev)
+        m_us = m0.elapsed_time(m1) * 1e3 / (mreps * len(Wm))
+        m_bytes = 2 * L0m.dout * L0m.din * 2 + a0.rank * (L0m.din + L0m.dout) * 2
+        merge = {"us_per_merge": m_us, "rank": a0.rank, "dout": L0m.dout, "din": L0m.din,
+                 "achieved_gbs": m_bytes / m_us / 1e3, "frac": m_bytes / m_us / 1e3 / peaks["hbm_gbs"],
+                 "copies": len(Wm)}
+        del Wm
+
     w0 = works[0]
     if per_step_items == 7:
         layer_bytes = sum(w["proj_bytes"] for w in works[:7])
@@ -428,7 +454,7 @@ def run_ours(args, dist, rank, local):
                    "seed": args.seed},
         "roofline": roof,
         "step_roofline": {"frac": step_roof_s / step_s, "bytes": int(layer_step_bytes), "flops": int(layer_flops)},
-        "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks, "spot_check": spot,
+        "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks, "spot_check": spot, "merge": merge,
     }
     return out, L0
 

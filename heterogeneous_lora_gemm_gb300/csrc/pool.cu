@@ -504,7 +504,10 @@ mlora_status mlora_merge(mlora_pool_t p, void* W, int slot, mlora_stream_t strea
     DeviceGuard g(p->device);
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t st = (cudaStream_t)stream;
-    CU_TRY(launch_merge_simt(p->dtype == MLORA_BF16, W, p->d_slots, slot, p->arena_down, p->arena_up, p->dims, st));
+    if (p->dtype == MLORA_BF16)   // tensor cores (MMA over the rank, W tile in and out by TMA)
+        CU_TRY(launch_merge_tc(W, p->d_slots, slot, p->maps, p->ws.status, p->dims, st));
+    else
+        CU_TRY(launch_merge_simt(false, W, p->d_slots, slot, p->arena_down, p->arena_up, p->dims, st));
     return note_reader(p, st);
 }
 

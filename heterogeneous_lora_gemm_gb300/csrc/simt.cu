@@ -120,48 +120,140 @@ base_expand_simt_kernel(const E* __restrict__ X, const E* __restrict__ W, const 
 }
 
 // W[o, i] += scale * sum_k Up[o, k] Down[k, i] (M031 §04), fp32 sum, one rounding.
-// A block owns a tile of MERGE_ROWS rows x MERGE_COLS columns of W: the Down slab
-// [k-chunk x MERGE_COLS] and the Up slab [MERGE_ROWS x k-chunk] sit in shared
-// memory, each thread keeps MERGE_ROWS accumulators for one column, so every
-// Down element is read from memory once per row tile and W is read and written
-// exactly once, with coalesced accesses.
-constexpr int MERGE_ROWS = 32, MERGE_COLS = 256, MERGE_KC = 32;
+// Merge.  A block owns a tile of MERGE_ROWS rows x MERGE_COLS columns of W; each
+// thread owns 8 rows x 8 consecutive columns (one 16-byte vector of a bf16 row).  The
+// thread's old W values are loaded first, so that the HBM round trip overlaps the
+// adapter loads and the FMAs.  Per chunk of MERGE_KC rank columns, the Down slab
+// [k][MERGE_COLS] (fp32) and the Up slab [MERGE_ROWS][k] sit in shared memory: a
+// thread reads its 8 Down values of column k once and multiplies them by the 8 Up
+// values of its rows (broadcast across the warp).  Sums in fp32, one rounding.
+constexpr int MERGE_ROWS = 64, MERGE_COLS = 256, MERGE_KC = 32, MERGE_THREADS = 256;
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, bool vec, int n, float* v) {
+    if (vec) {
+        const uint4 q = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            v[2 * j] = f.x;
+            v[2 * j + 1] = f.y;
+        }
+    } else {
+        for (int j = 0; j < 8; ++j) v[j] = j < n ? __bfloat162float(p[j]) : 0.f;
+    }
+}
+__device__ __forceinline__ void load8(const float* p, bool vec, int n, float* v) {
+    if (vec) {
+        const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+        v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+    } else {
+        for (int j = 0; j < 8; ++j) v[j] = j < n ? p[j] : 0.f;
+    }
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, bool vec, int n, const float* v) {
+    if (vec) {
+        uint4 q;
+        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) h[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+        *reinterpret_cast<uint4*>(p) = q;
+    } else {
+        for (int j = 0; j < n; ++j) p[j] = __float2bfloat16_rn(v[j]);
+    }
+}
+__device__ __forceinline__ void store8(float* p, bool vec, int n, const float* v) {
+    if (vec) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+        for (int j = 0; j < n; ++j) p[j] = v[j];
+    }
+}
 
 template <typename E>
-__global__ void __launch_bounds__(MERGE_COLS)
+__global__ void __launch_bounds__(MERGE_THREADS, 2)
 merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot,
                   const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout) {
-    __shared__ float down_s[MERGE_KC][MERGE_COLS];
+    __shared__ __align__(16) float down_s[MERGE_KC][MERGE_COLS];
     __shared__ float up_s[MERGE_ROWS][MERGE_KC + 1];
     const SlotRec rec = slots[slot];
     if (rec.rank <= 0) return;
-    const int o0 = blockIdx.y * MERGE_ROWS, i0 = blockIdx.x * MERGE_COLS;
-    const int i = i0 + threadIdx.x;
-    const E* down = arena_down + (size_t)rec.unit * din;
-    float acc[MERGE_ROWS];
+    const int cg = threadIdx.x & 31, rg = threadIdx.x >> 5;   // column group (8 columns), row group (8 rows)
+    const int c0 = blockIdx.x * MERGE_COLS, i0 = c0 + cg * 8;
+    const int o0 = blockIdx.y * MERGE_ROWS + rg * 8;
+    const int ncol = min(8, din - i0);                         // columns of this thread inside W
+    // 16-byte vectors need whole, aligned groups of 8 columns
+    const bool vec = ncol == 8 && (din % 8) == 0;
+
+    // bf16 rows as whole vectors: the raw 16 bytes of each of the 8 rows, loaded now
+    constexpr bool BF16 = sizeof(E) == 2;
+    const bool pre = BF16 && vec;
+    uint4 w_raw[8];
 #pragma unroll
-    for (int r = 0; r < MERGE_ROWS; ++r) acc[r] = 0.f;
+    for (int r = 0; r < 8; ++r)
+        w_raw[r] = (pre && o0 + r < dout) ? *reinterpret_cast<const uint4*>(W + (size_t)(o0 + r) * din + i0)
+                                          : make_uint4(0u, 0u, 0u, 0u);
+    float acc[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[r][j] = 0.f;
+
+    const E* down = arena_down + (size_t)rec.unit * din;
+    const bool dvec = (din % 8) == 0;
     for (int k0 = 0; k0 < rec.rank; k0 += MERGE_KC) {
         const int kn = min(MERGE_KC, rec.rank - k0);
         __syncthreads();
-        for (int k = 0; k < kn; ++k) down_s[k][threadIdx.x] = i < din ? to_f32(down[(size_t)(k0 + k) * din + i]) : 0.f;
-        for (int idx = threadIdx.x; idx < MERGE_ROWS * MERGE_KC; idx += MERGE_COLS) {
-            const int r = idx / MERGE_KC, k = idx % MERGE_KC;
-            up_s[r][k] = (o0 + r < dout && k < kn) ? to_f32(arena_up[up_index(rec.unit, k0 + k, o0 + r, dout)]) : 0.f;
+        for (int idx = threadIdx.x; idx < kn * (MERGE_COLS / 8); idx += MERGE_THREADS) {
+            const int k = idx / (MERGE_COLS / 8), c8 = (idx % (MERGE_COLS / 8)) * 8;
+            const int n = min(8, din - (c0 + c8));
+            float v[8];
+            if (n > 0) load8(down + (size_t)(k0 + k) * din + c0 + c8, dvec && n == 8, n, v);
+            else
+                for (int j = 0; j < 8; ++j) v[j] = 0.f;
+            *reinterpret_cast<float4*>(&down_s[k][c8]) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(&down_s[k][c8 + 4]) = make_float4(v[4], v[5], v[6], v[7]);
+        }
+        for (int idx = threadIdx.x; idx < MERGE_ROWS * kn; idx += MERGE_THREADS) {
+            const int r = idx / kn, k = idx % kn;
+            const int o = blockIdx.y * MERGE_ROWS + r;
+            up_s[r][k] = o < dout ? to_f32(arena_up[up_index(rec.unit, k0 + k, o, dout)]) : 0.f;
         }
         __syncthreads();
         for (int k = 0; k < kn; ++k) {
-            const float d = down_s[k][threadIdx.x];
+            const float4 da = *reinterpret_cast<const float4*>(&down_s[k][cg * 8]);
+            const float4 db = *reinterpret_cast<const float4*>(&down_s[k][cg * 8 + 4]);
+            const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
 #pragma unroll
-            for (int r = 0; r < MERGE_ROWS; ++r) acc[r] = fmaf(up_s[r][k], d, acc[r]);
+            for (int r = 0; r < 8; ++r) {
+                const float u = up_s[rg * 8 + r][k];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(u, dv[j], acc[r][j]);
+            }
         }
     }
-    if (i >= din) return;
+    if (ncol <= 0) return;
 #pragma unroll
-    for (int r = 0; r < MERGE_ROWS; ++r) {
+    for (int r = 0; r < 8; ++r) {
         if (o0 + r >= dout) break;
-        E* w = W + (size_t)(o0 + r) * din + i;
-        *w = from_f32<E>(fmaf(rec.scale, acc[r], to_f32(*w)));
+        E* w = W + (size_t)(o0 + r) * din + i0;
+        float old[8];
+        if (pre) {
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w_raw[r]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(h[j]);
+                old[2 * j] = f.x;
+                old[2 * j + 1] = f.y;
+            }
+        } else {
+            load8(w, vec, ncol, old);
+        }
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = fmaf(rec.scale, acc[r][j], old[j]);
+        store8(w, vec, ncol, v);
     }
 }
 
@@ -202,11 +294,11 @@ cudaError_t launch_merge_simt(bool bf16, void* W, const SlotRec* slots, int slot
                               cudaStream_t st) {
     const dim3 grid((d.din + MERGE_COLS - 1) / MERGE_COLS, (d.dout + MERGE_ROWS - 1) / MERGE_ROWS);
     if (bf16)
-        merge_simt_kernel<__nv_bfloat16><<<grid, MERGE_COLS, 0, st>>>(
+        merge_simt_kernel<__nv_bfloat16><<<grid, MERGE_THREADS, 0, st>>>(
             (__nv_bfloat16*)W, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din,
             d.dout);
     else
-        merge_simt_kernel<float><<<grid, MERGE_COLS, 0, st>>>((float*)W, slots, slot, (const float*)arena_down,
+        merge_simt_kernel<float><<<grid, MERGE_THREADS, 0, st>>>((float*)W, slots, slot, (const float*)arena_down,
                                                           (const float*)arena_up, d.din, d.dout);
     return cudaGetLastError();
 }

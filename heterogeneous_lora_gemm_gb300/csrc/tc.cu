@@ -863,6 +863,7 @@ cudaError_t tc_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(swapab_gemm_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess) e = prefill_init();
+    if (e == cudaSuccess) e = merge_tc_init();
     return e;
 }
 

@@ -64,6 +64,11 @@ cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din
                                    float* partials, size_t partial_bytes, int32_t* counters, int max_tiles,
                                    uint32_t* status, cudaStream_t st);
 
+// Static merge of one adapter into a bf16 W on the tensor cores (merge_tc.cu).
+cudaError_t merge_tc_init();
+cudaError_t launch_merge_tc(void* W, const SlotRec* slots, int slot, const TcArenaMaps& maps, uint32_t* status,
+                            const PoolDims& d, cudaStream_t st);
+
 // Encodes a bf16 tensor map (used by both tensor-core translation units).
 bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                const cuuint32_t* box, CUtensorMapSwizzle sw);

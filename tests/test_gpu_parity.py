@@ -251,6 +251,22 @@ def test_merge_matches_oracle(dtype):
         assert_within(to_f64(W), oracle.merge(layer.W_f64, a), dtype, f"merge slot {slot}")
 
 
+@pytest.mark.parametrize("din,dout,ranks", [
+    (72, 200, [8, 5, 24, 1]),      # ragged tiles; ranks 8, 5, 1 leave the second half of their chunk to the next adapter
+    (4096, 4096, [16, 64, 40]),    # the decode shapes, several chunks per adapter
+    (256, 136, [256]),             # the largest rank, one adapter filling the arena
+])
+def test_merge_ranks_and_ragged_tiles(din, dout, ranks):
+    layer = wl.random_layer(din + dout, T=1, din=din, dout=dout, ranks=ranks)
+    pool = make_pool(layer)
+    for slot in range(len(ranks)):
+        W = to_device(layer.W, "bf16")
+        pool.merge(W, slot)
+        torch.cuda.synchronize()
+        a = ora_adapters(layer)[slot]
+        assert_within(to_f64(W), oracle.merge(layer.W_f64, a), "bf16", f"merge {din}x{dout} slot {slot} rank {ranks[slot]}")
+
+
 def test_merged_weight_serves_only_its_adapter():
     layer = wl.decode_step(0)
     pool = make_pool(layer)
