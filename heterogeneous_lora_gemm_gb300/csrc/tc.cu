@@ -747,7 +747,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 const int et = threadIdx.x - 64;
                 if (p.splits == 1) staged_reduce<1>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
                 else if (p.splits == 2) staged_reduce<2>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
+                else if (p.splits == 3) staged_reduce<3>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
                 else if (p.splits == 4) staged_reduce<4>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
+                else if (p.splits == 6) staged_reduce<6>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
                 else staged_reduce<8>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
                 __syncwarp();
                 // no CTA refills or leaves while the others still read its shared memory
@@ -797,6 +799,7 @@ namespace {
 // Shared-memory budgets: the projection and the shrink that precedes it may share
 // an SM while both run, so their rings together stay inside one SM's 228 KiB.
 constexpr int PROJ_SMEM_BUDGET = 136 * 1024;
+constexpr int PROJ_SMEM_BUDGET_2 = 100 * 1024;   // two projection CTAs per SM
 constexpr int SHRINK_SMEM_BUDGET = 84 * 1024;
 
 int clamp_stages(int ns) { return ns < 2 ? 2 : (ns > MAX_STAGES ? MAX_STAGES : ns); }
@@ -1024,11 +1027,25 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         return cudaSuccess;
     }
 
-    // decode: W and X as 3D views {64, rows, K chunks}, so that one box carries
-    // PROJ_KC K chunks (needs din % 64 == 0)
-    // (at most as many as let two stages fit the budget)
+    const int tiles = proj_tiles(d);
+    // K splits of a tile: as many as fill the SMs with one CTA each (a power of two, the
+    // ring of PROJ_SMEM_BUDGET); when that leaves a quarter of the SMs idle (few row
+    // tiles, long K), two CTAs per SM with a smaller ring
+    int splits = cluster_splits(k_splits(tiles, kb_total, N, false));
+    int budget = PROJ_SMEM_BUDGET;
+    if (tiles * splits < 3 * sm_count() / 4) {
+        int s2 = 2 * sm_count() / tiles;
+        s2 = s2 > kb_total ? kb_total : s2;
+        s2 = s2 >= 8 ? 8 : (s2 >= 6 ? 6 : (s2 >= 4 ? 4 : s2));   // cluster sizes with a reducer
+        if (s2 > splits) {
+            splits = s2;
+            budget = PROJ_SMEM_BUDGET_2;
+        }
+    }
+    // decode: W and X as 3D views {64, rows, K chunks}, so that one box carries up to
+    // PROJ_KC K chunks (needs din % 64 == 0; at most as many as let two stages fit)
     int pkc = d.din % BK == 0 ? PROJ_KC : 1;
-    while (pkc > 1 && 2 * pkc * stage_bytes(N) > PROJ_SMEM_BUDGET - (N <= PUSH_MAX_N ? BM * N * 4 : 0)) --pkc;
+    while (pkc > 1 && 2 * pkc * stage_bytes(N) > budget - (N <= PUSH_MAX_N ? BM * N * 4 : 0)) --pkc;
     if (pkc > 1) {
         cuuint64_t wdims[3] = {(cuuint64_t)BK, (cuuint64_t)d.dout, (cuuint64_t)kb_total};
         cuuint64_t strides[2] = {(cuuint64_t)d.din * 2, (cuuint64_t)BK * 2};
@@ -1038,7 +1055,6 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         cuuint32_t xbox[3] = {BK, (cuuint32_t)N, (cuuint32_t)pkc};
         if (!tc_encode(&tmX, a.X, 3, xdims, strides, xbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
-    const int tiles = proj_tiles(d);
     GemmParams p{};
     p.chunks = a.ws.chunks;
     p.row_adapter = a.row_adapter;
@@ -1053,12 +1069,12 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.ksteps = (kb_total + pkc - 1) / pkc;
     p.n_chunks = n_chunks;
     p.ext_units = shrink ? (n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
-    p.splits = cluster_splits(k_splits(tiles, p.ksteps, N, false));
+    p.splits = splits < p.ksteps ? splits : p.ksteps;
     // small batches: the splits push their partial slices into a receive buffer
     p.push = (p.splits > 1 && N <= PUSH_MAX_N && N % p.splits == 0) ? 1 : 0;
     p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
     const int rx_bytes = p.push ? BM * N * 4 : 0;
-    p.stages = clamp_stages((PROJ_SMEM_BUDGET - rx_bytes) / (pkc * stage_bytes(N)));
+    p.stages = clamp_stages((budget - rx_bytes) / (pkc * stage_bytes(N)));
     p.a_sub = A_BYTES;
     p.ring_bytes = p.stages * pkc * stage_bytes(N);
     p.rx_off = p.ring_bytes;

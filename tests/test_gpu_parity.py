@@ -108,6 +108,7 @@ def test_stack7b_projection(module):
     (300, 128, 136, [16, 8, 64]),
     (129, 4096, 256, [16, 64, 8]),
     (5, 8, 8, [3, 5]),
+    (64, 1024, 5120, [16, 8]),     # 40 row tiles: 6 K splits, two CTAs per SM
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_ragged_shapes(T, din, dout, ranks, dtype):
