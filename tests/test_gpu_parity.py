@@ -135,7 +135,12 @@ def test_chained_forwards_read_the_previous_output():
     still run, and must read X only once it is written.  The kernels are
     deterministic (fixed split order), so the chain must equal, bit for bit, the same
     chain with a device synchronisation after every forward."""
-    layer = wl.random_layer(14, T=32, din=1024, dout=1024, ranks=[16, 8])
+    for shape in ((1024, [16, 8]), (4096, [16, 16, 16])):
+        chain_case(*shape)
+
+
+def chain_case(d, ranks):
+    layer = wl.random_layer(14, T=32, din=d, dout=d, ranks=ranks)
     pool = make_pool(layer)
     X0, W, ra, _ = upload(layer)
     for row_map in (ra, None):
