@@ -796,11 +796,18 @@ cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st) {
 
 namespace {
 
-// Shared-memory budgets: the projection and the shrink that precedes it may share
-// an SM while both run, so their rings together stay inside one SM's 228 KiB.
+// Shared-memory budgets of the rings.  A decode projection takes PROJ_SMEM_BUDGET
+// (one CTA per SM) or PROJ_SMEM_BUDGET_2 (two per SM).  The decode shrink launched
+// before it either runs on the SMs that the projection leaves idle (a few row tiles:
+// SHRINK_SMEM_BUDGET_APART) or shares SMs with it, both rings then sized to fit one
+// SM's 228 KiB together with their tails (PROJ_ and SHRINK_SMEM_BUDGET_SHARED).
+// Otherwise (prefill, two projection CTAs per SM) the shrink takes SHRINK_SMEM_BUDGET.
 constexpr int PROJ_SMEM_BUDGET = 136 * 1024;
 constexpr int PROJ_SMEM_BUDGET_2 = 100 * 1024;   // two projection CTAs per SM
+constexpr int PROJ_SMEM_BUDGET_SHARED = 112 * 1024;
 constexpr int SHRINK_SMEM_BUDGET = 84 * 1024;
+constexpr int SHRINK_SMEM_BUDGET_APART = 108 * 1024;
+constexpr int SHRINK_SMEM_BUDGET_SHARED = 104 * 1024;
 
 int clamp_stages(int ns) { return ns < 2 ? 2 : (ns > MAX_STAGES ? MAX_STAGES : ns); }
 
@@ -904,6 +911,48 @@ bool tc_supported(const PoolDims& d, int T) {
     return T >= 1;
 }
 
+namespace {
+
+// Launch shape of the decode projection for N token rows per tile; `budget1` is the
+// ring budget when one CTA per SM runs.
+struct DecodeShape {
+    int splits;   // K splits of a tile (the cluster)
+    int budget;   // shared-memory budget of the ring
+    int pkc;      // K chunks of 64 per pipeline step
+    int ksteps;   // pipeline steps over din
+};
+
+DecodeShape decode_shape(const PoolDims& d, int N, int budget1) {
+    const int tiles = proj_tiles(d);
+    const int kb_total = (d.din + BK - 1) / BK;
+    // K splits of a tile: as many as fill the SMs with one CTA each (a power of two);
+    // when that leaves a quarter of the SMs idle (few row tiles, long K), two CTAs per
+    // SM with a smaller ring
+    int splits = cluster_splits(k_splits(tiles, kb_total, N, false));
+    int budget = budget1;
+    if (tiles * splits < 3 * sm_count() / 4) {
+        int s2 = 2 * sm_count() / tiles;
+        s2 = s2 > kb_total ? kb_total : s2;
+        s2 = s2 >= 8 ? 8 : (s2 >= 6 ? 6 : (s2 >= 4 ? 4 : s2));   // cluster sizes with a reducer
+        if (s2 > splits) {
+            splits = s2;
+            budget = PROJ_SMEM_BUDGET_2;
+        }
+    }
+    // W and X as 3D views {64, rows, K chunks}, so that one box carries up to PROJ_KC
+    // K chunks (needs din % 64 == 0; at most as many as let two stages fit)
+    int pkc = d.din % BK == 0 ? PROJ_KC : 1;
+    while (pkc > 1 && 2 * pkc * stage_bytes(N) > budget - (N <= PUSH_MAX_N ? BM * N * 4 : 0)) --pkc;
+    DecodeShape s;
+    s.budget = budget;
+    s.pkc = pkc;
+    s.ksteps = (kb_total + pkc - 1) / pkc;
+    s.splits = splits < s.ksteps ? splits : s.ksteps;
+    return s;
+}
+
+}  // namespace
+
 cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const PoolDims& d = a.dims;
     const int T = a.T;
@@ -912,6 +961,21 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const int n_chunks = a.lora ? a.n_chunks : 0;
     const bool shrink = n_chunks > 0;
     cudaError_t e;
+    const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
+    DecodeShape ds = decode_shape(d, decode ? N : 16, PROJ_SMEM_BUDGET);
+    int shrink_budget = SHRINK_SMEM_BUDGET;
+    if (decode && shrink && ds.budget == PROJ_SMEM_BUDGET) {
+        // a shrink whose CTAs fit the SMs that the projection leaves idle gets a larger
+        // ring there; a larger one shares SMs with the projection, both rings smaller
+        const int stiles = (n_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
+        const int shrink_ctas = (stiles + 1) * cluster_splits(k_splits(stiles, kb_total, N, false));
+        if (shrink_ctas <= sm_count() - proj_tiles(d) * ds.splits) {
+            shrink_budget = SHRINK_SMEM_BUDGET_APART;
+        } else {
+            shrink_budget = SHRINK_SMEM_BUDGET_SHARED;
+            ds = decode_shape(d, N, PROJ_SMEM_BUDGET_SHARED);
+        }
+    }
 
     // ---- shrink: Vt = masked scale * Down_chunks X^T, per token tile, the used chunks
     if (shrink) {
@@ -948,7 +1012,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
             g.win_rows = R;
             g.a_sub = R * BK * 2;
             const int per = g.a_sub + b_bytes(Ns);
-            g.kc = SHRINK_SMEM_BUDGET / (2 * per);
+            g.kc = shrink_budget / (2 * per);
             g.kc = g.kc < 1 ? 1 : (g.kc > 4 ? 4 : g.kc);
             cuuint64_t dims[3] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)kb_total};
             cuuint64_t strides[2] = {(cuuint64_t)d.din * 2, (cuuint64_t)BK * 2};
@@ -973,7 +1037,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         g.ksteps = (kb_total + g.kc - 1) / g.kc;
         const int sb = g.kc * (g.a_sub + b_bytes(Ns));
         g.splits = cluster_splits(k_splits(tiles * ztiles, g.ksteps, Ns, false));
-        g.stages = clamp_stages(SHRINK_SMEM_BUDGET / sb);
+        g.stages = clamp_stages(shrink_budget / sb);
         // the MMA reads 128 rows of A from each K chunk's sub-block: slack after the ring
         const int slack = A_BYTES - g.a_sub - b_bytes(Ns) * g.kc;
         g.ring_bytes = g.stages * sb + (slack > 0 ? slack : 0);
@@ -999,7 +1063,6 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
 
-    const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
     CUtensorMap tmW, tmX, tmV;
     {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)d.dout};
@@ -1028,24 +1091,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     }
 
     const int tiles = proj_tiles(d);
-    // K splits of a tile: as many as fill the SMs with one CTA each (a power of two, the
-    // ring of PROJ_SMEM_BUDGET); when that leaves a quarter of the SMs idle (few row
-    // tiles, long K), two CTAs per SM with a smaller ring
-    int splits = cluster_splits(k_splits(tiles, kb_total, N, false));
-    int budget = PROJ_SMEM_BUDGET;
-    if (tiles * splits < 3 * sm_count() / 4) {
-        int s2 = 2 * sm_count() / tiles;
-        s2 = s2 > kb_total ? kb_total : s2;
-        s2 = s2 >= 8 ? 8 : (s2 >= 6 ? 6 : (s2 >= 4 ? 4 : s2));   // cluster sizes with a reducer
-        if (s2 > splits) {
-            splits = s2;
-            budget = PROJ_SMEM_BUDGET_2;
-        }
-    }
-    // decode: W and X as 3D views {64, rows, K chunks}, so that one box carries up to
-    // PROJ_KC K chunks (needs din % 64 == 0; at most as many as let two stages fit)
-    int pkc = d.din % BK == 0 ? PROJ_KC : 1;
-    while (pkc > 1 && 2 * pkc * stage_bytes(N) > budget - (N <= PUSH_MAX_N ? BM * N * 4 : 0)) --pkc;
+    const int budget = ds.budget, pkc = ds.pkc;
     if (pkc > 1) {
         cuuint64_t wdims[3] = {(cuuint64_t)BK, (cuuint64_t)d.dout, (cuuint64_t)kb_total};
         cuuint64_t strides[2] = {(cuuint64_t)d.din * 2, (cuuint64_t)BK * 2};
@@ -1066,10 +1112,10 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.dout = d.dout;
     p.N = N;
     p.kc = pkc;
-    p.ksteps = (kb_total + pkc - 1) / pkc;
+    p.ksteps = ds.ksteps;
     p.n_chunks = n_chunks;
     p.ext_units = shrink ? (n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
-    p.splits = splits < p.ksteps ? splits : p.ksteps;
+    p.splits = ds.splits;
     // small batches: the splits push their partial slices into a receive buffer
     p.push = (p.splits > 1 && N <= PUSH_MAX_N && N % p.splits == 0) ? 1 : 0;
     p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
