@@ -449,9 +449,18 @@ def run_ours(args, dist, rank, local):
         m1.record(stream)
         torch.cuda.synchronize(dev)
         m_us = m0.elapsed_time(m1) * 1e3 / (mreps * len(Wm))
+        # the un-merge (W <- W - s Up Down) on the same copies: the same kernel, sign flipped
+        m0.record(stream)
+        for _ in range(mreps):
+            for w in Wm:
+                pool0.unmerge(w, a0.slot, stream=stream)
+        m1.record(stream)
+        torch.cuda.synchronize(dev)
+        um_us = m0.elapsed_time(m1) * 1e3 / (mreps * len(Wm))
         m_bytes = 2 * L0m.dout * L0m.din * 2 + a0.rank * (L0m.din + L0m.dout) * 2
         merge = {"us_per_merge": m_us, "rank": a0.rank, "dout": L0m.dout, "din": L0m.din,
                  "achieved_gbs": m_bytes / m_us / 1e3, "frac": m_bytes / m_us / 1e3 / peaks["hbm_gbs"],
+                 "us_per_unmerge": um_us, "unmerge_frac": m_bytes / um_us / 1e3 / peaks["hbm_gbs"],
                  "copies": len(Wm)}
         del Wm
 

@@ -91,7 +91,7 @@ cudaError_t launch_base_expand_simt(bool bf16, const void* X, const void* W,
                                     const SlotRec* slots, const void* arena_up, const Workspace& ws,
                                     const PoolDims& d, bool with_lora, cudaStream_t st);
 cudaError_t launch_merge_simt(bool bf16, void* W, const SlotRec* slots, int slot,
-                              const void* arena_down, const void* arena_up, const PoolDims& d,
+                              const void* arena_down, const void* arena_up, const PoolDims& d, float sign,
                               cudaStream_t st);
 
 }  // namespace mlora

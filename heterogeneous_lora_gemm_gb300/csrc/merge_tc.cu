@@ -3,6 +3,11 @@
 //
 //     W[o, i] <- bf16( W[o, i] + scale * sum_k Up[o, k] Down[k, i] )      (fp32 sum)
 //
+// and, with the sign flipped, the un-merge that re-subtracts the same update
+// (airsota card "multi-LoRA serving vs merging", section 四 item ③: a merge
+// overwrites the base; switching back means subtracting it again, or restoring a
+// kept original).
+//
 // The update is an outer product with K = rank: one CTA per tile of 128 rows (o) x
 // 128 columns (i) computes it as tcgen05 MMAs of M = 128, N = 128, K = 16, one per 16
 // rank columns, into a TMEM accumulator.  A = the adapter's Up columns, read from the
@@ -54,6 +59,7 @@ struct MergeTail {
 struct MergeParams {
     const SlotRec* slots;
     int slot;
+    float sign;             // +1 merge, -1 un-merge
     uint32_t* status;
 };
 
@@ -73,6 +79,7 @@ merge_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
     const int i0 = blockIdx.x * MG_BN, o0 = blockIdx.y * MG_BM;
     const SlotRec rec = p.slots[p.slot];
     const int nk = (rec.rank + CHUNK - 1) / CHUNK;     // rank chunks (MMA K steps)
+    const float sc = p.sign * rec.scale;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < MG_STAGES; ++s) {
@@ -192,8 +199,7 @@ merge_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 f = __bfloat1622float2(hw[j]);
-                    hw[j] = __floats2bfloat162_rn(fmaf(rec.scale, v[h * 8 + 2 * j], f.x),
-                                                  fmaf(rec.scale, v[h * 8 + 2 * j + 1], f.y));
+                    hw[j] = __floats2bfloat162_rn(fmaf(sc, v[h * 8 + 2 * j], f.x), fmaf(sc, v[h * 8 + 2 * j + 1], f.y));
                 }
                 *cell = w;
             }
@@ -239,13 +245,13 @@ cudaError_t merge_tc_init() {
 }
 
 cudaError_t launch_merge_tc(void* W, const SlotRec* slots, int slot, const TcArenaMaps& maps, uint32_t* status,
-                            const PoolDims& d, cudaStream_t st) {
+                            const PoolDims& d, float sign, cudaStream_t st) {
     CUtensorMap tmW;
     cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)d.dout};
     cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)MG_BM};
     if (!tc_encode(&tmW, W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    MergeParams p{slots, slot, status};
+    MergeParams p{slots, slot, sign, status};
     const dim3 grid((d.din + MG_BN_USED - 1) / MG_BN_USED, (d.dout + MG_BM - 1) / MG_BM);
     return launch_k(merge_tc_kernel<MG_BN_USED>, grid, dim3(MG_THREADS), merge_smem<MG_BN_USED>(), st, false, 1, tmW,
                     maps.down, maps.up128, p);

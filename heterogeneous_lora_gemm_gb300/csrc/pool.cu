@@ -495,7 +495,8 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
     return note_reader(p, st);
 }
 
-mlora_status mlora_merge(mlora_pool_t p, void* W, int slot, mlora_stream_t stream) {
+// W <- W + sign * scale * Up Down of the adapter in `slot` (merge: +1, un-merge: -1).
+static mlora_status merge_signed(mlora_pool_t p, void* W, int slot, float sign, mlora_stream_t stream) {
     if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
     if (!W) return fail(MLORA_ERR_INVALID_ARG, "W is NULL");
     if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
@@ -505,10 +506,18 @@ mlora_status mlora_merge(mlora_pool_t p, void* W, int slot, mlora_stream_t strea
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t st = (cudaStream_t)stream;
     if (p->dtype == MLORA_BF16)   // tensor cores (MMA over the rank, W tile in and out by TMA)
-        CU_TRY(launch_merge_tc(W, p->d_slots, slot, p->maps, p->ws.status, p->dims, st));
+        CU_TRY(launch_merge_tc(W, p->d_slots, slot, p->maps, p->ws.status, p->dims, sign, st));
     else
-        CU_TRY(launch_merge_simt(false, W, p->d_slots, slot, p->arena_down, p->arena_up, p->dims, st));
+        CU_TRY(launch_merge_simt(false, W, p->d_slots, slot, p->arena_down, p->arena_up, p->dims, sign, st));
     return note_reader(p, st);
+}
+
+mlora_status mlora_merge(mlora_pool_t p, void* W, int slot, mlora_stream_t stream) {
+    return merge_signed(p, W, slot, 1.f, stream);
+}
+
+mlora_status mlora_unmerge(mlora_pool_t p, void* W, int slot, mlora_stream_t stream) {
+    return merge_signed(p, W, slot, -1.f, stream);
 }
 
 mlora_status mlora_pool_status(mlora_pool_t p, mlora_stream_t stream) {

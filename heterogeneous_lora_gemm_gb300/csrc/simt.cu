@@ -4,7 +4,7 @@
 // products and sums) and the bf16 shapes the tensor-core kernels do not take.
 //   shrink      v32[t, k] = scale_a * sum_i Down_a[k, i] x_t[i]       (rows of the segments)
 //   base_expand Y[t, o]  = sum_i W[o, i] x_t[i] + sum_k Up_a[o, k] v32[t, k]
-//   merge       W[o, i] += scale * sum_k Up[o, k] Down[k, i]
+//   merge       W[o, i] += sign * scale * sum_k Up[o, k] Down[k, i]   (sign -1: un-merge)
 // (ai-infra-kb "M031" tutorial §02 and §04.)  The expand reads the row's own
 // adapter and writes Y at the row's own index, so the result is in original row
 // order by construction.
@@ -174,7 +174,8 @@ __device__ __forceinline__ void store8(float* p, bool vec, int n, const float* v
 template <typename E>
 __global__ void __launch_bounds__(MERGE_THREADS, 2)
 merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot,
-                  const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout) {
+                  const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout,
+                  float sign) {
     __shared__ __align__(16) float down_s[MERGE_KC][MERGE_COLS];
     __shared__ float up_s[MERGE_ROWS][MERGE_KC + 1];
     const SlotRec rec = slots[slot];
@@ -252,7 +253,7 @@ merge_simt_kernel(E* __restrict__ W, const SlotRec* __restrict__ slots, int slot
         }
         float v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = fmaf(rec.scale, acc[r][j], old[j]);
+        for (int j = 0; j < 8; ++j) v[j] = fmaf(sign * rec.scale, acc[r][j], old[j]);
         store8(w, vec, ncol, v);
     }
 }
@@ -290,16 +291,16 @@ cudaError_t launch_base_expand_simt(bool bf16, const void* X, const void* W,
 }
 
 cudaError_t launch_merge_simt(bool bf16, void* W, const SlotRec* slots, int slot,
-                              const void* arena_down, const void* arena_up, const PoolDims& d,
+                              const void* arena_down, const void* arena_up, const PoolDims& d, float sign,
                               cudaStream_t st) {
     const dim3 grid((d.din + MERGE_COLS - 1) / MERGE_COLS, (d.dout + MERGE_ROWS - 1) / MERGE_ROWS);
     if (bf16)
         merge_simt_kernel<__nv_bfloat16><<<grid, MERGE_THREADS, 0, st>>>(
             (__nv_bfloat16*)W, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din,
-            d.dout);
+            d.dout, sign);
     else
         merge_simt_kernel<float><<<grid, MERGE_THREADS, 0, st>>>((float*)W, slots, slot, (const float*)arena_down,
-                                                          (const float*)arena_up, d.din, d.dout);
+                                                          (const float*)arena_up, d.din, d.dout, sign);
     return cudaGetLastError();
 }
 

@@ -67,7 +67,7 @@ cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din
 // Static merge of one adapter into a bf16 W on the tensor cores (merge_tc.cu).
 cudaError_t merge_tc_init();
 cudaError_t launch_merge_tc(void* W, const SlotRec* slots, int slot, const TcArenaMaps& maps, uint32_t* status,
-                            const PoolDims& d, cudaStream_t st);
+                            const PoolDims& d, float sign, cudaStream_t st);
 
 // Encodes a bf16 tensor map (used by both tensor-core translation units).
 bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,

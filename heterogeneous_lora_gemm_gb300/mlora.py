@@ -61,6 +61,7 @@ _SIGNATURES = {
     "mlora_adapter_version": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint64)]),
     "mlora_forward": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "mlora_merge": (_I, [_P, _P, _I, _P]),
+    "mlora_unmerge": (_I, [_P, _P, _I, _P]),
     "mlora_pool_status": (_I, [_P, _P]),
     "mlora_pool_info": (_I, [_P, ctypes.POINTER(PoolInfo)]),
     "mlora_debug_segments": (_I, [_P, _P, _I, _P, _P, _P]),
@@ -139,6 +140,10 @@ def mlora_forward(pool: int, X_ptr: int, W_ptr: int, row_adapter_ptr: Optional[i
 
 def mlora_merge(pool: int, W_ptr: int, slot: int, stream: int) -> None:
     check(lib().mlora_merge(pool, W_ptr, slot, stream or None), "mlora_merge")
+
+
+def mlora_unmerge(pool: int, W_ptr: int, slot: int, stream: int) -> None:
+    check(lib().mlora_unmerge(pool, W_ptr, slot, stream or None), "mlora_unmerge")
 
 
 def mlora_pool_status(pool: int, stream: int) -> int:
@@ -222,6 +227,9 @@ class Pool:
 
     def merge(self, W, slot: int, stream=None) -> None:
         mlora_merge(self.handle, W.data_ptr(), slot, _stream_handle(stream))
+
+    def unmerge(self, W, slot: int, stream=None) -> None:
+        mlora_unmerge(self.handle, W.data_ptr(), slot, _stream_handle(stream))
 
     def status(self, stream=None) -> int:
         return mlora_pool_status(self.handle, _stream_handle(stream))

@@ -164,6 +164,20 @@ mlora_status mlora_forward(mlora_pool_t pool, const void* X, const void* W,
 mlora_status mlora_merge(mlora_pool_t pool, void* W, int slot, mlora_stream_t stream);
 
 /*
+ * Un-merge: subtracts the same update again, in place (airsota card "multi-LoRA
+ * serving vs merging", section 四 item ③ -- a merge overwrites the base, so
+ * switching back means re-subtracting the adapter's update or restoring a kept
+ * original):
+ *   W[o,i] <- W[o,i] - scale * sum_k Up[o,k] Down[k,i]      (fp32 sum, one rounding)
+ * Applied to the output of mlora_merge with the same slot, it returns the original W
+ * up to the two roundings: per element |W'' - W| <= u (|W'| + |W''|) with W' the
+ * merged weight and u the unit roundoff of the pool dtype (2^-8 for bf16, 2^-24
+ * for fp32), plus the fp32 error of the update sum.  Keep the original W when an
+ * exact return is needed.  Arguments, ownership and errors as mlora_merge.
+ */
+mlora_status mlora_unmerge(mlora_pool_t pool, void* W, int slot, mlora_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the pool's device status word.
  * Returns MLORA_OK, MLORA_ERR_DEVICE_ROW (a forward since the last call saw a row
  * naming an invalid or empty slot), MLORA_ERR_DEVICE_TIMEOUT (a pipeline wait in a

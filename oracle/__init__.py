@@ -59,6 +59,8 @@ def _load():
         lib.oracle_forward.argtypes = [i64, i64, i64, p, p, p, i32, p, p, p, p, p, p, p, i64, p]
         lib.oracle_merge.restype = None
         lib.oracle_merge.argtypes = [i64, i64, p, i32, ctypes.c_double, p, p, p]
+        lib.oracle_unmerge.restype = None
+        lib.oracle_unmerge.argtypes = [i64, i64, p, i32, ctypes.c_double, p, p, p]
         lib.oracle_lora_flops.restype = None
         lib.oracle_lora_flops.argtypes = [i64, i64, i64, p, i32, p, p, p]
         lib.oracle_threads.restype = ctypes.c_int
@@ -163,6 +165,19 @@ def merge(W: np.ndarray, adapter: OracleAdapter) -> np.ndarray:
     lib.oracle_merge(din, dout, _ptr(W), adapter.rank, float(adapter.scale),
                      _ptr(np.ascontiguousarray(adapter.down, np.float64)),
                      _ptr(np.ascontiguousarray(adapter.up, np.float64)), _ptr(out))
+    return out
+
+
+def unmerge(W: np.ndarray, adapter: OracleAdapter) -> np.ndarray:
+    """W - scale * Up @ Down in fp64: the un-merge that switches a merged weight back
+    (airsota card "multi-LoRA serving vs merging", section 四 item ③)."""
+    lib = _load()
+    W = np.ascontiguousarray(W, np.float64)
+    dout, din = W.shape
+    out = np.empty_like(W)
+    lib.oracle_unmerge(din, dout, _ptr(W), adapter.rank, float(adapter.scale),
+                       _ptr(np.ascontiguousarray(adapter.down, np.float64)),
+                       _ptr(np.ascontiguousarray(adapter.up, np.float64)), _ptr(out))
     return out
 
 

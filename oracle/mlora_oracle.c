@@ -164,6 +164,22 @@ void oracle_merge(int64_t din, int64_t dout, const double* W, int32_t rank,
     }
 }
 
+/* Un-merge ([AIRSOTA] section 四 item ③: a merge overwrites the base; switching back
+ * re-subtracts the adapter's update): W_out = W - scale * Up Down, in fp64. */
+void oracle_unmerge(int64_t din, int64_t dout, const double* W, int32_t rank,
+                    double scale, const double* down, const double* up, double* W_out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t o = 0; o < dout; ++o) {
+        const double* u = up + o * rank;   /* row o of Up */
+        for (int64_t i = 0; i < din; ++i) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < rank; ++k) acc += u[k] * down[(int64_t)k * din + i];
+            W_out[o * din + i] = W[o * din + i] - scale * acc;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------- */
 /* Low-rank work count: [M031] §03.  Each adapter group costs
  * 2 * rows * rank * (din + dout) FLOP (Down then Up, multiply and add); the

@@ -273,6 +273,39 @@ def test_merge_ranks_and_ragged_tiles(din, dout, ranks):
         assert_within(to_f64(W), oracle.merge(layer.W_f64, a), "bf16", f"merge {din}x{dout} slot {slot} rank {ranks[slot]}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_unmerge_matches_oracle_and_bounds_the_round_trip(dtype):
+    """airsota card "multi-LoRA serving vs merging", section 四 item ③: a merge
+    overwrites the base and switching back re-subtracts the update.  The un-merge
+    matches the oracle's W - s Up Down; after a merge, it returns the original W up
+    to the two roundings, |W'' - W| <= u (|W'| + |W''|), with the fp32 error of the
+    update sum on top.  Ragged tiles; ranks 16, 40 (three chunks) and 5."""
+    layer = wl.random_layer(21, T=1, din=200, dout=136, ranks=[16, 40, 5], dtype=dtype)
+    pool = make_pool(layer)
+    u = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -24   # unit roundoff: 8 and 24 significant bits
+    u32 = 2.0 ** -24
+    for slot, a in enumerate(ora_adapters(layer)):
+        W = to_device(layer.W, dtype)
+        pool.unmerge(W, slot)
+        torch.cuda.synchronize()
+        assert_within(to_f64(W), oracle.unmerge(layer.W_f64, a), dtype, f"unmerge slot {slot}")
+        W = to_device(layer.W, dtype)
+        pool.merge(W, slot)
+        torch.cuda.synchronize()
+        Wm = to_f64(W)
+        pool.unmerge(W, slot)
+        torch.cuda.synchronize()
+        Wu = to_f64(W)
+        W0 = layer.W_f64
+        delta_abs = abs(a.scale) * (np.abs(a.up) @ np.abs(a.down))
+        bound = (u * (np.abs(Wm) + np.abs(Wu)) * (1 + 2.0 ** -7)
+                 + 2 * a.rank * u32 * delta_abs + 4 * u32 * (np.abs(W0) + np.abs(Wm)))
+        err = np.abs(Wu - W0)
+        assert (err <= bound).all(), f"slot {slot}: round trip error {err.max()} above its bound"
+        assert np.abs(Wm - W0).max() > 10 * err.max(), "the merge changed W"
+    assert pool.status() == mlora.MLORA_OK
+
+
 def test_merged_weight_serves_only_its_adapter():
     layer = wl.decode_step(0)
     pool = make_pool(layer)

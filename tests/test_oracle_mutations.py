@@ -29,6 +29,10 @@ MUTANTS = {
                           "W_out[o * din + i] = W[o * din + i] + acc;"),
     "merge transposed": ("acc += up[o * rank + k] * down[(int64_t)k * din + i];",
                          "acc += up[o * rank + k] * down[(int64_t)k + i * rank];"),
+    "unmerge adds": ("W_out[o * din + i] = W[o * din + i] - scale * acc;",
+                     "W_out[o * din + i] = W[o * din + i] + scale * acc;"),
+    "unmerge Down transposed": ("acc += u[k] * down[(int64_t)k * din + i];",
+                                "acc += u[k] * down[(int64_t)k + i * rank];"),
     "flops count din only": ("e += 2 * (int64_t)ranks[a] * (din + dout);", "e += 2 * (int64_t)ranks[a] * din;"),
     "padded budget uses valid rows": ("*padded = 2 * T * (int64_t)r_max * (din + dout);",
                                       "*padded = e / (r_max > 0 ? 1 : 1);"),
@@ -42,6 +46,8 @@ PIN_TESTS = [
     pins.test_rows_without_adapter_equal_library_matmul,
     lambda: pins.test_single_adapter_batch_equals_merged_weight(2),
     pins.test_merge_matches_library,
+    pins.test_unmerge_subtracts_the_update,
+    pins.test_unmerge_after_merge_restores_only_with_the_same_adapter,
     pins.test_rank_padding_leaves_output_unchanged,
     pins.test_rank1_unit_adapter_closed_form,
     pins.test_segments_match_sorted_definition,

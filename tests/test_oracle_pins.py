@@ -163,6 +163,28 @@ def test_merge_serves_only_its_adapter():
     assert not within(Xa[rows_b] @ Wa.T, Y[rows_b], "bf16").all()
 
 
+def test_unmerge_subtracts_the_update():
+    """airsota card, section 四 item ③: switching a merged weight back re-subtracts the
+    adapter's update: unmerge(W) x = W x - s Up (Down x), checked with numpy's matmul
+    on a random vector (a wrong sign, a transposed Up or Down, or a dropped scale fails)."""
+    layer = wl.random_layer(15, T=1, din=56, dout=36, ranks=[12])
+    ad = layer.adapters[0]
+    Wu = oracle.unmerge(layer.W_f64, oracle.OracleAdapter(ad.down_f64, ad.up_f64, ad.scale))
+    x = np.random.default_rng(3).standard_normal(56)
+    want = layer.W_f64 @ x - ad.scale * (ad.up_f64 @ (ad.down_f64 @ x))
+    np.testing.assert_allclose(Wu @ x, want, rtol=1e-12, atol=1e-12)
+
+
+def test_unmerge_after_merge_restores_only_with_the_same_adapter():
+    """The un-merge of the adapter that was merged returns the original weight (fp64:
+    to rounding); un-merging another adapter does not."""
+    layer = wl.random_layer(16, T=1, din=40, dout=24, ranks=[16, 8])
+    a, b = adapters_of(layer)
+    Wm = oracle.merge(layer.W_f64, a)
+    np.testing.assert_allclose(oracle.unmerge(Wm, a), layer.W_f64, rtol=0, atol=1e-13)
+    assert np.abs(oracle.unmerge(Wm, b) - layer.W_f64).max() > 1e-3
+
+
 # --------------------------------------------------------------------------- #
 # invariants and closed forms
 def test_rank_padding_leaves_output_unchanged():
