@@ -464,6 +464,54 @@ def run_ours(args, dist, rank, local):
                  "copies": len(Wm)}
         del Wm
 
+    # ---- host tier: a rank-16 adapter prefetched from pinned host memory into a spare
+    # slot (M031 §06).  Cost of a prefetch alone (its H2D copies and the table update,
+    # on the forward's stream), and the step time with one prefetch per step beside
+    # the forwards of the timed workload's first copy.
+    prefetch = None
+    if L0m.max_slots > 0 and L0m.dtype == "bf16" and args.workload != "stack7b":
+        from heterogeneous_lora_gemm_gb300 import Pool
+        src = layers[0].adapters[0]
+        ppool = Pool(L0m.max_slots + 1, sum((a.rank + 7) // 8 * 8 for a in layers[0].adapters) + 3 * 16,
+                     max(L0m.max_rank, 16), L0m.din, L0m.dout, "bf16", max(L0m.T, 1))
+        for a in layers[0].adapters:
+            ppool.load(a.slot, to_device(a.down, "bf16"), to_device(a.up, "bf16"), a.scale)
+        for hid in (0, 1):
+            ppool.host_add(hid, to_device(src.down, "bf16", "cpu"), to_device(src.up, "bf16", "cpu"), src.scale)
+        spare = L0m.max_slots
+        it0 = items[0]
+        reps = 64
+        torch.cuda.synchronize(dev)
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ppool.prefetch(spare, 0, stream=stream)
+            p0.record(stream)
+            for k in range(reps):
+                ppool.prefetch(spare, k & 1, stream=stream)
+            p1.record(stream)
+        torch.cuda.synchronize(dev)
+        pf_us = p0.elapsed_time(p1) * 1e3 / reps
+        pf_bytes = (src.rank + 7) // 8 * 8 * (L0m.din + L0m.dout) * 2
+
+        def steps_us(with_prefetch):
+            with torch.cuda.stream(stream):
+                for _ in range(8):
+                    ppool.forward(it0["X"], it0["W"], it0["ra"], it0["Y"], stream=stream)
+                p0.record(stream)
+                for k in range(reps):
+                    if with_prefetch:
+                        ppool.prefetch(spare, k & 1, stream=stream)
+                    ppool.forward(it0["X"], it0["W"], it0["ra"], it0["Y"], stream=stream)
+                p1.record(stream)
+            torch.cuda.synchronize(dev)
+            return p0.elapsed_time(p1) * 1e3 / reps
+
+        plain_us, with_us = steps_us(False), steps_us(True)
+        prefetch = {"us_per_prefetch": pf_us, "bytes": int(pf_bytes), "h2d_gbs": pf_bytes / pf_us / 1e3,
+                    "step_us_eager": plain_us, "step_us_eager_with_prefetch": with_us,
+                    "note": "eager launches (no graph), one copy of the workload: not the bench's step time"}
+        ppool.close()
+
     w0 = works[0]
     if per_step_items == 7:
         layer_bytes = sum(w["proj_bytes"] for w in works[:7])
@@ -501,7 +549,7 @@ def run_ours(args, dist, rank, local):
                    "seed": args.seed},
         "roofline": roof,
         "step_roofline": {"frac": step_roof_s / step_s, "bytes": int(layer_step_bytes), "flops": int(layer_flops)},
-        "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks, "spot_check": spot, "merge": merge,
+        "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks, "spot_check": spot, "merge": merge, "prefetch": prefetch,
     }
     return out, L0
 

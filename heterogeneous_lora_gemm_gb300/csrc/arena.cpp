@@ -33,6 +33,16 @@ bool Arena::release(int id) {
     return true;
 }
 
+bool Arena::rename(int from, int to) {
+    auto it = where_.find(from);
+    if (it == where_.end() || where_.count(to)) return false;
+    const int off = it->second;
+    blocks_[off].first = to;
+    where_.erase(it);
+    where_[to] = off;
+    return true;
+}
+
 int Arena::offset_of(int id) const {
     auto it = where_.find(id);
     return it == where_.end() ? -1 : it->second;
@@ -86,6 +96,10 @@ int mlora_arena_alloc(mlora_arena_t arena, int id, int n) {
 
 int mlora_arena_free(mlora_arena_t arena, int id) {
     return (arena && arena->a.release(id)) ? 0 : -1;
+}
+
+int mlora_arena_rename(mlora_arena_t arena, int from, int to) {
+    return (arena && arena->a.rename(from, to)) ? 0 : -1;
 }
 
 int mlora_arena_compact(mlora_arena_t arena, int32_t* moves, int cap) {

@@ -34,6 +34,8 @@ public:
     int alloc(int id, int n);
     // Releases the block of `id`; false if `id` holds none.
     bool release(int id);
+    // Gives the block of `from` to `to` (which holds none), in place; false otherwise.
+    bool rename(int from, int to);
     // Unit offset of `id`'s block, or -1.
     int offset_of(int id) const;
     int largest_hole() const;

@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <cstdarg>
+#include <map>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -107,6 +108,36 @@ struct mlora_pool {
 
     std::vector<cudaEvent_t> prof_start, prof_stop;
     size_t prof_next = 0;
+
+    // Host (cold) tier (M031 §06): adapters in pinned host memory, already in the
+    // arena's layout, copied into a slot on demand by mlora_prefetch.
+    struct HostAdapter {
+        char* down = nullptr;        // [rpad x din]
+        char* up = nullptr;          // [rpad / 8 blocks][dout][8]
+        int rank = 0, rpad = 0;
+        float scale = 0.f;
+        cudaEvent_t busy = nullptr;  // recorded after the last copy out of it
+        bool busy_pending = false;
+    };
+    std::map<int, HostAdapter> cold;
+    // Blocks of adapters evicted by a prefetch: kept out of the allocator (renamed to
+    // a quarantine id) until `free_at`, recorded once their last reader finished.
+    struct Quarantine {
+        int id;
+        cudaEvent_t free_at;
+    };
+    std::vector<Quarantine> quarantine;
+    int next_qid = 0;
+    // Pinned staging of the slot and chunk tables for their asynchronous updates: a
+    // ring, each entry reused once the copy out of it is done.
+    struct TableStage {
+        char* buf = nullptr;
+        cudaEvent_t done = nullptr;
+        bool pending = false;
+    };
+    std::vector<TableStage> stages;
+    int stage_next = 0;
+    cudaEvent_t tables_ready = nullptr;   // the last asynchronous table update has landed
 };
 
 namespace {
@@ -138,8 +169,8 @@ mlora_status push_slot(mlora_pool* p, int slot) {
 // forward reads it meanwhile: every caller waited for the pool's last reader).
 // The table is in arena order, so that 8 consecutive chunks (one row tile of the
 // tensor-core shrink) usually lie in one window of at most 128 arena rows.
-mlora_status push_chunks(mlora_pool* p) {
-    std::vector<ChunkRec> host;
+mlora_status build_chunks(mlora_pool* p, std::vector<ChunkRec>& host) {
+    host.clear();
     for (int s = 0; s < p->max_slots; ++s) {
         const SlotHost& h = p->slots[s];
         if (h.rank <= 0) continue;
@@ -158,6 +189,13 @@ mlora_status push_chunks(mlora_pool* p) {
         const int span = host[t1].unit + CHUNK - host[t0].unit;
         if (span > p->tile_span) p->tile_span = span;
     }
+    return MLORA_OK;
+}
+
+mlora_status push_chunks(mlora_pool* p) {
+    std::vector<ChunkRec> host;
+    mlora_status st = build_chunks(p, host);
+    if (st != MLORA_OK) return st;
     if (!host.empty()) {
         CU_TRY(cudaMemcpyAsync(p->d_chunks, host.data(), sizeof(ChunkRec) * host.size(), cudaMemcpyHostToDevice,
                                p->copy_stream));
@@ -186,6 +224,56 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
 // Records the pool's last-reader event after a forward/merge, or notes that the
 // call went into a graph under capture (then later loads wait for the device).
+constexpr int QUARANTINE_ID0 = 1 << 28;   // arena ids of quarantined blocks (slots are below)
+constexpr int TABLE_STAGES = 4;
+
+// Returns quarantined blocks whose last reader has finished to the allocator; with
+// `wait`, waits for all of them first.
+mlora_status reclaim(mlora_pool* p, bool wait) {
+    std::vector<mlora_pool::Quarantine> keep;
+    for (const auto& q : p->quarantine) {
+        cudaError_t e = wait ? cudaEventSynchronize(q.free_at) : cudaEventQuery(q.free_at);
+        if (e == cudaErrorNotReady) {
+            keep.push_back(q);
+            continue;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "quarantine event");
+        p->arena.release(q.id);
+        cudaEventDestroy(q.free_at);
+    }
+    p->quarantine.swap(keep);
+    return MLORA_OK;
+}
+
+// Copies the host mirrors of the slot table and the chunk table to the device on
+// the copy stream, from a pinned staging entry, without waiting on the host (unless
+// every entry of the ring is still in flight).  The caller has ordered the copy
+// stream behind the tables' readers.
+mlora_status push_tables_async(mlora_pool* p) {
+    std::vector<ChunkRec> chunks;
+    mlora_status st = build_chunks(p, chunks);
+    if (st != MLORA_OK) return st;
+    mlora_pool::TableStage& sg = p->stages[p->stage_next];
+    p->stage_next = (p->stage_next + 1) % (int)p->stages.size();
+    if (sg.pending) CU_TRY(cudaEventSynchronize(sg.done));
+    SlotRec* recs = reinterpret_cast<SlotRec*>(sg.buf);
+    for (int s = 0; s < p->max_slots; ++s) {
+        const SlotHost& h = p->slots[s];
+        recs[s] = SlotRec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit};
+    }
+    ChunkRec* cr = reinterpret_cast<ChunkRec*>(sg.buf + align_up(sizeof(SlotRec) * (size_t)p->max_slots, 128));
+    std::copy(chunks.begin(), chunks.end(), cr);
+    if (p->max_slots > 0)
+        CU_TRY(cudaMemcpyAsync(p->d_slots, recs, sizeof(SlotRec) * (size_t)p->max_slots, cudaMemcpyHostToDevice,
+                               p->copy_stream));
+    if (!chunks.empty())
+        CU_TRY(cudaMemcpyAsync(p->d_chunks, cr, sizeof(ChunkRec) * chunks.size(), cudaMemcpyHostToDevice,
+                               p->copy_stream));
+    CU_TRY(cudaEventRecord(sg.done, p->copy_stream));
+    sg.pending = true;
+    return MLORA_OK;
+}
+
 mlora_status note_reader(mlora_pool* p, cudaStream_t st) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     CU_TRY(cudaStreamIsCapturing(st, &cs));
@@ -338,6 +426,16 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaStreamCreate"));
     e = cudaEventCreateWithFlags(&p->last_reader, cudaEventDisableTiming);
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
+    e = cudaEventCreateWithFlags(&p->tables_ready, cudaEventDisableTiming);
+    if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
+    p->stages.resize(TABLE_STAGES);
+    for (auto& sg : p->stages) {
+        const size_t bytes = align_up(sizeof(SlotRec) * (size_t)max_slots, 128) + sizeof(ChunkRec) * (size_t)max_chunks;
+        e = cudaHostAlloc((void**)&sg.buf, bytes > 0 ? bytes : 1, cudaHostAllocDefault);
+        if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "pinned table staging: %s", cudaGetErrorString(e)));
+        e = cudaEventCreateWithFlags(&sg.done, cudaEventDisableTiming);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
+    }
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaDeviceSynchronize"));
     *out = p;
@@ -355,6 +453,17 @@ mlora_status mlora_pool_destroy(mlora_pool_t p) {
         cudaStreamSynchronize(p->copy_stream);
         cudaStreamDestroy(p->copy_stream);
     }
+    for (auto& kv : p->cold) {
+        if (kv.second.down) cudaFreeHost(kv.second.down);
+        if (kv.second.up) cudaFreeHost(kv.second.up);
+        if (kv.second.busy) cudaEventDestroy(kv.second.busy);
+    }
+    for (auto& q : p->quarantine) cudaEventDestroy(q.free_at);
+    for (auto& sg : p->stages) {
+        if (sg.buf) cudaFreeHost(sg.buf);
+        if (sg.done) cudaEventDestroy(sg.done);
+    }
+    if (p->tables_ready) cudaEventDestroy(p->tables_ready);
     if (p->ws_base) cudaFree(p->ws_base);
     if (p->table_base) cudaFree(p->table_base);
     if (p->arena_base) cudaFree(p->arena_base);
@@ -369,14 +478,15 @@ mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const void* down, cons
     if (rank < 1 || rank > p->max_rank) return fail(MLORA_ERR_RANK, "rank %d not in [1, %d]", rank, p->max_rank);
     if (!down || !up) return fail(MLORA_ERR_INVALID_ARG, "down/up is NULL");
     SlotHost& h = p->slots[slot];
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    mlora_status st = wait_readers(p);
+    if (st == MLORA_OK) st = reclaim(p, true);   // blocks of earlier prefetch evictions
+    if (st != MLORA_OK) return st;
     const int need = Arena::round8(rank);
     const int have = p->arena.free_units() + (h.rank > 0 ? Arena::round8(h.rank) : 0);
     if (need > have)
         return fail(MLORA_ERR_OOM, "rank budget: adapter needs %d units, %d free (of %d)", need, have, p->units);
-    DeviceGuard g(p->device);
-    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
-    mlora_status st = wait_readers(p);
-    if (st != MLORA_OK) return st;
 
     if (h.rank > 0) {
         p->arena.release(slot);
@@ -428,6 +538,7 @@ mlora_status mlora_unload_adapter(mlora_pool_t p, int slot) {
     DeviceGuard g(p->device);
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     mlora_status st = wait_readers(p);
+    if (st == MLORA_OK) st = reclaim(p, true);
     if (st != MLORA_OK) return st;
     p->arena.release(slot);
     h = SlotHost{0, 0, 0.f, -1, h.version + 1};
@@ -435,6 +546,149 @@ mlora_status mlora_unload_adapter(mlora_pool_t p, int slot) {
     st = push_slot(p, slot);
     if (st != MLORA_OK) return st;
     return push_chunks(p);
+}
+
+mlora_status mlora_host_adapter_add(mlora_pool_t p, int id, const void* down, const void* up, int rank,
+                                   float scale) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (rank < 1 || rank > p->max_rank) return fail(MLORA_ERR_RANK, "rank %d not in [1, %d]", rank, p->max_rank);
+    if (!down || !up) return fail(MLORA_ERR_INVALID_ARG, "down/up is NULL");
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    if (p->cold.count(id)) {   // replacing: the old copy goes first
+        const mlora_status st = mlora_host_adapter_remove(p, id);
+        if (st != MLORA_OK) return st;
+    }
+    mlora_pool::HostAdapter ha;
+    ha.rank = rank;
+    ha.rpad = Arena::round8(rank);
+    ha.scale = scale;
+    const size_t db = (size_t)ha.rpad * p->din * p->esize, ub = (size_t)ha.rpad * p->dout * p->esize;
+    auto drop = [&](mlora_status s) {
+        if (ha.down) cudaFreeHost(ha.down);
+        if (ha.up) cudaFreeHost(ha.up);
+        if (ha.busy) cudaEventDestroy(ha.busy);
+        return s;
+    };
+    cudaError_t e = cudaHostAlloc((void**)&ha.down, db, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaHostAlloc((void**)&ha.up, ub, cudaHostAllocDefault);
+    if (e != cudaSuccess) return drop(fail(MLORA_ERR_OOM, "pinned host tier: %s", cudaGetErrorString(e)));
+    std::memset(ha.down, 0, db);
+    std::memset(ha.up, 0, ub);
+    // Down as its rows; Up [dout x rank] in blocks of 8 rank columns, each [dout x 8]
+    // (the arena's layout, so that a prefetch is two plain copies)
+    e = cudaMemcpy(ha.down, down, (size_t)rank * p->din * p->esize, cudaMemcpyDefault);
+    for (int b = 0; e == cudaSuccess && b * 8 < rank; ++b) {
+        const int w = (rank - 8 * b) < 8 ? (rank - 8 * b) : 8;
+        e = cudaMemcpy2D(ha.up + (size_t)b * p->dout * 8 * p->esize, 8 * p->esize,
+                         (const char*)up + (size_t)8 * b * p->esize, (size_t)rank * p->esize, (size_t)w * p->esize,
+                         (size_t)p->dout, cudaMemcpyDefault);
+    }
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ha.busy, cudaEventDisableTiming);
+    if (e != cudaSuccess) return drop(cuda_fail(e, "host tier copy"));
+    p->cold[id] = ha;
+    return MLORA_OK;
+}
+
+mlora_status mlora_host_adapter_remove(mlora_pool_t p, int id) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    auto it = p->cold.find(id);
+    if (it == p->cold.end()) return fail(MLORA_ERR_NOT_LOADED, "no host-tier adapter %d", id);
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    mlora_pool::HostAdapter& ha = it->second;
+    if (ha.busy_pending) CU_TRY(cudaEventSynchronize(ha.busy));   // a prefetch may still copy out of it
+    cudaFreeHost(ha.down);
+    cudaFreeHost(ha.up);
+    cudaEventDestroy(ha.busy);
+    p->cold.erase(it);
+    return MLORA_OK;
+}
+
+mlora_status mlora_prefetch(mlora_pool_t p, int slot, int id, mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    auto it = p->cold.find(id);
+    if (it == p->cold.end()) return fail(MLORA_ERR_NOT_LOADED, "no host-tier adapter %d", id);
+    mlora_pool::HostAdapter& ha = it->second;
+    SlotHost& h = p->slots[slot];
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    mlora_status rs = reclaim(p, false);
+    if (rs == MLORA_OK && p->arena.free_units() < ha.rpad) rs = reclaim(p, true);
+    if (rs != MLORA_OK) return rs;
+
+    // Placement.  Normally the new copy goes to free units while the slot's current
+    // block stays allocated under a quarantine id, since forwards already enqueued
+    // may still read it; it returns to the allocator once they have finished.  When
+    // only the slot's own units, or a compaction, make room, the readers are waited
+    // for on the host first (the synchronous path of mlora_load_adapter).
+    const bool had = h.rank > 0;
+    int unit = -1;
+    int old_block = -1;
+    if (p->arena.free_units() >= ha.rpad) {
+        if (had) {
+            old_block = QUARANTINE_ID0 + p->next_qid++;
+            p->arena.rename(slot, old_block);
+        }
+        unit = p->arena.alloc(slot, ha.rank);
+    } else if ((had ? h.rpad : 0) + p->arena.free_units() < ha.rpad) {
+        return fail(MLORA_ERR_OOM, "rank budget: adapter needs %d units, %d free (of %d)", ha.rpad,
+                    p->arena.free_units() + (had ? h.rpad : 0), p->units);
+    }
+    if (unit < 0) {
+        rs = wait_readers(p);
+        if (rs == MLORA_OK) rs = reclaim(p, true);   // the compaction below moves slot blocks only
+        if (rs != MLORA_OK) return rs;
+        if (old_block >= 0) p->arena.release(old_block);
+        else if (had) p->arena.release(slot);
+        old_block = -1;
+        unit = p->arena.alloc(slot, ha.rank);
+        if (unit < 0) {
+            for (const ArenaMove& m : p->arena.compact()) {   // slot blocks only: the quarantine is empty
+                rs = move_units(p, m.from, m.to, m.size);
+                if (rs != MLORA_OK) return rs;
+                p->slots[m.id].unit = m.to;
+            }
+            unit = p->arena.alloc(slot, ha.rank);
+            if (unit < 0) return fail(MLORA_ERR_OOM, "arena placement failed after compaction");
+        }
+    }
+    if (had) --p->loaded;
+
+    // 1. the weights, into units that no enqueued forward reads: at once, beside them
+    CU_TRY(cudaMemcpyAsync(p->arena_down + (size_t)unit * p->din * p->esize, ha.down,
+                           (size_t)ha.rpad * p->din * p->esize, cudaMemcpyHostToDevice, p->copy_stream));
+    CU_TRY(cudaMemcpyAsync(p->arena_up + (size_t)unit * p->dout * p->esize, ha.up,
+                           (size_t)ha.rpad * p->dout * p->esize, cudaMemcpyHostToDevice, p->copy_stream));
+    CU_TRY(cudaEventRecord(ha.busy, p->copy_stream));
+    ha.busy_pending = true;
+    // 2. the tables, once the forwards enqueued so far (their readers) have finished
+    if (p->captured) {
+        rs = wait_readers(p);   // graph replays are invisible to the pool's events
+        if (rs != MLORA_OK) return rs;
+    } else if (p->reader_pending) {
+        CU_TRY(cudaStreamWaitEvent(p->copy_stream, p->last_reader, 0));
+    }
+    h.rank = ha.rank;
+    h.rpad = ha.rpad;
+    h.scale = ha.scale;
+    h.unit = unit;
+    h.version += 1;
+    ++p->loaded;
+    rs = push_tables_async(p);
+    if (rs != MLORA_OK) return rs;
+    CU_TRY(cudaEventRecord(p->tables_ready, p->copy_stream));
+    if (old_block >= 0) {   // the evicted block is free once no table names it and its readers are done
+        cudaEvent_t ev;
+        CU_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+        CU_TRY(cudaEventRecord(ev, p->copy_stream));
+        p->quarantine.push_back({old_block, ev});
+    }
+    // 3. later work on the caller's stream runs with the adapter in place
+    CU_TRY(cudaStreamWaitEvent(st, p->tables_ready, 0));
+    return MLORA_OK;
 }
 
 mlora_status mlora_adapter_version(mlora_pool_t p, int slot, uint64_t* version) {

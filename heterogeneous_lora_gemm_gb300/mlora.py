@@ -59,6 +59,9 @@ _SIGNATURES = {
     "mlora_load_adapter": (_I, [_P, _I, _P, _P, _I, ctypes.c_float]),
     "mlora_unload_adapter": (_I, [_P, _I]),
     "mlora_adapter_version": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint64)]),
+    "mlora_host_adapter_add": (_I, [_P, _I, _P, _P, _I, ctypes.c_float]),
+    "mlora_host_adapter_remove": (_I, [_P, _I]),
+    "mlora_prefetch": (_I, [_P, _I, _I, _P]),
     "mlora_forward": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "mlora_merge": (_I, [_P, _P, _I, _P]),
     "mlora_unmerge": (_I, [_P, _P, _I, _P]),
@@ -71,6 +74,7 @@ _SIGNATURES = {
     "mlora_arena_delete": (None, [_P]),
     "mlora_arena_alloc": (_I, [_P, _I, _I]),
     "mlora_arena_free": (_I, [_P, _I]),
+    "mlora_arena_rename": (_I, [_P, _I, _I]),
     "mlora_arena_compact": (_I, [_P, _P, _I]),
     "mlora_arena_used": (_I, [_P]),
     "mlora_arena_largest_hole": (_I, [_P]),
@@ -136,6 +140,18 @@ def mlora_forward(pool: int, X_ptr: int, W_ptr: int, row_adapter_ptr: Optional[i
                   stream: int) -> None:
     check(lib().mlora_forward(pool, X_ptr, W_ptr, row_adapter_ptr or None, T, Y_ptr, stream or None),
           "mlora_forward")
+
+
+def mlora_host_adapter_add(pool: int, id_: int, down_ptr: int, up_ptr: int, rank: int, scale: float) -> None:
+    check(lib().mlora_host_adapter_add(pool, id_, down_ptr, up_ptr, rank, scale), "mlora_host_adapter_add")
+
+
+def mlora_host_adapter_remove(pool: int, id_: int) -> None:
+    check(lib().mlora_host_adapter_remove(pool, id_), "mlora_host_adapter_remove")
+
+
+def mlora_prefetch(pool: int, slot: int, id_: int, stream: int) -> None:
+    check(lib().mlora_prefetch(pool, slot, id_, stream or None), "mlora_prefetch")
 
 
 def mlora_merge(pool: int, W_ptr: int, slot: int, stream: int) -> None:
@@ -216,6 +232,18 @@ class Pool:
 
     def unload(self, slot: int) -> None:
         mlora_unload_adapter(self.handle, slot)
+
+    def host_add(self, id_: int, down, up, scale: float) -> None:
+        """Copies an adapter (torch tensors, host or device) into the pool's pinned host tier."""
+        down = down.contiguous()
+        up = up.contiguous()
+        mlora_host_adapter_add(self.handle, id_, down.data_ptr(), up.data_ptr(), int(down.shape[0]), float(scale))
+
+    def host_remove(self, id_: int) -> None:
+        mlora_host_adapter_remove(self.handle, id_)
+
+    def prefetch(self, slot: int, id_: int, stream=None) -> None:
+        mlora_prefetch(self.handle, slot, id_, _stream_handle(stream))
 
     def version(self, slot: int) -> int:
         return mlora_adapter_version(self.handle, slot)

@@ -134,6 +134,37 @@ mlora_status mlora_unload_adapter(mlora_pool_t pool, int slot);
 mlora_status mlora_adapter_version(mlora_pool_t pool, int slot, uint64_t* version);
 
 /*
+ * Host (cold) tier of adapters (M031 §06: cold adapters on the host, hot ones on the
+ * device, fetched for the batch that needs them; the weights must be in place before
+ * the forward runs, and a slot is overwritten only after its last reader).
+ *
+ * mlora_host_adapter_add copies an adapter into pinned host memory owned by the
+ * pool, under the caller's `id` (any int; an existing id is replaced once no
+ * prefetch still copies out of it).  Down [rank x din], Up [dout x rank] as for
+ * mlora_load_adapter, host or device memory, pool dtype; the caller may free them
+ * when the call returns.  Errors: INVALID_ARG, RANK, OOM, CUDA.
+ */
+mlora_status mlora_host_adapter_add(mlora_pool_t pool, int id, const void* down, const void* up, int rank,
+                                   float scale);
+/* Frees the host-tier copy of `id` (waits for a prefetch still copying out of it).
+ * Errors: INVALID_ARG, NOT_LOADED (no such id), CUDA. */
+mlora_status mlora_host_adapter_remove(mlora_pool_t pool, int id);
+/*
+ * Loads host-tier adapter `id` into `slot` without waiting on the host.  On the
+ * pool's copy stream, the weights go into free arena units at once (overlapping
+ * forwards already enqueued); the slot and chunk tables change only once the
+ * forwards enqueued so far have finished (a GPU-side wait on their last event); the
+ * slot's previous adapter keeps its units until then.  `stream` is made to wait for
+ * the update: forwards enqueued on it afterwards see the new adapter, forwards
+ * enqueued before see the old one.  Forwards on other streams must be ordered after
+ * `stream` by the caller.  The slot's version advances.  When only the slot's own
+ * units or a compaction make room, or forwards of the pool were captured into a
+ * graph, the call waits for the pool's readers on the host first.
+ * Errors: INVALID_ARG, BAD_SLOT, NOT_LOADED (no such id), OOM (rank budget), CUDA.
+ */
+mlora_status mlora_prefetch(mlora_pool_t pool, int slot, int id, mlora_stream_t stream);
+
+/*
  * The multi-LoRA forward (M031 §02): Y = X W^T for all T rows, plus
  * scale_a Up_a (Down_a x) on every row x whose adapter is a, in original row
  * order.  Segment build, shrink, base projection and expand all run in this
@@ -255,6 +286,10 @@ void mlora_arena_delete(mlora_arena_t arena);
 int mlora_arena_alloc(mlora_arena_t arena, int id, int n);
 /* Frees the block of `id`; returns 0, or -1 if `id` holds no block. */
 int mlora_arena_free(mlora_arena_t arena, int id);
+/* Gives the block of `from` to `to` in place (the pool quarantines an evicted
+ * adapter's block this way until its last reader has finished); returns 0, or -1
+ * if `from` holds no block or `to` already holds one. */
+int mlora_arena_rename(mlora_arena_t arena, int from, int to);
 /* Compacts; writes up to `cap` moves as (id, old_offset, new_offset) triples; returns the count. */
 int mlora_arena_compact(mlora_arena_t arena, int32_t* moves, int cap);
 /* Units in use and largest free hole. */

@@ -150,3 +150,21 @@ def test_arena_compaction_recovers_fragmented_space(lib):
     assert L.mlora_arena_largest_hole(a) == 32
     assert L.mlora_arena_alloc(a, 20, 32) == 32
     L.mlora_arena_delete(a)
+
+
+def test_arena_rename_keeps_the_block_in_place(lib):
+    """An evicted adapter's block is renamed to a quarantine id, not freed: a new
+    allocation must land elsewhere until the quarantine is released."""
+    L = lib.lib()
+    a = L.mlora_arena_new(48)
+    assert L.mlora_arena_alloc(a, 0, 16) == 0
+    assert L.mlora_arena_alloc(a, 1, 16) == 16
+    assert L.mlora_arena_rename(a, 0, 1000) == 0
+    assert L.mlora_arena_rename(a, 0, 1001) == -1      # 0 holds nothing now
+    assert L.mlora_arena_rename(a, 1, 1000) == -1      # 1000 holds a block already
+    assert L.mlora_arena_used(a) == 32
+    assert L.mlora_arena_alloc(a, 0, 16) == 32         # not the quarantined units 0..15
+    assert L.mlora_arena_alloc(a, 2, 8) == -1
+    assert L.mlora_arena_free(a, 1000) == 0
+    assert L.mlora_arena_alloc(a, 2, 8) == 0
+    L.mlora_arena_delete(a)

@@ -348,6 +348,107 @@ def test_load_waits_for_last_reader_and_versions():
     assert e.value.status == mlora.MLORA_ERR_NOT_LOADED
 
 
+# --------------------------------------------------------------------------- #
+# host (cold) tier and asynchronous prefetch (M031 §06)
+def _host_tier_pool(layer, extra_budget=0, max_rank=None):
+    from heterogeneous_lora_gemm_gb300 import Pool
+    budget = sum((a.rank + 7) // 8 * 8 for a in layer.adapters) + extra_budget
+    return Pool(layer.max_slots, budget, max_rank or layer.max_rank, layer.din, layer.dout, layer.dtype,
+                max(layer.T, 1))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_prefetch_from_host_tier_matches_oracle(dtype):
+    """Adapters registered in the pinned host tier and prefetched into their slots
+    on the forward's stream: the forward enqueued right after sees them in place."""
+    layer = wl.random_layer(31, T=48, din=256, dout=192, ranks=[16, 8, 24, 40], dtype=dtype)
+    pool = _host_tier_pool(layer)
+    stream = torch.cuda.Stream()
+    for a in layer.adapters:   # host sources, ids unrelated to the slots
+        pool.host_add(1000 + a.slot, to_device(a.down, dtype, "cpu"), to_device(a.up, dtype, "cpu"), a.scale)
+    X, W, ra, Y = upload(layer)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for a in layer.adapters:
+            pool.prefetch(a.slot, 1000 + a.slot, stream=stream)
+        pool.forward(X, W, ra, Y, stream=stream)
+    torch.cuda.synchronize()
+    assert_within(to_f64(Y), want_of(layer), dtype, "forward after prefetches")
+    assert all(pool.version(a.slot) == 1 for a in layer.adapters)
+    check_segments(layer, pool)
+    assert pool.status() == mlora.MLORA_OK
+
+
+def test_prefetch_replaces_a_slot_only_after_its_readers():
+    """Forwards enqueued before a prefetch into their slot read the old adapter, the
+    ones after it the new one, with no host wait in between (the new weights go to
+    free units, the tables change behind the earlier forwards).  Repeated swaps
+    recycle the evicted blocks through the quarantine."""
+    layer = wl.random_layer(32, T=64, din=1024, dout=1024, ranks=[16, 16], p_none=0.0)
+    other = wl.random_layer(33, T=64, din=1024, dout=1024, ranks=[16, 16], p_none=0.0)
+    pool = _host_tier_pool(layer, extra_budget=32)   # room for the new copies beside the old
+    a0, a1 = layer.adapters
+    b0 = other.adapters[0]
+    for id_, a in ((0, a0), (1, a1), (2, b0)):
+        pool.host_add(id_, to_device(a.down, "bf16", "cpu"), to_device(a.up, "bf16", "cpu"), a.scale)
+    stream = torch.cuda.Stream()
+    X, W, ra, _ = upload(layer)
+    with torch.cuda.stream(stream):
+        pool.prefetch(0, 0, stream=stream)
+        pool.prefetch(1, 1, stream=stream)
+    want_a = want_of(layer)
+    swapped = [oracle.OracleAdapter(b0.down_f64, b0.up_f64, b0.scale), ora_adapters(layer)[1]]
+    want_b = oracle.forward(layer.X_f64, layer.W_f64, layer.row_adapter, swapped)
+    outs = []
+    with torch.cuda.stream(stream):
+        for rep in range(6):
+            ys_a = [torch.empty((layer.T, layer.dout), dtype=torch.bfloat16, device="cuda") for _ in range(8)]
+            for y in ys_a:
+                pool.forward(X, W, ra, y, stream=stream)
+            pool.prefetch(0, 2 if rep % 2 == 0 else 0, stream=stream)   # B, then A back, ...
+            y_b = torch.empty_like(ys_a[0])
+            pool.forward(X, W, ra, y_b, stream=stream)
+            outs.append((ys_a, y_b, rep))
+    torch.cuda.synchronize()
+    for ys_a, y_b, rep in outs:
+        before, after = (want_a, want_b) if rep % 2 == 0 else (want_b, want_a)
+        for k, y in enumerate(ys_a):
+            assert_within(to_f64(y), before, "bf16", f"swap {rep}: forward {k} before the prefetch")
+        assert_within(to_f64(y_b), after, "bf16", f"swap {rep}: forward after the prefetch")
+    assert pool.version(0) == 7
+    assert pool.status() == mlora.MLORA_OK
+
+
+def test_prefetch_errors_and_host_tier_lifecycle():
+    layer = wl.random_layer(34, T=8, din=64, dout=64, ranks=[16])
+    pool = _host_tier_pool(layer, max_rank=64)
+    a = layer.adapters[0]
+    down, up = to_device(a.down, "bf16", "cpu"), to_device(a.up, "bf16", "cpu")
+    with pytest.raises(mlora.MloraError) as e:
+        pool.prefetch(0, 5)
+    assert e.value.status == mlora.MLORA_ERR_NOT_LOADED
+    pool.host_add(5, down, up, a.scale)
+    with pytest.raises(mlora.MloraError) as e:
+        pool.prefetch(layer.max_slots, 5)
+    assert e.value.status == mlora.MLORA_ERR_BAD_SLOT
+    big = wl.random_layer(35, T=8, din=64, dout=64, ranks=[64]).adapters[0]
+    pool.host_add(6, to_device(big.down, "bf16", "cpu"), to_device(big.up, "bf16", "cpu"), big.scale)
+    with pytest.raises(mlora.MloraError) as e:     # 64 units against a budget of 16
+        pool.prefetch(0, 6)
+    assert e.value.status == mlora.MLORA_ERR_OOM
+    with pytest.raises(mlora.MloraError) as e:
+        pool.host_add(7, down[:0], up[:, :0], 1.0)
+    assert e.value.status == mlora.MLORA_ERR_RANK
+    pool.prefetch(0, 5)
+    pool.host_add(5, down, up, 2 * a.scale)          # replaced in the host tier, not in the slot
+    pool.host_remove(5)
+    with pytest.raises(mlora.MloraError) as e:
+        pool.host_remove(5)
+    assert e.value.status == mlora.MLORA_ERR_NOT_LOADED
+    torch.cuda.synchronize()
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "slot keeps the prefetched copy")
+
+
 def test_arena_compaction_keeps_adapters_correct():
     ranks = [16, 64, 8, 24, 16, 8]
     layer = wl.random_layer(11, T=96, din=256, dout=192, ranks=ranks, p_none=0.1)
