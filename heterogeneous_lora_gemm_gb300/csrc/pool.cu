@@ -89,9 +89,15 @@ struct mlora_pool {
     char* arena_down = nullptr;
     char* arena_up = nullptr;
     size_t arena_bytes = 0;
-    char* table_base = nullptr;      // slot table, then the chunk table
-    SlotRec* d_slots = nullptr;
-    ChunkRec* d_chunks = nullptr;    // chunks of the loaded slots, ascending slot (tensor path)
+    char* table_base = nullptr;      // two table sets, each the slot table then the chunk table
+    size_t slots_bytes = 0;          // the slot table's share of a set (the chunk table follows)
+    SlotRec* set_slots[2] = {nullptr, nullptr};
+    ChunkRec* set_chunks[2] = {nullptr, nullptr};
+    int cur = 0;                     // the set that forwards enqueued now read
+    cudaEvent_t set_retired[2] = {nullptr, nullptr};   // set s's readers done (recorded when it stopped being current)
+    bool set_retired_pending[2] = {false, false};
+    SlotRec* d_slots = nullptr;      // = set_slots[cur]
+    ChunkRec* d_chunks = nullptr;    // = set_chunks[cur]: chunks of the loaded slots, in arena order
     int n_chunks = 0;
     int tile_span = 0;               // largest arena span of 8 consecutive chunks of the table
     TcArenaMaps maps{};              // TMA descriptors of the whole arena (bf16 pools)
@@ -245,11 +251,11 @@ mlora_status reclaim(mlora_pool* p, bool wait) {
     return MLORA_OK;
 }
 
-// Copies the host mirrors of the slot table and the chunk table to the device on
-// the copy stream, from a pinned staging entry, without waiting on the host (unless
-// every entry of the ring is still in flight).  The caller has ordered the copy
-// stream behind the tables' readers.
-mlora_status push_tables_async(mlora_pool* p) {
+// Copies the host mirrors of the slot table and the chunk table into table set
+// `set` on the copy stream, as one copy from a pinned staging entry laid out like
+// the set, without waiting on the host (unless every entry of the ring is still in
+// flight).  The caller has ordered the copy stream behind the set's readers.
+mlora_status push_tables_async(mlora_pool* p, int set) {
     std::vector<ChunkRec> chunks;
     mlora_status st = build_chunks(p, chunks);
     if (st != MLORA_OK) return st;
@@ -261,14 +267,10 @@ mlora_status push_tables_async(mlora_pool* p) {
         const SlotHost& h = p->slots[s];
         recs[s] = SlotRec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit};
     }
-    ChunkRec* cr = reinterpret_cast<ChunkRec*>(sg.buf + align_up(sizeof(SlotRec) * (size_t)p->max_slots, 128));
+    ChunkRec* cr = reinterpret_cast<ChunkRec*>(sg.buf + p->slots_bytes);
     std::copy(chunks.begin(), chunks.end(), cr);
-    if (p->max_slots > 0)
-        CU_TRY(cudaMemcpyAsync(p->d_slots, recs, sizeof(SlotRec) * (size_t)p->max_slots, cudaMemcpyHostToDevice,
-                               p->copy_stream));
-    if (!chunks.empty())
-        CU_TRY(cudaMemcpyAsync(p->d_chunks, cr, sizeof(ChunkRec) * chunks.size(), cudaMemcpyHostToDevice,
-                               p->copy_stream));
+    CU_TRY(cudaMemcpyAsync(p->set_slots[set], sg.buf, p->slots_bytes + sizeof(ChunkRec) * chunks.size(),
+                           cudaMemcpyHostToDevice, p->copy_stream));
     CU_TRY(cudaEventRecord(sg.done, p->copy_stream));
     sg.pending = true;
     return MLORA_OK;
@@ -356,14 +358,22 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     // chunks of 16 rank columns: each slot's last chunk may be partial
     const int max_chunks = p->units / CHUNK + max_slots + 1;
     // slot table and chunk table
+    // Two sets of (slot table, chunk table): forwards read the current one while a
+    // prefetch writes the other, which then becomes current.
     const size_t slots_bytes = align_up(sizeof(SlotRec) * (size_t)(max_slots > 0 ? max_slots : 1), 128);
-    p->table_bytes = slots_bytes + align_up(sizeof(ChunkRec) * (size_t)max_chunks, 128);
+    const size_t set_bytes = slots_bytes + align_up(sizeof(ChunkRec) * (size_t)max_chunks, 128);
+    p->slots_bytes = slots_bytes;
+    p->table_bytes = 2 * set_bytes;
     e = cudaMalloc((void**)&p->table_base, p->table_bytes);
     if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "slot table: %s", cudaGetErrorString(e)));
     e = cudaMemset(p->table_base, 0, p->table_bytes);
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaMemset(slot table)"));
-    p->d_slots = (SlotRec*)p->table_base;
-    p->d_chunks = (ChunkRec*)(p->table_base + slots_bytes);
+    for (int k = 0; k < 2; ++k) {
+        p->set_slots[k] = (SlotRec*)(p->table_base + k * set_bytes);
+        p->set_chunks[k] = (ChunkRec*)(p->table_base + k * set_bytes + slots_bytes);
+    }
+    p->d_slots = p->set_slots[0];
+    p->d_chunks = p->set_chunks[0];
     if (dtype == MLORA_BF16 && p->units > 0 &&
         !tc_encode_arena_maps(&p->maps, p->arena_down, p->arena_up, p->units, din, dout))
         return bail(fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the adapter arena"));
@@ -428,9 +438,13 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
     e = cudaEventCreateWithFlags(&p->tables_ready, cudaEventDisableTiming);
     if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
+    for (int k = 0; k < 2; ++k) {
+        e = cudaEventCreateWithFlags(&p->set_retired[k], cudaEventDisableTiming);
+        if (e != cudaSuccess) return bail(cuda_fail(e, "cudaEventCreate"));
+    }
     p->stages.resize(TABLE_STAGES);
     for (auto& sg : p->stages) {
-        const size_t bytes = align_up(sizeof(SlotRec) * (size_t)max_slots, 128) + sizeof(ChunkRec) * (size_t)max_chunks;
+        const size_t bytes = set_bytes;
         e = cudaHostAlloc((void**)&sg.buf, bytes > 0 ? bytes : 1, cudaHostAllocDefault);
         if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "pinned table staging: %s", cudaGetErrorString(e)));
         e = cudaEventCreateWithFlags(&sg.done, cudaEventDisableTiming);
@@ -464,6 +478,8 @@ mlora_status mlora_pool_destroy(mlora_pool_t p) {
         if (sg.done) cudaEventDestroy(sg.done);
     }
     if (p->tables_ready) cudaEventDestroy(p->tables_ready);
+    for (int k = 0; k < 2; ++k)
+        if (p->set_retired[k]) cudaEventDestroy(p->set_retired[k]);
     if (p->ws_base) cudaFree(p->ws_base);
     if (p->table_base) cudaFree(p->table_base);
     if (p->arena_base) cudaFree(p->arena_base);
@@ -664,12 +680,14 @@ mlora_status mlora_prefetch(mlora_pool_t p, int slot, int id, mlora_stream_t str
                            (size_t)ha.rpad * p->dout * p->esize, cudaMemcpyHostToDevice, p->copy_stream));
     CU_TRY(cudaEventRecord(ha.busy, p->copy_stream));
     ha.busy_pending = true;
-    // 2. the tables, once the forwards enqueued so far (their readers) have finished
+    // 2. the tables, into the set that forwards do not read now, once the forwards that
+    //    read it before the last flip have finished; then that set becomes current
+    const int target = 1 - p->cur;
     if (p->captured) {
         rs = wait_readers(p);   // graph replays are invisible to the pool's events
         if (rs != MLORA_OK) return rs;
-    } else if (p->reader_pending) {
-        CU_TRY(cudaStreamWaitEvent(p->copy_stream, p->last_reader, 0));
+    } else if (p->set_retired_pending[target]) {
+        CU_TRY(cudaStreamWaitEvent(p->copy_stream, p->set_retired[target], 0));
     }
     h.rank = ha.rank;
     h.rpad = ha.rpad;
@@ -677,15 +695,22 @@ mlora_status mlora_prefetch(mlora_pool_t p, int slot, int id, mlora_stream_t str
     h.unit = unit;
     h.version += 1;
     ++p->loaded;
-    rs = push_tables_async(p);
+    rs = push_tables_async(p, target);
     if (rs != MLORA_OK) return rs;
     CU_TRY(cudaEventRecord(p->tables_ready, p->copy_stream));
-    if (old_block >= 0) {   // the evicted block is free once no table names it and its readers are done
+    // the current set's readers: everything enqueued on the caller's stream so far
+    CU_TRY(cudaEventRecord(p->set_retired[p->cur], st));
+    p->set_retired_pending[p->cur] = true;
+    if (old_block >= 0) {   // the evicted block is named only by the retiring set
         cudaEvent_t ev;
         CU_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
-        CU_TRY(cudaEventRecord(ev, p->copy_stream));
+        CU_TRY(cudaEventRecord(ev, st));
         p->quarantine.push_back({old_block, ev});
     }
+    p->cur = target;
+    p->d_slots = p->set_slots[target];
+    p->d_chunks = p->set_chunks[target];
+    p->ws.chunks = p->d_chunks;
     // 3. later work on the caller's stream runs with the adapter in place
     CU_TRY(cudaStreamWaitEvent(st, p->tables_ready, 0));
     return MLORA_OK;
