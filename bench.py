@@ -190,7 +190,72 @@ def profiled_traffic(kernel: str, workload: str):
     return d.get("dram_bytes_per_launch")
 
 
+def multi_module_timing(seed: int, dev, stream, reps: int = 64):
+    """q and v of one 7B-shaped layer in one launch -- a fused q|v projection whose
+    slots each hold a tenant's q and v adapters -- against the two projections
+    launched one after the other, on the same rows (the q rows' tenant mapping)."""
+    import torch
+
+    from heterogeneous_lora_gemm_gb300 import Pool
+    from tests.gpu_harness import make_pool, to_device
+    from tests.tolerance import within
+    Lq, Lv = wl.stack7b_projection(seed, 0, "q"), wl.stack7b_projection(seed, 0, "v")
+    T, din, dout = Lq.T, Lq.din, Lq.dout
+    ra = torch.from_numpy(Lq.row_adapter.astype(np.int32)).to(dev)
+    X = to_device(Lq.X, "bf16")
+    qa, va = {a.slot: a for a in Lq.adapters}, {a.slot: a for a in Lv.adapters}
+    budget = sum(-(-a.rank // 16) * 16 for a in Lq.adapters + Lv.adapters)
+    fpool = Pool(Lq.max_slots, budget, 64, din, 2 * dout, "bf16", T)
+    for s_ in range(Lq.max_slots):
+        mods = []
+        for off, ad in ((0, qa.get(s_)), (dout, va.get(s_))):
+            mods.append((off, dout, to_device(ad.down, "bf16"), to_device(ad.up, "bf16"), ad.scale) if ad
+                        else (off, dout, None, None, 0.0))
+        fpool.load_modules(s_, mods)
+    qpool, vpool = make_pool(Lq), make_pool(Lv)
+    copies = 3   # W of the pair: 64 MiB per copy, rotated
+    Wq = [to_device(Lq.W, "bf16") for _ in range(copies)]
+    Wv = [to_device(Lv.W, "bf16") for _ in range(copies)]
+    Wqv = [torch.cat([a, b], 0) for a, b in zip(Wq, Wv)]
+    Yqv = torch.empty((T, 2 * dout), dtype=torch.bfloat16, device=dev)
+    Yq, Yv = torch.empty((T, dout), dtype=torch.bfloat16, device=dev), torch.empty_like(Yqv[:, :dout])
+
+    def fused(k):
+        fpool.forward(X, Wqv[k % copies], ra, Yqv, stream=stream)
+
+    def apart(k):
+        qpool.forward(X, Wq[k % copies], ra, Yq, stream=stream)
+        vpool.forward(X, Wv[k % copies], ra, Yv, stream=stream)
+
+    out = {}
+    for name, fn in (("fused_qv_us", fused), ("separate_q_plus_v_us", apart)):
+        with torch.cuda.stream(stream):
+            for k in range(8):
+                fn(k)
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(reps):
+                fn(k)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out[name] = e0.elapsed_time(e1) * 1e3 / (4 * reps)
+    got = torch.cat([Yq, Yv], 1).to(torch.float64).cpu().numpy()
+    out["agree"] = bool(within(Yqv.to(torch.float64).cpu().numpy(), got, "bf16").all())
+    out.update({"T": T, "tenants": len(qa), "ranks": "16 (q) + 16 (v) per tenant"})
+    for pl in (fpool, qpool, vpool):
+        pl.close()
+    return out
+
+
 # --------------------------------------------------------------------------- #
+# workload bookkeeping# --------------------------------------------------------------------------- #
 # workload bookkeeping
 def layer_work(layer: wl.LayerData):
     """Algorithmic bytes and FLOPs of one forward and of its projection kernel."""
@@ -464,6 +529,11 @@ def run_ours(args, dist, rank, local):
                  "copies": len(Wm)}
         del Wm
 
+    # ---- q and v of a layer in one launch (fused projection) against two launches
+    multi_module = None
+    if args.workload == "stack7b" and rank == 0:
+        multi_module = multi_module_timing(args.seed, dev, stream)
+
     # ---- host tier: a rank-16 adapter prefetched from pinned host memory into a spare
     # slot (M031 §06).  Cost of a prefetch alone (its H2D copies and the table update,
     # on the forward's stream), and the step time with one prefetch per step beside
@@ -549,7 +619,7 @@ def run_ours(args, dist, rank, local):
                    "seed": args.seed},
         "roofline": roof,
         "step_roofline": {"frac": step_roof_s / step_s, "bytes": int(layer_step_bytes), "flops": int(layer_flops)},
-        "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks, "spot_check": spot, "merge": merge, "prefetch": prefetch,
+        "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks, "spot_check": spot, "merge": merge, "prefetch": prefetch, "multi_module": multi_module,
     }
     return out, L0
 

@@ -34,6 +34,8 @@ struct ChunkRec {
     int32_t unit;    // arena rank unit of the chunk's first column (a multiple of 8)
     int32_t kval;    // valid rank columns, 1..16
     float scale;
+    int32_t row0, row1;   // output rows [row0, row1) its Up columns reach (a module of a fused
+                          // projection); every row for an adapter of the whole layer
 };
 
 // Bits of the device status word.

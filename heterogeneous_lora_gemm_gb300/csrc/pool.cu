@@ -66,9 +66,27 @@ struct SlotHost {
     float scale = 0.f;
     int unit = -1;
     uint64_t version = 0;
+    // per chunk: output rows its Up columns reach (modules of a fused projection);
+    // empty for an adapter of the whole layer
+    std::vector<std::pair<int, int>> chunk_rows;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// bf16 <-> fp32 on the host: bf16 is the upper half of an fp32; rounding to nearest,
+// ties to even, on the dropped lower half (inputs here are finite)
+float bf16_to_f32(uint16_t b) {
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+}
+uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
 
 }  // namespace
 
@@ -182,7 +200,9 @@ mlora_status build_chunks(mlora_pool* p, std::vector<ChunkRec>& host) {
         if (h.rank <= 0) continue;
         for (int j = 0; j * CHUNK < h.rank; ++j) {
             const int kv = h.rank - j * CHUNK;
-            host.push_back(ChunkRec{s, h.unit + j * CHUNK, kv < CHUNK ? kv : CHUNK, h.scale});
+            const bool mod = j < (int)h.chunk_rows.size();
+            host.push_back(ChunkRec{s, h.unit + j * CHUNK, kv < CHUNK ? kv : CHUNK, h.scale,
+                                    mod ? h.chunk_rows[j].first : 0, mod ? h.chunk_rows[j].second : p->dout});
         }
     }
     std::sort(host.begin(), host.end(), [](const ChunkRec& x, const ChunkRec& y) { return x.unit < y.unit; });
@@ -540,9 +560,72 @@ mlora_status mlora_load_adapter(mlora_pool_t p, int slot, const void* down, cons
     h.scale = scale;
     h.unit = unit;
     h.version += 1;
+    h.chunk_rows.clear();   // an adapter of the whole layer
     ++p->loaded;
     st = push_slot(p, slot);
     if (st != MLORA_OK) return st;
+    return push_chunks(p);
+}
+
+mlora_status mlora_load_adapter_modules(mlora_pool_t p, int slot, int n, const int* row_offset, const int* rows,
+                                        const void* const* down, const void* const* up, const int* rank,
+                                        const float* scale) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    if (n < 1 || !row_offset || !rows || !down || !up || !rank || !scale)
+        return fail(MLORA_ERR_INVALID_ARG, "bad module arrays");
+    // The combined adapter: module m takes rank columns [col[m], col[m] + round16(rank[m]))
+    // (whole chunks, so that every chunk belongs to one module); Down stacks the
+    // modules' rows, Up places module m's [rows[m] x rank[m]] at its output rows and
+    // its columns, zero elsewhere.
+    int R = 0;
+    float common = 0.f;
+    bool same = true;
+    std::vector<int> col(n, 0);
+    for (int m = 0; m < n; ++m) {
+        if (rank[m] < 0 || rows[m] < 0 || row_offset[m] < 0 || row_offset[m] + rows[m] > p->dout)
+            return fail(MLORA_ERR_INVALID_ARG, "module %d: rows [%d, %d) or rank %d out of range", m, row_offset[m],
+                        row_offset[m] + rows[m], rank[m]);
+        if (rank[m] == 0) continue;
+        if (!down[m] || !up[m]) return fail(MLORA_ERR_INVALID_ARG, "module %d: down/up is NULL", m);
+        col[m] = R;
+        R += (rank[m] + CHUNK - 1) / CHUNK * CHUNK;
+        if (common == 0.f) common = scale[m];
+        else if (scale[m] != common) same = false;
+    }
+    if (R < 1 || R > p->max_rank) return fail(MLORA_ERR_RANK, "combined rank %d not in [1, %d]", R, p->max_rank);
+    const size_t es = p->esize;
+    std::vector<char> dc((size_t)R * p->din * es, 0), uc((size_t)p->dout * R * es, 0);
+    std::vector<std::pair<int, int>> chunk_rows(R / CHUNK);
+    for (int m = 0; m < n; ++m) {
+        if (rank[m] == 0) continue;
+        CU_TRY(cudaMemcpy(dc.data() + (size_t)col[m] * p->din * es, down[m], (size_t)rank[m] * p->din * es,
+                          cudaMemcpyDefault));
+        CU_TRY(cudaMemcpy2D(uc.data() + ((size_t)row_offset[m] * R + col[m]) * es, (size_t)R * es, up[m],
+                            (size_t)rank[m] * es, (size_t)rank[m] * es, (size_t)rows[m], cudaMemcpyDefault));
+        if (!same) {   // per-module scales differ: fold scale[m] into its Up (one rounding)
+            for (int r = 0; r < rows[m]; ++r)
+                for (int k = 0; k < rank[m]; ++k) {
+                    char* e = uc.data() + ((size_t)(row_offset[m] + r) * R + col[m] + k) * es;
+                    if (es == 4) {
+                        float v;
+                        std::memcpy(&v, e, 4);
+                        v *= scale[m];
+                        std::memcpy(e, &v, 4);
+                    } else {
+                        uint16_t b;
+                        std::memcpy(&b, e, 2);
+                        b = f32_to_bf16_rne(bf16_to_f32(b) * scale[m]);
+                        std::memcpy(e, &b, 2);
+                    }
+                }
+        }
+        for (int c = col[m] / CHUNK; c < (col[m] + rank[m] + CHUNK - 1) / CHUNK; ++c)
+            chunk_rows[c] = {row_offset[m], row_offset[m] + rows[m]};
+    }
+    mlora_status st = mlora_load_adapter(p, slot, dc.data(), uc.data(), R, same ? common : 1.f);
+    if (st != MLORA_OK) return st;
+    p->slots[slot].chunk_rows = chunk_rows;
     return push_chunks(p);
 }
 
@@ -694,6 +777,7 @@ mlora_status mlora_prefetch(mlora_pool_t p, int slot, int id, mlora_stream_t str
     h.scale = ha.scale;
     h.unit = unit;
     h.version += 1;
+    h.chunk_rows.clear();   // an adapter of the whole layer
     ++p->loaded;
     rs = push_tables_async(p, target);
     if (rs != MLORA_OK) return rs;

@@ -299,7 +299,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const int t = lane + 32 * i;
             av[i] = t < T ? p.row_adapter[tok0 + t] : -1;
         }
-        ChunkRec cr{-2, 0, 0, 0.f};
+        ChunkRec cr{-2, 0, 0, 0.f, 0, 0};
         if (lane < CHUNKS_PER_TILE && cb + lane < p.n_chunks) cr = p.chunks[cb + lane];
         // the table is in arena order: the window of the tile starts at its first chunk
         const int u0 = __shfl_sync(0xffffffffu, cr.unit, 0);
@@ -372,7 +372,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (c < p.n_chunks) {
                 const ChunkRec cr = p.chunks[c];
                 sl = cr.slot;
-                un = cr.unit;
+                // a chunk of a module whose rows miss this tile adds nothing here
+                un = (cr.row0 < (tile + 1) * BM && cr.row1 > tile * BM) ? cr.unit : -1;
             }
             tl.ext_slot[k] = sl;
             tl.ext_unit[k] = un;
@@ -467,7 +468,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                             v = tl.ext_unit[kx + j];
                         } else {
                             const ChunkRec cr = p.chunks[c];
-                            if ((tl.slot_bits[cr.slot >> 5] >> (cr.slot & 31)) & 1u) v = cr.unit;
+                            if (((tl.slot_bits[cr.slot >> 5] >> (cr.slot & 31)) & 1u) && cr.row0 < (tile + 1) * BM &&
+                                cr.row1 > tile * BM)
+                                v = cr.unit;
                         }
                     }
                     un[j] = v;

@@ -58,6 +58,8 @@ _SIGNATURES = {
     "mlora_pool_destroy": (_I, [_P]),
     "mlora_load_adapter": (_I, [_P, _I, _P, _P, _I, ctypes.c_float]),
     "mlora_unload_adapter": (_I, [_P, _I]),
+    "mlora_load_adapter_modules": (_I, [_P, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_P),
+                                        ctypes.POINTER(_P), ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_float)]),
     "mlora_adapter_version": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint64)]),
     "mlora_host_adapter_add": (_I, [_P, _I, _P, _P, _I, ctypes.c_float]),
     "mlora_host_adapter_remove": (_I, [_P, _I]),
@@ -140,6 +142,16 @@ def mlora_forward(pool: int, X_ptr: int, W_ptr: int, row_adapter_ptr: Optional[i
                   stream: int) -> None:
     check(lib().mlora_forward(pool, X_ptr, W_ptr, row_adapter_ptr or None, T, Y_ptr, stream or None),
           "mlora_forward")
+
+
+def mlora_load_adapter_modules(pool: int, slot: int, row_offset, rows, down_ptrs, up_ptrs, ranks, scales) -> None:
+    """One tenant's adapters of several row ranges (modules) of a fused projection; see include/mlora.h."""
+    n = len(ranks)
+    arr = lambda t, v: (t * n)(*v)   # noqa: E731
+    check(lib().mlora_load_adapter_modules(pool, slot, n, arr(_I, row_offset), arr(_I, rows),
+                                           arr(_P, [p or None for p in down_ptrs]),
+                                           arr(_P, [p or None for p in up_ptrs]), arr(_I, ranks),
+                                           arr(ctypes.c_float, scales)), "mlora_load_adapter_modules")
 
 
 def mlora_host_adapter_add(pool: int, id_: int, down_ptr: int, up_ptr: int, rank: int, scale: float) -> None:
@@ -232,6 +244,16 @@ class Pool:
 
     def unload(self, slot: int) -> None:
         mlora_unload_adapter(self.handle, slot)
+
+    def load_modules(self, slot: int, modules) -> None:
+        """modules: list of (row_offset, rows, down, up, scale) with torch tensors, or
+        (row_offset, rows, None, None, 0.0) for a module the tenant does not adapt."""
+        keep = [(d.contiguous(), u.contiguous()) if d is not None else (None, None) for _, _, d, u, _ in modules]
+        mlora_load_adapter_modules(self.handle, slot, [m[0] for m in modules], [m[1] for m in modules],
+                                   [d.data_ptr() if d is not None else 0 for d, _ in keep],
+                                   [u.data_ptr() if u is not None else 0 for _, u in keep],
+                                   [int(d.shape[0]) if d is not None else 0 for d, _ in keep],
+                                   [float(m[4]) for m in modules])
 
     def host_add(self, id_: int, down, up, scale: float) -> None:
         """Copies an adapter (torch tensors, host or device) into the pool's pinned host tier."""

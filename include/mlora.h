@@ -129,6 +129,27 @@ mlora_status mlora_load_adapter(mlora_pool_t pool, int slot, const void* down, c
  * Errors: BAD_SLOT, NOT_LOADED, CUDA. */
 mlora_status mlora_unload_adapter(mlora_pool_t pool, int slot);
 
+/*
+ * Loads one tenant's adapters of several modules of a fused projection into one slot
+ * (airsota card "multi-LoRA serving vs merging", section 四 item ④: engines serve
+ * adapters of mixed ranks and of different target modules).  The pool's W is the
+ * modules' weights stacked by rows (e.g. q, k, v as one [3 x 4096] x 4096 qkv
+ * projection); module m owns output rows [row_offset[m], row_offset[m] + rows[m]) and
+ * has Down [rank[m] x din], Up [rows[m] x rank[m]] and scale[m], or rank[m] == 0 when
+ * the tenant does not adapt it.  A forward then adds, to every row of this slot,
+ * scale[m] Up[m] (Down[m] x) on module m's rows, for every adapted module, in the one
+ * launch of the fused projection.  The slot holds one combined adapter whose rank
+ * is the sum of the modules' ranks, each rounded up to 16 (at most max_rank);
+ * module m's rank chunks only reach its own rows, and a projection tile skips the
+ * chunks of modules whose rows it does not hold.  When the modules' scales differ,
+ * each module's Up is scaled before it is stored (one rounding to the pool dtype).
+ * Ownership and lifecycle as mlora_load_adapter.
+ * Errors: INVALID_ARG (NULL arrays, a module outside [0, dout)), BAD_SLOT, RANK, OOM, CUDA.
+ */
+mlora_status mlora_load_adapter_modules(mlora_pool_t pool, int slot, int n_modules, const int* row_offset,
+                                        const int* rows, const void* const* down, const void* const* up,
+                                        const int* rank, const float* scale);
+
 /* Version counter of a slot: 0 before the first load, +1 at every load and unload
  * (the immutable compute identity of M031 §07). Errors: BAD_SLOT, INVALID_ARG. */
 mlora_status mlora_adapter_version(mlora_pool_t pool, int slot, uint64_t* version);

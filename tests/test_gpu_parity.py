@@ -349,6 +349,63 @@ def test_load_waits_for_last_reader_and_versions():
 
 
 # --------------------------------------------------------------------------- #
+# several modules of a fused projection in one launch (airsota card, section 四 item ④)
+@pytest.mark.parametrize("T", [48, 300])
+def test_fused_projection_with_per_module_adapters(T):
+    """q, k, v rows of one fused projection (boundaries inside 128-row tiles), four
+    tenants: q+v with one scale, q alone, k+v with different scales (folded into Up),
+    and an adapter of the whole layer; decode (T = 48) and prefill (T = 300) paths."""
+    from heterogeneous_lora_gemm_gb300 import Pool
+    rng = np.random.default_rng(41)
+    din, modules = 256, [(0, 200), (200, 90), (290, 170)]
+    dout = 460
+    def rnd(shape, std):   # bf16 bit patterns
+        return wl.f32_to_bf16_bits(rng.standard_normal(shape) * std)
+    spec = {0: [(0, 8, 2.0), (2, 16, 2.0)], 1: [(0, 24, 1.5)], 2: [(1, 16, 3.0), (2, 4, 0.5)]}
+    ads = {s_: {m: (rnd((r, din), 1 / 16), rnd((modules[m][1], r), 0.05), sc) for m, r, sc in mods}
+           for s_, mods in spec.items()}
+    plain = (rnd((16, din), 1 / 16), rnd((dout, 16), 0.05), 2.0)
+    W = rnd((dout, din), 0.02)
+    X = rnd((T, din), 1.0)
+    ra = rng.choice(np.array([0, 1, 2, 3, -1], np.int32), size=T).astype(np.int32)
+    pool = Pool(4, 32 + 32 + 32 + 16, 32, din, dout, "bf16", T)
+    for s_ in spec:
+        mods = []
+        for m, (off, n) in enumerate(modules):
+            if m in ads[s_]:
+                d, u, sc = ads[s_][m]
+                mods.append((off, n, to_device(d, "bf16"), to_device(u, "bf16", "cpu"), sc))
+            else:
+                mods.append((off, n, None, None, 0.0))
+        pool.load_modules(s_, mods)
+    pool.load(3, to_device(plain[0], "bf16"), to_device(plain[1], "bf16"), plain[2])
+    f64 = wl.bf16_bits_to_f64
+    tenants = []
+    for s_ in range(4):
+        row = []
+        for m, (off, n) in enumerate(modules):
+            if s_ == 3:
+                row.append(oracle.OracleAdapter(f64(plain[0]), f64(plain[1])[off:off + n], plain[2]))
+            elif m in ads[s_]:
+                d, u, sc = ads[s_][m]
+                row.append(oracle.OracleAdapter(f64(d), f64(u), sc))
+            else:
+                row.append(None)
+        tenants.append(row)
+    Xd, Wd = to_device(X, "bf16"), to_device(W, "bf16")
+    Y = torch.empty((T, dout), dtype=torch.bfloat16, device="cuda")
+    pool.forward(Xd, Wd, torch.from_numpy(ra).cuda(), Y)
+    torch.cuda.synchronize()
+    want = oracle.forward_modules(f64(X), f64(W), ra, modules, tenants)
+    assert_within(to_f64(Y), want, "bf16", f"fused projection, T = {T}")
+    assert pool.status() == mlora.MLORA_OK
+    with pytest.raises(mlora.MloraError) as e:   # combined rank 16 + 32 > max_rank 32
+        pool.load_modules(0, [(0, 200, to_device(ads[1][0][0], "bf16"), to_device(ads[1][0][1], "bf16"), 1.0),
+                              (200, 90, to_device(ads[2][1][0], "bf16"), to_device(ads[2][1][1], "bf16"), 1.0)])
+    assert e.value.status == mlora.MLORA_ERR_RANK
+
+
+# --------------------------------------------------------------------------- #
 # host (cold) tier and asynchronous prefetch (M031 §06)
 def _host_tier_pool(layer, extra_budget=0, max_rank=None):
     from heterogeneous_lora_gemm_gb300 import Pool

@@ -185,6 +185,43 @@ def test_unmerge_after_merge_restores_only_with_the_same_adapter():
     assert np.abs(oracle.unmerge(Wm, b) - layer.W_f64).max() > 1e-3
 
 
+def _module_case():
+    rng = np.random.default_rng(17)
+    din, modules = 24, [(0, 10), (10, 7), (17, 11)]          # q, k, v rows of a 28-row fused projection
+    W = rng.standard_normal((28, din))
+    X = rng.standard_normal((9, din))
+    def ad(r, n, s):
+        return oracle.OracleAdapter(rng.standard_normal((r, din)), rng.standard_normal((n, r)), s)
+    tenants = [[ad(2, 10, 2.0), None, ad(3, 11, 0.5)],       # q and v
+               [None, ad(4, 7, 1.5), None],                   # k only
+               None]                                          # slot 2 empty
+    ra = np.array([0, 1, -1, 0, 2, 1, 0, -1, 1], np.int32)
+    return X, W, ra, modules, tenants
+
+
+def test_module_rows_follow_their_own_adapters():
+    """airsota card, section 四 item ④ (adapters of different target modules): in a
+    fused projection, each module's rows get that module's own update, checked row by
+    row with numpy; rows of other modules, invalid or empty slots keep the base."""
+    X, W, ra, modules, tenants = _module_case()
+    Y = oracle.forward_modules(X, W, ra, modules, tenants)
+    want = X @ W.T
+    for t, s in enumerate(ra):
+        if s < 0 or tenants[s] is None:
+            continue
+        for (off, n), a in zip(modules, tenants[s]):
+            if a is not None:
+                want[t, off:off + n] += a.scale * (a.up @ (a.down @ X[t]))
+    np.testing.assert_allclose(Y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_one_module_over_all_rows_is_the_plain_layer():
+    X, W, ra, _, tenants = _module_case()
+    a = oracle.OracleAdapter(tenants[0][0].down, np.random.default_rng(5).standard_normal((28, 2)), 2.0)
+    np.testing.assert_array_equal(oracle.forward_modules(X, W, ra, [(0, 28)], [[a], None, None]),
+                                  oracle.forward(X, W, ra, [a, None, None]))
+
+
 # --------------------------------------------------------------------------- #
 # invariants and closed forms
 def test_rank_padding_leaves_output_unchanged():
