@@ -529,6 +529,43 @@ def run_ours(args, dist, rank, local):
                  "copies": len(Wm)}
         del Wm
 
+    # ---- quantized base (int8 codes x per-row scale): restoring W, the dynamic branch
+    # over it (restore + forward), and the merge that re-quantizes (M031 §05)
+    quantized = None
+    if L0m.max_slots > 0 and L0m.dtype == "bf16" and args.workload not in ("stack7b", "prefill"):
+        it0 = items[0]
+        Wf = it0["W"].float()
+        qscale = (Wf.abs().amax(1) / 127).contiguous()
+        Wq0 = torch.round(Wf / qscale[:, None]).clamp(-127, 127).to(torch.int8)
+        qcopies = 16   # 16 MiB of codes each: more than twice the L2
+        Wqs = [Wq0.clone() for _ in range(qcopies)]
+        scs = [qscale.clone() for _ in range(qcopies)]
+        scratch = torch.empty_like(it0["W"])
+        qreps = 20
+
+        def q_time(fn):
+            with torch.cuda.stream(stream):
+                fn(0)
+                p0.record(stream)
+                for k in range(qreps * qcopies):
+                    fn(k)
+                p1.record(stream)
+            torch.cuda.synchronize(dev)
+            return p0.elapsed_time(p1) * 1e3 / (qreps * qcopies)
+
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dq_us = q_time(lambda k: mlora.mlora_dequantize(Wqs[k % qcopies].data_ptr(), scs[k % qcopies].data_ptr(),
+                                                       L0m.dout, L0m.din, mlora.MLORA_BF16, scratch.data_ptr(),
+                                                       stream.cuda_stream))
+        fq_us = q_time(lambda k: it0["pool"].forward_quantized(it0["X"], Wqs[k % qcopies], scs[k % qcopies], scratch,
+                                                               it0["ra"], it0["Y"], stream=stream))
+        mq_us = q_time(lambda k: it0["pool"].merge_quantized(Wqs[k % qcopies], scs[k % qcopies], 0, stream=stream))
+        n_w = L0m.dout * L0m.din
+        quantized = {"dequantize_us": dq_us, "dequantize_gbs": (3 * n_w + 4 * L0m.dout) / dq_us / 1e3,
+                     "forward_quantized_us": fq_us, "merge_quantized_us": mq_us,
+                     "merge_quantized_gbs": (2 * n_w + 8 * L0m.dout) / mq_us / 1e3,
+                     "base": "int8 codes, fp32 scale per output row; the forward restores W (bf16) then runs"}
+
     # ---- q and v of a layer in one launch (fused projection) against two launches
     multi_module = None
     if args.workload == "stack7b" and rank == 0:
@@ -620,6 +657,7 @@ def run_ours(args, dist, rank, local):
         "roofline": roof,
         "step_roofline": {"frac": step_roof_s / step_s, "bytes": int(layer_step_bytes), "flops": int(layer_flops)},
         "e2e": e2e, "gpu_launches": int(gpu_launches), "clocks": clocks, "spot_check": spot, "merge": merge, "prefetch": prefetch, "multi_module": multi_module,
+        "quantized": quantized,
     }
     return out, L0
 

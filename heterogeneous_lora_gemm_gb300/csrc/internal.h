@@ -92,6 +92,10 @@ cudaError_t launch_base_expand_simt(bool bf16, const void* X, const void* W,
                                     const int32_t* row_adapter, int T, void* Y,
                                     const SlotRec* slots, const void* arena_up, const Workspace& ws,
                                     const PoolDims& d, bool with_lora, cudaStream_t st);
+// Quantized base (quant.cu): int8 codes x per-row scale.
+cudaError_t launch_dequant(bool bf16, const int8_t* q, const float* s, int dout, int din, void* W, cudaStream_t st);
+cudaError_t launch_merge_quant(bool bf16, int8_t* q, float* s, const SlotRec* slots, int slot, const void* arena_down,
+                               const void* arena_up, const PoolDims& d, cudaStream_t st);
 cudaError_t launch_merge_simt(bool bf16, void* W, const SlotRec* slots, int slot,
                               const void* arena_down, const void* arena_up, const PoolDims& d, float sign,
                               cudaStream_t st);

@@ -883,6 +883,44 @@ mlora_status mlora_unmerge(mlora_pool_t p, void* W, int slot, mlora_stream_t str
     return merge_signed(p, W, slot, -1.f, stream);
 }
 
+mlora_status mlora_dequantize(const void* Wq, const float* row_scale, int dout, int din, mlora_dtype dtype, void* W,
+                              mlora_stream_t stream) {
+    if (!Wq || !row_scale || !W) return fail(MLORA_ERR_INVALID_ARG, "Wq/row_scale/W is NULL");
+    if (dout < 0 || din < 0) return fail(MLORA_ERR_INVALID_ARG, "negative size");
+    if (dtype != MLORA_BF16 && dtype != MLORA_F32) return fail(MLORA_ERR_INVALID_ARG, "bad dtype");
+    if (!aligned16(Wq) || !aligned16(W)) return fail(MLORA_ERR_INVALID_ARG, "Wq and W must be 16-byte aligned");
+    CU_TRY(launch_dequant(dtype == MLORA_BF16, (const int8_t*)Wq, row_scale, dout, din, W, (cudaStream_t)stream));
+    return MLORA_OK;
+}
+
+mlora_status mlora_forward_quantized(mlora_pool_t p, const void* X, const void* Wq, const float* row_scale,
+                                     void* W_scratch, const int32_t* row_adapter, int T, void* Y,
+                                     mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
+    if (T == 0) return MLORA_OK;
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    mlora_status st = mlora_dequantize(Wq, row_scale, p->dout, p->din, p->dtype, W_scratch, stream);
+    if (st != MLORA_OK) return st;
+    return mlora_forward(p, X, W_scratch, row_adapter, T, Y, stream);
+}
+
+mlora_status mlora_merge_quantized(mlora_pool_t p, void* Wq, float* row_scale, int slot, mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (!Wq || !row_scale) return fail(MLORA_ERR_INVALID_ARG, "Wq/row_scale is NULL");
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    if (p->slots[slot].rank <= 0) return fail(MLORA_ERR_NOT_LOADED, "slot %d holds no adapter", slot);
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = launch_merge_quant(p->dtype == MLORA_BF16, (int8_t*)Wq, row_scale, p->d_slots, slot,
+                                             p->arena_down, p->arena_up, p->dims, st);
+    if (e == cudaErrorInvalidValue) return fail(MLORA_ERR_INVALID_ARG, "din %d too large for the quantized merge", p->din);
+    CU_TRY(e);
+    return note_reader(p, st);
+}
+
 mlora_status mlora_pool_status(mlora_pool_t p, mlora_stream_t stream) {
     if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
     DeviceGuard g(p->device);

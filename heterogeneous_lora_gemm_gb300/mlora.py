@@ -67,6 +67,9 @@ _SIGNATURES = {
     "mlora_forward": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "mlora_merge": (_I, [_P, _P, _I, _P]),
     "mlora_unmerge": (_I, [_P, _P, _I, _P]),
+    "mlora_dequantize": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "mlora_forward_quantized": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
+    "mlora_merge_quantized": (_I, [_P, _P, _P, _I, _P]),
     "mlora_pool_status": (_I, [_P, _P]),
     "mlora_pool_info": (_I, [_P, ctypes.POINTER(PoolInfo)]),
     "mlora_debug_segments": (_I, [_P, _P, _I, _P, _P, _P]),
@@ -168,6 +171,10 @@ def mlora_prefetch(pool: int, slot: int, id_: int, stream: int) -> None:
 
 def mlora_merge(pool: int, W_ptr: int, slot: int, stream: int) -> None:
     check(lib().mlora_merge(pool, W_ptr, slot, stream or None), "mlora_merge")
+
+
+def mlora_dequantize(Wq_ptr: int, scale_ptr: int, dout: int, din: int, dtype: int, W_ptr: int, stream: int) -> None:
+    check(lib().mlora_dequantize(Wq_ptr, scale_ptr, dout, din, dtype, W_ptr, stream or None), "mlora_dequantize")
 
 
 def mlora_unmerge(pool: int, W_ptr: int, slot: int, stream: int) -> None:
@@ -280,6 +287,17 @@ class Pool:
 
     def unmerge(self, W, slot: int, stream=None) -> None:
         mlora_unmerge(self.handle, W.data_ptr(), slot, _stream_handle(stream))
+
+    def forward_quantized(self, X, Wq, row_scale, W_scratch, row_adapter, Y, stream=None) -> None:
+        """The dynamic branch over an int8 base (codes Wq [dout x din] int8, row_scale [dout] fp32)."""
+        ra = None if row_adapter is None else row_adapter.data_ptr()
+        check(lib().mlora_forward_quantized(self.handle, X.data_ptr(), Wq.data_ptr(), row_scale.data_ptr(),
+                                            W_scratch.data_ptr(), ra, int(X.shape[0]), Y.data_ptr(),
+                                            _stream_handle(stream)), "mlora_forward_quantized")
+
+    def merge_quantized(self, Wq, row_scale, slot: int, stream=None) -> None:
+        check(lib().mlora_merge_quantized(self.handle, Wq.data_ptr(), row_scale.data_ptr(), slot,
+                                          _stream_handle(stream)), "mlora_merge_quantized")
 
     def status(self, stream=None) -> int:
         return mlora_pool_status(self.handle, _stream_handle(stream))

@@ -230,6 +230,33 @@ mlora_status mlora_merge(mlora_pool_t pool, void* W, int slot, mlora_stream_t st
 mlora_status mlora_unmerge(mlora_pool_t pool, void* W, int slot, mlora_stream_t stream);
 
 /*
+ * Quantized base weight (M031 §05): int8 codes with one scale per output row,
+ *   W[o,i] = Wq[o,i] * row_scale[o]          (symmetric; Wq device int8 [dout x din],
+ *                                            row_scale device fp32 [dout])
+ * The logical matrix is the restored W; a LoRA update is added to it, never to the
+ * codes (that would mix two numeric spaces).
+ *
+ * mlora_dequantize: W = Wq * row_scale, rounded once to `dtype`, into the caller's
+ *   buffer W [dout x din] (device).  Wq and W 16-byte aligned.  Errors: INVALID_ARG, CUDA.
+ * mlora_forward_quantized: the dynamic LoRA branch over the restored base: dequantizes
+ *   into W_scratch (device [dout x din], pool dtype, caller-owned) and runs
+ *   mlora_forward on it.  Arguments otherwise as mlora_forward.
+ * mlora_merge_quantized: the merge on a quantized base, in place: restore each row,
+ *   add scale * Up Down (fp32), then quantize the merged row again: new
+ *   row_scale[o] = max_i |w[o,i]| / 127 (fp32; 0 for an all-zero row), codes
+ *   rint(w / row_scale[o]) (to nearest, ties to even) clamped to [-127, 127].  The
+ *   re-quantization adds at most half a step (row_scale[o] / 2) per element on top
+ *   of the merged float weight.  Errors: INVALID_ARG (also din > 51 200), BAD_SLOT,
+ *   NOT_LOADED, CUDA.
+ */
+mlora_status mlora_dequantize(const void* Wq, const float* row_scale, int dout, int din, mlora_dtype dtype, void* W,
+                              mlora_stream_t stream);
+mlora_status mlora_forward_quantized(mlora_pool_t pool, const void* X, const void* Wq, const float* row_scale,
+                                     void* W_scratch, const int32_t* row_adapter, int T, void* Y,
+                                     mlora_stream_t stream);
+mlora_status mlora_merge_quantized(mlora_pool_t pool, void* Wq, float* row_scale, int slot, mlora_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the pool's device status word.
  * Returns MLORA_OK, MLORA_ERR_DEVICE_ROW (a forward since the last call saw a row
  * naming an invalid or empty slot), MLORA_ERR_DEVICE_TIMEOUT (a pipeline wait in a

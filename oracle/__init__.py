@@ -184,6 +184,29 @@ def forward_modules(X: np.ndarray, W: np.ndarray, row_adapter: np.ndarray, modul
     return Y
 
 
+def dequantize(codes: np.ndarray, row_scale: np.ndarray) -> np.ndarray:
+    """The logical matrix of an int8 base (M031 §05): W[o, i] = code[o, i] * scale[o]."""
+    return np.asarray(codes, np.float64) * np.asarray(row_scale, np.float64)[:, None]
+
+
+def quantize(W: np.ndarray):
+    """Symmetric per-row int8 quantization, decided in fp32 (the precision the kernel
+    decides in): scale[o] = max_i |w[o, i]| / 127, code = rint(w / scale[o]) (ties to
+    even) clamped to [-127, 127]; an all-zero row gets scale 0 and codes 0."""
+    w = np.asarray(W, np.float64).astype(np.float32)
+    scale = (np.abs(w).max(axis=1) / np.float32(127)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1))
+    codes = np.clip(np.rint(w / safe[:, None]), -127, 127)
+    codes = np.where(scale[:, None] > 0, codes, 0).astype(np.int8)
+    return codes, scale
+
+
+def merge_quantized(codes: np.ndarray, row_scale: np.ndarray, adapter: OracleAdapter):
+    """The merge on a quantized base (M031 §05): restore W, add scale * Up Down, and
+    quantize the merged matrix again -- never the update added to the codes."""
+    return quantize(merge(dequantize(codes, row_scale), adapter))
+
+
 def unmerge(W: np.ndarray, adapter: OracleAdapter) -> np.ndarray:
     """W - scale * Up @ Down in fp64: the un-merge that switches a merged weight back
     (airsota card "multi-LoRA serving vs merging", section 四 item ③)."""

@@ -349,6 +349,64 @@ def test_load_waits_for_last_reader_and_versions():
 
 
 # --------------------------------------------------------------------------- #
+# quantized base (M031 §05)
+def test_forward_over_a_quantized_base():
+    """The dynamic branch over an int8 base: the restored W (codes x row scale, one
+    rounding) under the usual forward; both against the oracle."""
+    layer = wl.random_layer(51, T=40, din=256, dout=192, ranks=[16, 8])
+    codes, scale = oracle.quantize(layer.W_f64)
+    pool = make_pool(layer)
+    X, _, ra, Y = upload(layer)
+    Wq, sc = torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda()
+    W_scratch = torch.empty((layer.dout, layer.din), dtype=torch.bfloat16, device="cuda")
+    pool.forward_quantized(X, Wq, sc, W_scratch, ra, Y)
+    torch.cuda.synchronize()
+    Wd = oracle.dequantize(codes, scale)
+    assert_within(to_f64(W_scratch), Wd, "bf16", "restored base")
+    assert_within(to_f64(Y), oracle.forward(layer.X_f64, Wd, layer.row_adapter, ora_adapters(layer)), "bf16",
+                  "forward over the quantized base")
+    assert pool.status() == mlora.MLORA_OK
+
+
+def test_merge_quantized_is_bit_exact_on_an_exact_grid():
+    """Codes, row scales, adapter entries and scale chosen so that every fp32 step of
+    the merge is exact: the re-quantized codes and scales equal the oracle's bit for
+    bit (both decide in fp32)."""
+    from heterogeneous_lora_gemm_gb300 import Pool
+    rng = np.random.default_rng(52)
+    din, dout, r = 128, 136, 16
+    codes = rng.integers(-127, 128, size=(dout, din)).astype(np.int8)
+    scale = (2.0 ** rng.integers(-9, -5, size=dout)).astype(np.float32)
+    down = rng.integers(-8, 9, size=(r, din)) / 16.0
+    up = rng.integers(-8, 9, size=(dout, r)) / 16.0
+    pool = Pool(1, 16, 16, din, dout, "bf16", 1)
+    pool.load(0, to_device(wl.f32_to_bf16_bits(down), "bf16"), to_device(wl.f32_to_bf16_bits(up), "bf16"), 0.5)
+    Wq, sc = torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda()
+    pool.merge_quantized(Wq, sc, 0)
+    torch.cuda.synchronize()
+    want_c, want_s = oracle.merge_quantized(codes, scale, oracle.OracleAdapter(down, up, 0.5))
+    np.testing.assert_array_equal(sc.cpu().numpy(), want_s)
+    np.testing.assert_array_equal(Wq.cpu().numpy(), want_c)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_merge_quantized_random_within_one_step(dtype):
+    """Random base and adapter (ragged sizes): row scales to fp32 rounding, codes equal
+    but for rare ties decided on an fp32 sum that differs in its last bit."""
+    layer = wl.random_layer(53, T=1, din=200, dout=72, ranks=[24], dtype=dtype)
+    codes, scale = oracle.quantize(layer.W_f64)
+    pool = make_pool(layer)
+    Wq, sc = torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda()
+    pool.merge_quantized(Wq, sc, 0)
+    torch.cuda.synchronize()
+    want_c, want_s = oracle.merge_quantized(codes, scale, ora_adapters(layer)[0])
+    got_c, got_s = Wq.cpu().numpy().astype(np.int32), sc.cpu().numpy()
+    np.testing.assert_allclose(got_s, want_s, rtol=1e-6, atol=0)
+    diff = np.abs(got_c - want_c.astype(np.int32))
+    assert diff.max() <= 1 and (diff > 0).mean() < 1e-3, (diff.max(), (diff > 0).mean())
+
+
+# --------------------------------------------------------------------------- #
 # several modules of a fused projection in one launch (airsota card, section 四 item ④)
 @pytest.mark.parametrize("T", [48, 300])
 def test_fused_projection_with_per_module_adapters(T):

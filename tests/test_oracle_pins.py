@@ -222,6 +222,49 @@ def test_one_module_over_all_rows_is_the_plain_layer():
                                   oracle.forward(X, W, ra, [a, None, None]))
 
 
+def test_quantize_recovers_an_exact_grid():
+    """M031 §05 (a quantized base is codes times a scale): codes whose row maximum is
+    127, times power-of-two row scales, quantize back to themselves exactly; an
+    all-zero row gets scale 0 and codes 0."""
+    rng = np.random.default_rng(21)
+    codes = rng.integers(-127, 128, size=(6, 40)).astype(np.int8)
+    codes[:, 3] = 127
+    codes[5] = 0
+    scale = 2.0 ** rng.integers(-9, -2, size=6)
+    scale[5] = 0.0
+    c2, s2 = oracle.quantize(oracle.dequantize(codes, scale))
+    np.testing.assert_array_equal(c2, codes)
+    np.testing.assert_array_equal(s2, scale.astype(np.float32))
+
+
+def test_quantization_error_is_at_most_half_a_step():
+    W = np.random.default_rng(22).standard_normal((9, 70)) * 0.02
+    codes, scale = oracle.quantize(W)
+    err = np.abs(oracle.dequantize(codes, scale) - W)
+    assert (err <= scale[:, None] / 2 * (1 + 2.0 ** -20) + 2.0 ** -23 * np.abs(W)).all()
+    assert np.abs(codes).max() == 127
+
+
+def test_merge_on_a_quantized_base_three_ways():
+    """M031 §05 acceptance: the dynamic branch over the restored base equals the merged
+    float weight (fp64), the re-quantized merge stays within half a step per weight,
+    and adding the update to the codes (ignoring the scale) does not."""
+    rng = np.random.default_rng(23)
+    codes, scale = oracle.quantize(rng.standard_normal((24, 32)) * 0.02)
+    a = oracle.OracleAdapter(rng.standard_normal((4, 32)) / 8, rng.standard_normal((24, 4)) * 0.05, 2.0)
+    X = rng.standard_normal((5, 32))
+    Wd = oracle.dequantize(codes, scale)
+    dynamic = oracle.forward(X, Wd, np.zeros(5, np.int32), [a])
+    merged_float = X @ (Wd + a.scale * a.up @ a.down).T
+    np.testing.assert_allclose(dynamic, merged_float, rtol=1e-12, atol=1e-12)
+    c2, s2 = oracle.merge_quantized(codes, scale, a)
+    quantized = X @ oracle.dequantize(c2, s2).T
+    bound = np.abs(X) @ np.broadcast_to(s2[:, None] / 2 * (1 + 2.0 ** -20), (24, 32)).T + 1e-9
+    assert (np.abs(quantized - merged_float) <= bound).all()
+    wrong = oracle.dequantize(np.clip(np.rint(codes + a.scale * a.up @ a.down), -127, 127), scale)
+    assert np.abs(X @ wrong.T - merged_float).max() > 10 * bound.max()
+
+
 # --------------------------------------------------------------------------- #
 # invariants and closed forms
 def test_rank_padding_leaves_output_unchanged():
