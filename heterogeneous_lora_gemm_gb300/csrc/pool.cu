@@ -909,6 +909,7 @@ mlora_status mlora_forward_quantized(mlora_pool_t p, const void* X, const void* 
 mlora_status mlora_merge_quantized(mlora_pool_t p, void* Wq, float* row_scale, int slot, mlora_stream_t stream) {
     if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
     if (!Wq || !row_scale) return fail(MLORA_ERR_INVALID_ARG, "Wq/row_scale is NULL");
+    if (!aligned16(Wq)) return fail(MLORA_ERR_INVALID_ARG, "Wq must be 16-byte aligned");
     if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
     if (p->slots[slot].rank <= 0) return fail(MLORA_ERR_NOT_LOADED, "slot %d holds no adapter", slot);
     DeviceGuard g(p->device);

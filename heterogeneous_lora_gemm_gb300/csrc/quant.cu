@@ -9,9 +9,9 @@
 //                       clamped to [-127, 127]), in place.  Adding the update to the
 //                       codes themselves would mix two numeric spaces (§05).
 //
-// Both are bandwidth-bound sweeps over W.  The merge runs one CTA per group of rows,
-// one row at a time: the row is read, updated and held in shared memory (fp32),
-// reduced to its max, then written back as codes.
+// Both are bandwidth-bound sweeps over W.  The merge runs one CTA per group of rows
+// (each Down value loaded serves all of them): the rows are read, updated and held in
+// shared memory (fp32), reduced to their max, then written back as codes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -25,8 +25,7 @@ namespace {
 
 constexpr int DQ_THREADS = 256;
 constexpr int MQ_THREADS = 256;
-constexpr int MQ_ROWS = 4;                   // rows per CTA of the merge
-constexpr int MQ_SMEM_MAX = 200 * 1024;      // one merged row held in shared memory (fp32)
+constexpr int MQ_SMEM_MAX = 200 * 1024;      // merged rows held in shared memory (fp32)
 
 template <typename E>
 __device__ __forceinline__ E from_f32(float v);
@@ -41,6 +40,35 @@ template <>
 __device__ __forceinline__ float as_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float as_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// 8 consecutive values as fp32: one 16-byte (bf16) or two 16-byte (fp32) loads when
+// `vec` (8 whole, aligned values), else one by one up to n.
+__device__ __forceinline__ void load8f(const __nv_bfloat16* p, bool vec, int n, float* v) {
+    if (vec) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            v[2 * j] = f.x;
+            v[2 * j + 1] = f.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = j < n ? __bfloat162float(p[j]) : 0.f;
+    }
+}
+__device__ __forceinline__ void load8f(const float* p, bool vec, int n, float* v) {
+    if (vec) {
+        const float4 a = *reinterpret_cast<const float4*>(p);
+        const float4 b = *reinterpret_cast<const float4*>(p + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = j < n ? p[j] : 0.f;
+    }
+}
 
 // One thread per 16 codes of a row (din % 16 == 0: one 16-byte load), else per code.
 template <typename E>
@@ -69,53 +97,139 @@ dequant_kernel(const int8_t* __restrict__ q, const float* __restrict__ s, int do
     }
 }
 
-// CTA per `rows` consecutive output rows, one after the other (shared memory: din fp32).
-template <typename E>
+// CTA per R consecutive output rows.  Each thread owns 8 consecutive columns of a
+// 2048-column block and all R rows of them (an R x 8 register tile): the update
+// scale * Up[rows, k] Down[k, cols] (fp32, k ascending), plus the restored codes,
+// goes to shared memory [R][din]; then each row's max, its new scale, and its codes.
+template <typename E, int R>
 __global__ void __launch_bounds__(MQ_THREADS)
 merge_quant_kernel(int8_t* __restrict__ q, float* __restrict__ s, const SlotRec* __restrict__ slots, int slot,
-                   const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout, int rows) {
-    extern __shared__ float wsh[];   // [din]: the row being merged
-    __shared__ float red[MQ_THREADS / 32];
+                   const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout) {
+    extern __shared__ float wsh[];   // [R][din] merged rows, then [R][rank] Up of the rows
+    __shared__ float red[MQ_THREADS / 32][R];
+    __shared__ float sn_s[R];
     const SlotRec rec = slots[slot];
-    const int o0 = blockIdx.x * rows;
-    const int nr = min(rows, dout - o0);
+    const int o0 = blockIdx.x * R;
+    const int nr = min(R, dout - o0);
+    float* up_s = wsh + (size_t)R * din;
+    for (int idx = threadIdx.x; idx < R * rec.rank; idx += MQ_THREADS) {
+        const int r = idx / rec.rank, k = idx % rec.rank;
+        up_s[idx] = r < nr ? as_f32(arena_up[up_index(rec.unit, k, o0 + r, dout)]) : 0.f;
+    }
+    __syncthreads();
     const E* down = arena_down + (size_t)rec.unit * din;
-    for (int r = 0; r < nr; ++r) {
-        const int o = o0 + r;
-        const float so = s[o];
-        float m = 0.f;
-        for (int i = threadIdx.x; i < din; i += MQ_THREADS) {
-            float acc = 0.f;
-            for (int k = 0; k < rec.rank; ++k)
-                acc = fmaf(as_f32(arena_up[up_index(rec.unit, k, o, dout)]), as_f32(down[(size_t)k * din + i]), acc);
-            const float w = fmaf(rec.scale, acc, (float)q[(size_t)o * din + i] * so);
-            wsh[i] = w;
-            m = fmaxf(m, fabsf(w));
-        }
-        // max over the row: warp shuffle, then across warps
+    float m[R];
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            float v = threadIdx.x < MQ_THREADS / 32 ? red[threadIdx.x] : 0.f;
+    for (int r = 0; r < R; ++r) m[r] = 0.f;
+    for (int c0 = 0; c0 < din; c0 += MQ_THREADS * 8) {
+        const int i0 = c0 + threadIdx.x * 8;
+        if (i0 >= din) continue;
+        const int nc = min(8, din - i0);
+        const bool vec = nc == 8 && (din % 8) == 0;   // whole, 16-byte aligned groups of 8
+        float acc[R][8];
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
-            if (threadIdx.x == 0) red[0] = v;
-        }
-        __syncthreads();
-        const float mx = red[0];
-        __syncthreads();   // red is reused by the next row
-        const float sn = mx / 127.f;   // new row scale (0 for an all-zero row: codes 0)
-        for (int i = threadIdx.x; i < din; i += MQ_THREADS) {
-            int c = 0;
-            if (sn > 0.f) {
-                c = __float2int_rn(wsh[i] / sn);
-                c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[r][j] = 0.f;
+        // four rank steps' Down loads in flight, then their FMAs (k ascending)
+        for (int k0 = 0; k0 < rec.rank; k0 += 4) {
+            float d[4][8];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                if (k0 + kk < rec.rank) load8f(down + (size_t)(k0 + kk) * din + i0, vec, nc, d[kk]);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                if (k0 + kk >= rec.rank) break;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float u = up_s[r * rec.rank + k0 + kk];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(u, d[kk][j], acc[r][j]);
+                }
             }
-            q[(size_t)o * din + i] = (int8_t)c;
         }
-        if (threadIdx.x == 0) s[o] = sn;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            if (r >= nr) break;
+            const int o = o0 + r;
+            const float so = s[o];
+            __align__(8) int8_t c8[8];
+            if (vec) {
+                *reinterpret_cast<uint2*>(c8) = *reinterpret_cast<const uint2*>(q + (size_t)o * din + i0);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) c8[j] = j < nc ? q[(size_t)o * din + i0 + j] : (int8_t)0;
+            }
+            float w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                w[j] = fmaf(rec.scale, acc[r][j], (float)c8[j] * so);
+                if (j < nc) m[r] = fmaxf(m[r], fabsf(w[j]));
+            }
+            float* dst = wsh + (size_t)r * din + i0;
+            if (vec) {
+                *reinterpret_cast<float4*>(dst) = make_float4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(w[4], w[5], w[6], w[7]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < nc) dst[j] = w[j];
+            }
+        }
+    }
+    // the rows' max: warp shuffle, then across warps
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float v = m[r];
+#pragma unroll
+        for (int dd = 16; dd > 0; dd >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, dd));
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5][r] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < R) {
+        float v = 0.f;
+        for (int w = 0; w < MQ_THREADS / 32; ++w) v = fmaxf(v, red[w][threadIdx.x]);
+        sn_s[threadIdx.x] = v / 127.f;   // new row scale (0 for an all-zero row: codes 0)
+        if (threadIdx.x < nr) s[o0 + threadIdx.x] = sn_s[threadIdx.x];
+    }
+    __syncthreads();
+    // codes: each thread its own 8 columns of each row (as in the first pass)
+    for (int r = 0; r < nr; ++r) {
+        const float sn = sn_s[r];
+        const int o = o0 + r;
+        for (int c0 = 0; c0 < din; c0 += MQ_THREADS * 8) {
+            const int i0 = c0 + threadIdx.x * 8;
+            if (i0 >= din) continue;
+            const int nc = min(8, din - i0);
+            const bool vec = nc == 8 && (din % 8) == 0;
+            const float* src = wsh + (size_t)r * din + i0;
+            float w[8];
+            if (vec) {
+                const float4 a = *reinterpret_cast<const float4*>(src);
+                const float4 b = *reinterpret_cast<const float4*>(src + 4);
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) w[j] = j < nc ? src[j] : 0.f;
+            }
+            __align__(8) int8_t c8[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                int c = 0;
+                if (j < nc && sn > 0.f) {
+                    c = __float2int_rn(w[j] / sn);
+                    c = c > 127 ? 127 : (c < -127 ? -127 : c);
+                }
+                c8[j] = (int8_t)c;
+            }
+            int8_t* dst = q + (size_t)o * din + i0;
+            if (vec) {
+                *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(c8);
+            } else {
+                for (int j = 0; j < nc; ++j) dst[j] = c8[j];
+            }
+        }
     }
 }
 
@@ -144,26 +258,32 @@ cudaError_t launch_dequant(bool bf16, const int8_t* q, const float* s, int dout,
     return cudaGetLastError();
 }
 
+template <typename E, int R>
+cudaError_t launch_merge_quant_r(int8_t* q, float* s, const SlotRec* slots, int slot, const void* arena_down,
+                                 const void* arena_up, const PoolDims& d, cudaStream_t st) {
+    const size_t smem = sizeof(float) * ((size_t)R * d.din + (size_t)R * d.max_rank);
+    cudaError_t e = cudaFuncSetAttribute(merge_quant_kernel<E, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    merge_quant_kernel<E, R><<<(unsigned)((d.dout + R - 1) / R), MQ_THREADS, smem, st>>>(
+        q, s, slots, slot, (const E*)arena_down, (const E*)arena_up, d.din, d.dout);
+    return cudaGetLastError();
+}
+
+template <typename E>
+cudaError_t launch_merge_quant_e(int8_t* q, float* s, const SlotRec* slots, int slot, const void* arena_down,
+                                 const void* arena_up, const PoolDims& d, cudaStream_t st) {
+    // as many rows per CTA (4, 2, 1) as leave the held rows in shared memory
+    const size_t per_row = sizeof(float) * ((size_t)d.din + (size_t)d.max_rank);
+    if (4 * per_row <= (size_t)MQ_SMEM_MAX) return launch_merge_quant_r<E, 4>(q, s, slots, slot, arena_down, arena_up, d, st);
+    if (2 * per_row <= (size_t)MQ_SMEM_MAX) return launch_merge_quant_r<E, 2>(q, s, slots, slot, arena_down, arena_up, d, st);
+    if (per_row <= (size_t)MQ_SMEM_MAX) return launch_merge_quant_r<E, 1>(q, s, slots, slot, arena_down, arena_up, d, st);
+    return cudaErrorInvalidValue;   // a row of din fp32 does not fit
+}
+
 cudaError_t launch_merge_quant(bool bf16, int8_t* q, float* s, const SlotRec* slots, int slot, const void* arena_down,
                                const void* arena_up, const PoolDims& d, cudaStream_t st) {
-    const int rows = MQ_ROWS;
-    const size_t smem = sizeof(float) * (size_t)d.din;
-    if (smem > (size_t)MQ_SMEM_MAX) return cudaErrorInvalidValue;   // din above 51 200
-    const unsigned grid = (unsigned)((d.dout + rows - 1) / rows);
-    cudaError_t e;
-    if (bf16) {
-        e = cudaFuncSetAttribute(merge_quant_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        merge_quant_kernel<__nv_bfloat16><<<grid, MQ_THREADS, smem, st>>>(
-            q, s, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din, d.dout, rows);
-    } else {
-        e = cudaFuncSetAttribute(merge_quant_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        merge_quant_kernel<float><<<grid, MQ_THREADS, smem, st>>>(q, s, slots, slot, (const float*)arena_down,
-                                                                  (const float*)arena_up, d.din, d.dout, rows);
-    }
-    return cudaGetLastError();
+    return bf16 ? launch_merge_quant_e<__nv_bfloat16>(q, s, slots, slot, arena_down, arena_up, d, st)
+                : launch_merge_quant_e<float>(q, s, slots, slot, arena_down, arena_up, d, st);
 }
 
 }  // namespace mlora
