@@ -14,9 +14,10 @@ constexpr int SEG_THREADS = 1024;
 __global__ void __launch_bounds__(SEG_THREADS, 1)
 seg_build_kernel(const int32_t* __restrict__ row_adapter, int T, const SlotRec* __restrict__ slots, Workspace ws,
                  int S, int P, int max_chunks, int stage_rows) {
-    extern __shared__ int smem[];
+    extern __shared__ __align__(16) int smem[];
     const seg::Scratch sc = seg::carve(smem, S, P, stage_rows != 0);
-    seg::build(row_adapter, T, slots, S, P, max_chunks, sc, ws);
+    seg::stage(slots, S, ws, row_adapter, T, max_chunks, sc);
+    seg::build(S, P, sc);
 }
 
 }  // namespace

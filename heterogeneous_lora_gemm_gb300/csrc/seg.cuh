@@ -25,13 +25,28 @@
 //
 // The whole block of one CTA runs it (no CTA ever waits on another): the
 // standalone segment kernel, or a CTA of its own in the tensor-core shrink's grid.
+// It runs in two steps: stage() copies the slot table and the builder's arguments
+// into shared memory, build() then reads only the row map from global memory.  In
+// the shrink's grid, stage() runs before the wait for the kernel before (the slot
+// table is pool state that no kernel writes), so that only the row map's round
+// trip follows the wait.
 #pragma once
 #include "internal.h"
 
 namespace mlora {
 namespace seg {
 
+// The builder's arguments, staged in shared memory.
+struct Staged {
+    Workspace ws;
+    const int32_t* row_adapter;
+    int T;
+    int max_chunks;
+};
+constexpr int STAGED_INTS = (int)((sizeof(Staged) + 15) / 16 * 4);   // 16-byte multiple
+
 struct Scratch {
+    Staged* in;      // the arguments
     int* rank_s;     // [S]
     int* unit_s;     // [S]
     int* scan;       // [S]
@@ -40,11 +55,15 @@ struct Scratch {
     int* ra_s;       // [T] the row map staged once, or nullptr (read from global memory)
 };
 
-__host__ __device__ inline int scratch_ints(int S, int P, int T_staged) { return 3 * S + P * S + 40 + T_staged; }
+__host__ __device__ inline int scratch_ints(int S, int P, int T_staged) {
+    return STAGED_INTS + 3 * S + P * S + 40 + T_staged;
+}
 
+// `base` 16-byte aligned
 __device__ inline Scratch carve(int* base, int S, int P, bool stage_rows) {
     Scratch s;
-    s.rank_s = base;
+    s.in = reinterpret_cast<Staged*>(base);
+    s.rank_s = base + STAGED_INTS;
     s.unit_s = s.rank_s + S;
     s.scan = s.unit_s + S;
     s.cur = s.scan + S;
@@ -98,22 +117,38 @@ __device__ inline int block_exclusive_scan(int* a, int n, int* warp_tmp) {
     return total;
 }
 
-// Builds the segments of row_adapter[0..T) over S slots in shared memory, with P
-// row ranges (at most the block's warps; warps past P only help with the scans),
-// and publishes them to the workspace.  Every thread of the block must call it.
-__device__ inline void build(const int32_t* __restrict__ row_adapter, int T, const SlotRec* __restrict__ slots,
-                             int S, int P, int max_chunks, const Scratch& sc, const Workspace& ws) {
-    const int nt = blockDim.x, lane = threadIdx.x & 31;
-    const int tid = threadIdx.x, warp = threadIdx.x >> 5;
-    int* warp_tmp = sc.misc;
-    // all global reads of the builder are issued here, together
-    if (sc.ra_s)
-        for (int t = tid; t < T; t += nt) sc.ra_s[t] = row_adapter[t];
-    for (int s = tid; s < S; s += nt) {
+// Copies the slot table and the builder's arguments into shared memory.  Every
+// thread of the block must call it (the block barrier is in build()).
+__device__ inline void stage(const SlotRec* __restrict__ slots, int S, const Workspace& ws,
+                             const int32_t* row_adapter, int T, int max_chunks, const Scratch& sc) {
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const SlotRec r = slots[s];
         sc.rank_s[s] = r.rank;
         sc.unit_s[s] = r.unit;
     }
+    if (threadIdx.x == 0) {
+        sc.in->ws = ws;
+        sc.in->row_adapter = row_adapter;
+        sc.in->T = T;
+        sc.in->max_chunks = max_chunks;
+    }
+}
+
+// Builds the segments of the staged row map over S slots in shared memory, with P
+// row ranges (at most the block's warps; warps past P only help with the scans),
+// and publishes them to the workspace.  Every thread of the block must call it,
+// after stage().
+__device__ inline void build(int S, int P, const Scratch& sc) {
+    const int nt = blockDim.x, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = threadIdx.x >> 5;
+    int* warp_tmp = sc.misc;
+    __syncthreads();   // the staged arguments
+    const Workspace& ws = sc.in->ws;
+    const int32_t* row_adapter = sc.in->row_adapter;
+    const int T = sc.in->T, max_chunks = sc.in->max_chunks;
+    // the builder's only global reads: the row map
+    if (sc.ra_s)
+        for (int t = tid; t < T; t += nt) sc.ra_s[t] = row_adapter[t];
     for (int i = tid; i < P * S; i += nt) sc.cur[i] = 0;
     if (tid == 0) sc.misc[33] = 0;
     __syncthreads();

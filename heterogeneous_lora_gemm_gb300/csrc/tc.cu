@@ -237,13 +237,15 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     if (SHRINK) {
         if (tile == p.seg_tile) {
             // the segment builder's column: its first CTA builds and publishes the
-            // segments (and the bad-row status), the others have nothing to do
+            // segments (and the bad-row status), the others have nothing to do.  The
+            // slot table and the arguments are staged before the wait for the kernel
+            // before: only the row map is read after it.
+            const bool builder = split == 0 && ztile == 0;
+            const seg::Scratch sc = seg::carve(reinterpret_cast<int*>(smem), p.S, p.seg_P, p.seg_stage_rows != 0);
+            if (builder) seg::stage(p.slots, p.S, p.ws, p.row_adapter, p.T, p.max_chunks, sc);
             pdl_wait();
             pdl_trigger();
-            if (split == 0 && ztile == 0) {
-                const seg::Scratch sc = seg::carve(reinterpret_cast<int*>(smem), p.S, p.seg_P, p.seg_stage_rows != 0);
-                seg::build(p.row_adapter, p.T, p.slots, p.S, p.seg_P, p.max_chunks, sc, p.ws);
-            }
+            if (builder) seg::build(p.S, p.seg_P, sc);
             return;
         }
     }
