@@ -70,30 +70,47 @@ __device__ __forceinline__ void load8f(const float* p, bool vec, int n, float* v
     }
 }
 
-// One thread per 16 codes of a row (din % 16 == 0: one 16-byte load), else per code.
+// Groups of 16 codes of a row (din % 16 == 0: one 16-byte load each), four groups
+// per thread and step with their loads issued first; else one code per thread.
+template <typename E>
+__device__ __forceinline__ void dequant16(const int4 raw, float so, E* dst) {
+    const int8_t* c = reinterpret_cast<const int8_t*>(&raw);
+    __align__(16) E out[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[j] = from_f32<E>((float)c[j] * so);
+    const int4* src = reinterpret_cast<const int4*>(out);
+    int4* d = reinterpret_cast<int4*>(dst);
+#pragma unroll
+    for (int j = 0; j < (int)(16 * sizeof(E) / 16); ++j) d[j] = src[j];
+}
+
 template <typename E>
 __global__ void __launch_bounds__(DQ_THREADS)
 dequant_kernel(const int8_t* __restrict__ q, const float* __restrict__ s, int dout, int din, E* __restrict__ W) {
-    const bool vec = (din % 16) == 0;
-    const size_t groups = vec ? (size_t)dout * (din / 16) : (size_t)dout * din;
-    for (size_t g = blockIdx.x * (size_t)blockDim.x + threadIdx.x; g < groups; g += (size_t)gridDim.x * blockDim.x) {
-        if (vec) {
-            const size_t e0 = g * 16;
-            const int o = (int)(e0 / din);
-            const float so = s[o];
-            const int4 raw = *reinterpret_cast<const int4*>(q + e0);
-            const int8_t* c = reinterpret_cast<const int8_t*>(&raw);
-            __align__(16) E out[16];
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t first = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    if ((din % 16) == 0) {
+        const size_t groups = (size_t)dout * (din / 16);
+        for (size_t g0 = first; g0 < groups; g0 += 4 * stride) {
+            int4 raw[4];
+            float so[4];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) out[j] = from_f32<E>((float)c[j] * so);
-            const int4* src = reinterpret_cast<const int4*>(out);
-            int4* dst = reinterpret_cast<int4*>(W + e0);
+            for (int u = 0; u < 4; ++u) {
+                const size_t g = g0 + u * stride;
+                if (g < groups) {
+                    raw[u] = *reinterpret_cast<const int4*>(q + g * 16);
+                    so[u] = s[(g * 16) / din];
+                }
+            }
 #pragma unroll
-            for (int j = 0; j < (int)(16 * sizeof(E) / 16); ++j) dst[j] = src[j];
-        } else {
-            const int o = (int)(g / din);
-            W[g] = from_f32<E>((float)q[g] * s[o]);
+            for (int u = 0; u < 4; ++u) {
+                const size_t g = g0 + u * stride;
+                if (g < groups) dequant16<E>(raw[u], so[u], W + g * 16);
+            }
         }
+    } else {
+        const size_t n = (size_t)dout * din;
+        for (size_t g = first; g < n; g += stride) W[g] = from_f32<E>((float)q[g] * s[g / din]);
     }
 }
 
