@@ -700,7 +700,10 @@ def run_reference(args, rank):
     oracle.forward(X, W, L.row_adapter, ads, rows=np.array([0], np.int64))
     row_s = max(time.perf_counter() - t0, 1e-6)
     budget = 90.0       # whole timed run, seconds
-    per_step = int(max(1, min(L.T, budget / (args.steps + args.warmup) / row_s * oracle.threads())))
+    # at least one row per host core: the oracle's row loop runs them in parallel, so
+    # a step costs about the same up to that many rows
+    per_step = int(max(min(L.T, oracle.threads()),
+                       min(L.T, budget / (args.steps + args.warmup) / row_s * oracle.threads())))
     rng = np.random.default_rng(args.seed)
     samples = [np.sort(rng.choice(L.T, size=per_step, replace=False)).astype(np.int64)
                for _ in range(min(args.steps, 64))]
