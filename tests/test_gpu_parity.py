@@ -534,6 +534,26 @@ def test_prefetch_replaces_a_slot_only_after_its_readers():
     assert pool.status() == mlora.MLORA_OK
 
 
+def test_prefetch_into_a_slot_that_held_module_adapters():
+    """A slot loaded with per-module adapters (chunks that reach only their module's
+    rows), then given a whole-layer adapter by prefetch: the new chunks reach every
+    row again, and a plain load after that as well."""
+    layer = wl.random_layer(36, T=40, din=128, dout=256, ranks=[16, 16], p_none=0.0)
+    pool = _host_tier_pool(layer, extra_budget=64, max_rank=32)
+    a0, a1 = layer.adapters
+    half = layer.dout // 2
+    pool.load_modules(0, [(0, half, to_device(a0.down, "bf16"), to_device(a0.up[:half], "bf16"), a0.scale),
+                          (half, half, None, None, 0.0)])
+    pool.load(1, to_device(a1.down, "bf16"), to_device(a1.up, "bf16"), a1.scale)
+    pool.host_add(9, to_device(a0.down, "bf16", "cpu"), to_device(a0.up, "bf16", "cpu"), a0.scale)
+    pool.prefetch(0, 9)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "whole-layer adapter after module adapters")
+    pool.load_modules(0, [(0, half, to_device(a0.down, "bf16"), to_device(a0.up[:half], "bf16"), a0.scale),
+                          (half, half, None, None, 0.0)])
+    pool.load(0, to_device(a0.down, "bf16"), to_device(a0.up, "bf16"), a0.scale)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "plain load after module adapters")
+
+
 def test_prefetch_errors_and_host_tier_lifecycle():
     layer = wl.random_layer(34, T=8, din=64, dout=64, ranks=[16])
     pool = _host_tier_pool(layer, max_rank=64)
