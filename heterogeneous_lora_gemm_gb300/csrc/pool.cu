@@ -248,8 +248,6 @@ mlora_status move_units(mlora_pool* p, int from, int to, int size) {
 
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
-// Records the pool's last-reader event after a forward/merge, or notes that the
-// call went into a graph under capture (then later loads wait for the device).
 constexpr int QUARANTINE_ID0 = 1 << 28;   // arena ids of quarantined blocks (slots are below)
 constexpr int TABLE_STAGES = 4;
 
@@ -257,18 +255,21 @@ constexpr int TABLE_STAGES = 4;
 // `wait`, waits for all of them first.
 mlora_status reclaim(mlora_pool* p, bool wait) {
     std::vector<mlora_pool::Quarantine> keep;
+    mlora_status st = MLORA_OK;
     for (const auto& q : p->quarantine) {
-        cudaError_t e = wait ? cudaEventSynchronize(q.free_at) : cudaEventQuery(q.free_at);
-        if (e == cudaErrorNotReady) {
+        cudaError_t e = cudaErrorNotReady;
+        if (st == MLORA_OK) e = wait ? cudaEventSynchronize(q.free_at) : cudaEventQuery(q.free_at);
+        if (e != cudaSuccess) {
+            // not finished, or the query failed (the block stays out of the allocator)
+            if (e != cudaErrorNotReady) st = cuda_fail(e, "quarantine event");
             keep.push_back(q);
             continue;
         }
-        if (e != cudaSuccess) return cuda_fail(e, "quarantine event");
         p->arena.release(q.id);
         cudaEventDestroy(q.free_at);
     }
-    p->quarantine.swap(keep);
-    return MLORA_OK;
+    p->quarantine.swap(keep);   // only the blocks not returned above
+    return st;
 }
 
 // Copies the host mirrors of the slot table and the chunk table into table set
@@ -296,6 +297,8 @@ mlora_status push_tables_async(mlora_pool* p, int set) {
     return MLORA_OK;
 }
 
+// Records the pool's last-reader event after a forward/merge, or notes that the
+// call went into a graph under capture (then later loads wait for the device).
 mlora_status note_reader(mlora_pool* p, cudaStream_t st) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     CU_TRY(cudaStreamIsCapturing(st, &cs));
