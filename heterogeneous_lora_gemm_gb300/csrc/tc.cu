@@ -171,19 +171,19 @@ struct GemmParams {
     Workspace ws;
 };
 
-// Sum of one slice of the staged partial tiles: groups g in [et, ng) step 128 of 4
+// Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
 // rows x 1 token, gpt groups per token, group i of a token at staged row row_of(i),
 // loaded from the shared memory of all NSP CTAs of the cluster (or, NSP = 1, of this
 // CTA), 8 float4 loads in flight per thread, summed in split order.
 template <int NSP, typename RowOf, typename Emit>
-__device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng, int gpt, int et, RowOf&& row_of,
-                                              Emit&& emit) {
+__device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng, int gpt, int et, int nthr,
+                                              RowOf&& row_of, Emit&& emit) {
     constexpr int U = NSP >= 8 ? 1 : 8 / NSP;
-    for (int g0 = et; g0 < ng; g0 += 128 * U) {
+    for (int g0 = et; g0 < ng; g0 += nthr * U) {
         float4 q[U][NSP];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int g = g0 + 128 * u;
+            const int g = g0 + nthr * u;
             if (g < ng) {
                 const int t = t_lo + g / gpt;
                 const uint32_t off = part_a + (uint32_t)((t * BM + row_of(g % gpt)) * 4);
@@ -197,7 +197,7 @@ __device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng,
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int g = g0 + 128 * u;
+            const int g = g0 + nthr * u;
             if (g < ng) {
                 float4 acc = q[u][0];
 #pragma unroll
@@ -394,6 +394,32 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         if (lane == 0) mbar_expect_tx(&tl.info_ready, 0);
     }
 
+    // epilogue warps: the TMEM lane quarter a warp may access, its row of the tile, and
+    // whether the accumulator holds this CTA's products (else it counts as zero)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
+    bool have = false;
+    // projection: final write of rows r0..r0+3 (a multiple of 4) of token t
+    auto emit4 = [&](int t, int r0, const float4& v) {
+        const int o0 = tile * BM + r0;
+        __nv_bfloat16* y = p.Y + (size_t)t * p.dout + o0;
+        if (p.dout % 4 == 0 && o0 + 4 <= p.dout) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+            uint2 w;
+            w.x = *reinterpret_cast<uint32_t*>(&lo);
+            w.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(y) = w;
+        } else {
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+            for (int j = 0; j < 4; ++j)
+                if (o0 + j < p.dout) y[j] = __float2bfloat16_rn(vv[j]);
+        }
+    };
+    // the K splits sum their partial tiles by staging them in shared memory
+    const bool staged = SHRINK || (p.splits > 1 && !p.push && p.cluster);
+
     if (warp == 0 && lane == 0) {
         // ---------------- producer: TMA loads into the stage ring
         int s = 0;
@@ -562,31 +588,10 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
     } else if (warp >= 2) {
         // ---------------- epilogue: TMEM -> partial tile, or the final values
-        const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;          // row of the tile
         const bool ok = mbar_wait(&tl.acc_full, 0, abort_flag, p.status);
         __syncwarp();   // reconverge: lanes may leave the wait loop apart; tcgen05.ld is warp-collective
         tc_fence_after();
-        const bool have = __all_sync(0xffffffffu, ok) && tl.flags[0] != 0;
-        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16);
-
-        // projection: final write of rows r0..r0+3 (a multiple of 4) of token t
-        auto emit4 = [&](int t, int r0, const float4& v) {
-            const int o0 = tile * BM + r0;
-            __nv_bfloat16* y = p.Y + (size_t)t * p.dout + o0;
-            if (p.dout % 4 == 0 && o0 + 4 <= p.dout) {
-                __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-                uint2 w;
-                w.x = *reinterpret_cast<uint32_t*>(&lo);
-                w.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(y) = w;
-            } else {
-                const float vv[4] = {v.x, v.y, v.z, v.w};
-                for (int j = 0; j < 4; ++j)
-                    if (o0 + j < p.dout) y[j] = __float2bfloat16_rn(vv[j]);
-            }
-        };
+        have = __all_sync(0xffffffffu, ok) && tl.flags[0] != 0;
 
         if (!SHRINK && p.splits == 1) {
             const int o = tile * BM + row;
@@ -697,70 +702,6 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     emit4(g / (BM / 4), (g % (BM / 4)) * 4, acc);
                 }
             }
-        } else {
-            // Staged reduction: each split stages its partial tile [token][row] in its
-            // own shared memory (the ring is idle: every load has been consumed by the
-            // finished MMAs), then, after a barrier (over the cluster when the splits
-            // form one), sums one slice of tokens over the shared memory of all splits,
-            // in split order, and writes it.  Passes of tp tokens when the whole tile
-            // does not fit the ring.  The shrink stages only the rows of its window
-            // (or of its chunks) and writes each used chunk's 16 columns of Vt, in
-            // groups of 4: the row's value for this chunk's own rank columns (scaled,
-            // for the tokens of the chunk's adapter), zero elsewhere.
-            float* part_s = reinterpret_cast<float*>(smem);
-            const uint32_t part_a = smem_u32(part_s);
-            const bool multi = p.splits > 1;
-            const int tp = min(p.N, (p.ring_bytes / (BM * 4)) & ~15);
-            const int rows = SHRINK ? (p.window ? p.win_rows : tile_chunks * CHUNK) : BM;
-            const int gpt = SHRINK ? tile_chunks * 4 : BM / 4;   // groups of 4 rows per token
-            auto row_of = [&](int gi) { return SHRINK ? tl.my_off[gi >> 2] + (gi & 3) * 4 : gi * 4; };
-            for (int p0 = 0; p0 < T; p0 += tp) {
-                const int pt = min(tp, T - p0);
-                if (q * 32 < rows)
-                    for (int t0 = 0; t0 < pt; t0 += 16) {
-                        float v[16];
-                        if (have) tmem_ld16(tbase + p0 + t0, v);
-                        else
-                            for (int j = 0; j < 16; ++j) v[j] = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) part_s[(t0 + j) * BM + row] = v[j];
-                    }
-                __syncwarp();
-                if (multi) cluster_sync();
-                else epi_bar();
-                const int ts = (pt + p.splits - 1) / p.splits;
-                const int t_lo = multi ? (int)cluster_rank() * ts : 0;
-                const int t_hi = min(pt, t_lo + ts);
-                const int ng = t_hi > t_lo ? (t_hi - t_lo) * gpt : 0;
-                auto emit_g = [&](int t, int gi, const float4& v) {
-                    if (SHRINK) {
-                        const int k = gi >> 2, j0 = (gi & 3) * 4;
-                        const int kval = tl.my_kval[k];
-                        const float sc = tl.tile_ra[p0 + t] == tl.my_slot[k] ? tl.my_scale[k] : 0.f;
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(j0 < kval ? sc * v.x : 0.f,
-                                                                  j0 + 1 < kval ? sc * v.y : 0.f);
-                        __nv_bfloat162 hi = __floats2bfloat162_rn(j0 + 2 < kval ? sc * v.z : 0.f,
-                                                                  j0 + 3 < kval ? sc * v.w : 0.f);
-                        uint2 w;
-                        w.x = *reinterpret_cast<uint32_t*>(&lo);
-                        w.y = *reinterpret_cast<uint32_t*>(&hi);
-                        *reinterpret_cast<uint2*>(p.vt + ((size_t)tl.my_c[k] * p.tcap + tok0 + p0 + t) * CHUNK + j0) = w;
-                    } else {
-                        emit4(p0 + t, gi * 4, v);
-                    }
-                };
-                const int et = threadIdx.x - 64;
-                if (p.splits == 1) staged_reduce<1>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
-                else if (p.splits == 2) staged_reduce<2>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
-                else if (p.splits == 3) staged_reduce<3>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
-                else if (p.splits == 4) staged_reduce<4>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
-                else if (p.splits == 6) staged_reduce<6>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
-                else staged_reduce<8>(part_a, t_lo, ng, gpt, et, row_of, emit_g);
-                __syncwarp();
-                // no CTA refills or leaves while the others still read its shared memory
-                if (multi) cluster_sync();
-                else epi_bar();
-            }
         }
     }
     if (warp < 2 && !SHRINK && p.push) {   // the epilogue warps' two split cluster barriers
@@ -768,12 +709,73 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         cluster_wait();
         cluster_arrive();
         cluster_wait();
-    } else if (warp < 2 && p.cluster && p.splits > 1) {   // the epilogue warps' cluster barriers, two per pass
-        __syncwarp();
+    }
+    if (staged && (warp >= 2 || p.splits > 1)) {
+        // Staged reduction: each split stages its partial tile [token][row] in its
+        // own shared memory (the ring is idle: every load has been consumed by the
+        // finished MMAs), then, after a barrier (over the cluster when the splits
+        // form one), sums one slice of tokens over the shared memory of all splits,
+        // in split order, and writes it.  Passes of tp tokens when the whole tile
+        // does not fit the ring.  The shrink stages only the rows of its window
+        // (or of its chunks) and writes each used chunk's 16 columns of Vt, in
+        // groups of 4: the row's value for this chunk's own rank columns (scaled,
+        // for the tokens of the chunk's adapter), zero elsewhere.  Across a cluster,
+        // warps 0 and 1 (done with the loads and the MMAs) share the sums.
+        __syncwarp();   // lane 0 of warps 0 and 1 ran its role alone
+        float* part_s = reinterpret_cast<float*>(smem);
+        const uint32_t part_a = smem_u32(part_s);
+        const bool multi = p.splits > 1;
         const int tp = min(p.N, (p.ring_bytes / (BM * 4)) & ~15);
+        const int rows = SHRINK ? (p.window ? p.win_rows : tile_chunks * CHUNK) : BM;
+        const int gpt = SHRINK ? tile_chunks * 4 : BM / 4;   // groups of 4 rows per token
+        const int et = multi ? (int)threadIdx.x : (int)threadIdx.x - 64;
+        const int nthr = multi ? NUM_THREADS : 128;
+        auto row_of = [&](int gi) { return SHRINK ? tl.my_off[gi >> 2] + (gi & 3) * 4 : gi * 4; };
         for (int p0 = 0; p0 < T; p0 += tp) {
-            cluster_sync();
-            cluster_sync();
+            const int pt = min(tp, T - p0);
+            if (warp >= 2 && q * 32 < rows)
+                for (int t0 = 0; t0 < pt; t0 += 16) {
+                    float v[16];
+                    if (have) tmem_ld16(tbase + p0 + t0, v);
+                    else
+                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) part_s[(t0 + j) * BM + row] = v[j];
+                }
+            __syncwarp();
+            if (multi) cluster_sync();
+            else epi_bar();
+            const int ts = (pt + p.splits - 1) / p.splits;
+            const int t_lo = multi ? (int)cluster_rank() * ts : 0;
+            const int t_hi = min(pt, t_lo + ts);
+            const int ng = t_hi > t_lo ? (t_hi - t_lo) * gpt : 0;
+            auto emit_g = [&](int t, int gi, const float4& v) {
+                if (SHRINK) {
+                    const int k = gi >> 2, j0 = (gi & 3) * 4;
+                    const int kval = tl.my_kval[k];
+                    const float sc = tl.tile_ra[p0 + t] == tl.my_slot[k] ? tl.my_scale[k] : 0.f;
+                    __nv_bfloat162 lo = __floats2bfloat162_rn(j0 < kval ? sc * v.x : 0.f,
+                                                              j0 + 1 < kval ? sc * v.y : 0.f);
+                    __nv_bfloat162 hi = __floats2bfloat162_rn(j0 + 2 < kval ? sc * v.z : 0.f,
+                                                              j0 + 3 < kval ? sc * v.w : 0.f);
+                    uint2 w;
+                    w.x = *reinterpret_cast<uint32_t*>(&lo);
+                    w.y = *reinterpret_cast<uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(p.vt + ((size_t)tl.my_c[k] * p.tcap + tok0 + p0 + t) * CHUNK + j0) = w;
+                } else {
+                    emit4(p0 + t, gi * 4, v);
+                }
+            };
+            if (p.splits == 1) staged_reduce<1>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
+            else if (p.splits == 2) staged_reduce<2>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
+            else if (p.splits == 3) staged_reduce<3>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
+            else if (p.splits == 4) staged_reduce<4>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
+            else if (p.splits == 6) staged_reduce<6>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
+            else staged_reduce<8>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
+            __syncwarp();
+            // no CTA refills or leaves while the others still read its shared memory
+            if (multi) cluster_sync();
+            else epi_bar();
         }
     }
     // A block barrier needs converged warps: lanes that skipped a one-thread branch
