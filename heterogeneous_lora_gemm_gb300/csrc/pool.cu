@@ -123,6 +123,7 @@ struct mlora_pool {
     char* ws_base = nullptr;
     size_t ws_bytes = 0;
     Workspace ws{};
+    uint32_t* row_max = nullptr;     // quantized merge: per-row max word (zero between calls)
     PoolDims dims{};
 
     cudaStream_t copy_stream = nullptr;
@@ -430,6 +431,7 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     const size_t o_part = carve(tcn.partial_bytes);
     const size_t o_ctr = carve(tcn.counter_bytes);
     const size_t o_tmask = carve(tcn.tmask_bytes);
+    const size_t o_rowmax = carve(sizeof(uint32_t) * (size_t)dout);
     p->ws_bytes = off;
     e = cudaMalloc((void**)&p->ws_base, p->ws_bytes);
     if (e != cudaSuccess) return bail(fail(MLORA_ERR_OOM, "workspace of %zu bytes: %s", p->ws_bytes, cudaGetErrorString(e)));
@@ -450,6 +452,7 @@ mlora_status mlora_pool_create(int max_slots, int rank_budget, int max_rank, int
     w.tile_ctr = (int32_t*)(p->ws_base + o_ctr);
     w.chunks = p->d_chunks;
     w.tmask = (uint8_t*)(p->ws_base + o_tmask);
+    p->row_max = (uint32_t*)(p->ws_base + o_rowmax);
 
     e = seg_init();
     if (e != cudaSuccess) return bail(cuda_fail(e, "seg_init"));
@@ -918,8 +921,13 @@ mlora_status mlora_merge_quantized(mlora_pool_t p, void* Wq, float* row_scale, i
     DeviceGuard g(p->device);
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t st = (cudaStream_t)stream;
-    const cudaError_t e = launch_merge_quant(p->dtype == MLORA_BF16, (int8_t*)Wq, row_scale, p->d_slots, slot,
-                                             p->arena_down, p->arena_up, p->dims, st);
+    // bf16 pools with whole 16-byte code rows: tensor cores (merged rows' max, new codes,
+    // new scales); otherwise CUDA cores, the merged rows held in shared memory
+    const cudaError_t e = p->dtype == MLORA_BF16 && p->din % 16 == 0
+                              ? launch_merge_quant_tc((int8_t*)Wq, row_scale, p->row_max, p->d_slots, slot, p->maps,
+                                                      p->ws.status, p->dims, st)
+                              : launch_merge_quant(p->dtype == MLORA_BF16, (int8_t*)Wq, row_scale, p->d_slots, slot,
+                                                   p->arena_down, p->arena_up, p->dims, st);
     if (e == cudaErrorInvalidValue) return fail(MLORA_ERR_INVALID_ARG, "din %d too large for the quantized merge", p->din);
     CU_TRY(e);
     return note_reader(p, st);

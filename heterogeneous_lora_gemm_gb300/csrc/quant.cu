@@ -9,9 +9,11 @@
 //                       clamped to [-127, 127]), in place.  Adding the update to the
 //                       codes themselves would mix two numeric spaces (§05).
 //
-// Both are bandwidth-bound sweeps over W.  The merge runs one CTA per group of rows
-// (each Down value loaded serves all of them): the rows are read, updated and held in
-// shared memory (fp32), reduced to their max, then written back as codes.
+// Both are bandwidth-bound sweeps over W.  The merge here serves fp32 pools and code
+// rows that are not whole 16-byte units (bf16 pools otherwise merge on the tensor
+// cores, merge_tc.cu).  It runs one CTA per group of rows (each Down value loaded
+// serves all of them): the rows are read, updated and held in shared memory (fp32),
+// reduced to their max, then written back as codes.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

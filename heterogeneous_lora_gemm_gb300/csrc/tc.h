@@ -68,6 +68,11 @@ cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din
 cudaError_t merge_tc_init();
 cudaError_t launch_merge_tc(void* W, const SlotRec* slots, int slot, const TcArenaMaps& maps, uint32_t* status,
                             const PoolDims& d, float sign, cudaStream_t st);
+// The merge into an int8 base (codes [dout x din], din % 16 == 0, 16-byte aligned; one
+// fp32 scale per row) on the tensor cores: the merged rows' max, their new codes, then
+// their new scales.  `row_max`: dout words of scratch, zero on entry and on return.
+cudaError_t launch_merge_quant_tc(int8_t* Wq, float* row_scale, uint32_t* row_max, const SlotRec* slots, int slot,
+                                  const TcArenaMaps& maps, uint32_t* status, const PoolDims& d, cudaStream_t st);
 
 // Encodes a bf16 tensor map (used by both tensor-core translation units).
 bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,

@@ -246,9 +246,13 @@ mlora_status mlora_unmerge(mlora_pool_t pool, void* W, int slot, mlora_stream_t 
  *   row_scale[o] = max_i |w[o,i]| / 127 (fp32; 0 for an all-zero row), codes
  *   rint(w / row_scale[o]) (to nearest, ties to even) clamped to [-127, 127].  The
  *   re-quantization adds at most half a step (row_scale[o] / 2) per element on top
- *   of the merged float weight.  Wq 16-byte aligned.  Errors: INVALID_ARG (also din
- *   too large for a row in shared memory, about 51 000), BAD_SLOT,
- *   NOT_LOADED, CUDA.
+ *   of the merged float weight.  Wq 16-byte aligned.  A bf16 pool with din a
+ *   multiple of 16 runs it on the tensor cores in three launches (the merged rows'
+ *   max, their codes, their scales; the fp32 sum over the rank may then round
+ *   differently from a sequential one, which moves a code by one only at a tie);
+ *   otherwise one CUDA-core launch holds each merged row in shared memory.
+ *   Errors: INVALID_ARG (also, on the CUDA-core path, din too large for a row in
+ *   shared memory, about 51 000), BAD_SLOT, NOT_LOADED, CUDA.
  */
 mlora_status mlora_dequantize(const void* Wq, const float* row_scale, int dout, int din, mlora_dtype dtype, void* W,
                               mlora_stream_t stream);

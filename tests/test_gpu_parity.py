@@ -406,6 +406,54 @@ def test_merge_quantized_random_within_one_step(dtype):
     assert diff.max() <= 1 and (diff > 0).mean() < 1e-3, (diff.max(), (diff > 0).mean())
 
 
+def test_merge_quantized_ties_round_to_even():
+    """Every merged value but one per row lands exactly halfway between two codes
+    (w / new scale = code + 1/2 in exact arithmetic): the codes must be the even
+    neighbours, as the oracle's fp32 division and rint give."""
+    from heterogeneous_lora_gemm_gb300 import Pool
+    rng = np.random.default_rng(55)
+    din, dout, r = 256, 136, 16
+    codes = rng.integers(-127, 127, size=(dout, din)).astype(np.int8)
+    codes[:, 0] = 127                     # w[o, 0] = 127 * 2^-6: the row max, new scale 2^-6
+    scale = np.full(dout, 2.0 ** -6, dtype=np.float32)
+    down = np.zeros((r, din))
+    down[0, 1:] = 2.0 ** -7               # update 2^-7 = half a step everywhere but column 0
+    up = np.zeros((dout, r))
+    up[:, 0] = 1.0
+    pool = Pool(1, 16, 16, din, dout, "bf16", 1)
+    pool.load(0, to_device(wl.f32_to_bf16_bits(down), "bf16"), to_device(wl.f32_to_bf16_bits(up), "bf16"), 1.0)
+    Wq, sc = torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda()
+    pool.merge_quantized(Wq, sc, 0)
+    torch.cuda.synchronize()
+    want_c, want_s = oracle.merge_quantized(codes, scale, oracle.OracleAdapter(down, up, 1.0))
+    np.testing.assert_array_equal(sc.cpu().numpy(), want_s)
+    np.testing.assert_array_equal(Wq.cpu().numpy(), want_c)
+    assert (want_c[:, 1:].astype(np.int32) % 2 == 0).all()   # the ties went to the even codes
+
+
+@pytest.mark.parametrize("din,dout,ranks", [(208, 200, [24]), (1024, 520, [40])])
+def test_merge_quantized_tensor_cores_ragged_and_repeated(din, dout, ranks):
+    """A bf16 pool whose code rows are whole 16-byte units merges on the tensor cores:
+    ragged tiles in both directions, a last rank chunk half used, and a second merge
+    after the first (the per-row scratch is cleared between calls).  Each merge is
+    checked against the oracle applied to the codes and scales it started from."""
+    layer = wl.random_layer(54, T=1, din=din, dout=dout, ranks=ranks, dtype="bf16")
+    codes, scale = oracle.quantize(layer.W_f64)
+    pool = make_pool(layer)
+    Wq, sc = torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda()
+    ad = ora_adapters(layer)[0]
+    for k in range(2):
+        start_c, start_s = Wq.cpu().numpy().copy(), sc.cpu().numpy().copy()
+        pool.merge_quantized(Wq, sc, 0)
+        torch.cuda.synchronize()
+        want_c, want_s = oracle.merge_quantized(start_c, start_s, ad)
+        got_c, got_s = Wq.cpu().numpy().astype(np.int32), sc.cpu().numpy()
+        np.testing.assert_allclose(got_s, want_s, rtol=1e-6, atol=0, err_msg=f"merge {k}: row scales")
+        diff = np.abs(got_c - want_c.astype(np.int32))
+        assert diff.max() <= 1 and (diff > 0).mean() < 1e-3, (k, diff.max(), (diff > 0).mean())
+    assert pool.status() == mlora.MLORA_OK
+
+
 # --------------------------------------------------------------------------- #
 # several modules of a fused projection in one launch (airsota card, section 四 item ④)
 @pytest.mark.parametrize("T", [48, 300])
