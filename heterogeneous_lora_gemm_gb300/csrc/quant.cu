@@ -72,14 +72,24 @@ __device__ __forceinline__ void load8f(const float* p, bool vec, int n, float* v
     }
 }
 
+// A code as a float without a conversion instruction: 2^23 + 128 + c holds c + 128 in
+// its low mantissa bits.
+__device__ __forceinline__ float code_f32(int8_t c) { return __int_as_float(0x4B000000 + 128 + (int)c) - 8388736.f; }
+
 // Groups of 16 codes of a row (din % 16 == 0: one 16-byte load each), four groups
 // per thread and step with their loads issued first; else one code per thread.
 template <typename E>
 __device__ __forceinline__ void dequant16(const int4 raw, float so, E* dst) {
     const int8_t* c = reinterpret_cast<const int8_t*>(&raw);
     __align__(16) E out[16];
+    if constexpr (sizeof(E) == 2) {   // bf16: two values per rounding instruction
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) out[j] = from_f32<E>((float)c[j] * so);
+        for (int j = 0; j < 8; ++j) o2[j] = __floats2bfloat162_rn(code_f32(c[2 * j]) * so, code_f32(c[2 * j + 1]) * so);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) out[j] = from_f32<E>(code_f32(c[j]) * so);
+    }
     const int4* src = reinterpret_cast<const int4*>(out);
     int4* d = reinterpret_cast<int4*>(dst);
 #pragma unroll
@@ -93,6 +103,8 @@ dequant_kernel(const int8_t* __restrict__ q, const float* __restrict__ s, int do
     const size_t first = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
     if ((din % 16) == 0) {
         const size_t groups = (size_t)dout * (din / 16);
+        const uint32_t gpr = (uint32_t)(din / 16);          // groups per row
+        const bool narrow = groups <= 0xFFFFFFFFull;        // row of a group by a 32-bit division
         for (size_t g0 = first; g0 < groups; g0 += 4 * stride) {
             int4 raw[4];
             float so[4];
@@ -101,7 +113,7 @@ dequant_kernel(const int8_t* __restrict__ q, const float* __restrict__ s, int do
                 const size_t g = g0 + u * stride;
                 if (g < groups) {
                     raw[u] = *reinterpret_cast<const int4*>(q + g * 16);
-                    so[u] = s[(g * 16) / din];
+                    so[u] = s[narrow ? (size_t)((uint32_t)g / gpr) : g / gpr];
                 }
             }
 #pragma unroll
