@@ -384,10 +384,13 @@ cudaError_t launch_merge_quant_tc(int8_t* Wq, float* row_scale, uint32_t* row_ma
     const dim3 grid((d.din + MG_BN_USED - 1) / MG_BN_USED, (d.dout + MG_BM - 1) / MG_BM);
     cudaError_t e = launch_k(merge_tc_kernel<MG_BN_USED, MODE_QMAX>, grid, dim3(MG_THREADS),
                              merge_smem<MG_BN_USED, MODE_QMAX>(), st, false, 1, tmQ, maps.down, maps.up128, p);
-    if (e == cudaSuccess)
-        e = launch_k(merge_tc_kernel<MG_BN_USED, MODE_QCODES>, grid, dim3(MG_THREADS),
-                     merge_smem<MG_BN_USED, MODE_QCODES>(), st, false, 1, tmQ, maps.down, maps.up128, p);
     if (e != cudaSuccess) return e;
+    e = launch_k(merge_tc_kernel<MG_BN_USED, MODE_QCODES>, grid, dim3(MG_THREADS), merge_smem<MG_BN_USED, MODE_QCODES>(),
+                 st, false, 1, tmQ, maps.down, maps.up128, p);
+    if (e != cudaSuccess) {   // the words hold this call's maxima: clear them for the next call
+        cudaMemsetAsync(row_max, 0, sizeof(uint32_t) * (size_t)d.dout, st);
+        return e;
+    }
     row_scale_kernel<<<(d.dout + 255) / 256, 256, 0, st>>>(row_scale, row_max, d.dout);
     return cudaGetLastError();
 }
