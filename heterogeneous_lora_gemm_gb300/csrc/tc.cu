@@ -174,17 +174,20 @@ struct GemmParams {
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
 // rows x 1 token, gpt groups per token, group i of a token at staged row row_of(i),
 // loaded from the shared memory of all NSP CTAs of the cluster (or, NSP = 1, of this
-// CTA), 8 float4 loads in flight per thread, summed in split order.
-template <int NSP, typename RowOf, typename Emit>
+// CTA), 8 float4 loads in flight per thread, summed in split order.  A group that
+// need(token, i) rejects is not loaded: it is emitted as zeros.
+template <int NSP, typename RowOf, typename Need, typename Emit>
 __device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng, int gpt, int et, int nthr,
-                                              RowOf&& row_of, Emit&& emit) {
+                                              RowOf&& row_of, Need&& need, Emit&& emit) {
     constexpr int U = NSP >= 8 ? 1 : 8 / NSP;
     for (int g0 = et; g0 < ng; g0 += nthr * U) {
         float4 q[U][NSP];
+        bool ok[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int g = g0 + nthr * u;
-            if (g < ng) {
+            ok[u] = g < ng && need(t_lo + g / gpt, g % gpt);
+            if (ok[u]) {
                 const int t = t_lo + g / gpt;
                 const uint32_t off = part_a + (uint32_t)((t * BM + row_of(g % gpt)) * 4);
                 if (NSP == 1) {
@@ -199,13 +202,16 @@ __device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng,
         for (int u = 0; u < U; ++u) {
             const int g = g0 + nthr * u;
             if (g < ng) {
-                float4 acc = q[u][0];
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ok[u]) {
+                    acc = q[u][0];
 #pragma unroll
-                for (int sp = 1; sp < NSP; ++sp) {
-                    acc.x += q[u][sp].x;
-                    acc.y += q[u][sp].y;
-                    acc.z += q[u][sp].z;
-                    acc.w += q[u][sp].w;
+                    for (int sp = 1; sp < NSP; ++sp) {
+                        acc.x += q[u][sp].x;
+                        acc.y += q[u][sp].y;
+                        acc.z += q[u][sp].z;
+                        acc.w += q[u][sp].w;
+                    }
                 }
                 emit(t_lo + g / gpt, g % gpt, acc);
             }
@@ -749,6 +755,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const int t_lo = multi ? (int)cluster_rank() * ts : 0;
             const int t_hi = min(pt, t_lo + ts);
             const int ng = t_hi > t_lo ? (t_hi - t_lo) * gpt : 0;
+            // the shrink keeps a chunk's values only for the tokens of the chunk's adapter
+            // (the others are written as zeros): their sums need no loads
+            auto need = [&](int t, int gi) { return !SHRINK || tl.tile_ra[p0 + t] == tl.my_slot[gi >> 2]; };
             auto emit_g = [&](int t, int gi, const float4& v) {
                 if (SHRINK) {
                     const int k = gi >> 2, j0 = (gi & 3) * 4;
@@ -766,12 +775,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     emit4(p0 + t, gi * 4, v);
                 }
             };
-            if (p.splits == 1) staged_reduce<1>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
-            else if (p.splits == 2) staged_reduce<2>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
-            else if (p.splits == 3) staged_reduce<3>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
-            else if (p.splits == 4) staged_reduce<4>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
-            else if (p.splits == 6) staged_reduce<6>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
-            else staged_reduce<8>(part_a, t_lo, ng, gpt, et, nthr, row_of, emit_g);
+            if (p.splits == 1) staged_reduce<1>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 2) staged_reduce<2>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 3) staged_reduce<3>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 4) staged_reduce<4>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 6) staged_reduce<6>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else staged_reduce<8>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
             __syncwarp();
             // no CTA refills or leaves while the others still read its shared memory
             if (multi) cluster_sync();
