@@ -3,12 +3,16 @@ the pins of tests/test_oracle_pins.py catch every one of them.
 
 Each mutant is the oracle's C source with one edit (a dropped term, a wrong
 sign or index, a transposed operand, an unstable group order), compiled into a
-temporary library and swapped in for the duration of the pin run.
+temporary library and swapped in for the duration of the pin run.  The oracle's
+numpy functions get the same treatment: one edit to a function's source, run in
+the oracle module's namespace and swapped in for the pins.
 """
 import ctypes
+import inspect
 import os
 import subprocess
 import tempfile
+import textwrap
 
 import pytest
 
@@ -93,3 +97,46 @@ def test_every_planted_mistake_is_caught(name, monkeypatch):
     with tempfile.TemporaryDirectory() as d:
         lib = _build_mutant(name, d)
         assert _run_pins_with(lib) > 0, f"no pin caught the mutant {name!r}"
+
+
+# numpy parts of the oracle: (function, text replaced, replacement)
+PY_MUTANTS = {
+    "quantize ties away from zero": ("quantize", "np.rint(w / safe[:, None])",
+                                     "np.trunc(w / safe[:, None] + np.copysign(0.5, w))"),
+    "quantize scale from 128 levels": ("quantize", "np.float32(127)", "np.float32(128)"),
+    "quantized merge adds to the codes": ("merge_quantized", "quantize(merge(dequantize(codes, row_scale), adapter))",
+                                          "(np.clip(codes + np.rint(adapter.scale * adapter.up @ adapter.down), "
+                                          "-127, 127).astype(np.int8), row_scale)"),
+}
+
+PY_PIN_TESTS = [
+    pins.test_quantize_recovers_an_exact_grid,
+    pins.test_quantize_sends_exact_ties_to_the_even_code,
+    pins.test_quantization_error_is_at_most_half_a_step,
+    pins.test_merge_on_a_quantized_base_three_ways,
+]
+
+
+def _count_failures(tests):
+    failures = 0
+    for t in tests:
+        try:
+            t()
+        except AssertionError:
+            failures += 1
+    return failures
+
+
+def test_numpy_pins_pass_on_the_real_oracle():
+    assert _count_failures(PY_PIN_TESTS) == 0
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_every_planted_numpy_mistake_is_caught(name, monkeypatch):
+    fn, old, new = PY_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fn)))
+    assert src.count(old) == 1, f"mutation site of {name!r} not found exactly once"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, fn, ns[fn])
+    assert _count_failures(PY_PIN_TESTS) > 0, f"no pin caught the mutant {name!r}"

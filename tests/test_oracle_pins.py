@@ -237,6 +237,18 @@ def test_quantize_recovers_an_exact_grid():
     np.testing.assert_array_equal(s2, scale.astype(np.float32))
 
 
+def test_quantize_sends_exact_ties_to_the_even_code():
+    """Rounding to nearest with ties to even (IEEE 754 roundTiesToEven, the rule the
+    kernels' fp32 rounding uses): a row whose maximum is 127 units and whose other
+    weights sit exactly halfway between two units gets the even neighbour for each --
+    2.5 -> 2, 3.5 -> 4, -0.5 -> 0, -1.5 -> -2."""
+    unit = 2.0 ** -6
+    row = np.array([127.0, 2.5, 3.5, -0.5, -1.5, 126.5, -126.5, 0.5]) * unit
+    codes, scale = oracle.quantize(row[None, :])
+    assert scale[0] == np.float32(unit)
+    np.testing.assert_array_equal(codes[0], [127, 2, 4, 0, -2, 126, -126, 0])
+
+
 def test_quantization_error_is_at_most_half_a_step():
     W = np.random.default_rng(22).standard_normal((9, 70)) * 0.02
     codes, scale = oracle.quantize(W)
