@@ -923,13 +923,15 @@ mlora_status mlora_merge_quantized(mlora_pool_t p, void* Wq, float* row_scale, i
     cudaStream_t st = (cudaStream_t)stream;
     // bf16 pools with whole 16-byte code rows: tensor cores (merged rows' max, new codes,
     // new scales); otherwise CUDA cores, the merged rows held in shared memory
-    const cudaError_t e = p->dtype == MLORA_BF16 && p->din % 16 == 0
+    const bool tensor_cores = p->dtype == MLORA_BF16 && p->din % 16 == 0;
+    const cudaError_t e = tensor_cores
                               ? launch_merge_quant_tc((int8_t*)Wq, row_scale, p->row_max, p->d_slots, slot, p->maps,
                                                       p->ws.status, p->dims, st)
                               : launch_merge_quant(p->dtype == MLORA_BF16, (int8_t*)Wq, row_scale, p->d_slots, slot,
                                                    p->arena_down, p->arena_up, p->dims, st);
-    if (e == cudaErrorInvalidValue) return fail(MLORA_ERR_INVALID_ARG, "din %d too large for the quantized merge", p->din);
-    CU_TRY(e);
+    if (e == cudaErrorInvalidValue && !tensor_cores)
+        return fail(MLORA_ERR_INVALID_ARG, "din %d too large for the quantized merge", p->din);
+    if (e != cudaSuccess) return cuda_fail(e, tensor_cores ? "quantized merge (tensor cores)" : "quantized merge");
     return note_reader(p, st);
 }
 
