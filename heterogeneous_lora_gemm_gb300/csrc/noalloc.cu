@@ -21,6 +21,7 @@
 #include "../../include/mlora.h"
 #include "internal.h"
 #include "tc.h"
+#include "tc_ptx.cuh"
 
 namespace mlora {
 
@@ -87,11 +88,69 @@ extern "C" mlora_status mlora_project_noalloc(const void* X, const void* W, int 
     int32_t* counters = (int32_t*)((char*)base + NOALLOC_PARTIAL_BYTES);
     uint32_t* status = (uint32_t*)(counters + NOALLOC_MAX_TILES);
     cudaStream_t s = (cudaStream_t)stream;
-    // the counters and the status word must start at zero; the array keeps what the last call left
-    e = cudaMemsetAsync(counters, 0, NOALLOC_MAX_TILES * sizeof(int32_t) + sizeof(uint32_t), s);
+    // the counters must start at zero (the array keeps what the last call left); the
+    // status word keeps its bits until mlora_project_noalloc_status reads and clears it
+    e = cudaMemsetAsync(counters, 0, NOALLOC_MAX_TILES * sizeof(int32_t), s);
     if (e == cudaSuccess)
         e = tc_project_with_scratch(X, W, T, din, dout, Y, partials, NOALLOC_PARTIAL_BYTES, counters,
                                     NOALLOC_MAX_TILES, status, s);
+    if (e != cudaSuccess) return noalloc_fail(MLORA_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
+    return MLORA_OK;
+}
+
+// Status of the allocation-free calls on the current device: synchronizes `stream`,
+// reads the status word of the scratch array and clears it.
+extern "C" mlora_status mlora_project_noalloc_status(mlora_stream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return noalloc_fail(MLORA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return noalloc_fail(MLORA_ERR_UNSUPPORTED, "device index above 63");
+    void* base = nullptr;
+    mlora_status st = noalloc_setup(dev, &base);
+    if (st != MLORA_OK) return st;
+    uint32_t* status = (uint32_t*)((char*)base + NOALLOC_PARTIAL_BYTES + NOALLOC_MAX_TILES * sizeof(int32_t));
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word = 0;
+    e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&word, status, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof word, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return noalloc_fail(MLORA_ERR_CUDA, std::string("status read: ") + cudaGetErrorString(e));
+    if (word & STATUS_TIMEOUT) return noalloc_fail(MLORA_ERR_DEVICE_TIMEOUT, "a kernel pipeline wait gave up");
+    return MLORA_OK;
+}
+
+namespace mlora {
+namespace {
+
+// One pipeline wait that nothing completes: an mbarrier expecting one arrival that
+// never comes, waited on with the kernels' bounded wait and the given limit.  Its
+// expiry raises STATUS_TIMEOUT in `status`, as a real pipeline wait that gave up would.
+__global__ void noalloc_expire_wait_kernel(uint32_t* status, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    ptx::mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    ptx::mbar_wait_limit(&bar, 0, &abort_flag, status, limit);
+}
+
+}  // namespace
+}  // namespace mlora
+
+extern "C" mlora_status mlora_debug_noalloc_expire_wait(long long cycles, mlora_stream_t stream) {
+    if (cycles < 1 || cycles > (1ll << 31)) return noalloc_fail(MLORA_ERR_INVALID_ARG, "cycles not in [1, 2^31]");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return noalloc_fail(MLORA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return noalloc_fail(MLORA_ERR_UNSUPPORTED, "device index above 63");
+    void* base = nullptr;
+    mlora_status st = noalloc_setup(dev, &base);
+    if (st != MLORA_OK) return st;
+    uint32_t* status = (uint32_t*)((char*)base + NOALLOC_PARTIAL_BYTES + NOALLOC_MAX_TILES * sizeof(int32_t));
+    noalloc_expire_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status, cycles);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return noalloc_fail(MLORA_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
     return MLORA_OK;
 }

@@ -131,8 +131,9 @@ struct mlora_pool {
     bool reader_pending = false;
     bool captured = false;           // a forward or merge was captured into a graph
 
-    std::vector<cudaEvent_t> prof_start, prof_stop;
-    size_t prof_next = 0;
+    unsigned long long* prof_stamps = nullptr;   // caller's profiling record buffer (NULL = off)
+    int prof_cap = 0;
+    int last_T = 0;                  // rows of the last forward that built segments
 
     // Host (cold) tier (M031 §06): adapters in pinned host memory, already in the
     // arena's layout, copied into a slot on demand by mlora_prefetch.
@@ -830,12 +831,6 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
     // the tensor-core shrink builds the segments itself; otherwise a separate segment
     // kernel runs (fp32 path, or nothing loaded: only the status bit)
     if (lora && (!tc || p->n_chunks == 0)) CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
-    cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
-    if (!p->prof_start.empty()) {
-        const size_t k = p->prof_next++ % p->prof_start.size();
-        ev_start = p->prof_start[k];
-        ev_stop = p->prof_stop[k];
-    }
     if (tc) {
         TcForwardArgs a{};
         a.X = X;
@@ -852,15 +847,15 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
         a.n_chunks = p->n_chunks;
         a.tile_span = p->tile_span;
         a.units = p->units;
-        a.ev_start = ev_start;
-        a.ev_stop = ev_stop;
+        a.n_loaded = p->loaded;
+        a.stamps = p->prof_stamps;
+        a.stamp_cap = p->prof_cap;
         CU_TRY(tc_forward(a, st));
     } else {
         if (lora) CU_TRY(launch_shrink_simt(bf16, X, row_adapter, T, p->d_slots, p->arena_down, p->ws, p->dims, st));
-        if (ev_start) CU_TRY(record_profile(ev_start, st));
         CU_TRY(launch_base_expand_simt(bf16, X, W, row_adapter, T, Y, p->d_slots, p->arena_up, p->ws, p->dims, lora, st));
-        if (ev_stop) CU_TRY(record_profile(ev_stop, st));
     }
+    if (lora) p->last_T = T;
     return note_reader(p, st);
 }
 
@@ -981,22 +976,33 @@ mlora_status mlora_debug_segments(mlora_pool_t p, const int32_t* row_adapter, in
         return MLORA_OK;
     }
     CU_TRY(launch_seg_build(row_adapter, T, p->d_slots, p->ws, p->dims, st));
+    p->last_T = -1;   // the workspace now holds this builder's segments, not a forward's
     CU_TRY(cudaMemcpyAsync(perm, p->ws.perm, sizeof(int32_t) * (size_t)T, cudaMemcpyDeviceToDevice, st));
     CU_TRY(cudaMemcpyAsync(offsets, p->ws.offsets, sizeof(int32_t) * (size_t)(p->max_slots + 1),
                            cudaMemcpyDeviceToDevice, st));
     return note_reader(p, st);
 }
 
-mlora_status mlora_profile_events(mlora_pool_t p, void* const* starts, void* const* stops, int n) {
-    if (!p || n < 0 || (n > 0 && (!starts || !stops))) return fail(MLORA_ERR_INVALID_ARG, "bad profiling events");
-    p->prof_start.clear();
-    p->prof_stop.clear();
-    for (int i = 0; i < n; ++i) {
-        if (!starts[i] || !stops[i]) return fail(MLORA_ERR_INVALID_ARG, "event %d is NULL", i);
-        p->prof_start.push_back((cudaEvent_t)starts[i]);
-        p->prof_stop.push_back((cudaEvent_t)stops[i]);
-    }
-    p->prof_next = 0;
+mlora_status mlora_debug_last_segments(mlora_pool_t p, int T, int32_t* perm, int32_t* offsets,
+                                       mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
+    if (!offsets || (T > 0 && !perm)) return fail(MLORA_ERR_INVALID_ARG, "perm/offsets is NULL");
+    if (p->last_T != T) return fail(MLORA_ERR_INVALID_ARG, "the last forward with a row map had %d rows, not %d", p->last_T, T);
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T > 0) CU_TRY(cudaMemcpyAsync(perm, p->ws.perm, sizeof(int32_t) * (size_t)T, cudaMemcpyDeviceToDevice, st));
+    CU_TRY(cudaMemcpyAsync(offsets, p->ws.offsets, sizeof(int32_t) * (size_t)(p->max_slots + 1),
+                           cudaMemcpyDeviceToDevice, st));
+    return MLORA_OK;
+}
+
+mlora_status mlora_profile_stamps(mlora_pool_t p, void* records, int cap) {
+    if (!p || cap < 0 || (cap > 0 && !records)) return fail(MLORA_ERR_INVALID_ARG, "bad profiling record buffer");
+    if (((uintptr_t)records & 7u) != 0) return fail(MLORA_ERR_INVALID_ARG, "record buffer must be 8-byte aligned");
+    p->prof_stamps = cap > 0 ? (unsigned long long*)records : nullptr;
+    p->prof_cap = cap;
     return MLORA_OK;
 }
 

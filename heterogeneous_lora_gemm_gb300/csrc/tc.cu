@@ -137,6 +137,7 @@ struct Tail {
     uint32_t slot_bits[MAX_SLOT_WORDS];   // projection: slots some row of the batch uses
     int ext_unit[EXT_CAP];            // projection: arena unit of each K-extension chunk, -1 = skip
     int ext_slot[EXT_CAP];
+    unsigned long long t_start;       // profiling: globaltimer at the CTA's start
 };
 
 struct GemmParams {
@@ -169,6 +170,8 @@ struct GemmParams {
     int S, max_chunks;
     int seg_tile, seg_P, seg_stage_rows;   // shrink: grid column of the segment builder, its plan
     Workspace ws;
+    unsigned long long* stamps;     // profiling records (NULL = off), see ptx::stamp_record
+    int stamp_cap;
 };
 
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
@@ -237,11 +240,14 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
+    constexpr int kStampKind = SHRINK ? STAMP_SHRINK : STAMP_PROJECTION;
     const int tok0 = ztile * MAX_N;                  // first token of this token tile
     const int T = min(p.T - tok0, p.N);              // tokens in this tile
 
     if (SHRINK) {
         if (tile == p.seg_tile) {
+            // (the builder's scratch may cover the Tail: this start time stays in a register)
+            const unsigned long long t_seg = (p.stamps && threadIdx.x == 0) ? gtimer() : 0ull;
             // the segment builder's column: its first CTA builds and publishes the
             // segments (and the bad-row status), the others have nothing to do.  The
             // slot table and the arguments are staged before the wait for the kernel
@@ -252,9 +258,11 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             pdl_wait();
             pdl_trigger();
             if (builder) seg::build(p.S, p.seg_P, sc);
+            if (threadIdx.x == 0) stamp_record(p.stamps, p.stamp_cap, t_seg, kStampKind);
             return;
         }
     }
+    if (p.stamps && threadIdx.x == 0) tl.t_start = gtimer();
 
     const int kb0 = (int)((long long)split * p.ksteps / p.splits);
     const int kb1 = (int)((long long)(split + 1) * p.ksteps / p.splits);
@@ -358,6 +366,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             tc_fence_after();
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
         }
+        if (threadIdx.x == 0) stamp_record(p.stamps, p.stamp_cap, tl.t_start, kStampKind);
         return;
     }
 
@@ -797,19 +806,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
     }
+    if (threadIdx.x == 0) stamp_record(p.stamps, p.stamp_cap, tl.t_start, kStampKind);
 }
 
 }  // namespace
 
 // ---------------------------------------------------------------- host side
-cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    cudaError_t e = cudaStreamIsCapturing(st, &cs);
-    if (e != cudaSuccess) return e;
-    return cs != cudaStreamCaptureStatusNone ? cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal)
-                                             : cudaEventRecord(ev, st);
-}
-
 namespace {
 
 // Shared-memory budgets of the rings.  A decode projection takes PROJ_SMEM_BUDGET
@@ -818,7 +820,10 @@ namespace {
 // SHRINK_SMEM_BUDGET_APART) or shares SMs with it, both rings then sized to fit one
 // SM's 228 KiB together with their tails (PROJ_ and SHRINK_SMEM_BUDGET_SHARED).
 // Otherwise (prefill, two projection CTAs per SM) the shrink takes SHRINK_SMEM_BUDGET.
+// A projection with no shrink in its forward takes PROJ_SMEM_BUDGET_ALONE when one CTA
+// per SM runs: a deeper ring keeps more W (and, for wide batches, X) in flight.
 constexpr int PROJ_SMEM_BUDGET = 136 * 1024;
+constexpr int PROJ_SMEM_BUDGET_ALONE = 208 * 1024;
 constexpr int PROJ_SMEM_BUDGET_2 = 100 * 1024;   // two projection CTAs per SM
 constexpr int PROJ_SMEM_BUDGET_SHARED = 112 * 1024;
 constexpr int SHRINK_SMEM_BUDGET = 84 * 1024;
@@ -889,6 +894,7 @@ cudaError_t tc_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(swapab_gemm_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess) e = prefill_init();
+    if (e == cudaSuccess) e = gemv_init();
     if (e == cudaSuccess) e = merge_tc_init();
     return e;
 }
@@ -946,7 +952,12 @@ DecodeShape decode_shape(const PoolDims& d, int N, int budget1) {
     // SM with a smaller ring
     int splits = cluster_splits(k_splits(tiles, kb_total, N, false));
     int budget = budget1;
-    if (tiles * splits < 3 * sm_count() / 4) {
+    if (tiles >= sm_count()) {
+        // more row tiles than SMs (e.g. a fused gate|up of 22016 features): two CTAs
+        // per SM and three K splits, so that the waves of small work units balance
+        splits = kb_total < 3 ? kb_total : 3;
+        budget = PROJ_SMEM_BUDGET_2;
+    } else if (tiles * splits < 3 * sm_count() / 4) {
         int s2 = 2 * sm_count() / tiles;
         s2 = s2 > kb_total ? kb_total : s2;
         s2 = s2 >= 8 ? 8 : (s2 >= 6 ? 6 : (s2 >= 4 ? 4 : s2));   // cluster sizes with a reducer
@@ -956,9 +967,13 @@ DecodeShape decode_shape(const PoolDims& d, int N, int budget1) {
         }
     }
     // W and X as 3D views {64, rows, K chunks}, so that one box carries up to PROJ_KC
-    // K chunks (needs din % 64 == 0; at most as many as let two stages fit)
+    // K chunks (needs din % 64 == 0): at least two stages, and three or more narrower
+    // ones rather than two wide ones
     int pkc = d.din % BK == 0 ? PROJ_KC : 1;
-    while (pkc > 1 && 2 * pkc * stage_bytes(N) > budget - (N <= PUSH_MAX_N ? BM * N * 4 : 0)) --pkc;
+    const int avail = budget - (N <= PUSH_MAX_N ? BM * N * 4 : 0);
+    while (pkc > 1 && (2 * pkc * stage_bytes(N) > avail ||
+                       (avail / (pkc * stage_bytes(N)) < 3 && avail / stage_bytes(N) >= 3)))
+        --pkc;
     DecodeShape s;
     s.budget = budget;
     s.pkc = pkc;
@@ -978,9 +993,16 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const bool shrink = n_chunks > 0;
     cudaError_t e;
     const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
-    DecodeShape ds = decode_shape(d, decode ? N : 16, PROJ_SMEM_BUDGET);
+    DecodeShape ds = decode_shape(d, decode ? N : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE);
+    // A decode batch with at most two rows per loaded adapter (on average) takes the
+    // CUDA-core shrink: its adapters are read once each, with no split-K reduction.
+    const bool gemv = decode && shrink && gemv_shrink_fits(d, T) && a.n_loaded > 0 && T <= 2 * a.n_loaded;
     int shrink_budget = SHRINK_SMEM_BUDGET;
-    if (decode && shrink && ds.budget == PROJ_SMEM_BUDGET) {
+    if (gemv) {
+        // its Down rows are prefetched into L2 before the wait for the kernel before
+        // when most loaded adapters are likely to be used
+        if ((e = launch_shrink_gemv(a, T >= a.n_loaded, st)) != cudaSuccess) return e;
+    } else if (decode && shrink && ds.budget == PROJ_SMEM_BUDGET) {
         // a shrink whose CTAs fit the SMs that the projection leaves idle gets a larger
         // ring there; a larger one shares SMs with the projection, both rings smaller
         const int stiles = (n_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
@@ -994,7 +1016,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     }
 
     // ---- shrink: Vt = masked scale * Down_chunks X^T, per token tile, the used chunks
-    if (shrink) {
+    if (shrink && !gemv) {
         const int Ns = decode ? (T + 15) / 16 * 16 : MAX_N;
         CUtensorMap tmXs, tmNone, tmDown;
         std::memset(&tmNone, 0, sizeof tmNone);
@@ -1072,6 +1094,8 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         g.seg_P = sp.P;
         g.seg_stage_rows = sp.stage_rows ? 1 : 0;
         g.cluster = g.splits > 1 ? 1 : 0;
+        g.stamps = a.stamps;
+        g.stamp_cap = a.stamp_cap;
         // first kernel of the forward: it may launch while the stream's previous kernel
         // runs, and waits for it before reading X or the row map
         e = launch_k(swapab_gemm_kernel<true>, dim3(tiles + 1, g.splits, ztiles), dim3(NUM_THREADS), smem_bytes(g),
@@ -1100,10 +1124,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     }
 
     if (!decode) {
-        if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
-        if ((e = launch_prefill(a, tmX, tmW, tmV, sm_count(), shrink, st)) != cudaSuccess) return e;
-        if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
-        return cudaSuccess;
+        return launch_prefill(a, tmX, tmW, tmV, sm_count(), shrink, st);
     }
 
     const int tiles = proj_tiles(d);
@@ -1147,16 +1168,14 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     // kernel before it may run, its W goes out at once and its X after that kernel
     // has completed.  After a shrink it launches once the shrink has seen the kernel
     // before the forward complete, so X may be read at once.
-    p.xwait = (!shrink && !a.ev_start) ? 1 : 0;
+    p.xwait = shrink ? 0 : 1;
     p.cluster = p.splits > 1 ? 1 : 0;
     p.S = d.S;
     p.max_chunks = d.max_chunks;
-    if (a.ev_start && (e = record_profile(a.ev_start, st)) != cudaSuccess) return e;
-    e = launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p), st,
-                 !a.ev_start, p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
-    if (e != cudaSuccess) return e;
-    if (a.ev_stop && (e = record_profile(a.ev_stop, st)) != cudaSuccess) return e;
-    return cudaSuccess;
+    p.stamps = a.stamps;
+    p.stamp_cap = a.stamp_cap;
+    return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p), st, true,
+                    p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
 }
 
 cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din, int dout, void* Y,

@@ -45,12 +45,16 @@ struct TcForwardArgs {
     int n_chunks;           // chunks of the loaded slots (entries of ws.chunks, in arena order)
     int tile_span;          // largest arena span of 8 consecutive chunks (first unit to last unit + 16)
     int units;              // rank units of the arena
-    cudaEvent_t ev_start;   // optional profiling events around the projection kernel
-    cudaEvent_t ev_stop;
+    int n_loaded;           // loaded slots
+    unsigned long long* stamps;   // profiling records of the kernels' CTAs (NULL = off)
+    int stamp_cap;
 };
 
-// Records a profiling event; inside stream capture it becomes an event-record node.
-cudaError_t record_profile(cudaEvent_t ev, cudaStream_t st);
+// Shrink on the CUDA cores for decode batches over many adapters with a few rows each
+// (shrink_gemv.cu): one CTA per chunk of the pool plus the segment builder's CTA.
+cudaError_t gemv_init();
+bool gemv_shrink_fits(const PoolDims& d, int T);
+cudaError_t launch_shrink_gemv(const TcForwardArgs& a, bool prefetch, cudaStream_t st);
 
 // Prefill-shaped projection (T > 256), tc_prefill.cu.
 cudaError_t prefill_init();

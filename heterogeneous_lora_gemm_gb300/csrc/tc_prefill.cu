@@ -44,6 +44,8 @@ struct PrefillParams {
     int n_chunks, max_chunks;
     int ext_steps;              // K-extension steps per tile (EXT_SUB chunks each), 0 without adapters
     int pdl;    // launched while the shrink may still run: wait before reading its outputs
+    unsigned long long* stamps;   // profiling records (NULL = off), see ptx::stamp_record
+    int stamp_cap;
 };
 
 __device__ __forceinline__ void tile_coords(int i, int m_tiles, int n_tiles, int& m, int& n) {
@@ -72,6 +74,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = p.m_tiles * p.n_tiles;
+    const unsigned long long t_start = (p.stamps && threadIdx.x == 0) ? gtimer() : 0ull;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < PSTAGES; ++s) {
@@ -265,6 +268,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
     }
+    if (threadIdx.x == 0) stamp_record(p.stamps, p.stamp_cap, t_start, STAMP_PREFILL);
 }
 
 }  // namespace
@@ -301,10 +305,12 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
     p.ext_steps = after_shrink ? (p.n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
     p.vec_store = (d.dout % 8 == 0) ? 1 : 0;
     p.pdl = after_shrink ? 1 : 0;
+    p.stamps = a.stamps;
+    p.stamp_cap = a.stamp_cap;
     const int total = p.m_tiles * p.n_tiles;
     const int grid = total < num_sms ? total : num_sms;
     const size_t smem = 1024 + (size_t)PSTAGES * PSTAGE + (2 * PSTAGES + 5) * 8 + PSTAGES * 4 + 16;
-    return launch_k(prefill_gemm_kernel, dim3(grid), dim3(P_THREADS), smem, st, after_shrink && !a.ev_start, 1, tmX,
+    return launch_k(prefill_gemm_kernel, dim3(grid), dim3(P_THREADS), smem, st, after_shrink, 1, tmX,
                     tmW, tmV, a.maps.up256, p);
 }
 

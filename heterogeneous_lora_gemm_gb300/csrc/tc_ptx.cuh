@@ -40,14 +40,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after WAIT_LIMIT cycles or when another role gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* status) {
+// Bounded wait: gives up after `limit` cycles (raising STATUS_TIMEOUT and the CTA's
+// abort flag) or when another role gave up.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                uint32_t* status, long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > WAIT_LIMIT) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(status, STATUS_TIMEOUT);
             return false;
@@ -55,6 +56,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
     return true;
 }
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status) {
+    return mbar_wait_limit(bar, parity, abort_flag, status, WAIT_LIMIT);
+}
+
+// Profiling stamps (off when `buf` is NULL): one record per CTA, written by one
+// thread as the CTA ends: {start, end} in globaltimer nanoseconds, the kernel kind
+// and the linear block index.  buf[0] counts the records; record i sits at
+// buf + 4 + 4 i; records past `cap` are counted but not written.
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void stamp_record(unsigned long long* buf, int cap, unsigned long long t0, int kind) {
+    if (!buf) return;
+    const unsigned long long i = atomicAdd(buf, 1ull);
+    if (i < (unsigned long long)cap) {
+        unsigned long long* r = buf + 4 + 4 * i;
+        r[0] = t0;
+        r[1] = gtimer();
+        r[2] = (unsigned long long)kind;
+        r[3] = blockIdx.x + (unsigned long long)gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z);
+    }
+}
+enum : int { STAMP_SHRINK = 0, STAMP_PROJECTION = 1, STAMP_PREFILL = 2 };
 
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
     asm volatile(

@@ -73,8 +73,11 @@ _SIGNATURES = {
     "mlora_pool_status": (_I, [_P, _P]),
     "mlora_pool_info": (_I, [_P, ctypes.POINTER(PoolInfo)]),
     "mlora_debug_segments": (_I, [_P, _P, _I, _P, _P, _P]),
-    "mlora_profile_events": (_I, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I]),
+    "mlora_debug_last_segments": (_I, [_P, _I, _P, _P, _P]),
+    "mlora_profile_stamps": (_I, [_P, _P, _I]),
     "mlora_project_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P]),
+    "mlora_project_noalloc_status": (_I, [_P]),
+    "mlora_debug_noalloc_expire_wait": (_I, [ctypes.c_longlong, _P]),
     "mlora_arena_new": (_P, [_I]),
     "mlora_arena_delete": (None, [_P]),
     "mlora_arena_alloc": (_I, [_P, _I, _I]),
@@ -201,17 +204,32 @@ def mlora_debug_segments(pool: int, row_adapter_ptr: Optional[int], T: int, perm
           "mlora_debug_segments")
 
 
-def mlora_profile_events(pool: int, starts, stops) -> None:
-    """starts/stops: sequences of cudaEvent_t handles (ints); empty turns recording off."""
-    n = len(starts)
-    a = (_P * max(n, 1))(*[int(x) for x in starts])
-    b = (_P * max(n, 1))(*[int(x) for x in stops])
-    check(lib().mlora_profile_events(pool, a, b, n), "mlora_profile_events")
+def mlora_debug_last_segments(pool: int, T: int, perm_ptr: int, offsets_ptr: int, stream: int) -> None:
+    check(lib().mlora_debug_last_segments(pool, T, perm_ptr or None, offsets_ptr, stream or None),
+          "mlora_debug_last_segments")
+
+
+def mlora_profile_stamps(pool: int, records_ptr: int, cap: int) -> None:
+    """records_ptr: device buffer of 4 + 4 cap uint64 words (0 / cap 0 turns recording off)."""
+    check(lib().mlora_profile_stamps(pool, records_ptr or None, cap), "mlora_profile_stamps")
 
 
 def mlora_project_noalloc(X_ptr: int, W_ptr: int, T: int, din: int, dout: int, Y_ptr: int, stream: int) -> None:
     """Y = X W^T (bf16, T <= 256) without any device allocation; see include/mlora.h."""
     check(lib().mlora_project_noalloc(X_ptr, W_ptr, T, din, dout, Y_ptr, stream or None), "mlora_project_noalloc")
+
+
+def mlora_project_noalloc_status(stream: int) -> int:
+    """Reads and clears the allocation-free calls' status word: MLORA_OK or
+    MLORA_ERR_DEVICE_TIMEOUT; raises on other errors."""
+    s = int(lib().mlora_project_noalloc_status(stream or None))
+    if s not in (MLORA_OK, MLORA_ERR_DEVICE_TIMEOUT):
+        check(s, "mlora_project_noalloc_status")
+    return s
+
+
+def mlora_debug_noalloc_expire_wait(cycles: int, stream: int) -> None:
+    check(lib().mlora_debug_noalloc_expire_wait(int(cycles), stream or None), "mlora_debug_noalloc_expire_wait")
 
 
 # ---- torch-facing convenience ------------------------------------------- #
@@ -305,9 +323,14 @@ class Pool:
     def info(self) -> PoolInfo:
         return mlora_pool_info(self.handle)
 
-    def profile_events(self, starts, stops) -> None:
-        """torch.cuda.Event objects (created with enable_timing=True); [] turns recording off."""
-        mlora_profile_events(self.handle, [e.cuda_event for e in starts], [e.cuda_event for e in stops])
+    def profile_stamps(self, records, cap: int) -> None:
+        """records: a device torch tensor of >= 4 + 4 cap int64/uint64 words; cap 0 turns recording off."""
+        mlora_profile_stamps(self.handle, records.data_ptr() if cap > 0 else 0, cap)
+
+    def last_segments(self, perm, offsets, stream=None) -> None:
+        """The segments the last forward with a row map built (perm [T], offsets [max_slots + 1], device int32)."""
+        mlora_debug_last_segments(self.handle, int(perm.shape[0]), perm.data_ptr(), offsets.data_ptr(),
+                                  _stream_handle(stream))
 
     def segments(self, row_adapter, perm, offsets, stream=None) -> None:
         ra = None if row_adapter is None else row_adapter.data_ptr()

@@ -286,14 +286,38 @@ mlora_status mlora_debug_segments(mlora_pool_t pool, const int32_t* row_adapter,
                                   int32_t* perm, int32_t* offsets, mlora_stream_t stream);
 
 /*
- * Profiling hook for timing the projection kernel with CUDA events (no work is
- * skipped or changed).  With n > 0, the k-th later forward call of this pool
- * records starts[k % n] and stops[k % n] (cudaEvent_t handles owned by the
- * caller) on its stream immediately before and after launching its base +
- * expand projection kernel; inside stream capture they become event-record
- * nodes of the graph.  n == 0 turns recording off.  Errors: INVALID_ARG.
+ * Reads back the segments (M031 §03: rows grouped by adapter, original order kept
+ * inside a group, groups in ascending slot id) that the most recent mlora_forward
+ * of this pool built with its row map -- on the bf16 path, the builder that runs
+ * inside the shrink kernel; otherwise the standalone segment kernel -- into the
+ * caller's device buffers, on `stream` (order it after that forward):
+ *   T        the rows of that forward (INVALID_ARG if it had another T, if no forward
+ *            with a row map ran since the pool was made, or if mlora_debug_segments
+ *            ran after it)
+ *   perm     device int32 [T], layout as in mlora_debug_segments
+ *   offsets  device int32 [max_slots + 1]
+ * Errors: INVALID_ARG, CUDA.
  */
-mlora_status mlora_profile_events(mlora_pool_t pool, void* const* starts, void* const* stops, int n);
+mlora_status mlora_debug_last_segments(mlora_pool_t pool, int T, int32_t* perm, int32_t* offsets,
+                                       mlora_stream_t stream);
+
+/*
+ * Profiling records of the tensor-core kernels' thread blocks, for measuring kernel
+ * durations inside a timed run (no work is skipped or changed; each block adds one
+ * atomic add and one 32-byte store as it ends).  With cap > 0, every CTA of the
+ * shrink and projection kernels launched by later forwards of this pool (captured
+ * forwards included: the buffer is baked into the launch) appends one record to
+ * `records`, a caller-owned device buffer of 8-byte words, 8-byte aligned, of
+ * 4 + 4 cap words:
+ *   records[0]            number of records appended so far (the caller zeroes it)
+ *   records[4+4i .. 7+4i] record i: start and end of the block in the device's
+ *                         %globaltimer nanoseconds, the kernel kind (0 shrink,
+ *                         1 decode projection, 2 prefill projection) and the block's
+ *                         linear index
+ * Records past `cap` are counted but not stored.  cap == 0 turns recording off.
+ * Errors: INVALID_ARG.
+ */
+mlora_status mlora_profile_stamps(mlora_pool_t pool, void* records, int cap);
 
 /*
  * Base projection Y = X W^T for a decode-sized batch that allocates nothing.
@@ -320,11 +344,33 @@ mlora_status mlora_profile_events(mlora_pool_t pool, void* const* starts, void* 
  * that first call outside any stream capture.  All calls share the one array
  * (it keeps what the last call left; the counters are cleared on every call), so
  * calls whose work overlaps on the GPU -- on different streams, or from several
- * host threads -- race and must be ordered by the caller.
+ * host threads -- race and must be ordered by the caller.  A pipeline wait of
+ * the kernel that gives up after its bounded limit leaves that call's Y invalid
+ * and sets a bit in the array's status word, which stays set until
+ * mlora_project_noalloc_status reads it.
  * Errors: INVALID_ARG (NULL or misaligned pointer), UNSUPPORTED, CUDA.
  */
 mlora_status mlora_project_noalloc(const void* X, const void* W, int T, int din, int dout, void* Y,
                                    mlora_stream_t stream);
+
+/*
+ * Status of the allocation-free calls made on the current device since the last
+ * read: synchronizes `stream`, then reads and clears the status word of the fixed
+ * scratch array (no allocation).  Returns MLORA_OK, MLORA_ERR_DEVICE_TIMEOUT (a
+ * pipeline wait in one of those calls gave up after its bounded limit; that call's
+ * Y is not valid) or MLORA_ERR_CUDA.  Like the calls it reports on, its first use
+ * on a device sets up the array's address; make it outside any stream capture.
+ */
+mlora_status mlora_project_noalloc_status(mlora_stream_t stream);
+
+/*
+ * Test hook for the status above: enqueues on `stream` one kernel whose single
+ * pipeline wait has nothing to wait for and gives up after `cycles` SM clock
+ * cycles (1 .. 2^31), with the same bounded wait the projection kernels use, so
+ * that mlora_project_noalloc_status then reports MLORA_ERR_DEVICE_TIMEOUT.
+ * Nothing faults or hangs.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+mlora_status mlora_debug_noalloc_expire_wait(long long cycles, mlora_stream_t stream);
 
 /*
  * Host-only view of the arena allocator the pool uses (no CUDA calls), for tests

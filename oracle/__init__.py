@@ -168,19 +168,22 @@ def merge(W: np.ndarray, adapter: OracleAdapter) -> np.ndarray:
     return out
 
 
-def forward_modules(X: np.ndarray, W: np.ndarray, row_adapter: np.ndarray, modules, tenants) -> np.ndarray:
+def forward_modules(X: np.ndarray, W: np.ndarray, row_adapter: np.ndarray, modules, tenants,
+                    rows: Optional[np.ndarray] = None) -> np.ndarray:
     """Fused projection of several modules (airsota card "multi-LoRA serving vs
     merging", section 四 item ④): W stacks the modules' weights by rows, module m
     owning output rows modules[m] = (row_offset, rows); tenants[s][m] is slot s's
     adapter of module m (or None).  By definition, the rows of module m are the
     single-module layer over W's rows of m with each slot's module-m adapter; rows
-    outside every module are the base product."""
+    outside every module are the base product.  ``rows`` selects output rows of the
+    batch (all by default), in the given order."""
     X = np.asarray(X, np.float64)
     W = np.asarray(W, np.float64)
-    Y = X @ W.T
+    sel = np.arange(X.shape[0]) if rows is None else np.asarray(rows, np.int64)
+    Y = X[sel] @ W.T
     for m, (off, n) in enumerate(modules):
         ads = [None if t is None else t[m] for t in tenants]
-        Y[:, off:off + n] = forward(X, W[off:off + n], row_adapter, ads)
+        Y[:, off:off + n] = forward(X, W[off:off + n], row_adapter, ads, rows=rows)
     return Y
 
 

@@ -5,43 +5,10 @@ forward itself is one ``mlora_forward`` call into libmlora.so.
 """
 from __future__ import annotations
 
-from typing import Optional
-
 import numpy as np
 
 import workloads as wl
-
-
-def to_device(payload: np.ndarray, dtype: str, device="cuda"):
-    import torch
-    if dtype == "bf16":
-        t = torch.from_numpy(np.ascontiguousarray(payload).view(np.int16)).view(torch.bfloat16)
-    else:
-        t = torch.from_numpy(np.ascontiguousarray(payload, np.float32))
-    return t.to(device)
-
-
-def to_f64(t) -> np.ndarray:
-    import torch
-    return t.detach().to("cpu", torch.float64).numpy()
-
-
-def make_pool(layer: wl.LayerData, max_tokens: Optional[int] = None, rank_budget: Optional[int] = None,
-              max_rank: Optional[int] = None, host_sources: bool = False):
-    from heterogeneous_lora_gemm_gb300 import Pool
-    budget = sum((a.rank + 7) // 8 * 8 for a in layer.adapters) if rank_budget is None else rank_budget
-    pool = Pool(layer.max_slots, budget, max_rank or layer.max_rank, layer.din, layer.dout, layer.dtype,
-                max_tokens or max(layer.T, 1))
-    for a in layer.adapters:
-        if host_sources:
-            import torch
-            down = to_device(a.down, layer.dtype, "cpu")
-            up = to_device(a.up, layer.dtype, "cpu")
-        else:
-            down = to_device(a.down, layer.dtype)
-            up = to_device(a.up, layer.dtype)
-        pool.load(a.slot, down, up, a.scale)
-    return pool
+from heterogeneous_lora_gemm_gb300.torch_io import make_pool, to_device, to_f64  # noqa: F401
 
 
 def upload(layer: wl.LayerData):

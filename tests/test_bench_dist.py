@@ -63,13 +63,45 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     assert capsys.readouterr().out == ""
 
 
-def test_layer_work_counts_touched_adapters_once():
+def test_call_work_counts_touched_adapters_once():
     sys.path.insert(0, ROOT)
     import bench
     import workloads as wl
     L = wl.decode_step(0)
-    w = bench.layer_work(L)
+    w = bench.call_work(L.din, L.dout, L.T, L.row_adapter, bench.layer_ranks(L))
     e = 2
     assert w["touched"] == 3 and w["r_touched"] == 48
     assert w["step_bytes"] == (4096 * 4096 + 32 * 4096 * 2 + 48 * 8192) * e + 4 * 32
+    assert w["proj_bytes"] == (4096 * 4096 + 32 * 4096 * 2 + 48 * 4096) * e
     assert w["step_flops"] == 2 * 32 * 4096 * 4096 + 2 * 32 * 16 * 8192
+
+
+def test_call_work_of_the_fused_qkv_group():
+    """q|k|v of a 7B-shaped layer: 100 tenants, each with a rank-16 q and a rank-16 v
+    adapter whose Up reaches 4096 rows; every tenant is used."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as wl
+    G = wl.stack7b_group(0, 0, 0)
+    ranks = [[(a.rank, n) for (_, n), a in zip(G.modules, row) if a is not None] for row in G.tenants]
+    w = bench.call_work(G.din, G.dout, G.T, G.row_adapter, ranks)
+    e = 2
+    assert w["touched"] == 100 and w["r_touched"] == 3200
+    adapters = 100 * 2 * 16 * (4096 + 4096) * e
+    assert w["step_bytes"] == (12288 * 4096 + 128 * 4096 + 128 * 12288) * e + adapters + 4 * 128
+    assert w["proj_bytes"] == (12288 * 4096 + 128 * 4096 + 128 * 12288) * e + 100 * 2 * 16 * 4096 * e
+    assert w["step_flops"] == 2 * 128 * 4096 * 12288 + 128 * 2 * 2 * 16 * (4096 + 4096)
+
+
+def test_busy_union_of_block_records():
+    """The kernel's busy time is the measure of the union of its blocks' intervals:
+    overlapping blocks count once, gaps not at all, other kinds are ignored."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    rec = np.array([[100, 200, 1, 0], [150, 260, 1, 1], [300, 350, 1, 2], [310, 320, 1, 3],
+                    [0, 1000, 0, 0], [400, 400, 1, 4]], np.int64)
+    assert abs(bench.busy_union(rec, 1) - 210e-9) < 1e-15
+    assert abs(bench.busy_union(rec, 0) - 1000e-9) < 1e-15
+    assert bench.busy_union(rec, 2) == 0.0

@@ -49,19 +49,39 @@ def check_segments(layer, pool, row_adapter=None):
     assert np.all(perm[n:] == -1)
 
 
+def check_forward_segments(layer, pool, row_adapter=None):
+    """The segments the forward's own builder produced (on the bf16 path, the builder
+    inside the shrink kernel) equal the oracle's, bit for bit."""
+    ra = layer.row_adapter if row_adapter is None else row_adapter
+    T = ra.shape[0]
+    perm = torch.full((max(T, 1),), -7, dtype=torch.int32, device="cuda")
+    offs = torch.full((layer.max_slots + 1,), -7, dtype=torch.int32, device="cuda")
+    pool.last_segments(perm[:T], offs)
+    torch.cuda.synchronize()
+    perm, offs = perm[:T].cpu().numpy(), offs.cpu().numpy()
+    counts, w_offs, w_perm, _ = oracle.segments(ra, oracle.slot_ranks(ora_adapters(layer)), layer.max_slots)
+    assert np.array_equal(offs, w_offs), (offs, w_offs)
+    n = w_perm.size
+    assert np.array_equal(perm[:n], w_perm)
+    assert np.all(perm[n:] == -1)
+
+
 # --------------------------------------------------------------------------- #
 def test_worked_example_fp32():
     layer = wl.worked_example(0)
-    Y = run_layer(layer)
-    assert_within(Y, want_of(layer), "f32", "worked example")
     pool = make_pool(layer)
+    Y = run_layer(layer, pool)
+    assert_within(Y, want_of(layer), "f32", "worked example")
+    check_forward_segments(layer, pool)
     check_segments(layer, pool)
 
 
 @pytest.mark.parametrize("seed", [0, 1])
 def test_decode_step(seed):
     layer = wl.decode_step(seed)
-    assert_within(run_layer(layer), want_of(layer), "bf16", "decode_step")
+    pool = make_pool(layer)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", "decode_step")
+    check_forward_segments(layer, pool)
 
 
 def test_fragmented_decode():
@@ -69,6 +89,7 @@ def test_fragmented_decode():
     pool = make_pool(layer)
     check_segments(layer, pool)
     assert_within(run_layer(layer, pool), want_of(layer), "bf16", "fragmented_decode")
+    check_forward_segments(layer, pool)
 
 
 def prefill_sample_rows(seed):
@@ -86,6 +107,7 @@ def test_prefill_sampled_rows():
     pool = make_pool(layer)
     check_segments(layer, pool)
     Y = run_layer(layer, pool)
+    check_forward_segments(layer, pool)
     rows = prefill_sample_rows(0)
     assert_within(Y[rows], want_of(layer, rows=rows), "bf16", "prefill")
     assert np.isfinite(Y).all()
@@ -127,6 +149,25 @@ def test_many_loaded_slots_few_used():
     pool = make_pool(layer)
     check_segments(layer, pool)
     assert_within(run_layer(layer, pool), want_of(layer), "bf16", "300 slots, 3 used")
+    check_forward_segments(layer, pool)
+
+
+@pytest.mark.parametrize("T,din,n_slots", [(200, 1000, 120), (100, 1000, 120), (128, 11008, 90)])
+def test_many_adapters_few_rows_each(T, din, n_slots):
+    """Decode batches with at most two rows per loaded adapter on average take the
+    CUDA-core shrink: ranks that are not multiples of 16 (partial chunks), one slot
+    with more rows than one pass over its Down rows holds, rows without adapter,
+    din not a multiple of 256 (and 11008, two rows per pass), with and without the
+    L2 prefetch before the wait (T >= loaded slots or not)."""
+    rng = np.random.default_rng(T + din)
+    ranks = list(rng.choice(np.array([5, 16, 24, 8]), size=n_slots))
+    ra = rng.integers(0, n_slots, size=T).astype(np.int32)
+    ra[: 20] = 3                                  # slot 3: 20 rows (three passes of 8)
+    ra[rng.random(T) < 0.1] = -1
+    layer = wl.random_layer(T, T=T, din=din, dout=384, ranks=ranks, row_adapter=ra)
+    pool = make_pool(layer)
+    assert_within(run_layer(layer, pool), want_of(layer), "bf16", f"many adapters, T = {T}, din = {din}")
+    check_forward_segments(layer, pool)
 
 
 def test_chained_forwards_read_the_previous_output():
@@ -135,7 +176,7 @@ def test_chained_forwards_read_the_previous_output():
     still run, and must read X only once it is written.  The kernels are
     deterministic (fixed split order), so the chain must equal, bit for bit, the same
     chain with a device synchronisation after every forward."""
-    for shape in ((1024, [16, 8]), (4096, [16, 16, 16])):
+    for shape in ((1024, [16, 8]), (4096, [16, 16, 16]), (1024, [16, 8, 24] * 7)):   # the last: CUDA-core shrink
         chain_case(*shape)
 
 
@@ -215,7 +256,10 @@ def test_invalid_ids_set_status_and_act_as_none():
     assert_within(Y, want_of(layer), "bf16", "invalid ids")
     base = layer.X_f64 @ layer.W_f64.T
     assert_within(Y[[1, 2, 3, 6, 7]], base[[1, 2, 3, 6, 7]], "bf16", "invalid rows keep base")
+    check_forward_segments(layer, pool)
     check_segments(layer, pool)
+    with pytest.raises(mlora.MloraError):   # the standalone builder replaced the forward's segments
+        check_forward_segments(layer, pool)
 
 
 def test_zero_rows_is_noop():

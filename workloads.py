@@ -23,7 +23,10 @@ Workloads (the pages publish no dataset; all inputs are synthetic):
 * ``stack7b``          -- a 7B-shaped decode stack: 32 layers of q, k, v, o
   (4096 -> 4096), gate, up (4096 -> 11008), down (11008 -> 4096); 100 resident
   rank-16 adapters on q and v only (M031 §06 sizes: 0.25 MiB per projection,
-  16 MiB per adapter); 128 rows.
+  16 MiB per adapter); 128 rows.  As in a transformer layer, q, k and v read one
+  input (the attention input) and gate and up another (the MLP input), so a layer
+  runs as four projections: fused q|k|v (4096 -> 12288, the q and v adapters of a
+  tenant in one slot), o, fused gate|up (4096 -> 22016) and down.
 
 Value distributions for the bf16 workloads: W ~ N(0, 0.02^2), X ~ N(0, 1),
 Down ~ N(0, 1/din) (variance 1/din, so that Down @ x has unit scale),
@@ -43,6 +46,9 @@ STACK7B_MODULES = (("q", 4096, 4096, True), ("k", 4096, 4096, False), ("v", 4096
 STACK7B_LAYERS = 32
 STACK7B_ADAPTERS = 100
 STACK7B_T = 128
+# the projections of a layer that share an input, in order: (group, din, modules)
+STACK7B_GROUPS = (("qkv", 4096, ("q", "k", "v")), ("o", 4096, ("o",)), ("gate_up", 4096, ("gate", "up")),
+                  ("down", 11008, ("down",)))
 
 
 # --------------------------------------------------------------------------- #
@@ -231,15 +237,70 @@ def stack7b_row_adapter(seed: int) -> np.ndarray:
     return pi[np.arange(STACK7B_T) % STACK7B_ADAPTERS]
 
 
+def stack7b_group_of(module: str) -> int:
+    return [i for i, g in enumerate(STACK7B_GROUPS) if module in g[2]][0]
+
+
+def stack7b_input(seed: int, layer: int, group: int) -> np.ndarray:
+    """The input rows [T x din] that the projections of one group of a layer share (bf16 payload)."""
+    din = STACK7B_GROUPS[group][1]
+    return _store(_normal(_rng(seed, 4, layer, 100 + group), (STACK7B_T, din), 1.0), "bf16")
+
+
 def stack7b_projection(seed: int, layer: int, module: str) -> LayerData:
     """One projection of the 7B-shaped stack; q and v carry the 100 rank-16 adapters."""
     idx = [m[0] for m in STACK7B_MODULES].index(module)
     _, din, dout, adapted = STACK7B_MODULES[idx]
     ra = stack7b_row_adapter(seed) if adapted else np.full(STACK7B_T, -1, np.int32)
     ranks = [16] * STACK7B_ADAPTERS if adapted else []
-    return make_layer(f"stack7b.L{layer}.{module}", seed, (4, layer, idx), T=STACK7B_T, din=din,
-                      dout=dout, ranks=ranks, scales=[2.0] * len(ranks), row_adapter=ra,
-                      max_slots=STACK7B_ADAPTERS if adapted else 0)
+    L = make_layer(f"stack7b.L{layer}.{module}", seed, (4, layer, idx), T=STACK7B_T, din=din,
+                   dout=dout, ranks=ranks, scales=[2.0] * len(ranks), row_adapter=ra,
+                   max_slots=STACK7B_ADAPTERS if adapted else 0)
+    L.X = stack7b_input(seed, layer, stack7b_group_of(module))
+    return L
+
+
+@dataclass
+class FusedLayerData:
+    """Several projections that read one input, run as one projection over their weights
+    stacked by rows: module m owns output rows [row_offset[m], row_offset[m] + rows[m]).
+    ``tenants[s][m]`` is slot s's adapter of module m (None: not adapted)."""
+    name: str
+    din: int
+    X: np.ndarray                       # payload [T x din]
+    W: np.ndarray                       # payload [sum(rows) x din]
+    row_adapter: np.ndarray
+    modules: List[tuple]                # (row_offset, rows) per module
+    tenants: List[List[Optional[AdapterData]]]
+    dtype: str = "bf16"
+
+    @property
+    def T(self) -> int:
+        return int(self.X.shape[0])
+
+    @property
+    def dout(self) -> int:
+        return int(self.W.shape[0])
+
+    @property
+    def max_slots(self) -> int:
+        return len(self.tenants)
+
+
+def stack7b_group(seed: int, layer: int, group: int) -> FusedLayerData:
+    """One input group of a 7B-shaped layer as a fused projection (q|k|v, o, gate|up or down)."""
+    name, din, mods = STACK7B_GROUPS[group]
+    parts = [stack7b_projection(seed, layer, m) for m in mods]
+    offsets = np.concatenate([[0], np.cumsum([P.dout for P in parts])[:-1]]).astype(int)
+    adapted = any(P.max_slots > 0 for P in parts)
+    n_slots = STACK7B_ADAPTERS if adapted else 0
+    tenants = []
+    for s_ in range(n_slots):
+        tenants.append([P.slot_list()[s_] if P.max_slots > 0 else None for P in parts])
+    ra = stack7b_row_adapter(seed) if adapted else np.full(STACK7B_T, -1, np.int32)
+    return FusedLayerData(name=f"stack7b.L{layer}.{name}", din=din, X=parts[0].X,
+                          W=np.ascontiguousarray(np.concatenate([P.W for P in parts], 0)), row_adapter=ra,
+                          modules=[(int(o), P.dout) for o, P in zip(offsets, parts)], tenants=tenants)
 
 
 def by_name(name: str, seed: int = 0) -> LayerData:
@@ -273,3 +334,56 @@ def oracle_adapters(layer: LayerData):
     for a in layer.slot_list():
         out.append(None if a is None else (a.down_f64, a.up_f64, a.scale))
     return out
+
+
+# --------------------------------------------------------------------------- #
+# device draws for the full 7B-shaped stack (about 13 GB of weights): the same
+# recipe and distributions as stack7b_group, drawn by torch's counter-based
+# generator on the device instead of numpy on the host (which would take minutes);
+# the values differ from the host draws, the shapes and distributions do not.
+def _device_gen(device, seed: int, *key: int):
+    import torch
+    h = int(np.random.SeedSequence(entropy=int(seed), spawn_key=tuple(int(k) for k in key)).generate_state(1)[0])
+    g = torch.Generator(device=device)
+    g.manual_seed(h)
+    return g
+
+
+def _device_normal(device, shape, std: float, seed: int, *key: int):
+    import torch
+    g = _device_gen(device, seed, *key)
+    return (torch.randn(shape, device=device, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def stack7b_group_device(seed: int, layer: int, group: int, device):
+    """Device tensors of one input group of a 7B-shaped layer: X [T x din], the stacked
+    W, module row ranges, and per slot the (down, up, scale) of each adapted module."""
+    name, din, mods = STACK7B_GROUPS[group]
+    X = _device_normal(device, (STACK7B_T, din), 1.0, seed, 5, layer, group, 0)
+    Ws, modules, tenants_mods, off = [], [], [], 0
+    for m in mods:
+        idx = [x[0] for x in STACK7B_MODULES].index(m)
+        _, _, dout, adapted = STACK7B_MODULES[idx]
+        Ws.append(_device_normal(device, (dout, din), 0.02, seed, 5, layer, group, 1, idx))
+        modules.append((off, dout))
+        off += dout
+        tenants_mods.append(adapted)
+    import torch
+    W = torch.cat(Ws, 0) if len(Ws) > 1 else Ws[0]
+    del Ws
+    tenants = []
+    if any(tenants_mods):
+        for s_ in range(STACK7B_ADAPTERS):
+            row = []
+            for mi, adapted in enumerate(tenants_mods):
+                if not adapted:
+                    row.append(None)
+                    continue
+                rows = modules[mi][1]
+                down = _device_normal(device, (16, din), 1.0 / np.sqrt(din), seed, 5, layer, group, 2, mi, s_)
+                up = _device_normal(device, (rows, 16), 0.02, seed, 5, layer, group, 3, mi, s_)
+                row.append((down, up, 2.0))
+            tenants.append(row)
+    ra = stack7b_row_adapter(seed) if tenants else np.full(STACK7B_T, -1, np.int32)
+    return {"name": f"stack7b.L{layer}.{name}", "X": X, "W": W, "modules": modules, "tenants": tenants,
+            "row_adapter": ra, "din": din, "dout": off}
