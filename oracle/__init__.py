@@ -210,6 +210,67 @@ def merge_quantized(codes: np.ndarray, row_scale: np.ndarray, adapter: OracleAda
     return quantize(merge(dequantize(codes, row_scale), adapter))
 
 
+NF4_BLOCK = 64   # input columns that share one absmax scale
+
+
+def nf4_unpack(packed: np.ndarray) -> np.ndarray:
+    """4-bit codes [dout x din] from bytes [dout x din/2]: column 2m is the low nibble of
+    byte m, column 2m + 1 the high nibble."""
+    packed = np.asarray(packed, np.uint8)
+    codes = np.empty((packed.shape[0], 2 * packed.shape[1]), np.uint8)
+    codes[:, 0::2] = packed & 15
+    codes[:, 1::2] = packed >> 4
+    return codes
+
+
+def nf4_pack(codes: np.ndarray) -> np.ndarray:
+    codes = np.asarray(codes, np.uint8)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+
+
+def nf4_dequantize(packed: np.ndarray, absmax: np.ndarray, codebook: np.ndarray) -> np.ndarray:
+    """The logical matrix of an NF4 base (M031 §05: W restored by scale and codebook):
+    W[o, i] = codebook[code[o, i]] * absmax[i // 64, o], in fp64."""
+    codes = nf4_unpack(packed)
+    cb = np.asarray(codebook, np.float32).astype(np.float64)
+    scale = np.repeat(np.asarray(absmax, np.float32).astype(np.float64).T, NF4_BLOCK, axis=1)
+    return cb[codes] * scale
+
+
+def nf4_quantize(W: np.ndarray, codebook: np.ndarray):
+    """NF4 quantization, decided in fp32 (the precision the kernel decides in): per row
+    and block of 64 columns, absmax = max |w|; each w / absmax (fp32 division) takes the
+    code of the nearest codebook value (fp32 distances, ties to the lower code); an
+    all-zero block gets absmax 0 and the code of the value nearest 0.  Returns packed
+    codes [dout x din/2] and absmax [din/64 x dout]."""
+    w = np.asarray(W, np.float64).astype(np.float32)
+    dout, din = w.shape
+    blocks = w.reshape(dout, din // NF4_BLOCK, NF4_BLOCK)
+    absmax = np.abs(blocks).max(axis=2).astype(np.float32)                    # [dout, nb]
+    safe = np.where(absmax > 0, absmax, np.float32(1))
+    v = np.where(absmax[:, :, None] > 0, blocks / safe[:, :, None], np.float32(0)).astype(np.float32)
+    cb = np.asarray(codebook, np.float32)
+    dist = np.abs(v[..., None] - cb).astype(np.float32)                        # fp32 distances
+    codes = np.argmin(dist, axis=-1).astype(np.uint8).reshape(dout, din)       # first minimum wins
+    return nf4_pack(codes), np.ascontiguousarray(absmax.T)
+
+
+def nf4_restore_f32(packed: np.ndarray, absmax: np.ndarray, codebook: np.ndarray) -> np.ndarray:
+    """The restored values as fp32 products codebook[code] * absmax (the merge's input)."""
+    codes = nf4_unpack(packed)
+    cb = np.asarray(codebook, np.float32)
+    scale = np.repeat(np.asarray(absmax, np.float32).T, NF4_BLOCK, axis=1)
+    return (cb[codes] * scale).astype(np.float32)
+
+
+def nf4_merge(packed: np.ndarray, absmax: np.ndarray, codebook: np.ndarray, adapter: OracleAdapter):
+    """The merge on an NF4 base (M031 §05): restore W, add scale * Up Down, quantize the
+    merged matrix again -- never the update added to the codes.  The merged value is
+    the fp64 sum of the fp32 restored value and the update, rounded to fp32."""
+    merged = merge(nf4_restore_f32(packed, absmax, codebook).astype(np.float64), adapter)
+    return nf4_quantize(merged.astype(np.float32), codebook)
+
+
 def unmerge(W: np.ndarray, adapter: OracleAdapter) -> np.ndarray:
     """W - scale * Up @ Down in fp64: the un-merge that switches a merged weight back
     (airsota card "multi-LoRA serving vs merging", section 四 item ③)."""

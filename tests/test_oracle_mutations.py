@@ -107,6 +107,17 @@ PY_MUTANTS = {
     "quantized merge adds to the codes": ("merge_quantized", "quantize(merge(dequantize(codes, row_scale), adapter))",
                                           "(np.clip(codes + np.rint(adapter.scale * adapter.up @ adapter.down), "
                                           "-127, 127).astype(np.int8), row_scale)"),
+    "nf4 nibbles swapped": ("nf4_unpack", "codes[:, 0::2] = packed & 15\n    codes[:, 1::2] = packed >> 4",
+                            "codes[:, 0::2] = packed >> 4\n    codes[:, 1::2] = packed & 15"),
+    "nf4 restore ignores the block scale": ("nf4_dequantize", "return cb[codes] * scale",
+                                            "return cb[codes] * np.ones_like(scale)"),
+    "nf4 ties to the upper code": ("nf4_quantize", "np.argmin(dist, axis=-1)",
+                                   "(15 - np.argmin(dist[..., ::-1], axis=-1))"),
+    "nf4 absmax without the magnitude": ("nf4_quantize", "absmax = np.abs(blocks).max(axis=2)",
+                                         "absmax = blocks.max(axis=2)"),
+    "nf4 merge adds to the codes": ("nf4_merge", "return nf4_quantize(merged.astype(np.float32), codebook)",
+                                    "return nf4_pack(np.clip(nf4_unpack(packed) + np.rint(adapter.scale * adapter.up "
+                                    "@ adapter.down), 0, 15).astype(np.uint8)), absmax"),
 }
 
 PY_PIN_TESTS = [
@@ -114,6 +125,11 @@ PY_PIN_TESTS = [
     pins.test_quantize_sends_exact_ties_to_the_even_code,
     pins.test_quantization_error_is_at_most_half_a_step,
     pins.test_merge_on_a_quantized_base_three_ways,
+    pins.test_nf4_packing_puts_even_columns_in_the_low_nibble,
+    pins.test_nf4_quantize_recovers_an_exact_grid,
+    pins.test_nf4_ties_go_to_the_lower_code,
+    pins.test_nf4_error_is_at_most_half_the_widest_gap,
+    pins.test_nf4_merge_three_ways,
 ]
 
 

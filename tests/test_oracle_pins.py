@@ -279,6 +279,102 @@ def test_merge_on_a_quantized_base_three_ways():
 
 # --------------------------------------------------------------------------- #
 # invariants and closed forms
+# --------------------------------------------------------------------------- #
+# NF4 base (M031 §05: W restored "by scale/codebook"; the NF4 codebook)
+def test_nf4_codebook_is_the_normal_float_definition():
+    """16 ascending values with an exact 0 and ends -1 and 1; under the normal CDF the
+    positive values (times the top quantile) sit at evenly spaced probabilities between
+    1/2 and 1 - delta, 8 steps, and the negative ones at 7 such steps (the NormalFloat
+    construction the pages' source defines)."""
+    from scipy.stats import norm
+    cb = wl.nf4_codebook().astype(np.float64)
+    assert cb.shape == (16,) and np.all(np.diff(cb) > 0)
+    assert cb[0] == -1.0 and cb[15] == 1.0 and cb[7] == 0.0
+    p_max = 1.0 - 0.5 * (1.0 / 32 + 1.0 / 30)
+    top = norm.ppf(p_max)
+    pos = norm.cdf(cb[8:] * top)
+    neg = norm.cdf(-cb[:7][::-1] * top)
+    np.testing.assert_allclose(np.diff(np.concatenate([[0.5], pos])), (p_max - 0.5) / 8, rtol=1e-5)
+    np.testing.assert_allclose(np.diff(np.concatenate([[0.5], neg])), (p_max - 0.5) / 7, rtol=1e-5)
+
+
+def test_nf4_packing_puts_even_columns_in_the_low_nibble():
+    codes = np.array([[1, 2, 15, 0, 7, 9]], np.uint8)
+    packed = oracle.nf4_pack(codes)
+    np.testing.assert_array_equal(packed, [[0x21, 0x0F, 0x97]])
+    np.testing.assert_array_equal(oracle.nf4_unpack(packed), codes)
+
+
+def test_nf4_quantize_recovers_an_exact_grid():
+    """Codebook values times power-of-two block scales, with a +-1 entry in every block
+    (so that the block's absmax is its scale), quantize back to the same codes and
+    scales; restoring gives the weights exactly.  An all-zero block gets absmax 0 and
+    the code of 0."""
+    cb = wl.nf4_codebook()
+    rng = np.random.default_rng(31)
+    codes = rng.integers(0, 16, size=(5, 192)).astype(np.uint8)
+    codes[:, ::64] = rng.choice([0, 15], size=(5, 3))
+    scale = (2.0 ** rng.integers(-9, -3, size=(3, 5))).astype(np.float32)
+    codes[4, 64:128] = 7
+    scale[1, 4] = 0.0
+    W = oracle.nf4_dequantize(oracle.nf4_pack(codes), scale, cb)
+    pk, am = oracle.nf4_quantize(W, cb)
+    np.testing.assert_array_equal(oracle.nf4_unpack(pk), codes)
+    np.testing.assert_array_equal(am, scale)
+    np.testing.assert_array_equal(oracle.nf4_dequantize(pk, am, cb), W)
+    assert np.all(W[4, 64:128] == 0.0)
+
+
+def test_nf4_ties_go_to_the_lower_code():
+    """A value exactly halfway between two codebook entries takes the lower code; the
+    next fp32 value above it, the upper one (a synthetic codebook of eighths, where the
+    halfway points and the distances are exact in fp32)."""
+    cb = (np.arange(-8, 8) / 8.0).astype(np.float32)
+    row = np.zeros((1, 64), np.float64)
+    row[0, 0] = 1.0                                                    # absmax 1: w / absmax = w exactly
+    row[0, 1] = -0.5625                                                # halfway between -0.625 (3) and -0.5 (4)
+    row[0, 2] = np.nextafter(np.float32(-0.5625), np.float32(1))
+    row[0, 3] = 0.0625                                                 # halfway between 0 (8) and 0.125 (9)
+    pk, am = oracle.nf4_quantize(row, cb)
+    c = oracle.nf4_unpack(pk)[0]
+    assert am[0, 0] == 1.0
+    assert (c[0], c[1], c[2], c[3]) == (15, 3, 4, 8)
+
+
+def test_nf4_error_is_at_most_half_the_widest_gap():
+    cb = wl.nf4_codebook()
+    W = np.random.default_rng(32).standard_normal((7, 256)) * 0.02
+    pk, am = oracle.nf4_quantize(W, cb)
+    err = np.abs(oracle.nf4_dequantize(pk, am, cb) - W)
+    half_gap = np.max(np.diff(cb.astype(np.float64))) / 2
+    bound = np.repeat(am.T.astype(np.float64), 64, axis=1) * half_gap * (1 + 2.0 ** -18) + 2.0 ** -23 * np.abs(W)
+    assert (err <= bound).all()
+
+
+def test_nf4_merge_three_ways():
+    """M031 §05 acceptance on an NF4 base: the dynamic branch over the restored base
+    equals the merged float weight (fp64), the re-quantized merge stays within half the
+    widest codebook gap per weight, and adding the update to the codes does not."""
+    cb = wl.nf4_codebook()
+    rng = np.random.default_rng(33)
+    pk, am = oracle.nf4_quantize(rng.standard_normal((24, 128)) * 0.02, cb)
+    a = oracle.OracleAdapter(rng.standard_normal((4, 128)) / 8, rng.standard_normal((24, 4)) * 0.05, 2.0)
+    X = rng.standard_normal((5, 128))
+    Wd = oracle.nf4_dequantize(pk, am, cb)
+    dynamic = oracle.forward(X, Wd, np.zeros(5, np.int32), [a])
+    merged_float = X @ (Wd + a.scale * a.up @ a.down).T
+    np.testing.assert_allclose(dynamic, merged_float, rtol=1e-12, atol=1e-12)
+    pk2, am2 = oracle.nf4_merge(pk, am, cb, a)
+    half_gap = np.max(np.diff(cb.astype(np.float64))) / 2
+    per_w = np.repeat(am2.T.astype(np.float64), 64, axis=1) * half_gap * (1 + 2.0 ** -18) + 1e-9
+    assert (np.abs(oracle.nf4_dequantize(pk2, am2, cb) - (Wd + a.scale * a.up @ a.down)) <= per_w).all()
+    # the update added to the codes (ignoring scale and codebook) rounds away: most weights
+    # then miss the merged value by more than the bound the right way keeps
+    wrong = oracle.nf4_dequantize(oracle.nf4_pack(np.clip(np.rint(
+        oracle.nf4_unpack(pk) + a.scale * a.up @ a.down), 0, 15).astype(np.uint8)), am, cb)
+    assert np.mean(np.abs(wrong - (Wd + a.scale * a.up @ a.down)) > per_w) > 0.2
+
+
 def test_rank_padding_leaves_output_unchanged():
     """M031 §03: giving an adapter zero rows/columns up to the max rank costs FLOPs, not values."""
     layer = wl.random_layer(14, T=23, din=40, dout=32, ranks=[4, 12, 16], p_none=0.2)

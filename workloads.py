@@ -387,3 +387,32 @@ def stack7b_group_device(seed: int, layer: int, group: int, device):
     ra = stack7b_row_adapter(seed) if tenants else np.full(STACK7B_T, -1, np.int32)
     return {"name": f"stack7b.L{layer}.{name}", "X": X, "W": W, "modules": modules, "tenants": tenants,
             "row_adapter": ra, "din": din, "dout": off}
+
+
+# --------------------------------------------------------------------------- #
+# 4-bit NormalFloat base (ai-infra-kb "M031" §05 names restoring W "by scale/codebook"
+# and the NF4 codebook; the pages cite the QLoRA paper, which defines the data type)
+NF4_BLOCK = 64          # input columns that share one absmax scale
+
+
+def nf4_codebook() -> np.ndarray:
+    """The 16 NormalFloat values, ascending, in fp32: quantiles of the standard normal
+    at evenly spaced probabilities from 1/2 up to 1 - delta (delta = (1/32 + 1/30) / 2),
+    8 of them on the positive side and 7 on the negative side, each side divided by its
+    largest quantile so that the values end at -1 and 1, plus an exact 0."""
+    from scipy.stats import norm
+    p_max = 1.0 - 0.5 * (1.0 / 32 + 1.0 / 30)
+    top = norm.ppf(p_max)
+    pos = norm.ppf(np.linspace(0.5, p_max, 9)[1:]) / top
+    neg = -norm.ppf(np.linspace(0.5, p_max, 8)[1:]) / top
+    return np.sort(np.concatenate([neg, [0.0], pos])).astype(np.float32)
+
+
+def nf4_random_base(seed: int, dout: int, din: int, key: int = 0):
+    """A seeded NF4 base: packed codes [dout x din/2] (column 2m in the low nibble of byte
+    m, 2m+1 in the high one) and fp32 block scales [din/64 x dout] ~ |N(0, 0.02)| * 3."""
+    rng = _rng(seed, 7, key)
+    codes = rng.integers(0, 16, size=(dout, din)).astype(np.uint8)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    absmax = (np.abs(rng.standard_normal((din // NF4_BLOCK, dout))) * 0.06 + 1e-3).astype(np.float32)
+    return packed, absmax
