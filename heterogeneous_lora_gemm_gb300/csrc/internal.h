@@ -96,6 +96,12 @@ cudaError_t launch_base_expand_simt(bool bf16, const void* X, const void* W,
 cudaError_t launch_dequant(bool bf16, const int8_t* q, const float* s, int dout, int din, void* W, cudaStream_t st);
 cudaError_t launch_merge_quant(bool bf16, int8_t* q, float* s, const SlotRec* slots, int slot, const void* arena_down,
                                const void* arena_up, const PoolDims& d, cudaStream_t st);
+// NF4 base (quant.cu): 4-bit codes [dout x din/2], absmax [din/64][dout], codebook [16] (host).
+cudaError_t launch_dequant_nf4(bool bf16, const uint8_t* q, const float* absmax, const float* codebook, int dout,
+                               int din, void* W, cudaStream_t st);
+cudaError_t launch_merge_nf4(bool bf16, uint8_t* q, float* absmax, const float* codebook, const SlotRec* slots,
+                             int slot, const void* arena_down, const void* arena_up, const PoolDims& d,
+                             cudaStream_t st);
 cudaError_t launch_merge_simt(bool bf16, void* W, const SlotRec* slots, int slot,
                               const void* arena_down, const void* arena_up, const PoolDims& d, float sign,
                               cudaStream_t st);

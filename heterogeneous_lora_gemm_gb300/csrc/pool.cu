@@ -814,14 +814,18 @@ mlora_status mlora_adapter_version(mlora_pool_t p, int slot, uint64_t* version) 
     return MLORA_OK;
 }
 
-mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const int32_t* row_adapter, int T,
-                           void* Y, mlora_stream_t stream) {
-    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
-    if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
-    if (T == 0) return MLORA_OK;
-    if (!X || !W || !Y) return fail(MLORA_ERR_INVALID_ARG, "X/W/Y is NULL");
-    if (p->dtype == MLORA_BF16 && (!aligned16(X) || !aligned16(W) || !aligned16(Y)))
-        return fail(MLORA_ERR_INVALID_ARG, "bf16 X/W/Y must be 16-byte aligned");
+// A quantized base weight read by the decode projection itself (codes, scales, codebook).
+struct QuantW {
+    int qmode;   // 1 int8 codes, per-row scale; 2 4-bit codes, per-(row, 64 columns) scale, codebook
+    const void* codes;
+    const float* scale;
+    const float* codebook;   // host [16] (qmode 2)
+};
+
+// The forward over W (bf16 or fp32) or, with q, over a quantized W on the tensor-core
+// decode path.  Arguments already checked by the callers.
+static mlora_status forward_impl(mlora_pool_t p, const void* X, const void* W, const int32_t* row_adapter, int T,
+                                 void* Y, mlora_stream_t stream, const QuantW* q) {
     DeviceGuard g(p->device);
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     cudaStream_t st = (cudaStream_t)stream;
@@ -850,6 +854,12 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
         a.n_loaded = p->loaded;
         a.stamps = p->prof_stamps;
         a.stamp_cap = p->prof_cap;
+        if (q) {
+            a.qmode = q->qmode;
+            a.Wq = q->codes;
+            a.qscale = q->scale;
+            for (int i = 0; i < 16; ++i) a.qcb[i] = q->codebook ? q->codebook[i] : 0.f;
+        }
         CU_TRY(tc_forward(a, st));
     } else {
         if (lora) CU_TRY(launch_shrink_simt(bf16, X, row_adapter, T, p->d_slots, p->arena_down, p->ws, p->dims, st));
@@ -857,6 +867,17 @@ mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const i
     }
     if (lora) p->last_T = T;
     return note_reader(p, st);
+}
+
+mlora_status mlora_forward(mlora_pool_t p, const void* X, const void* W, const int32_t* row_adapter, int T,
+                           void* Y, mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
+    if (T == 0) return MLORA_OK;
+    if (!X || !W || !Y) return fail(MLORA_ERR_INVALID_ARG, "X/W/Y is NULL");
+    if (p->dtype == MLORA_BF16 && (!aligned16(X) || !aligned16(W) || !aligned16(Y)))
+        return fail(MLORA_ERR_INVALID_ARG, "bf16 X/W/Y must be 16-byte aligned");
+    return forward_impl(p, X, W, row_adapter, T, Y, stream, nullptr);
 }
 
 // W <- W + sign * scale * Up Down of the adapter in `slot` (merge: +1, un-merge: -1).
@@ -900,6 +921,15 @@ mlora_status mlora_forward_quantized(mlora_pool_t p, const void* X, const void* 
     if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
     if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
     if (T == 0) return MLORA_OK;
+    if (p->dtype == MLORA_BF16 && tc_quantized_fits(p->dims, T)) {
+        // decode-sized batch: the projection reads the codes and restores each W tile in
+        // shared memory (no restore pass over W; W_scratch is not used)
+        if (!X || !Wq || !row_scale || !Y) return fail(MLORA_ERR_INVALID_ARG, "X/Wq/row_scale/Y is NULL");
+        if (!aligned16(X) || !aligned16(Wq) || !aligned16(Y))
+            return fail(MLORA_ERR_INVALID_ARG, "X/Wq/Y must be 16-byte aligned");
+        const QuantW q{1, Wq, row_scale, nullptr};
+        return forward_impl(p, X, nullptr, row_adapter, T, Y, stream, &q);
+    }
     DeviceGuard g(p->device);
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     mlora_status st = mlora_dequantize(Wq, row_scale, p->dout, p->din, p->dtype, W_scratch, stream);
@@ -927,6 +957,54 @@ mlora_status mlora_merge_quantized(mlora_pool_t p, void* Wq, float* row_scale, i
     if (e == cudaErrorInvalidValue && !tensor_cores)
         return fail(MLORA_ERR_INVALID_ARG, "din %d too large for the quantized merge", p->din);
     if (e != cudaSuccess) return cuda_fail(e, tensor_cores ? "quantized merge (tensor cores)" : "quantized merge");
+    return note_reader(p, st);
+}
+
+mlora_status mlora_dequantize_nf4(const void* codes, const float* absmax, const float* codebook, int dout, int din,
+                                  mlora_dtype dtype, void* W, mlora_stream_t stream) {
+    if (!codes || !absmax || !codebook || !W) return fail(MLORA_ERR_INVALID_ARG, "codes/absmax/codebook/W is NULL");
+    if (dout < 0 || din < 0 || din % 64 != 0) return fail(MLORA_ERR_INVALID_ARG, "din %d must be a multiple of 64", din);
+    if (dtype != MLORA_BF16 && dtype != MLORA_F32) return fail(MLORA_ERR_INVALID_ARG, "bad dtype");
+    if (!aligned16(codes) || !aligned16(W)) return fail(MLORA_ERR_INVALID_ARG, "codes and W must be 16-byte aligned");
+    CU_TRY(launch_dequant_nf4(dtype == MLORA_BF16, (const uint8_t*)codes, absmax, codebook, dout, din, W,
+                              (cudaStream_t)stream));
+    return MLORA_OK;
+}
+
+mlora_status mlora_forward_nf4(mlora_pool_t p, const void* X, const void* codes, const float* absmax,
+                               const float* codebook, void* W_scratch, const int32_t* row_adapter, int T, void* Y,
+                               mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
+    if (T == 0) return MLORA_OK;
+    if (!X || !codes || !absmax || !codebook || !Y) return fail(MLORA_ERR_INVALID_ARG, "X/codes/absmax/codebook/Y is NULL");
+    if (p->din % 64 != 0) return fail(MLORA_ERR_INVALID_ARG, "din %d must be a multiple of 64", p->din);
+    if (!aligned16(X) || !aligned16(codes) || !aligned16(Y))
+        return fail(MLORA_ERR_INVALID_ARG, "X/codes/Y must be 16-byte aligned");
+    if (p->dtype == MLORA_BF16 && tc_quantized_fits(p->dims, T)) {
+        const QuantW q{2, codes, absmax, codebook};
+        return forward_impl(p, X, nullptr, row_adapter, T, Y, stream, &q);
+    }
+    if (!W_scratch) return fail(MLORA_ERR_INVALID_ARG, "W_scratch is NULL (needed unless bf16 and T <= 256)");
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    mlora_status st = mlora_dequantize_nf4(codes, absmax, codebook, p->dout, p->din, p->dtype, W_scratch, stream);
+    if (st != MLORA_OK) return st;
+    return mlora_forward(p, X, W_scratch, row_adapter, T, Y, stream);
+}
+
+mlora_status mlora_merge_nf4(mlora_pool_t p, void* codes, float* absmax, const float* codebook, int slot,
+                             mlora_stream_t stream) {
+    if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
+    if (!codes || !absmax || !codebook) return fail(MLORA_ERR_INVALID_ARG, "codes/absmax/codebook is NULL");
+    if (p->din % 64 != 0) return fail(MLORA_ERR_INVALID_ARG, "din %d must be a multiple of 64", p->din);
+    if (slot < 0 || slot >= p->max_slots) return fail(MLORA_ERR_BAD_SLOT, "slot %d not in [0, %d)", slot, p->max_slots);
+    if (p->slots[slot].rank <= 0) return fail(MLORA_ERR_NOT_LOADED, "slot %d holds no adapter", slot);
+    DeviceGuard g(p->device);
+    if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    CU_TRY(launch_merge_nf4(p->dtype == MLORA_BF16, (uint8_t*)codes, absmax, codebook, p->d_slots, slot,
+                            p->arena_down, p->arena_up, p->dims, st));
     return note_reader(p, st);
 }
 

@@ -317,4 +317,137 @@ cudaError_t launch_merge_quant(bool bf16, int8_t* q, float* s, const SlotRec* sl
                 : launch_merge_quant_e<float>(q, s, slots, slot, arena_down, arena_up, d, st);
 }
 
+// ---------------------------------------------------------------- NF4 base
+// 4-bit codes, two per byte (column 2m in the low nibble of byte m of a row), an fp32
+// absmax per output row and block of 64 input columns stored block-major
+// ([din/64][dout]: consecutive rows of one block are adjacent), and a 16-entry
+// codebook (ai-infra-kb "M031" §05: W restored by scale and codebook).
+namespace {
+
+constexpr int NF4_BLOCK = 64;
+
+struct Codebook {
+    float v[16];
+};
+
+// 16 codes (8 bytes) of row o from column i0 (a multiple of 16): W = codebook[code] *
+// absmax, rounded once to the pool dtype.
+template <typename E>
+__global__ void __launch_bounds__(DQ_THREADS)
+dequant_nf4_kernel(const uint8_t* __restrict__ q, const float* __restrict__ absmax, Codebook cb, int dout, int din,
+                   E* __restrict__ W) {
+    __shared__ float cb_s[16];
+    if (threadIdx.x < 16) cb_s[threadIdx.x] = cb.v[threadIdx.x];
+    __syncthreads();
+    const size_t groups = (size_t)dout * (din / 16);
+    const uint32_t gpr = (uint32_t)(din / 16);
+    for (size_t g = blockIdx.x * (size_t)blockDim.x + threadIdx.x; g < groups; g += (size_t)gridDim.x * blockDim.x) {
+        const size_t o = g / gpr;
+        const int i0 = (int)(g - o * gpr) * 16;
+        const uint2 raw = *reinterpret_cast<const uint2*>(q + o * (din / 2) + i0 / 2);
+        const float sc = absmax[(size_t)(i0 / NF4_BLOCK) * dout + o];
+        const uint32_t b[2] = {raw.x, raw.y};
+        __align__(16) E out[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t byte = (b[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+            out[2 * j] = from_f32<E>(cb_s[byte & 15u] * sc);
+            out[2 * j + 1] = from_f32<E>(cb_s[byte >> 4] * sc);
+        }
+        const int4* src = reinterpret_cast<const int4*>(out);
+        int4* d = reinterpret_cast<int4*>(W + o * din + i0);
+#pragma unroll
+        for (int j = 0; j < (int)(16 * sizeof(E) / 16); ++j) d[j] = src[j];
+    }
+}
+
+// The merge on an NF4 base, in place: one warp per (row o, block of 64 columns); lane l
+// owns columns 2l and 2l+1 (one byte of codes).  Restore (fp32 codebook value times
+// the block's absmax), add scale * sum_k Up[o,k] Down[k,i] (fp32, k ascending), take
+// the block's new absmax, and give each w / absmax (fp32 division) the code of the
+// nearest codebook value (fp32 distances, the first of equal ones).
+template <typename E>
+__global__ void __launch_bounds__(256)
+merge_nf4_kernel(uint8_t* __restrict__ q, float* __restrict__ absmax, Codebook cb, const SlotRec* __restrict__ slots,
+                 int slot, const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout) {
+    __shared__ float cb_s[16];
+    if (threadIdx.x < 16) cb_s[threadIdx.x] = cb.v[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const size_t warp_id = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
+    const int nb = din / NF4_BLOCK;
+    if (warp_id >= (size_t)dout * nb) return;
+    const int o = (int)(warp_id / nb), blk = (int)(warp_id % nb);
+    const SlotRec rec = slots[slot];
+    const int i = blk * NF4_BLOCK + 2 * lane;
+    uint8_t* qb = q + (size_t)o * (din / 2) + blk * (NF4_BLOCK / 2) + lane;
+    float* am = absmax + (size_t)blk * dout + o;
+    const uint32_t byte = *qb;
+    const float old = *am;
+    float w0 = cb_s[byte & 15u] * old, w1 = cb_s[byte >> 4] * old;
+    float u0 = 0.f, u1 = 0.f;
+    const E* down = arena_down + (size_t)rec.unit * din + i;
+    for (int k = 0; k < rec.rank; ++k) {
+        const float up = as_f32(arena_up[up_index(rec.unit, k, o, dout)]);
+        u0 = fmaf(up, as_f32(down[(size_t)k * din]), u0);
+        u1 = fmaf(up, as_f32(down[(size_t)k * din + 1]), u1);
+    }
+    w0 = w0 + rec.scale * u0;
+    w1 = w1 + rec.scale * u1;
+    float m = fmaxf(fabsf(w0), fabsf(w1));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    auto code_of = [&](float w) {
+        const float v = m > 0.f ? w / m : 0.f;
+        int best = 0;
+        float bd = fabsf(v - cb_s[0]);
+        for (int j = 1; j < 16; ++j) {
+            const float dj = fabsf(v - cb_s[j]);
+            if (dj < bd) {
+                bd = dj;
+                best = j;
+            }
+        }
+        return (uint32_t)best;
+    };
+    *qb = (uint8_t)(code_of(w0) | (code_of(w1) << 4));
+    if (lane == 0) *am = m;
+}
+
+}  // namespace
+
+cudaError_t launch_dequant_nf4(bool bf16, const uint8_t* q, const float* absmax, const float* codebook, int dout,
+                               int din, void* W, cudaStream_t st) {
+    Codebook cb;
+    for (int j = 0; j < 16; ++j) cb.v[j] = codebook[j];
+    const size_t groups = (size_t)dout * (din / 16);
+    size_t blocks = (groups + DQ_THREADS - 1) / DQ_THREADS;
+    const size_t cap = (size_t)quant_sms() * 8;
+    blocks = blocks < cap ? blocks : cap;
+    if (blocks == 0) return cudaSuccess;
+    if (bf16)
+        dequant_nf4_kernel<__nv_bfloat16><<<(unsigned)blocks, DQ_THREADS, 0, st>>>(q, absmax, cb, dout, din,
+                                                                                  (__nv_bfloat16*)W);
+    else
+        dequant_nf4_kernel<float><<<(unsigned)blocks, DQ_THREADS, 0, st>>>(q, absmax, cb, dout, din, (float*)W);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_nf4(bool bf16, uint8_t* q, float* absmax, const float* codebook, const SlotRec* slots,
+                             int slot, const void* arena_down, const void* arena_up, const PoolDims& d,
+                             cudaStream_t st) {
+    Codebook cb;
+    for (int j = 0; j < 16; ++j) cb.v[j] = codebook[j];
+    const size_t warps = (size_t)d.dout * (d.din / NF4_BLOCK);
+    const size_t blocks = (warps * 32 + 255) / 256;
+    if (blocks == 0) return cudaSuccess;
+    if (bf16)
+        merge_nf4_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
+            q, absmax, cb, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din, d.dout);
+    else
+        merge_nf4_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(q, absmax, cb, slots, slot, (const float*)arena_down,
+                                                                 (const float*)arena_up, d.din, d.dout);
+    return cudaGetLastError();
+}
+
 }  // namespace mlora

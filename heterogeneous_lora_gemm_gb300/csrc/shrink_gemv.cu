@@ -35,9 +35,9 @@ namespace {
 
 constexpr int G_THREADS = 256;
 constexpr int G_WARPS = G_THREADS / 32;
-constexpr int G_NT = 8;                    // rows of the chunk's adapter per pass over its Down rows
-constexpr int G_XS_BYTES = 64 * 1024;      // shared memory for the X rows of one pass
-constexpr int G_MAX_T = 256;               // decode batches only
+constexpr int G_TOK = 2;                   // rows of the chunk's adapter per pass over its Down rows
+constexpr int G_U = 4;                     // 16-byte words of a row per lane in flight at once
+constexpr int G_MAX_T = G_THREADS;         // decode batches only: one row id per thread
 
 struct GemvParams {
     const __nv_bfloat16* X;        // [T x din]
@@ -49,28 +49,34 @@ struct GemvParams {
     Workspace ws;
     int T, din, n_chunks, tcap, S, max_chunks;
     int seg_P, seg_stage_rows;
-    int nt;                        // rows per pass (X rows staged in shared memory)
     int prefetch;                  // L2 prefetch of the chunk's Down rows before the wait
     unsigned long long* stamps;    // profiling records (NULL = off)
     int stamp_cap;
 };
 
-// 8 bf16 of a 16-byte word, as floats (exact)
-__device__ __forceinline__ void bf16x8(const uint4 w, float* f) {
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+// sum over the 8 bf16 pairs of two 16-byte words, added to acc (fp32 FMAs)
+__device__ __forceinline__ float dot8(const uint4 a, const uint4 b, float acc) {
+    const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, ub[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(u[i] << 16);
-        f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+        acc = fmaf(__uint_as_float(ua[i] << 16), __uint_as_float(ub[i] << 16), acc);
+        acc = fmaf(__uint_as_float(ua[i] & 0xFFFF0000u), __uint_as_float(ub[i] & 0xFFFF0000u), acc);
     }
+    return acc;
 }
 
-__global__ void __launch_bounds__(G_THREADS) shrink_gemv_kernel(const GemvParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+    return v;
+}
+
+__global__ void __launch_bounds__(G_THREADS, 1) shrink_gemv_kernel(const GemvParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];   // the segment builder's scratch
     __shared__ int rows_s[G_MAX_T];          // the chunk's rows, in row order
     __shared__ int pos_s[G_MAX_T];           // row -> its index in rows_s, or -1
-    __shared__ float vals_s[G_MAX_T][CHUNK];  // scale * Down_chunk x per row of rows_s
-    __shared__ int n_rows_s;
+    __shared__ float vals_s[G_MAX_T][CHUNK];  // Down_chunk x per row of rows_s
+    __shared__ int warp_n[G_WARPS];
     const unsigned long long t_start = (p.stamps && threadIdx.x == 0) ? gtimer() : 0ull;
     const int c = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -96,100 +102,99 @@ __global__ void __launch_bounds__(G_THREADS) shrink_gemv_kernel(const GemvParams
     pdl_wait();
     pdl_trigger();
 
-    // rows of the chunk's slot, in row order (warp 0), and the inverse map
-    for (int t = threadIdx.x; t < p.T; t += G_THREADS) pos_s[t] = -1;
+    // rows of the chunk's slot, in row order: one row id per thread, one round trip
+    const int t = threadIdx.x;
+    const bool mine = t < p.T && p.row_adapter[t] == cr.slot;
+    const unsigned b = __ballot_sync(0xffffffffu, mine);
+    if (lane == 0) warp_n[warp] = __popc(b);
     __syncthreads();
-    if (warp == 0) {
-        int n = 0;
-        for (int base = 0; base < p.T; base += 32) {
-            const int t = base + lane;
-            const bool mine = t < p.T && p.row_adapter[t] == cr.slot;
-            const unsigned b = __ballot_sync(0xffffffffu, mine);
-            if (mine) {
-                const int k = n + __popc(b & seg::lanemask_lt());
-                rows_s[k] = t;
-                pos_s[t] = k;
-            }
-            n += __popc(b);
-        }
-        if (lane == 0) n_rows_s = n;
+    int off = 0, n = 0;
+#pragma unroll
+    for (int w = 0; w < G_WARPS; ++w) {
+        off += w < warp ? warp_n[w] : 0;
+        n += warp_n[w];
+    }
+    if (t < p.T) {
+        const int k = mine ? off + __popc(b & seg::lanemask_lt()) : -1;
+        pos_s[t] = k;
+        if (mine) rows_s[k] = t;
     }
     __syncthreads();
-    const int n = n_rows_s;
     if (n == 0) {
         if (threadIdx.x == 0) stamp_record(p.stamps, p.stamp_cap, t_start, STAMP_SHRINK);
         return;
     }
 
-    // warp w owns rank rows w and w + 8 of the chunk; lane l covers din columns
-    // l*8 .. l*8+7 of every 256
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
+    // warp w owns rank rows w and w + 8 of the chunk; lane l the 16-byte words
+    // l, l + 32, ... of a row; X rows come from L2 (written by the kernel before)
     const int r0 = warp, r1 = warp + G_WARPS;
     const bool has0 = r0 < cr.kval, has1 = r1 < cr.kval;
     const uint4* d0p = reinterpret_cast<const uint4*>(p.down + (size_t)(cr.unit + (has0 ? r0 : 0)) * din);
     const uint4* d1p = reinterpret_cast<const uint4*>(p.down + (size_t)(cr.unit + (has1 ? r1 : 0)) * din);
-    const int words = din / 8;   // 16-byte words per row
-    for (int g0 = 0; g0 < n; g0 += p.nt) {
-        const int ng = min(p.nt, n - g0);
-        for (int i = threadIdx.x; i < ng * words; i += G_THREADS) {
-            const int j = i / words, k = i - j * words;
-            reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(p.X + (size_t)rows_s[g0 + j] * din)[k];
-        }
-        __syncthreads();
-        float acc0[G_NT], acc1[G_NT];
+    const int words = din / 8;
+    for (int g0 = 0; g0 < n; g0 += G_TOK) {
+        const bool two = g0 + 1 < n;
+        // (rows past the chunk's valid ones read row 0 and a missing second row reads the
+        // first: the loads need no predicate, and the Vt write drops those values)
+        const uint4* xa = reinterpret_cast<const uint4*>(p.X + (size_t)rows_s[g0] * din);
+        const uint4* xb = reinterpret_cast<const uint4*>(p.X + (size_t)rows_s[two ? g0 + 1 : g0] * din);
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+        // G_U words per lane in flight at once: every load of a block is issued before
+        // any of them is used
+        int k0 = lane;
+        for (; k0 + 32 * (G_U - 1) < words; k0 += 32 * G_U) {
+            uint4 w0[G_U], w1[G_U], x0[G_U], x1[G_U];
 #pragma unroll
-        for (int j = 0; j < G_NT; ++j) acc0[j] = acc1[j] = 0.f;
-        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 4
-        for (int k = lane; k < words; k += 32) {
-            float w0[8], w1[8];
-            bf16x8(has0 ? __ldg(d0p + k) : zero, w0);
-            bf16x8(has1 ? __ldg(d1p + k) : zero, w1);
+            for (int u = 0; u < G_U; ++u) {
+                w0[u] = __ldg(d0p + k0 + 32 * u);
+                w1[u] = __ldg(d1p + k0 + 32 * u);
+                x0[u] = __ldcg(xa + k0 + 32 * u);
+                x1[u] = __ldcg(xb + k0 + 32 * u);
+            }
 #pragma unroll
-            for (int j = 0; j < G_NT; ++j) {
-                if (j < ng) {
-                    float x[8];
-                    bf16x8(reinterpret_cast<const uint4*>(xs)[j * words + k], x);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc0[j] = fmaf(w0[e], x[e], acc0[j]);
-                        acc1[j] = fmaf(w1[e], x[e], acc1[j]);
-                    }
-                }
+            for (int u = 0; u < G_U; ++u) {
+                a00 = dot8(w0[u], x0[u], a00);
+                a10 = dot8(w1[u], x0[u], a10);
+                a01 = dot8(w0[u], x1[u], a01);
+                a11 = dot8(w1[u], x1[u], a11);
             }
         }
-#pragma unroll
-        for (int j = 0; j < G_NT; ++j) {
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                acc0[j] += __shfl_xor_sync(0xffffffffu, acc0[j], d);
-                acc1[j] += __shfl_xor_sync(0xffffffffu, acc1[j], d);
-            }
+        for (; k0 < words; k0 += 32) {
+            const uint4 w0 = __ldg(d0p + k0), w1 = __ldg(d1p + k0);
+            const uint4 x0 = __ldcg(xa + k0), x1 = __ldcg(xb + k0);
+            a00 = dot8(w0, x0, a00);
+            a10 = dot8(w1, x0, a10);
+            a01 = dot8(w0, x1, a01);
+            a11 = dot8(w1, x1, a11);
         }
+        a00 = warp_sum(a00);
+        a10 = warp_sum(a10);
+        a01 = warp_sum(a01);
+        a11 = warp_sum(a11);
         if (lane == 0) {
-#pragma unroll
-            for (int j = 0; j < G_NT; ++j)
-                if (j < ng) {
-                    vals_s[g0 + j][r0] = acc0[j];
-                    vals_s[g0 + j][r1] = acc1[j];
-                }
+            vals_s[g0][r0] = a00;
+            vals_s[g0][r1] = a10;
+            if (two) {
+                vals_s[g0 + 1][r0] = a01;
+                vals_s[g0 + 1][r1] = a11;
+            }
         }
-        __syncthreads();   // the X rows of the next pass overwrite xs
     }
+    __syncthreads();
 
     // Vt[c][t][0..15] for every row of the batch, 32 bytes each: the scaled values
     // for the chunk's own rows (zero past the chunk's valid columns), zero elsewhere
-    for (int t = threadIdx.x; t < p.T; t += G_THREADS) {
+    if (t < p.T) {
         const int k = pos_s[t];
         uint32_t w[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float a = 0.f, b = 0.f;
+            float lo = 0.f, hi = 0.f;
             if (k >= 0) {
-                a = 2 * e < cr.kval ? cr.scale * vals_s[k][2 * e] : 0.f;
-                b = 2 * e + 1 < cr.kval ? cr.scale * vals_s[k][2 * e + 1] : 0.f;
+                lo = 2 * e < cr.kval ? cr.scale * vals_s[k][2 * e] : 0.f;
+                hi = 2 * e + 1 < cr.kval ? cr.scale * vals_s[k][2 * e + 1] : 0.f;
             }
-            __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
             w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
         uint4* dst = reinterpret_cast<uint4*>(p.vt + ((size_t)c * p.tcap + t) * CHUNK);
@@ -225,6 +230,7 @@ bool gemv_shrink_fits(const PoolDims& d, int T) {
     return T >= 1 && T <= G_MAX_T && d.din % 8 == 0;
 }
 
+
 cudaError_t launch_shrink_gemv(const TcForwardArgs& a, bool prefetch, cudaStream_t st) {
     const PoolDims& d = a.dims;
     GemvParams p{};
@@ -241,24 +247,20 @@ cudaError_t launch_shrink_gemv(const TcForwardArgs& a, bool prefetch, cudaStream
     p.tcap = d.tcap;
     p.S = d.S;
     p.max_chunks = d.max_chunks;
-    p.nt = G_XS_BYTES / (d.din * 2);
-    p.nt = p.nt < 1 ? 1 : (p.nt > G_NT ? G_NT : p.nt);
     p.prefetch = prefetch ? 1 : 0;
     p.stamps = a.stamps;
     p.stamp_cap = a.stamp_cap;
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, shrink_gemv_kernel);
     if (e != cudaSuccess) return e;
-    const int avail_ints = (max_dyn_smem_gemv() - (int)fa.sharedSizeBytes) / 4;
-    const size_t xs_bytes = (size_t)p.nt * d.din * 2;
-    // the builder CTA uses the same dynamic shared memory: as many row ranges as fit
-    SegPlan sp = seg_plan(d.S, G_WARPS, (int)(xs_bytes / 4), a.T);
-    if (sp.P < 1) sp = seg_plan(d.S, G_WARPS, avail_ints, a.T);
+    // the builder CTA's scratch is the only dynamic shared memory: as many row ranges
+    // as fit a small budget, more memory only if not even one does
+    SegPlan sp = seg_plan(d.S, G_WARPS, 16 * 1024 / 4, a.T);
+    if (sp.P < 1) sp = seg_plan(d.S, G_WARPS, (max_dyn_smem_gemv() - (int)fa.sharedSizeBytes) / 4, a.T);
     if (sp.P < 1) return cudaErrorInvalidConfiguration;
     p.seg_P = sp.P;
     p.seg_stage_rows = sp.stage_rows ? 1 : 0;
-    const size_t smem = xs_bytes > (size_t)sp.ints * 4 ? xs_bytes : (size_t)sp.ints * 4;
-    return launch_k(shrink_gemv_kernel, dim3(a.n_chunks + 1), dim3(G_THREADS), smem, st, true, 1, p);
+    return launch_k(shrink_gemv_kernel, dim3(a.n_chunks + 1), dim3(G_THREADS), (size_t)sp.ints * 4, st, true, 1, p);
 }
 
 }  // namespace mlora

@@ -72,12 +72,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                const cuuint32_t* box, CUtensorMapSwizzle sw) {
+    return tc_encode_typed(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box, sw);
+}
+
+bool tc_encode_typed(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, type, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -110,6 +114,7 @@ constexpr int MAX_SLOT_WORDS = 4096 / 32;
 constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
 constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
 constexpr int PROJ_KC = 2;         // projection: K chunks of 64 per pipeline step (one 3D box each for W and X)
+constexpr int QMODE_INT8 = 1, QMODE_NF4 = 2;
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
 __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(n); }
@@ -118,6 +123,7 @@ __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(
 struct Tail {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
+    uint64_t conv[MAX_STAGES];        // projection over codes: the stage's W tile is converted
     uint64_t acc_full;
     uint64_t info_ready;              // projection: the K-extension chunk info is in place
     uint64_t rx_bar;                  // projection, push reduction: all splits' slices have landed
@@ -138,6 +144,7 @@ struct Tail {
     int ext_unit[EXT_CAP];            // projection: arena unit of each K-extension chunk, -1 = skip
     int ext_slot[EXT_CAP];
     unsigned long long t_start;       // profiling: globaltimer at the CTA's start
+    float qcb[16];                    // projection over 4-bit codes: the codebook
 };
 
 struct GemmParams {
@@ -172,6 +179,13 @@ struct GemmParams {
     Workspace ws;
     unsigned long long* stamps;     // profiling records (NULL = off), see ptx::stamp_record
     int stamp_cap;
+    // projection over a quantized W (tmW maps the codes): 0 bf16 W; QMODE_INT8 int8 codes
+    // with an fp32 scale per output row; QMODE_NF4 4-bit codes (two per byte, the even
+    // column in the low nibble) with an fp32 scale per output row and 64 columns
+    int qmode;
+    int q_x;                        // code bytes per row and K chunk of 64 columns
+    const float* qscale;            // QMODE_INT8: [dout]; QMODE_NF4: [din / 64][dout]
+    float qcb[16];                  // QMODE_NF4: the codebook
 };
 
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
@@ -222,6 +236,54 @@ __device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng,
     }
 }
 
+// A code as a float without a conversion instruction: 2^23 + 128 + c holds c + 128 in
+// its low mantissa bits.
+__device__ __forceinline__ float code_f32(int8_t c) { return __int_as_float(0x4B000000 + 128 + (int)c) - 8388736.f; }
+
+// One row of a stage's W tile restored from its codes: 64 columns of bf16(code value *
+// scale) -- the value and the single rounding of the restore kernels -- written as the
+// 128-byte row `row` of a K-major tile with the 128-byte swizzle (16-byte chunk j of the
+// row at position j ^ (row % 8)), the layout a TMA load of a bf16 W tile leaves.  The
+// 16-byte reads start at a row-dependent chunk to spread shared-memory banks.
+__device__ __forceinline__ void restore_row(const uint8_t* codes, uint8_t* arow, int row, float sc, int qmode,
+                                            const float* cb) {
+    const int sw = row & 7;
+    if (qmode == QMODE_INT8) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = (jj + row) & 3;   // codes of columns 16j .. 16j+15
+            const int4 raw = *reinterpret_cast<const int4*>(codes + 16 * j);
+            const int8_t* c = reinterpret_cast<const int8_t*>(&raw);
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(code_f32(c[2 * e]) * sc, code_f32(c[2 * e + 1]) * sc);
+                w[e] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(arow + (((2 * j) ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(arow + (((2 * j + 1) ^ sw) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    } else {
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            const int j = (jj + row) & 1;   // codes of columns 32j .. 32j+31, two per byte
+            const uint4 raw = *reinterpret_cast<const uint4*>(codes + 16 * j);
+            const uint32_t b4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {   // 16-byte chunk 4j + q: columns 32j + 8q .. +7
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t byte = (b4[q] >> (8 * e)) & 0xFFu;
+                    __nv_bfloat162 h = __floats2bfloat162_rn(cb[byte & 15u] * sc, cb[byte >> 4] * sc);
+                    w[e] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(arow + (((4 * j + q) ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- the GEMM kernel
 // Two CTAs per SM: a shrink CTA and a projection CTA launched behind it share an SM.
 template <bool SHRINK>
@@ -236,7 +298,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int NS = p.stages;
     const int B_SUB = b_bytes(p.N);                  // bytes of the B operand per K chunk
     const int A_STAGE = p.kc * p.a_sub;
-    const int SB = A_STAGE + p.kc * B_SUB;
+    const int Q_OFF = A_STAGE + p.kc * B_SUB;        // projection over codes: the code tile (kc == 1)
+    const int SB = Q_OFF + (!SHRINK && p.qmode ? BM * p.q_x : 0);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
@@ -275,6 +338,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         for (int s = 0; s < NS; ++s) {
             mbar_init(&tl.full[s], 1);
             mbar_init(&tl.empty[s], 1);
+            mbar_init(&tl.conv[s], 4);   // one arrival per converting (epilogue) warp
         }
         mbar_init(&tl.acc_full, 1);
         mbar_init(&tl.info_ready, 1);
@@ -288,6 +352,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
         if (SHRINK || p.ext_units > 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmArena) : "memory");
     }
+    if (!SHRINK && p.qmode == QMODE_NF4 && threadIdx.x < 16) tl.qcb[threadIdx.x] = p.qcb[threadIdx.x];
     if (warp == 1) {
         __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl.tmem_slot)),
@@ -301,9 +366,10 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // after the set-up, then let the projection launch and stream W meanwhile.
         pdl_wait();
         pdl_trigger();
-    } else {
-        pdl_trigger();   // the next forward's shrink may get resident and set up meanwhile
     }
+    // (the projection lets the next kernel launch once its last MMA is issued: CTAs of
+    // the next forward that got resident earlier would only wait, holding the shared
+    // memory and registers that this kernel's later CTAs need)
     if (warp == 2 && SHRINK) {
         // Which of this row tile's chunks does some token of the token tile use?  The
         // row ids and the chunk entries are read together; a chunk is needed if a
@@ -448,9 +514,14 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int i = 0; i < pre; ++i) {
                 uint8_t* a = smem + (size_t)i * SB;
                 tl.stage_kind[i] = -1;
-                mbar_expect_tx_only(&tl.full[i], (uint32_t)A_STAGE);
-                if (p.kc > 1) tma_3d(a, &tmW, &tl.full[i], 0, tile * BM, (kb0 + i) * p.kc);
-                else tma_2d(a, &tmW, &tl.full[i], (kb0 + i) * BK, tile * BM);
+                if (p.qmode) {
+                    mbar_expect_tx_only(&tl.full[i], (uint32_t)(BM * p.q_x));
+                    tma_2d(a + Q_OFF, &tmW, &tl.full[i], (kb0 + i) * p.q_x, tile * BM);
+                } else {
+                    mbar_expect_tx_only(&tl.full[i], (uint32_t)A_STAGE);
+                    if (p.kc > 1) tma_3d(a, &tmW, &tl.full[i], 0, tile * BM, (kb0 + i) * p.kc);
+                    else tma_2d(a, &tmW, &tl.full[i], (kb0 + i) * BK, tile * BM);
+                }
             }
             pdl_wait();
             for (int i = 0; i < pre; ++i) {
@@ -486,6 +557,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         tma_2d(a + j * CHUNK_BYTES, &tmArena, &tl.full[s], kb * BK, tl.my_unit[j]);
                     tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
                 }
+            } else if (!ext && p.qmode) {
+                // the code tile and X; the epilogue warps restore the bf16 W tile from the codes
+                tl.stage_kind[s] = -1;
+                mbar_expect_tx(&tl.full[s], (uint32_t)(BM * p.q_x + B_SUB));
+                tma_2d(a + Q_OFF, &tmW, &tl.full[s], kb * p.q_x, tile * BM);
+                tma_2d(b, &tmX, &tl.full[s], kb * BK, 0);
             } else if (!ext) {
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)SB);
@@ -559,12 +636,21 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         int s = 0;
         uint32_t ph = 0;
         uint32_t acc = 0;
+        uint32_t cph = 0;   // over codes: parity of each stage's next conversion
+        const int ne_m = eu1 - eu0, ins_m = max(0, (kb1 - kb0) - p.ext_lead);
         for (int i = 0; i < n_steps; ++i) {
-            if (!mbar_wait(&tl.full[s], ph, abort_flag, p.status)) break;
+            const bool din_step = !(i >= ins_m && i < ins_m + ne_m);
+            if (!SHRINK && p.qmode && din_step) {
+                // the converting warps saw the stage land and restored its W tile
+                if (!mbar_wait(&tl.conv[s], (cph >> s) & 1u, abort_flag, p.status)) break;
+                cph ^= 1u << s;
+            } else if (!mbar_wait(&tl.full[s], ph, abort_flag, p.status)) {
+                break;
+            }
             tc_fence_after();
             const uint32_t a = smem_u32(smem + (size_t)s * SB);
             const uint32_t b = a + A_STAGE;
-            const int kind = tl.stage_kind[s];
+            const int kind = (!SHRINK && p.qmode && din_step) ? -1 : tl.stage_kind[s];
             if (kind < 0) {
                 // each K chunk: A spans 128 rows (16 KiB) from its sub-block; in the shrink,
                 // rows past the loaded ones hold whatever lies there and give accumulator
@@ -596,12 +682,43 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         tl.flags[0] = (int)acc;
         mma_commit(&tl.acc_full);
+        if (!SHRINK) pdl_trigger();
         if (*abort_flag) {   // MMAs already issued must finish before TMEM is released
             const long long t0 = clock64();
             while (!mbar_try_wait(&tl.acc_full, 0) && clock64() - t0 < 200000000ll) {
             }
         }
     } else if (warp >= 2) {
+        if (!SHRINK && p.qmode) {
+            // ---------------- over codes: restore each din step's W tile (row `row` per
+            // thread) once its codes land, then release the stage to the MMA warp
+            const int o = tile * BM + row;
+            const float row_sc = (p.qmode == QMODE_INT8 && o < p.dout) ? __ldg(p.qscale + o) : 0.f;
+            const int ne_c = eu1 - eu0, ins_c = max(0, (kb1 - kb0) - p.ext_lead);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int i = 0; i < n_steps; ++i) {
+                if (!(i >= ins_c && i < ins_c + ne_c)) {
+                    const int kb = kb0 + (i < ins_c ? i : i - ne_c);
+                    const float sc = p.qmode == QMODE_NF4
+                                         ? (o < p.dout ? __ldg(p.qscale + (size_t)kb * p.dout + o) : 0.f)
+                                         : row_sc;
+                    const bool got = mbar_wait(&tl.full[s], ph, abort_flag, p.status);
+                    __syncwarp();
+                    if (!__all_sync(0xffffffffu, got)) break;
+                    uint8_t* stg = smem + (size_t)s * SB;
+                    restore_row(stg + Q_OFF + row * p.q_x, stg + row * 128, row, sc, p.qmode, tl.qcb);
+                    fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
+                    __syncwarp();
+                    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tl.conv[s]))
+                                                : "memory");
+                }
+                if (++s == NS) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+        }
         // ---------------- epilogue: TMEM -> partial tile, or the final values
         const bool ok = mbar_wait(&tl.acc_full, 0, abort_flag, p.status);
         __syncwarp();   // reconverge: lanes may leave the wait loop apart; tcgen05.ld is warp-collective
@@ -928,6 +1045,8 @@ bool tc_encode_arena_maps(TcArenaMaps* m, void* arena_down, void* arena_up, int 
            tc_encode(&m->up256, arena_up, 3, dims, strides, box256, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+bool tc_quantized_fits(const PoolDims& d, int T) { return T >= 1 && T <= MAX_N && d.din % BK == 0; }
+
 bool tc_supported(const PoolDims& d, int T) {
     (void)d;
     return T >= 1;
@@ -993,7 +1112,14 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const bool shrink = n_chunks > 0;
     cudaError_t e;
     const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
+    if (a.qmode && !(decode && d.din % BK == 0)) return cudaErrorInvalidValue;
     DecodeShape ds = decode_shape(d, decode ? N : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE);
+    if (a.qmode) {   // over codes: one K chunk per stage (the code tile is one 2D box)
+        ds.pkc = 1;
+        ds.ksteps = kb_total;
+        ds.splits = ds.splits < kb_total ? ds.splits : kb_total;
+    }
+    const int q_x = a.qmode == QMODE_INT8 ? BK : (a.qmode == QMODE_NF4 ? BK / 2 : 0);   // code bytes per row and K chunk
     // A decode batch with at most two rows per loaded adapter (on average) takes the
     // CUDA-core shrink: its adapters are read once each, with no split-K reduction.
     const bool gemv = decode && shrink && gemv_shrink_fits(d, T) && a.n_loaded > 0 && T <= 2 * a.n_loaded;
@@ -1104,7 +1230,15 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     }
 
     CUtensorMap tmW, tmX, tmV;
-    {
+    if (a.qmode) {
+        // the codes as bytes {din / (8 / bits), dout}; boxes of one K chunk x 128 rows
+        cuuint64_t dims[2] = {(cuuint64_t)d.din / (BK / q_x), (cuuint64_t)d.dout};
+        cuuint64_t strides[1] = {(cuuint64_t)(d.din / (BK / q_x))};
+        cuuint32_t box[2] = {(cuuint32_t)q_x, (cuuint32_t)BM};
+        if (!tc_encode_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, 2, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)d.dout};
         cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
         cuuint32_t box[2] = {BK, decode ? (cuuint32_t)BM : 256u};
@@ -1157,9 +1291,10 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.push = (p.splits > 1 && N <= PUSH_MAX_N && N % p.splits == 0) ? 1 : 0;
     p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
     const int rx_bytes = p.push ? BM * N * 4 : 0;
-    p.stages = clamp_stages((budget - rx_bytes) / (pkc * stage_bytes(N)));
+    const int sbytes = pkc * stage_bytes(N) + BM * q_x;   // (over codes, the code tile too)
+    p.stages = clamp_stages((budget - rx_bytes) / sbytes);
     p.a_sub = A_BYTES;
-    p.ring_bytes = p.stages * pkc * stage_bytes(N);
+    p.ring_bytes = p.stages * sbytes;
     p.rx_off = p.ring_bytes;
     p.tail_off = p.ring_bytes + rx_bytes;
     p.tcap = d.tcap;
@@ -1174,6 +1309,10 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.max_chunks = d.max_chunks;
     p.stamps = a.stamps;
     p.stamp_cap = a.stamp_cap;
+    p.qmode = a.qmode;
+    p.q_x = q_x;
+    p.qscale = a.qscale;
+    for (int i = 0; i < 16; ++i) p.qcb[i] = a.qcb[i];
     return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p), st, true,
                     p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
 }

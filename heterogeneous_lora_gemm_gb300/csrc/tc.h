@@ -48,7 +48,16 @@ struct TcForwardArgs {
     int n_loaded;           // loaded slots
     unsigned long long* stamps;   // profiling records of the kernels' CTAs (NULL = off)
     int stamp_cap;
+    // decode projection over a quantized W (W unused): 1 int8 codes [dout x din] with an
+    // fp32 scale per row (qscale [dout]); 2 4-bit codes [dout x din/2] (even column in the
+    // low nibble) with an fp32 scale per row and 64 columns (qscale [din/64][dout]) and
+    // the 16-entry codebook qcb.  Needs T <= 256 and din % 64 == 0 (tc_quantized_fits).
+    int qmode;
+    const void* Wq;
+    const float* qscale;
+    float qcb[16];
 };
+bool tc_quantized_fits(const PoolDims& d, int T);
 
 // Shrink on the CUDA cores for decode batches over many adapters with a few rows each
 // (shrink_gemv.cu): one CTA per chunk of the pool plus the segment builder's CTA.
@@ -81,6 +90,8 @@ cudaError_t launch_merge_quant_tc(int8_t* Wq, float* row_scale, uint32_t* row_ma
 // Encodes a bf16 tensor map (used by both tensor-core translation units).
 bool tc_encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                const cuuint32_t* box, CUtensorMapSwizzle sw);
+bool tc_encode_typed(CUtensorMap* map, CUtensorMapDataType type, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw);
 cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st);
 
 }  // namespace mlora

@@ -6,7 +6,10 @@
 // the weight tiles in flight stay in L2).  Warp 0 issues TMA loads into a 4-stage
 // ring, warp 1 issues the MMAs into one of two TMEM accumulators (2 x 256
 // columns), and warps 2-5 drain the other accumulator to bf16 Y while the next
-// tile is being multiplied.  As in the decode kernel, the K loop of every tile is
+// tile is being multiplied.  The raster walks all weight tiles for a group of token
+// tiles whose X tiles together take about 40 MB, so that they stay in L2 while the
+// weight streams past: W is read once per group (groups of 8 token tiles re-read it
+// from DRAM once per 1024 tokens, three times the algorithmic bytes in all).  As in the decode kernel, the K loop of every tile is
 // din columns of X W^T followed by the K-extension over the loaded adapters'
 // chunks (ai-infra-kb "M031" §02), so each row's delta is added to its own output
 // row before the single rounding.  A tile multiplies only the chunks the shrink
@@ -32,7 +35,8 @@ constexpr int PB_BYTES = PN * PK * 2;           // 32 KiB
 constexpr int PSTAGE = PA_BYTES + PB_BYTES;     // 48 KiB
 constexpr int PSTAGES = 4;
 constexpr int P_THREADS = 192;
-constexpr int GROUP_M = 8;
+constexpr int GROUP_MIN = 8;                    // token tiles per raster group, at least
+constexpr size_t GROUP_X_BYTES = 40u << 20;     // X bytes of one raster group, about
 constexpr int EXT_SUB = 4;
 
 struct PrefillParams {
@@ -44,14 +48,15 @@ struct PrefillParams {
     int n_chunks, max_chunks;
     int ext_steps;              // K-extension steps per tile (EXT_SUB chunks each), 0 without adapters
     int pdl;    // launched while the shrink may still run: wait before reading its outputs
+    int group_m;   // token tiles per raster group
     unsigned long long* stamps;   // profiling records (NULL = off), see ptx::stamp_record
     int stamp_cap;
 };
 
-__device__ __forceinline__ void tile_coords(int i, int m_tiles, int n_tiles, int& m, int& n) {
-    const int per_group = GROUP_M * n_tiles;
-    const int first_m = (i / per_group) * GROUP_M;
-    const int gm = min(m_tiles - first_m, GROUP_M);
+__device__ __forceinline__ void tile_coords(int i, int m_tiles, int n_tiles, int group_m, int& m, int& n) {
+    const int per_group = group_m * n_tiles;
+    const int first_m = (i / per_group) * group_m;
+    const int gm = min(m_tiles - first_m, group_m);
     const int r = i % per_group;
     m = first_m + r % gm;
     n = r / gm;
@@ -116,7 +121,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         int armed[PSTAGES] = {0, 0, 0, 0};
         for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
             int m, n;
-            tile_coords(tile, p.m_tiles, p.n_tiles, m, n);
+            tile_coords(tile, p.m_tiles, p.n_tiles, p.group_m, m, n);
             for (int i = 0; i < steps; ++i) {
                 if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) break;
                 ++armed[s];
@@ -226,7 +231,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
         int local = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++local) {
             int m, n;
-            tile_coords(tile, p.m_tiles, p.n_tiles, m, n);
+            tile_coords(tile, p.m_tiles, p.n_tiles, p.group_m, m, n);
             const int buf = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             const bool got = mbar_wait(&tfull[buf], use & 1, abort_flag, p.status);
@@ -305,6 +310,13 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
     p.ext_steps = after_shrink ? (p.n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
     p.vec_store = (d.dout % 8 == 0) ? 1 : 0;
     p.pdl = after_shrink ? 1 : 0;
+    {
+        const size_t per_tile = (size_t)PM * d.din * 2;
+        size_t g = GROUP_X_BYTES / (per_tile > 0 ? per_tile : 1);
+        g = g < (size_t)GROUP_MIN ? (size_t)GROUP_MIN : g;
+        p.group_m = (int)(g < (size_t)p.m_tiles ? g : (size_t)p.m_tiles);
+        if (p.group_m < 1) p.group_m = 1;
+    }
     p.stamps = a.stamps;
     p.stamp_cap = a.stamp_cap;
     const int total = p.m_tiles * p.n_tiles;

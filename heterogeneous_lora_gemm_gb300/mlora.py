@@ -70,6 +70,9 @@ _SIGNATURES = {
     "mlora_dequantize": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "mlora_forward_quantized": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P]),
     "mlora_merge_quantized": (_I, [_P, _P, _P, _I, _P]),
+    "mlora_dequantize_nf4": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "mlora_forward_nf4": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _P, _P]),
+    "mlora_merge_nf4": (_I, [_P, _P, _P, _P, _I, _P]),
     "mlora_pool_status": (_I, [_P, _P]),
     "mlora_pool_info": (_I, [_P, ctypes.POINTER(PoolInfo)]),
     "mlora_debug_segments": (_I, [_P, _P, _I, _P, _P, _P]),
@@ -232,6 +235,20 @@ def mlora_debug_noalloc_expire_wait(cycles: int, stream: int) -> None:
     check(lib().mlora_debug_noalloc_expire_wait(int(cycles), stream or None), "mlora_debug_noalloc_expire_wait")
 
 
+def _codebook(values) -> "ctypes.Array":
+    """16 floats as a C array (host memory, copied by the callee)."""
+    vals = [float(v) for v in values]
+    if len(vals) != 16:
+        raise ValueError("a codebook has 16 values")
+    return (ctypes.c_float * 16)(*vals)
+
+
+def mlora_dequantize_nf4(codes_ptr: int, absmax_ptr: int, codebook, dout: int, din: int, dtype: int, W_ptr: int,
+                         stream: int) -> None:
+    check(lib().mlora_dequantize_nf4(codes_ptr, absmax_ptr, _codebook(codebook), dout, din, dtype, W_ptr,
+                                     stream or None), "mlora_dequantize_nf4")
+
+
 # ---- torch-facing convenience ------------------------------------------- #
 def _stream_handle(stream) -> int:
     import torch
@@ -316,6 +333,19 @@ class Pool:
     def merge_quantized(self, Wq, row_scale, slot: int, stream=None) -> None:
         check(lib().mlora_merge_quantized(self.handle, Wq.data_ptr(), row_scale.data_ptr(), slot,
                                           _stream_handle(stream)), "mlora_merge_quantized")
+
+    def forward_nf4(self, X, codes, absmax, codebook, W_scratch, row_adapter, Y, stream=None) -> None:
+        """The dynamic branch over an NF4 base (codes uint8 [dout x din/2], absmax fp32
+        [din/64 x dout], codebook: 16 host floats)."""
+        ra = None if row_adapter is None else row_adapter.data_ptr()
+        cb = _codebook(codebook)
+        check(lib().mlora_forward_nf4(self.handle, X.data_ptr(), codes.data_ptr(), absmax.data_ptr(), cb,
+                                      None if W_scratch is None else W_scratch.data_ptr(), ra, int(X.shape[0]),
+                                      Y.data_ptr(), _stream_handle(stream)), "mlora_forward_nf4")
+
+    def merge_nf4(self, codes, absmax, codebook, slot: int, stream=None) -> None:
+        check(lib().mlora_merge_nf4(self.handle, codes.data_ptr(), absmax.data_ptr(), _codebook(codebook), slot,
+                                    _stream_handle(stream)), "mlora_merge_nf4")
 
     def status(self, stream=None) -> int:
         return mlora_pool_status(self.handle, _stream_handle(stream))

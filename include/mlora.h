@@ -238,9 +238,12 @@ mlora_status mlora_unmerge(mlora_pool_t pool, void* W, int slot, mlora_stream_t 
  *
  * mlora_dequantize: W = Wq * row_scale, rounded once to `dtype`, into the caller's
  *   buffer W [dout x din] (device).  Wq and W 16-byte aligned.  Errors: INVALID_ARG, CUDA.
- * mlora_forward_quantized: the dynamic LoRA branch over the restored base: dequantizes
- *   into W_scratch (device [dout x din], pool dtype, caller-owned) and runs
- *   mlora_forward on it.  Arguments otherwise as mlora_forward.
+ * mlora_forward_quantized: the dynamic LoRA branch over the restored base.  A bf16 pool
+ *   with T <= 256 and din a multiple of 64 reads the codes in its projection kernel
+ *   (each W tile restored in shared memory: the same values as mlora_dequantize, half
+ *   the bytes of a bf16 W; W_scratch unused, may be NULL); otherwise it dequantizes into
+ *   W_scratch (device [dout x din], pool dtype, caller-owned) and runs mlora_forward on
+ *   it.  Arguments otherwise as mlora_forward.
  * mlora_merge_quantized: the merge on a quantized base, in place: restore each row,
  *   add scale * Up Down (fp32), then quantize the merged row again: new
  *   row_scale[o] = max_i |w[o,i]| / 127 (fp32; 0 for an all-zero row), codes
@@ -260,6 +263,39 @@ mlora_status mlora_forward_quantized(mlora_pool_t pool, const void* X, const voi
                                      void* W_scratch, const int32_t* row_adapter, int T, void* Y,
                                      mlora_stream_t stream);
 mlora_status mlora_merge_quantized(mlora_pool_t pool, void* Wq, float* row_scale, int slot, mlora_stream_t stream);
+
+/*
+ * NF4 base weight (M031 §05: the logical matrix is W restored by scale and codebook;
+ * the page names the NF4 codebook): 4-bit codes with an fp32 absmax per output row and
+ * block of 64 input columns and a 16-entry codebook,
+ *   W[o,i] = codebook[code[o,i]] * absmax[i / 64][o]
+ *   codes    device uint8 [dout x din/2]: column 2m of a row in the low nibble of byte
+ *            m, column 2m+1 in the high nibble; 16-byte aligned
+ *   absmax   device fp32 [din/64][dout] (block-major: one block's rows adjacent)
+ *   codebook HOST fp32 [16], copied at the call (e.g. the NormalFloat values)
+ * din must be a multiple of 64.
+ *
+ * mlora_dequantize_nf4: W = codebook[code] * absmax, rounded once to `dtype`, into the
+ *   caller's W [dout x din] (device, 16-byte aligned).  Errors: INVALID_ARG, CUDA.
+ * mlora_forward_nf4: the dynamic LoRA branch over the restored base.  A bf16 pool with
+ *   T <= 256 reads the codes in its projection kernel (each W tile restored in shared
+ *   memory, the same values as mlora_dequantize_nf4; W_scratch unused, may be NULL);
+ *   otherwise W_scratch (device [dout x din], pool dtype) receives the restored W and
+ *   mlora_forward runs on it.  Arguments otherwise as mlora_forward.
+ * mlora_merge_nf4: the merge on an NF4 base, in place: per row and block, restore
+ *   (fp32 codebook value * absmax), add scale * sum_k Up[o,k] Down[k,i] (fp32), take the
+ *   block's new absmax = max |w|, and give each w / absmax (fp32) the code of the
+ *   nearest codebook value (the lower code on a tie).  The codebook must be ascending
+ *   and hold 0 (an all-zero block keeps absmax 0).  Errors: INVALID_ARG, BAD_SLOT,
+ *   NOT_LOADED, CUDA.
+ */
+mlora_status mlora_dequantize_nf4(const void* codes, const float* absmax, const float* codebook, int dout, int din,
+                                  mlora_dtype dtype, void* W, mlora_stream_t stream);
+mlora_status mlora_forward_nf4(mlora_pool_t pool, const void* X, const void* codes, const float* absmax,
+                               const float* codebook, void* W_scratch, const int32_t* row_adapter, int T, void* Y,
+                               mlora_stream_t stream);
+mlora_status mlora_merge_nf4(mlora_pool_t pool, void* codes, float* absmax, const float* codebook, int slot,
+                             mlora_stream_t stream);
 
 /*
  * Synchronizes `stream`, then reads and clears the pool's device status word.

@@ -394,21 +394,38 @@ def test_load_waits_for_last_reader_and_versions():
 
 # --------------------------------------------------------------------------- #
 # quantized base (M031 §05)
-def test_forward_over_a_quantized_base():
-    """The dynamic branch over an int8 base: the restored W (codes x row scale, one
-    rounding) under the usual forward; both against the oracle."""
-    layer = wl.random_layer(51, T=40, din=256, dout=192, ranks=[16, 8])
+@pytest.mark.parametrize("T,din,dout,ranks", [
+    (40, 256, 192, [16, 8]),          # decode: the projection reads the codes (push reduction)
+    (200, 1024, 640, [16] * 120),     # decode, many adapters (CUDA-core shrink), staged reduction
+    (300, 256, 192, [16, 8]),         # prefill: restore pass into W_scratch, then the forward
+    (40, 136, 192, [16, 8]),          # din not a multiple of 64: restore pass
+])
+def test_forward_over_a_quantized_base(T, din, dout, ranks):
+    """The dynamic branch over an int8 base (codes x row scale, one rounding of the
+    restored value): against the oracle over the restored W, and against the restore
+    pass followed by the ordinary forward."""
+    layer = wl.random_layer(51, T=T, din=din, dout=dout, ranks=ranks)
     codes, scale = oracle.quantize(layer.W_f64)
     pool = make_pool(layer)
     X, _, ra, Y = upload(layer)
     Wq, sc = torch.from_numpy(codes).cuda(), torch.from_numpy(scale).cuda()
-    W_scratch = torch.empty((layer.dout, layer.din), dtype=torch.bfloat16, device="cuda")
+    W_scratch = torch.zeros((layer.dout, layer.din), dtype=torch.bfloat16, device="cuda")
     pool.forward_quantized(X, Wq, sc, W_scratch, ra, Y)
     torch.cuda.synchronize()
     Wd = oracle.dequantize(codes, scale)
-    assert_within(to_f64(W_scratch), Wd, "bf16", "restored base")
-    assert_within(to_f64(Y), oracle.forward(layer.X_f64, Wd, layer.row_adapter, ora_adapters(layer)), "bf16",
-                  "forward over the quantized base")
+    want = oracle.forward(layer.X_f64, Wd, layer.row_adapter, ora_adapters(layer))
+    assert_within(to_f64(Y), want, "bf16", "forward over the quantized base")
+    W_rest = torch.empty_like(W_scratch)
+    mlora.mlora_dequantize(Wq.data_ptr(), sc.data_ptr(), dout, din, mlora.MLORA_BF16, W_rest.data_ptr(), 0)
+    Y2 = torch.empty_like(Y)
+    pool.forward(X, W_rest, ra, Y2)
+    torch.cuda.synchronize()
+    assert_within(to_f64(W_rest), Wd, "bf16", "restored base")
+    assert_within(to_f64(Y), to_f64(Y2), "bf16", "codes read by the projection vs restore + forward")
+    if T <= 256 and din % 64 == 0:
+        assert torch.count_nonzero(W_scratch) == 0   # the decode path does not use the scratch
+    else:
+        assert torch.equal(W_scratch, W_rest)
     assert pool.status() == mlora.MLORA_OK
 
 
