@@ -645,11 +645,36 @@ def run_extras(calls, L, stream, dev, peaks):
                                                      stream=stream), 20 * qn)
     mq_us = t_us(lambda k: c0.pool.merge_quantized(Wqs[k % qn], scs[k % qn], a0.slot, stream=stream), 20 * qn)
     n_w = L.dout * L.din
+    fwd_us = t_us(lambda k: c0.pool.forward(c0.X, calls[k % len(calls)].W, c0.ra, c0.Y, stream=stream),
+                  20 * len(calls))
+    fq_bytes = n_w + 4 * L.dout + L.T * (L.din + L.dout) * 2 + sum(a.rank for a in L.adapters) * L.dout * 2
     out["quantized"] = {"dequantize_us": dq_us, "dequantize_gbs": (3 * n_w + 4 * L.dout) / dq_us / 1e3,
-                        "forward_quantized_us": fq_us, "merge_quantized_us": mq_us,
+                        "forward_quantized_us": fq_us, "forward_bf16_us": fwd_us,
+                        "forward_quantized_frac": fq_bytes / fq_us / 1e3 / peaks["hbm_gbs"],
+                        "merge_quantized_us": mq_us,
                         "merge_quantized_gbs": (2 * n_w + 8 * L.dout) / mq_us / 1e3,
-                        "base": "int8 codes, fp32 scale per output row"}
+                        "base": "int8 codes, fp32 scale per output row; the decode projection reads the codes",
+                        "copies": qn}
     del Wqs, scs, scratch
+
+    # NF4 base (4-bit codes, fp32 absmax per row and 64 columns, the NormalFloat codebook)
+    cb = wl.nf4_codebook()
+    packed, absmax = wl.nf4_random_base(0, L.dout, L.din)
+    Q4 = [torch.from_numpy(packed).to(dev) for _ in range(qn)]
+    A4 = [torch.from_numpy(absmax).to(dev) for _ in range(qn)]
+    f4_us = t_us(lambda k: c0.pool.forward_nf4(c0.X, Q4[k % qn], A4[k % qn], cb, None, c0.ra, c0.Y, stream=stream),
+                 20 * qn)
+    Wr = torch.empty_like(c0.W)
+    d4_us = t_us(lambda k: mlora.mlora_dequantize_nf4(Q4[k % qn].data_ptr(), A4[k % qn].data_ptr(), cb, L.dout, L.din,
+                                                       mlora.MLORA_BF16, Wr.data_ptr(), stream.cuda_stream), 20 * qn)
+    m4_us = t_us(lambda k: c0.pool.merge_nf4(Q4[k % qn], A4[k % qn], cb, a0.slot, stream=stream), 20 * qn)
+    f4_bytes = n_w // 2 + n_w // 64 * 4 + L.T * (L.din + L.dout) * 2 + sum(a.rank for a in L.adapters) * L.dout * 2
+    out["nf4"] = {"forward_nf4_us": f4_us, "forward_nf4_frac": f4_bytes / f4_us / 1e3 / peaks["hbm_gbs"],
+                  "dequantize_nf4_us": d4_us, "dequantize_nf4_gbs": (n_w // 2 + n_w // 16 + 2 * n_w) / d4_us / 1e3,
+                  "merge_nf4_us": m4_us, "merge_nf4_gbs": (n_w + n_w // 8) / m4_us / 1e3,
+                  "base": "4-bit codes, fp32 absmax per row and 64 columns, NormalFloat codebook; "
+                          "the decode projection reads the codes", "copies": qn}
+    del Q4, A4, Wr
 
     src = L.adapters[0]
     ppool = Pool(L.max_slots + 1, sum((a.rank + 7) // 8 * 8 for a in L.adapters) + 3 * 16,
@@ -826,6 +851,8 @@ def run_ours(args, dist, rank, local):
             el, tok = reduce_job(dist, sub["ms_per_step"] * args.steps / 1e3, args.steps * L.T)
             head = dict(sub)
             head["value"], head["ms_per_step"] = tok / el, el / args.steps * 1e3
+            if args.workload == "decode_step" and not args.no_extras:
+                head.update(run_extras(calls, L, stream, dev, peaks))
             head["dtype"] = L.dtype
             head["e2e"] = None
             host0, L_single = None, (L, None)
@@ -834,7 +861,8 @@ def run_ours(args, dist, rank, local):
            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic",
            "config": dict(config_of(args.workload, args.seed, args.layers), parallelism=f"replicas x{args.gpus}")}
-    for k in ("timing", "roofline", "other_kernels", "step_roofline", "per_projection", "e2e", "gpu_launches"):
+    for k in ("timing", "roofline", "other_kernels", "step_roofline", "per_projection", "e2e", "gpu_launches",
+              "merge", "quantized", "nf4", "prefetch"):
         if k in head:
             out[k] = head[k]
     out["clocks"] = clocks
