@@ -184,7 +184,7 @@ mlora_status wait_readers(mlora_pool* p) {
 
 mlora_status push_slot(mlora_pool* p, int slot) {
     const SlotHost& h = p->slots[slot];
-    SlotRec rec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit};
+    SlotRec rec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit, 0};   // chunk0: set by push_chunks
     CU_TRY(cudaMemcpyAsync(p->d_slots + slot, &rec, sizeof rec, cudaMemcpyHostToDevice, p->copy_stream));
     // the staging object above lives on this stack frame: finish before returning
     CU_TRY(cudaStreamSynchronize(p->copy_stream));
@@ -220,16 +220,31 @@ mlora_status build_chunks(mlora_pool* p, std::vector<ChunkRec>& host) {
     return MLORA_OK;
 }
 
+// The slot table's records, each with the index of its slot's first chunk in `chunks`
+// (a slot's chunks are consecutive there: its units are contiguous and the table is
+// in arena order).
+void slot_records(const mlora_pool* p, const std::vector<ChunkRec>& chunks, SlotRec* out) {
+    for (int s = 0; s < p->max_slots; ++s) {
+        const SlotHost& h = p->slots[s];
+        out[s] = SlotRec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit, 0};
+    }
+    for (int c = (int)chunks.size() - 1; c >= 0; --c) out[chunks[c].slot].chunk0 = c;
+}
+
 mlora_status push_chunks(mlora_pool* p) {
     std::vector<ChunkRec> host;
     mlora_status st = build_chunks(p, host);
     if (st != MLORA_OK) return st;
-    if (!host.empty()) {
+    std::vector<SlotRec> recs((size_t)(p->max_slots > 0 ? p->max_slots : 1));
+    slot_records(p, host, recs.data());
+    if (p->max_slots > 0)
+        CU_TRY(cudaMemcpyAsync(p->d_slots, recs.data(), sizeof(SlotRec) * (size_t)p->max_slots,
+                               cudaMemcpyHostToDevice, p->copy_stream));
+    if (!host.empty())
         CU_TRY(cudaMemcpyAsync(p->d_chunks, host.data(), sizeof(ChunkRec) * host.size(), cudaMemcpyHostToDevice,
                                p->copy_stream));
-        // the staging vector lives on this stack frame: finish before returning
-        CU_TRY(cudaStreamSynchronize(p->copy_stream));
-    }
+    // the staging vectors live on this stack frame: finish before returning
+    CU_TRY(cudaStreamSynchronize(p->copy_stream));
     return MLORA_OK;
 }
 
@@ -286,10 +301,7 @@ mlora_status push_tables_async(mlora_pool* p, int set) {
     p->stage_next = (p->stage_next + 1) % (int)p->stages.size();
     if (sg.pending) CU_TRY(cudaEventSynchronize(sg.done));
     SlotRec* recs = reinterpret_cast<SlotRec*>(sg.buf);
-    for (int s = 0; s < p->max_slots; ++s) {
-        const SlotHost& h = p->slots[s];
-        recs[s] = SlotRec{h.rank, h.rpad, h.scale, h.unit < 0 ? 0 : h.unit};
-    }
+    slot_records(p, chunks, recs);
     ChunkRec* cr = reinterpret_cast<ChunkRec*>(sg.buf + p->slots_bytes);
     std::copy(chunks.begin(), chunks.end(), cr);
     CU_TRY(cudaMemcpyAsync(p->set_slots[set], sg.buf, p->slots_bytes + sizeof(ChunkRec) * chunks.size(),

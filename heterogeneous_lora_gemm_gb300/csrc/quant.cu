@@ -361,57 +361,75 @@ dequant_nf4_kernel(const uint8_t* __restrict__ q, const float* __restrict__ absm
     }
 }
 
-// The merge on an NF4 base, in place: one warp per (row o, block of 64 columns); lane l
-// owns columns 2l and 2l+1 (one byte of codes).  Restore (fp32 codebook value times
-// the block's absmax), add scale * sum_k Up[o,k] Down[k,i] (fp32, k ascending), take
-// the block's new absmax, and give each w / absmax (fp32 division) the code of the
-// nearest codebook value (fp32 distances, the first of equal ones).
+// The merge on an NF4 base, in place.  One CTA per (block of 64 columns, 64 rows): the
+// block's Down columns and the rows' Up values go to shared memory once (fp32); each
+// warp then takes 8 rows, lane l columns 2l and 2l+1 (one byte of codes).  Restore
+// (fp32 codebook value times the block's absmax), add scale * sum_k Up[o,k] Down[k,i]
+// (fp32, k ascending), take the block's new absmax, and give each w / absmax (fp32
+// division) the code of the nearest codebook value (fp32 distances, the first of equal
+// ones).
+constexpr int MN4_ROWS = 64;
+
 template <typename E>
 __global__ void __launch_bounds__(256)
 merge_nf4_kernel(uint8_t* __restrict__ q, float* __restrict__ absmax, Codebook cb, const SlotRec* __restrict__ slots,
                  int slot, const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout) {
+    extern __shared__ float mn4_s[];   // [rank][64] Down columns, then [64 rows][rank] Up
     __shared__ float cb_s[16];
-    if (threadIdx.x < 16) cb_s[threadIdx.x] = cb.v[threadIdx.x];
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const size_t warp_id = (blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5;
-    const int nb = din / NF4_BLOCK;
-    if (warp_id >= (size_t)dout * nb) return;
-    const int o = (int)(warp_id / nb), blk = (int)(warp_id % nb);
     const SlotRec rec = slots[slot];
-    const int i = blk * NF4_BLOCK + 2 * lane;
-    uint8_t* qb = q + (size_t)o * (din / 2) + blk * (NF4_BLOCK / 2) + lane;
-    float* am = absmax + (size_t)blk * dout + o;
-    const uint32_t byte = *qb;
-    const float old = *am;
-    float w0 = cb_s[byte & 15u] * old, w1 = cb_s[byte >> 4] * old;
-    float u0 = 0.f, u1 = 0.f;
-    const E* down = arena_down + (size_t)rec.unit * din + i;
-    for (int k = 0; k < rec.rank; ++k) {
-        const float up = as_f32(arena_up[up_index(rec.unit, k, o, dout)]);
-        u0 = fmaf(up, as_f32(down[(size_t)k * din]), u0);
-        u1 = fmaf(up, as_f32(down[(size_t)k * din + 1]), u1);
+    const int rank = rec.rank;
+    const int blk = blockIdx.x, o0 = blockIdx.y * MN4_ROWS;
+    const int nr = min(MN4_ROWS, dout - o0);
+    float* down_s = mn4_s;
+    float* up_s = mn4_s + (size_t)rank * NF4_BLOCK;
+    if (threadIdx.x < 16) cb_s[threadIdx.x] = cb.v[threadIdx.x];
+    const E* down = arena_down + (size_t)rec.unit * din + blk * NF4_BLOCK;
+    for (int idx = threadIdx.x; idx < rank * NF4_BLOCK; idx += blockDim.x) {
+        const int k = idx / NF4_BLOCK, c = idx % NF4_BLOCK;
+        down_s[idx] = as_f32(down[(size_t)k * din + c]);
     }
-    w0 = w0 + rec.scale * u0;
-    w1 = w1 + rec.scale * u1;
-    float m = fmaxf(fabsf(w0), fabsf(w1));
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-    auto code_of = [&](float w) {
-        const float v = m > 0.f ? w / m : 0.f;
-        int best = 0;
-        float bd = fabsf(v - cb_s[0]);
-        for (int j = 1; j < 16; ++j) {
-            const float dj = fabsf(v - cb_s[j]);
-            if (dj < bd) {
-                bd = dj;
-                best = j;
-            }
+    for (int idx = threadIdx.x; idx < MN4_ROWS * rank; idx += blockDim.x) {
+        const int r = idx / rank, k = idx % rank;
+        up_s[idx] = r < nr ? as_f32(arena_up[up_index(rec.unit, k, o0 + r, dout)]) : 0.f;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int r = warp; r < nr; r += blockDim.x / 32) {
+        const int o = o0 + r;
+        uint8_t* qb = q + (size_t)o * (din / 2) + blk * (NF4_BLOCK / 2) + lane;
+        float* am = absmax + (size_t)blk * dout + o;
+        const uint32_t byte = *qb;
+        const float old = *am;
+        float w0 = cb_s[byte & 15u] * old, w1 = cb_s[byte >> 4] * old;
+        float u0 = 0.f, u1 = 0.f;
+        const float* ur = up_s + (size_t)r * rank;
+        for (int k = 0; k < rank; ++k) {
+            const float up = ur[k];
+            const float2 dk = *reinterpret_cast<const float2*>(down_s + k * NF4_BLOCK + 2 * lane);
+            u0 = fmaf(up, dk.x, u0);
+            u1 = fmaf(up, dk.y, u1);
         }
-        return (uint32_t)best;
-    };
-    *qb = (uint8_t)(code_of(w0) | (code_of(w1) << 4));
-    if (lane == 0) *am = m;
+        w0 = w0 + rec.scale * u0;
+        w1 = w1 + rec.scale * u1;
+        float m = fmaxf(fabsf(w0), fabsf(w1));
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+        auto code_of = [&](float w) {
+            const float v = m > 0.f ? w / m : 0.f;
+            int best = 0;
+            float bd = fabsf(v - cb_s[0]);
+            for (int j = 1; j < 16; ++j) {
+                const float dj = fabsf(v - cb_s[j]);
+                if (dj < bd) {
+                    bd = dj;
+                    best = j;
+                }
+            }
+            return (uint32_t)best;
+        };
+        *qb = (uint8_t)(code_of(w0) | (code_of(w1) << 4));
+        if (lane == 0) *am = m;
+    }
 }
 
 }  // namespace
@@ -438,15 +456,22 @@ cudaError_t launch_merge_nf4(bool bf16, uint8_t* q, float* absmax, const float* 
                              cudaStream_t st) {
     Codebook cb;
     for (int j = 0; j < 16; ++j) cb.v[j] = codebook[j];
-    const size_t warps = (size_t)d.dout * (d.din / NF4_BLOCK);
-    const size_t blocks = (warps * 32 + 255) / 256;
-    if (blocks == 0) return cudaSuccess;
-    if (bf16)
-        merge_nf4_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
+    if (d.dout == 0 || d.din == 0) return cudaSuccess;
+    // shared memory for the largest rank the pool takes: Down [rank][64] and Up [64][rank], fp32
+    const size_t smem = sizeof(float) * (size_t)d.max_rank * (NF4_BLOCK + MN4_ROWS);
+    const dim3 grid((unsigned)(d.din / NF4_BLOCK), (unsigned)((d.dout + MN4_ROWS - 1) / MN4_ROWS));
+    cudaError_t e;
+    if (bf16) {
+        e = cudaFuncSetAttribute(merge_nf4_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        merge_nf4_kernel<__nv_bfloat16><<<grid, 256, smem, st>>>(
             q, absmax, cb, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din, d.dout);
-    else
-        merge_nf4_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(q, absmax, cb, slots, slot, (const float*)arena_down,
-                                                                 (const float*)arena_up, d.din, d.dout);
+    } else {
+        e = cudaFuncSetAttribute(merge_nf4_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        merge_nf4_kernel<float><<<grid, 256, smem, st>>>(q, absmax, cb, slots, slot, (const float*)arena_down,
+                                                       (const float*)arena_up, d.din, d.dout);
+    }
     return cudaGetLastError();
 }
 

@@ -108,7 +108,7 @@ constexpr int CHUNKS_PER_TILE = BM / CHUNK;     // shrink: 8 chunks of 16 rank r
 constexpr int CHUNK_BYTES = CHUNK * BK * 2;     // 2 KiB: 16 rank rows x 64 din columns of Down
 constexpr int MAX_SPLITS = 16;     // K splits per tile at most
 constexpr int MAX_CLUSTER = 8;     // K splits of a tile reduced inside one (portable) cluster
-constexpr int MAX_STAGES = 8;
+constexpr int MAX_STAGES = 12;
 constexpr int EXT_CAP = 256;       // projection: K-extension chunks of a CTA kept in shared memory
 constexpr int MAX_SLOT_WORDS = 4096 / 32;
 constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
@@ -123,7 +123,7 @@ __host__ __device__ constexpr int stage_bytes(int n) { return A_BYTES + b_bytes(
 struct Tail {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
-    uint64_t conv[MAX_STAGES];        // projection over codes: the stage's W tile is converted
+    uint64_t conv[MAX_STAGES];        // projection over codes: the stage's W tile is restored
     uint64_t acc_full;
     uint64_t info_ready;              // projection: the K-extension chunk info is in place
     uint64_t rx_bar;                  // projection, push reduction: all splits' slices have landed
@@ -641,7 +641,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         for (int i = 0; i < n_steps; ++i) {
             const bool din_step = !(i >= ins_m && i < ins_m + ne_m);
             if (!SHRINK && p.qmode && din_step) {
-                // the converting warps saw the stage land and restored its W tile
+                // the epilogue warps saw the stage land and restored its W tile from the codes
                 if (!mbar_wait(&tl.conv[s], (cph >> s) & 1u, abort_flag, p.status)) break;
                 cph ^= 1u << s;
             } else if (!mbar_wait(&tl.full[s], ph, abort_flag, p.status)) {
@@ -703,6 +703,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const float sc = p.qmode == QMODE_NF4
                                          ? (o < p.dout ? __ldg(p.qscale + (size_t)kb * p.dout + o) : 0.f)
                                          : row_sc;
+                    // every din step is waited for in order (the MMA waits for this warp's
+                    // release), so the parity never runs a phase ahead
                     const bool got = mbar_wait(&tl.full[s], ph, abort_flag, p.status);
                     __syncwarp();
                     if (!__all_sync(0xffffffffu, got)) break;
@@ -1114,10 +1116,14 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
     if (a.qmode && !(decode && d.din % BK == 0)) return cudaErrorInvalidValue;
     DecodeShape ds = decode_shape(d, decode ? N : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE);
-    if (a.qmode) {   // over codes: one K chunk per stage (the code tile is one 2D box)
+    if (a.qmode) {
+        // over codes: one K chunk per stage (the code tile is one 2D box); a stage also
+        // holds the restored 16 KiB W tile, which comes from no load, so a deeper ring
+        // keeps as many code bytes in flight as the bf16 path keeps W bytes
         ds.pkc = 1;
         ds.ksteps = kb_total;
         ds.splits = ds.splits < kb_total ? ds.splits : kb_total;
+        if (ds.budget == PROJ_SMEM_BUDGET || ds.budget == PROJ_SMEM_BUDGET_SHARED) ds.budget = PROJ_SMEM_BUDGET_ALONE;
     }
     const int q_x = a.qmode == QMODE_INT8 ? BK : (a.qmode == QMODE_NF4 ? BK / 2 : 0);   // code bytes per row and K chunk
     // A decode batch with at most two rows per loaded adapter (on average) takes the
