@@ -114,6 +114,7 @@ constexpr int MAX_SLOT_WORDS = 4096 / 32;
 constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
 constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
 constexpr int PROJ_KC = 2;         // projection: K chunks of 64 per pipeline step (one 3D box each for W and X)
+constexpr int PROJ_ZT_N = 128;     // projection: tokens per token tile of a decode batch above this size
 constexpr int QMODE_INT8 = 1, QMODE_NF4 = 2;
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
@@ -304,7 +305,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
     constexpr int kStampKind = SHRINK ? STAMP_SHRINK : STAMP_PROJECTION;
-    const int tok0 = ztile * MAX_N;                  // first token of this token tile
+    const int tok0 = ztile * p.N;                    // first token of this token tile
     const int T = min(p.T - tok0, p.N);              // tokens in this tile
 
     if (SHRINK) {
@@ -445,7 +446,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 #pragma unroll
         for (int i = 0; i < MAX_N / 32; ++i) {
             const int t = lane + 32 * i;
-            av[i] = t < T ? p.row_adapter[t] : -1;
+            av[i] = t < T ? p.row_adapter[tok0 + t] : -1;
         }
         const int c0 = eu0 * EXT_SUB;
         const int nx = min((eu1 - eu0) * EXT_SUB, EXT_CAP);
@@ -484,7 +485,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // projection: final write of rows r0..r0+3 (a multiple of 4) of token t
     auto emit4 = [&](int t, int r0, const float4& v) {
         const int o0 = tile * BM + r0;
-        __nv_bfloat16* y = p.Y + (size_t)t * p.dout + o0;
+        __nv_bfloat16* y = p.Y + (size_t)(tok0 + t) * p.dout + o0;
         if (p.dout % 4 == 0 && o0 + 4 <= p.dout) {
             __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
             __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
@@ -527,8 +528,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int i = 0; i < pre; ++i) {
                 uint8_t* b = smem + (size_t)i * SB + A_STAGE;
                 mbar_expect_tx(&tl.full[i], (uint32_t)(p.kc * B_SUB));
-                if (p.kc > 1) tma_3d(b, &tmX, &tl.full[i], 0, 0, (kb0 + i) * p.kc);
-                else tma_2d(b, &tmX, &tl.full[i], (kb0 + i) * BK, 0);
+                if (p.kc > 1) tma_3d(b, &tmX, &tl.full[i], 0, tok0, (kb0 + i) * p.kc);
+                else tma_2d(b, &tmX, &tl.full[i], (kb0 + i) * BK, tok0);
             }
             issued = pre;
             s = pre % NS;
@@ -562,16 +563,16 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)(BM * p.q_x + B_SUB));
                 tma_2d(a + Q_OFF, &tmW, &tl.full[s], kb * p.q_x, tile * BM);
-                tma_2d(b, &tmX, &tl.full[s], kb * BK, 0);
+                tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
             } else if (!ext) {
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)SB);
                 if (p.kc > 1) {   // kc K chunks of W (128 rows) and of X (N tokens), one box each
                     tma_3d(a, &tmW, &tl.full[s], 0, tile * BM, kb * p.kc);
-                    tma_3d(b, &tmX, &tl.full[s], 0, 0, kb * p.kc);
+                    tma_3d(b, &tmX, &tl.full[s], 0, tok0, kb * p.kc);
                 } else {
                     tma_2d(a, &tmW, &tl.full[s], kb * BK, tile * BM);
-                    tma_2d(b, &tmX, &tl.full[s], kb * BK, 0);
+                    tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
                 }
             } else {
                 const int u = eu0 + (i - ins);
@@ -612,7 +613,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         waited = true;
                     }
                     mbar_expect_tx(&tl.full[s], (uint32_t)B_SUB);
-                    tma_3d(b, &tmV, &tl.full[s], 0, 0, u * EXT_SUB);
+                    tma_3d(b, &tmV, &tl.full[s], 0, tok0, u * EXT_SUB);
                 }
             }
             if (++s == NS) {
@@ -736,7 +737,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     for (int j = 0; j < 16; ++j) v[j] = 0.f;
                 if (o < p.dout)
                     for (int j = 0; j < 16 && t0 + j < T; ++j)
-                        p.Y[(size_t)(t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
+                        p.Y[(size_t)(tok0 + t0 + j) * p.dout + o] = __float2bfloat16_rn(v[j]);
             }
         } else if (!SHRINK && p.push) {
             // Push reduction.  Stage this split's partial tile [token][row] in its idle
@@ -1065,8 +1066,8 @@ struct DecodeShape {
     int ksteps;   // pipeline steps over din
 };
 
-DecodeShape decode_shape(const PoolDims& d, int N, int budget1) {
-    const int tiles = proj_tiles(d);
+DecodeShape decode_shape(const PoolDims& d, int N, int budget1, int zt) {
+    const int tiles = proj_tiles(d) * zt;   // (row tile, token tile) pairs
     const int kb_total = (d.din + BK - 1) / BK;
     // K splits of a tile: as many as fill the SMs with one CTA each (a power of two);
     // when that leaves a quarter of the SMs idle (few row tiles, long K), two CTAs per
@@ -1115,7 +1116,14 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     cudaError_t e;
     const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
     if (a.qmode && !(decode && d.din % BK == 0)) return cudaErrorInvalidValue;
-    DecodeShape ds = decode_shape(d, decode ? N : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE);
+    // A decode batch of more than 128 tokens runs its projection as token tiles of 128
+    // (grid z): half the K splits per row tile, and a split's partial tile half as
+    // large, for the same number of CTAs.  The token tiles of a row tile read the same
+    // W slice at about the same time, so W is fetched from DRAM about once.  Over
+    // codes every token tile would restore the W tile again: one tile there.
+    const int zt = (decode && !a.qmode && N > PROJ_ZT_N) ? (T + PROJ_ZT_N - 1) / PROJ_ZT_N : 1;
+    const int Np = zt > 1 ? PROJ_ZT_N : N;               // token rows per projection tile
+    DecodeShape ds = decode_shape(d, decode ? Np : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE, zt);
     if (a.qmode) {
         // over codes: one K chunk per stage (the code tile is one 2D box); a stage also
         // holds the restored 16 KiB W tile, which comes from no load, so a deeper ring
@@ -1139,11 +1147,11 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         // ring there; a larger one shares SMs with the projection, both rings smaller
         const int stiles = (n_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
         const int shrink_ctas = (stiles + 1) * cluster_splits(k_splits(stiles, kb_total, N, false));
-        if (shrink_ctas <= sm_count() - proj_tiles(d) * ds.splits) {
+        if (shrink_ctas <= sm_count() - proj_tiles(d) * zt * ds.splits) {
             shrink_budget = SHRINK_SMEM_BUDGET_APART;
         } else {
             shrink_budget = SHRINK_SMEM_BUDGET_SHARED;
-            ds = decode_shape(d, N, PROJ_SMEM_BUDGET_SHARED);
+            ds = decode_shape(d, Np, PROJ_SMEM_BUDGET_SHARED, zt);
         }
     }
 
@@ -1253,13 +1261,13 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)T};
         cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
-        cuuint32_t box[2] = {BK, (cuuint32_t)N};
+        cuuint32_t box[2] = {BK, (cuuint32_t)Np};
         if (!tc_encode(&tmX, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
         cuuint64_t dims[3] = {(cuuint64_t)CHUNK, (cuuint64_t)d.tcap, (cuuint64_t)d.max_chunks};
         cuuint64_t strides[2] = {(cuuint64_t)CHUNK * 2, (cuuint64_t)d.tcap * CHUNK * 2};
-        cuuint32_t box[3] = {CHUNK, (cuuint32_t)N, EXT_SUB};
+        cuuint32_t box[3] = {CHUNK, (cuuint32_t)Np, EXT_SUB};
         if (!tc_encode(&tmV, a.ws.vt, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
     }
 
@@ -1275,7 +1283,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         cuuint32_t wbox[3] = {BK, (cuuint32_t)BM, (cuuint32_t)pkc};
         if (!tc_encode(&tmW, a.W, 3, wdims, strides, wbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
         cuuint64_t xdims[3] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)kb_total};
-        cuuint32_t xbox[3] = {BK, (cuuint32_t)N, (cuuint32_t)pkc};
+        cuuint32_t xbox[3] = {BK, (cuuint32_t)Np, (cuuint32_t)pkc};
         if (!tc_encode(&tmX, a.X, 3, xdims, strides, xbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     GemmParams p{};
@@ -1287,17 +1295,17 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.status = a.ws.status;
     p.T = T;
     p.dout = d.dout;
-    p.N = N;
+    p.N = Np;
     p.kc = pkc;
     p.ksteps = ds.ksteps;
     p.n_chunks = n_chunks;
     p.ext_units = shrink ? (n_chunks + EXT_SUB - 1) / EXT_SUB : 0;
     p.splits = ds.splits;
     // small batches: the splits push their partial slices into a receive buffer
-    p.push = (p.splits > 1 && N <= PUSH_MAX_N && N % p.splits == 0) ? 1 : 0;
+    p.push = (p.splits > 1 && Np <= PUSH_MAX_N && Np % p.splits == 0) ? 1 : 0;
     p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
-    const int rx_bytes = p.push ? BM * N * 4 : 0;
-    const int sbytes = pkc * stage_bytes(N) + BM * q_x;   // (over codes, the code tile too)
+    const int rx_bytes = p.push ? BM * Np * 4 : 0;
+    const int sbytes = pkc * stage_bytes(Np) + BM * q_x;   // (over codes, the code tile too)
     p.stages = clamp_stages((budget - rx_bytes) / sbytes);
     p.a_sub = A_BYTES;
     p.ring_bytes = p.stages * sbytes;
@@ -1319,7 +1327,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.q_x = q_x;
     p.qscale = a.qscale;
     for (int i = 0; i < 16; ++i) p.qcb[i] = a.qcb[i];
-    return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p), st, true,
+    return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, zt), dim3(NUM_THREADS), smem_bytes(p), st, true,
                     p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
 }
 

@@ -131,6 +131,8 @@ def test_stack7b_projection(module):
     (129, 4096, 256, [16, 64, 8]),
     (5, 8, 8, [3, 5]),
     (64, 1024, 5120, [16, 8]),     # 40 row tiles: 6 K splits, two CTAs per SM
+    (200, 512, 384, [16, 8, 64]),  # two token tiles of the projection, the second ragged (72)
+    (250, 64, 128, [8, 16]),       # two token tiles, one K step, no K split
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_ragged_shapes(T, din, dout, ranks, dtype):
