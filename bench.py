@@ -402,6 +402,8 @@ def timed_steps(calls, per_step: int, steps: int, warmup: int, stream, dev, cloc
     wq, wr = divmod(max(warmup, 3), big)
     g_wbig = g_big if g_big is not None else capture(big, rec)
     g_wrest = capture(wr, rec) if wr > 0 else None
+    for p in pools.values():                     # later eager calls record nothing
+        p.profile_stamps(None, 0)
     with torch.cuda.stream(stream):
         for _ in range(wq):
             g_wbig.replay()

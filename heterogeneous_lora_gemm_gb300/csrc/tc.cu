@@ -413,7 +413,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             tl.tile_chunks = __popc(m);
             tl.win_u0 = u0;
         }
-        if (split == 0 && lane < CHUNKS_PER_TILE && cb + lane < p.n_chunks)
+        if (p.tmask && split == 0 && lane < CHUNKS_PER_TILE && cb + lane < p.n_chunks)
             p.tmask[(size_t)ztile * p.max_chunks + cb + lane] = (uint8_t)((m >> lane) & 1u);
     }
     // A block barrier needs converged warps: lanes that skipped a one-thread branch
@@ -1116,11 +1116,13 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     cudaError_t e;
     const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
     if (a.qmode && !(decode && d.din % BK == 0)) return cudaErrorInvalidValue;
-    // A decode batch of more than 128 tokens runs its projection as token tiles of 128
-    // (grid z): half the K splits per row tile, and a split's partial tile half as
-    // large, for the same number of CTAs.  The token tiles of a row tile read the same
-    // W slice at about the same time, so W is fetched from DRAM about once.  Over
-    // codes every token tile would restore the W tile again: one tile there.
+    // A decode batch of more than 128 tokens runs its shrink and its projection as token
+    // tiles of 128 (grid z): half the K splits per row tile, and a split's partial tile
+    // half as large, for the same number of CTAs.  The token tiles of a row tile read
+    // the same W slice at about the same time, so W is fetched from DRAM about once.
+    // Over codes every token tile would restore the W tile again: one tile there.  Both
+    // kernels tile alike: a token tile's projection reads the Vt of exactly the chunks
+    // whose slots its own tokens use, which its shrink tile wrote.
     const int zt = (decode && !a.qmode && N > PROJ_ZT_N) ? (T + PROJ_ZT_N - 1) / PROJ_ZT_N : 1;
     const int Np = zt > 1 ? PROJ_ZT_N : N;               // token rows per projection tile
     DecodeShape ds = decode_shape(d, decode ? Np : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE, zt);
@@ -1146,7 +1148,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         // a shrink whose CTAs fit the SMs that the projection leaves idle gets a larger
         // ring there; a larger one shares SMs with the projection, both rings smaller
         const int stiles = (n_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
-        const int shrink_ctas = (stiles + 1) * cluster_splits(k_splits(stiles, kb_total, N, false));
+        const int shrink_ctas = (stiles + 1) * zt * cluster_splits(k_splits(stiles * zt, kb_total, Np, false));
         if (shrink_ctas <= sm_count() - proj_tiles(d) * zt * ds.splits) {
             shrink_budget = SHRINK_SMEM_BUDGET_APART;
         } else {
@@ -1157,17 +1159,17 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
 
     // ---- shrink: Vt = masked scale * Down_chunks X^T, per token tile, the used chunks
     if (shrink && !gemv) {
-        const int Ns = decode ? (T + 15) / 16 * 16 : MAX_N;
+        const int Ns = decode ? Np : MAX_N;
         CUtensorMap tmXs, tmNone, tmDown;
         std::memset(&tmNone, 0, sizeof tmNone);
         const int tiles = (n_chunks + CHUNKS_PER_TILE - 1) / CHUNKS_PER_TILE;
-        const int ztiles = token_tiles(T);
+        const int ztiles = decode ? zt : token_tiles(T);
         GemmParams g{};
         g.chunks = a.ws.chunks;
         g.row_adapter = a.row_adapter;
         g.slots = a.slots;
         g.vt = (__nv_bfloat16*)a.ws.vt;
-        g.tmask = a.ws.tmask;
+        g.tmask = decode ? nullptr : a.ws.tmask;   // (the prefill projection reads it)
         g.partials = a.ws.partials;
         g.tile_ctr = a.ws.tile_ctr;
         g.status = a.ws.status;
