@@ -133,6 +133,8 @@ def test_stack7b_projection(module):
     (64, 1024, 5120, [16, 8]),     # 40 row tiles: 6 K splits, two CTAs per SM
     (200, 512, 384, [16, 8, 64]),  # two token tiles of the projection, the second ragged (72)
     (250, 64, 128, [8, 16]),       # two token tiles, one K step, no K split
+    (100, 256, 7200, [16, 8]),     # 57 row tiles (odd), two K splits, ragged last tile
+    (256, 256, 3600, [16, 64]),    # two token tiles over 29 row tiles, ragged last tile
 ])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_ragged_shapes(T, din, dout, ranks, dtype):
@@ -399,6 +401,7 @@ def test_load_waits_for_last_reader_and_versions():
 @pytest.mark.parametrize("T,din,dout,ranks", [
     (40, 256, 192, [16, 8]),          # decode: the projection reads the codes (push reduction)
     (200, 1024, 640, [16] * 120),     # decode, many adapters (CUDA-core shrink), staged reduction
+    (128, 512, 7200, [16, 8]),        # decode, 57 row tiles (odd), two K splits
     (300, 256, 192, [16, 8]),         # prefill: restore pass into W_scratch, then the forward
     (40, 136, 192, [16, 8]),          # din not a multiple of 64: restore pass
 ])
