@@ -933,7 +933,7 @@ mlora_status mlora_forward_quantized(mlora_pool_t p, const void* X, const void* 
     if (!p) return fail(MLORA_ERR_INVALID_ARG, "pool is NULL");
     if (T < 0 || T > p->max_tokens) return fail(MLORA_ERR_INVALID_ARG, "T %d not in [0, %d]", T, p->max_tokens);
     if (T == 0) return MLORA_OK;
-    if (p->dtype == MLORA_BF16 && tc_quantized_fits(p->dims, T)) {
+    if (p->dtype == MLORA_BF16 && tc_quantized_fits(p->dims, T, false)) {
         // decode-sized batch: the projection reads the codes and restores each W tile in
         // shared memory (no restore pass over W; W_scratch is not used)
         if (!X || !Wq || !row_scale || !Y) return fail(MLORA_ERR_INVALID_ARG, "X/Wq/row_scale/Y is NULL");
@@ -993,11 +993,13 @@ mlora_status mlora_forward_nf4(mlora_pool_t p, const void* X, const void* codes,
     if (p->din % 64 != 0) return fail(MLORA_ERR_INVALID_ARG, "din %d must be a multiple of 64", p->din);
     if (!aligned16(X) || !aligned16(codes) || !aligned16(Y))
         return fail(MLORA_ERR_INVALID_ARG, "X/codes/Y must be 16-byte aligned");
-    if (p->dtype == MLORA_BF16 && tc_quantized_fits(p->dims, T)) {
+    if (p->dtype == MLORA_BF16 && tc_quantized_fits(p->dims, T, true) && aligned16(absmax)) {
         const QuantW q{2, codes, absmax, codebook};
         return forward_impl(p, X, nullptr, row_adapter, T, Y, stream, &q);
     }
-    if (!W_scratch) return fail(MLORA_ERR_INVALID_ARG, "W_scratch is NULL (needed unless bf16 and T <= 256)");
+    if (!W_scratch)
+        return fail(MLORA_ERR_INVALID_ARG, "W_scratch is NULL (needed unless bf16, T <= 256, dout %% 4 == 0 and absmax "
+                                           "16-byte aligned)");
     DeviceGuard g(p->device);
     if (g.err != cudaSuccess) return cuda_fail(g.err, "cudaSetDevice");
     mlora_status st = mlora_dequantize_nf4(codes, absmax, codebook, p->dout, p->din, p->dtype, W_scratch, stream);

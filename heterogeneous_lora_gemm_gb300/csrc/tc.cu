@@ -145,7 +145,6 @@ struct Tail {
     int ext_unit[EXT_CAP];            // projection: arena unit of each K-extension chunk, -1 = skip
     int ext_slot[EXT_CAP];
     unsigned long long t_start;       // profiling: globaltimer at the CTA's start
-    float qcb[16];                    // projection over 4-bit codes: the codebook
 };
 
 struct GemmParams {
@@ -187,6 +186,7 @@ struct GemmParams {
     int q_x;                        // code bytes per row and K chunk of 64 columns
     const float* qscale;            // QMODE_INT8: [dout]; QMODE_NF4: [din / 64][dout]
     float qcb[16];                  // QMODE_NF4: the codebook
+    int qtab_off;                   // QMODE_NF4: shared-memory offset of the codebook (16 floats)
 };
 
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
@@ -237,34 +237,85 @@ __device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng,
     }
 }
 
-// A code as a float without a conversion instruction: 2^23 + 128 + c holds c + 128 in
-// its low mantissa bits.
-__device__ __forceinline__ float code_f32(int8_t c) { return __int_as_float(0x4B000000 + 128 + (int)c) - 8388736.f; }
+// Two values bf16(v0 * sc), bf16(v1 * sc) (v0 in the low half): the products in fp32,
+// one rounding each, two lanes per instruction; with bias, v = f + bias first (exact
+// for the code floats below).
+__device__ __forceinline__ uint32_t scaled_pair_bf16(uint32_t f0, uint32_t f1, float bias, float sc) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 t, b, s;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 t, {%1, %2};\n\t"
+        "mov.b64 b, {%3, %3};\n\t"
+        "mov.b64 s, {%4, %4};\n\t"
+        "add.rn.f32x2 t, t, b;\n\t"
+        "mul.rn.f32x2 t, t, s;\n\t"
+        "mov.b64 {lo, hi}, t;\n\t"
+        "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "r"(f0), "r"(f1), "f"(bias), "f"(sc));
+    return r;
+}
+__device__ __forceinline__ uint32_t scaled_pair_bf16(float2 v, float sc) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 t, s;\n\t.reg .f32 lo, hi;\n\t"
+        "mov.b64 t, {%1, %2};\n\t"
+        "mov.b64 s, {%3, %3};\n\t"
+        "mul.rn.f32x2 t, t, s;\n\t"
+        "mov.b64 {lo, hi}, t;\n\t"
+        "cvt.rn.bf16x2.f32 %0, hi, lo;\n\t}"
+        : "=r"(r)
+        : "f"(v.x), "f"(v.y), "f"(sc));
+    return r;
+}
 
 // One row of a stage's W tile restored from its codes: 64 columns of bf16(code value *
 // scale) -- the value and the single rounding of the restore kernels -- written as the
 // 128-byte row `row` of a K-major tile with the 128-byte swizzle (16-byte chunk j of the
 // row at position j ^ (row % 8)), the layout a TMA load of a bf16 W tile leaves.  The
 // 16-byte reads start at a row-dependent chunk to spread shared-memory banks.
+// int8: the code byte c becomes the float 2^23 + 128 + c by a byte permutation (its
+// low mantissa bits), and c exactly by subtracting 2^23 + 128.  NF4: the row's 16
+// restored values bf16(codebook[i] * scale) are formed once per K block and kept as
+// byte tables in registers (low bytes, high bytes); byte permutations then look up
+// four codes at a time, no per-code arithmetic and no memory access.
 __device__ __forceinline__ void restore_row(const uint8_t* codes, uint8_t* arow, int row, float sc, int qmode,
-                                            const float* cb) {
+                                            const float* qcb) {
     const int sw = row & 7;
     if (qmode == QMODE_INT8) {
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
             const int j = (jj + row) & 3;   // codes of columns 16j .. 16j+15
-            const int4 raw = *reinterpret_cast<const int4*>(codes + 16 * j);
-            const int8_t* c = reinterpret_cast<const int8_t*>(&raw);
+            const uint4 raw = *reinterpret_cast<const uint4*>(codes + 16 * j);
+            const uint32_t wd[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
+                                    raw.w ^ 0x80808080u};   // bytes c + 128
             uint32_t w[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(code_f32(c[2 * e]) * sc, code_f32(c[2 * e + 1]) * sc);
-                w[e] = *reinterpret_cast<uint32_t*>(&h);
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t f0 = __byte_perm(wd[e], 0x4B000000u, 0x7540), f1 = __byte_perm(wd[e], 0x4B000000u, 0x7541);
+                const uint32_t f2 = __byte_perm(wd[e], 0x4B000000u, 0x7542), f3 = __byte_perm(wd[e], 0x4B000000u, 0x7543);
+                w[2 * e] = scaled_pair_bf16(f0, f1, -8388736.f, sc);
+                w[2 * e + 1] = scaled_pair_bf16(f2, f3, -8388736.f, sc);
             }
             *reinterpret_cast<uint4*>(arow + (((2 * j) ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(arow + (((2 * j + 1) ^ sw) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
     } else {
+        uint32_t lo_t[4], hi_t[4];   // lo_t[j] byte e: low byte of value 4j + e; hi_t: high bytes
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 c4 = reinterpret_cast<const float4*>(qcb)[j];
+            const uint32_t p0 = scaled_pair_bf16(make_float2(c4.x, c4.y), sc);
+            const uint32_t p1 = scaled_pair_bf16(make_float2(c4.z, c4.w), sc);
+            lo_t[j] = __byte_perm(p0, p1, 0x6420);
+            hi_t[j] = __byte_perm(p0, p1, 0x7531);
+        }
+        // the values of four codes given one per byte (0..15): their low and high bytes
+        auto lookup4 = [&](uint32_t nb, uint32_t& lob, uint32_t& hib) {
+            const uint32_t v = nb & 0x07070707u;
+            const uint32_t sel = __byte_perm(v | (v >> 4), 0u, 0x0020);   // nibble k: code k mod 8
+            const uint32_t m = ((nb >> 3) & 0x01010101u) * 0xFFu;         // byte k all ones: code k >= 8
+            lob = (__byte_perm(lo_t[0], lo_t[1], sel) & ~m) | (__byte_perm(lo_t[2], lo_t[3], sel) & m);
+            hib = (__byte_perm(hi_t[0], hi_t[1], sel) & ~m) | (__byte_perm(hi_t[2], hi_t[3], sel) & m);
+        };
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
             const int j = (jj + row) & 1;   // codes of columns 32j .. 32j+31, two per byte
@@ -272,14 +323,14 @@ __device__ __forceinline__ void restore_row(const uint8_t* codes, uint8_t* arow,
             const uint32_t b4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {   // 16-byte chunk 4j + q: columns 32j + 8q .. +7
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t byte = (b4[q] >> (8 * e)) & 0xFFu;
-                    __nv_bfloat162 h = __floats2bfloat162_rn(cb[byte & 15u] * sc, cb[byte >> 4] * sc);
-                    w[e] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                *reinterpret_cast<uint4*>(arow + (((4 * j + q) ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+                uint32_t le, he, lo, ho;   // even columns (low nibbles), odd columns (high nibbles)
+                lookup4(b4[q] & 0x0F0F0F0Fu, le, he);
+                lookup4((b4[q] >> 4) & 0x0F0F0F0Fu, lo, ho);
+                const uint32_t t1 = __byte_perm(le, he, 0x5140), t2 = __byte_perm(lo, ho, 0x5140);   // columns 0,2 / 1,3
+                const uint32_t t3 = __byte_perm(le, he, 0x7362), t4 = __byte_perm(lo, ho, 0x7362);   // columns 4,6 / 5,7
+                *reinterpret_cast<uint4*>(arow + (((4 * j + q) ^ sw) * 16)) =
+                    make_uint4(__byte_perm(t1, t2, 0x5410), __byte_perm(t1, t2, 0x7632), __byte_perm(t3, t4, 0x5410),
+                               __byte_perm(t3, t4, 0x7632));
             }
         }
     }
@@ -291,7 +342,7 @@ template <bool SHRINK>
 __global__ void __launch_bounds__(NUM_THREADS, 2)
 swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmArena,
-                   GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmQs, GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Tail& tl = *reinterpret_cast<Tail*>(smem + p.tail_off);
@@ -300,7 +351,11 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int B_SUB = b_bytes(p.N);                  // bytes of the B operand per K chunk
     const int A_STAGE = p.kc * p.a_sub;
     const int Q_OFF = A_STAGE + p.kc * B_SUB;        // projection over codes: the code tile (kc == 1)
-    const int SB = Q_OFF + (!SHRINK && p.qmode ? BM * p.q_x : 0);
+    // over 4-bit codes the stage also holds the K block's 128 fp32 scales
+    const int QS_OFF = Q_OFF + BM * p.q_x;
+    const int Q_BYTES = BM * p.q_x + (p.qmode == QMODE_NF4 ? BM * 4 : 0);   // bytes of the codes (+ scales)
+    // (stages start on 1024-byte swizzle atoms)
+    const int SB = (!SHRINK && p.qmode) ? (Q_OFF + Q_BYTES + 1023) & ~1023 : Q_OFF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
@@ -350,10 +405,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (!SHRINK && p.push) mbar_expect_tx(&tl.rx_bar, (uint32_t)(BM * p.N * 4));   // every split's slice
         if (!SHRINK) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+        if (!SHRINK && p.qmode == QMODE_NF4) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmQs) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
         if (SHRINK || p.ext_units > 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmArena) : "memory");
     }
-    if (!SHRINK && p.qmode == QMODE_NF4 && threadIdx.x < 16) tl.qcb[threadIdx.x] = p.qcb[threadIdx.x];
+    if (!SHRINK && p.qmode == QMODE_NF4 && threadIdx.x < 16)   // the codebook of the 4-bit restore
+        reinterpret_cast<float*>(smem + p.qtab_off)[threadIdx.x] = p.qcb[threadIdx.x];
     if (warp == 1) {
         __syncwarp();
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tl.tmem_slot)),
@@ -516,8 +573,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 uint8_t* a = smem + (size_t)i * SB;
                 tl.stage_kind[i] = -1;
                 if (p.qmode) {
-                    mbar_expect_tx_only(&tl.full[i], (uint32_t)(BM * p.q_x));
+                    mbar_expect_tx_only(&tl.full[i], (uint32_t)Q_BYTES);
                     tma_2d(a + Q_OFF, &tmW, &tl.full[i], (kb0 + i) * p.q_x, tile * BM);
+                    if (p.qmode == QMODE_NF4) tma_2d(a + QS_OFF, &tmQs, &tl.full[i], tile * BM, kb0 + i);
                 } else {
                     mbar_expect_tx_only(&tl.full[i], (uint32_t)A_STAGE);
                     if (p.kc > 1) tma_3d(a, &tmW, &tl.full[i], 0, tile * BM, (kb0 + i) * p.kc);
@@ -561,8 +619,9 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             } else if (!ext && p.qmode) {
                 // the code tile and X; the epilogue warps restore the bf16 W tile from the codes
                 tl.stage_kind[s] = -1;
-                mbar_expect_tx(&tl.full[s], (uint32_t)(BM * p.q_x + B_SUB));
+                mbar_expect_tx(&tl.full[s], (uint32_t)(Q_BYTES + B_SUB));
                 tma_2d(a + Q_OFF, &tmW, &tl.full[s], kb * p.q_x, tile * BM);
+                if (p.qmode == QMODE_NF4) tma_2d(a + QS_OFF, &tmQs, &tl.full[s], tile * BM, kb);
                 tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
             } else if (!ext) {
                 tl.stage_kind[s] = -1;
@@ -700,17 +759,16 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             uint32_t ph = 0;
             for (int i = 0; i < n_steps; ++i) {
                 if (!(i >= ins_c && i < ins_c + ne_c)) {
-                    const int kb = kb0 + (i < ins_c ? i : i - ne_c);
-                    const float sc = p.qmode == QMODE_NF4
-                                         ? (o < p.dout ? __ldg(p.qscale + (size_t)kb * p.dout + o) : 0.f)
-                                         : row_sc;
                     // every din step is waited for in order (the MMA waits for this warp's
                     // release), so the parity never runs a phase ahead
                     const bool got = mbar_wait(&tl.full[s], ph, abort_flag, p.status);
                     __syncwarp();
                     if (!__all_sync(0xffffffffu, got)) break;
                     uint8_t* stg = smem + (size_t)s * SB;
-                    restore_row(stg + Q_OFF + row * p.q_x, stg + row * 128, row, sc, p.qmode, tl.qcb);
+                    // (4-bit codes: the row's scale of this K block came with the codes)
+                    const float sc = p.qmode == QMODE_NF4 ? reinterpret_cast<const float*>(stg + QS_OFF)[row] : row_sc;
+                    restore_row(stg + Q_OFF + row * p.q_x, stg + row * 128, row, sc, p.qmode,
+                                reinterpret_cast<const float*>(smem + p.qtab_off));
                     fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
                     __syncwarp();
                     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tl.conv[s]))
@@ -1048,7 +1106,10 @@ bool tc_encode_arena_maps(TcArenaMaps* m, void* arena_down, void* arena_up, int 
            tc_encode(&m->up256, arena_up, 3, dims, strides, box256, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-bool tc_quantized_fits(const PoolDims& d, int T) { return T >= 1 && T <= MAX_N && d.din % BK == 0; }
+bool tc_quantized_fits(const PoolDims& d, int T, bool nf4) {
+    // 4-bit codes: the block scales come by TMA (rows of 16-byte multiples)
+    return T >= 1 && T <= MAX_N && d.din % BK == 0 && (!nf4 || d.dout % 4 == 0);
+}
 
 bool tc_supported(const PoolDims& d, int T) {
     (void)d;
@@ -1241,11 +1302,21 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         // first kernel of the forward: it may launch while the stream's previous kernel
         // runs, and waits for it before reading X or the row map
         e = launch_k(swapab_gemm_kernel<true>, dim3(tiles + 1, g.splits, ztiles), dim3(NUM_THREADS), smem_bytes(g),
-                     st, true, g.cluster ? g.splits : 1, tmNone, tmXs, tmNone, tmDown, g);
+                     st, true, g.cluster ? g.splits : 1, tmNone, tmXs, tmNone, tmDown, tmNone, g);
         if (e != cudaSuccess) return e;
     }
 
-    CUtensorMap tmW, tmX, tmV;
+    CUtensorMap tmW, tmX, tmV, tmQs;
+    std::memset(&tmQs, 0, sizeof tmQs);
+    if (a.qmode == QMODE_NF4) {
+        // the block scales [din / 64][dout] fp32: boxes of 128 rows of one K block
+        cuuint64_t dims[2] = {(cuuint64_t)d.dout, (cuuint64_t)(d.din / BK)};
+        cuuint64_t strides[1] = {(cuuint64_t)d.dout * 4};
+        cuuint32_t box[2] = {(cuuint32_t)BM, 1};
+        if (!tc_encode_typed(&tmQs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.qscale, 2, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
     if (a.qmode) {
         // the codes as bytes {din / (8 / bits), dout}; boxes of one K chunk x 128 rows
         cuuint64_t dims[2] = {(cuuint64_t)d.din / (BK / q_x), (cuuint64_t)d.dout};
@@ -1307,12 +1378,15 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.push = (p.splits > 1 && Np <= PUSH_MAX_N && Np % p.splits == 0) ? 1 : 0;
     p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
     const int rx_bytes = p.push ? BM * Np * 4 : 0;
-    const int sbytes = pkc * stage_bytes(Np) + BM * q_x;   // (over codes, the code tile too)
-    p.stages = clamp_stages((budget - rx_bytes) / sbytes);
+    // (over codes, the code tile too, and over 4-bit codes the K block's scales)
+    const int sbytes = (pkc * stage_bytes(Np) + BM * q_x + (a.qmode == QMODE_NF4 ? BM * 4 : 0) + 1023) & ~1023;
+    const int qtab_bytes = a.qmode == QMODE_NF4 ? 64 : 0;
+    p.stages = clamp_stages((budget - rx_bytes - qtab_bytes) / sbytes);
     p.a_sub = A_BYTES;
     p.ring_bytes = p.stages * sbytes;
     p.rx_off = p.ring_bytes;
-    p.tail_off = p.ring_bytes + rx_bytes;
+    p.qtab_off = p.ring_bytes + rx_bytes;
+    p.tail_off = p.qtab_off + qtab_bytes;
     p.tcap = d.tcap;
     p.pdl = shrink ? 1 : 0;
     // Without a shrink the projection is the forward's first kernel: launched while the
@@ -1330,7 +1404,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.qscale = a.qscale;
     for (int i = 0; i < 16; ++i) p.qcb[i] = a.qcb[i];
     return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, zt), dim3(NUM_THREADS), smem_bytes(p), st, true,
-                    p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, p);
+                    p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, tmQs, p);
 }
 
 cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din, int dout, void* Y,
@@ -1379,7 +1453,7 @@ cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din
     p.pdl = 0;
     p.cluster = 0;   // the K splits meet through the given scratch
     return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, 1), dim3(NUM_THREADS), smem_bytes(p), st, false,
-                    1, tmW, tmX, tmNone, tmNone, p);
+                    1, tmW, tmX, tmNone, tmNone, tmNone, p);
 }
 
 }  // namespace mlora

@@ -51,13 +51,14 @@ struct TcForwardArgs {
     // decode projection over a quantized W (W unused): 1 int8 codes [dout x din] with an
     // fp32 scale per row (qscale [dout]); 2 4-bit codes [dout x din/2] (even column in the
     // low nibble) with an fp32 scale per row and 64 columns (qscale [din/64][dout]) and
-    // the 16-entry codebook qcb.  Needs T <= 256 and din % 64 == 0 (tc_quantized_fits).
+    // the 16-entry codebook qcb.  Needs T <= 256 and din % 64 == 0, and for 4-bit codes
+    // dout % 4 == 0 and qscale 16-byte aligned (tc_quantized_fits).
     int qmode;
     const void* Wq;
     const float* qscale;
     float qcb[16];
 };
-bool tc_quantized_fits(const PoolDims& d, int T);
+bool tc_quantized_fits(const PoolDims& d, int T, bool nf4);
 
 // Shrink on the CUDA cores for decode batches over many adapters with a few rows each
 // (shrink_gemv.cu): one CTA per chunk of the pool plus the segment builder's CTA.

@@ -278,8 +278,9 @@ mlora_status mlora_merge_quantized(mlora_pool_t pool, void* Wq, float* row_scale
  * mlora_dequantize_nf4: W = codebook[code] * absmax, rounded once to `dtype`, into the
  *   caller's W [dout x din] (device, 16-byte aligned).  Errors: INVALID_ARG, CUDA.
  * mlora_forward_nf4: the dynamic LoRA branch over the restored base.  A bf16 pool with
- *   T <= 256 reads the codes in its projection kernel (each W tile restored in shared
- *   memory, the same values as mlora_dequantize_nf4; W_scratch unused, may be NULL);
+ *   T <= 256, dout a multiple of 4 and absmax 16-byte aligned reads the codes (and the
+ *   block scales) in its projection kernel (each W tile restored in shared memory, the
+ *   same values as mlora_dequantize_nf4; W_scratch unused, may be NULL);
  *   otherwise W_scratch (device [dout x din], pool dtype) receives the restored W and
  *   mlora_forward runs on it.  Arguments otherwise as mlora_forward.
  * mlora_merge_nf4: the merge on an NF4 base, in place: per row and block, restore

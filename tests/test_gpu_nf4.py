@@ -40,6 +40,7 @@ def test_nf4_restore_matches_oracle(dtype):
     (40, 256, 192, [16, 8]),          # decode: the projection reads the codes (push reduction)
     (128, 1024, 640, [16] * 100),     # decode, many adapters (CUDA-core shrink), staged reduction
     (300, 256, 192, [16, 8]),         # prefill: restore pass into W_scratch, then the forward
+    (40, 256, 198, [16, 8]),          # decode, dout not a multiple of 4: restore pass (scales not by TMA)
 ])
 def test_forward_over_an_nf4_base(T, din, dout, ranks):
     cb = wl.nf4_codebook()
@@ -60,7 +61,7 @@ def test_forward_over_an_nf4_base(T, din, dout, ranks):
     pool.forward(X, W_rest, ra, Y2)
     torch.cuda.synchronize()
     assert_within(to_f64(Y), to_f64(Y2), "bf16", "codes read by the projection vs restore + forward")
-    if T <= 256:
+    if T <= 256 and dout % 4 == 0:   # the projection read the codes
         assert torch.count_nonzero(W_scratch) == 0
     else:
         assert torch.equal(W_scratch, W_rest)
