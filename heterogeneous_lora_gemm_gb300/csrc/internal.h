@@ -14,7 +14,7 @@ struct SlotRec {
     int32_t rpad;    // roundup(rank, 8): rank units the adapter holds
     float scale;
     int32_t unit;    // first rank unit in the arena (a multiple of 8)
-    int32_t chunk0;  // index of the slot's first chunk in the chunk table (its chunks follow)
+    int32_t chunk0;  // index of the slot's first chunk in the chunk table
 };
 
 // Arena layout, per rank unit u (one rank row of one adapter):

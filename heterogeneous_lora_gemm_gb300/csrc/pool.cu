@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <map>
 #include <cstdio>
@@ -193,8 +194,10 @@ mlora_status push_slot(mlora_pool* p, int slot) {
 
 // Rewrites the chunk table of the loaded slots after a load, unload or move (no
 // forward reads it meanwhile: every caller waited for the pool's last reader).
-// The table is in arena order, so that 8 consecutive chunks (one row tile of the
-// tensor-core shrink) usually lie in one window of at most 128 arena rows.
+// The table is in arena order within each module (output row range) of a fused
+// projection, modules in row order: 8 consecutive chunks (one row tile of the
+// tensor-core shrink) usually lie in one window of at most 128 arena rows, and the
+// K-extension units (4 consecutive chunks) of a row tile hold chunks of its own module.
 mlora_status build_chunks(mlora_pool* p, std::vector<ChunkRec>& host) {
     host.clear();
     for (int s = 0; s < p->max_slots; ++s) {
@@ -207,22 +210,27 @@ mlora_status build_chunks(mlora_pool* p, std::vector<ChunkRec>& host) {
                                     mod ? h.chunk_rows[j].first : 0, mod ? h.chunk_rows[j].second : p->dout});
         }
     }
-    std::sort(host.begin(), host.end(), [](const ChunkRec& x, const ChunkRec& y) { return x.unit < y.unit; });
+    std::sort(host.begin(), host.end(), [](const ChunkRec& x, const ChunkRec& y) {
+        return x.row0 != y.row0 ? x.row0 < y.row0 : x.unit < y.unit;
+    });
     if ((int)host.size() > p->dims.max_chunks)
         return fail(MLORA_ERR_CUDA, "chunk table overflow: %zu > %d", host.size(), p->dims.max_chunks);
     p->n_chunks = (int)host.size();
     p->tile_span = 0;
     for (size_t t0 = 0; t0 < host.size(); t0 += 8) {
+        // a window starts at the tile's first chunk: units must not decrease within the
+        // tile (they may where one module's chunks end and the next module's begin)
         const size_t t1 = (t0 + 8 < host.size() ? t0 + 8 : host.size()) - 1;
-        const int span = host[t1].unit + CHUNK - host[t0].unit;
+        int span = host[t1].unit + CHUNK - host[t0].unit;
+        for (size_t c = t0 + 1; c <= t1; ++c)
+            if (host[c].unit < host[c - 1].unit) span = INT_MAX;
         if (span > p->tile_span) p->tile_span = span;
     }
     return MLORA_OK;
 }
 
 // The slot table's records, each with the index of its slot's first chunk in `chunks`
-// (a slot's chunks are consecutive there: its units are contiguous and the table is
-// in arena order).
+// (the lowest; in a fused projection the slot's chunks of other modules come later).
 void slot_records(const mlora_pool* p, const std::vector<ChunkRec>& chunks, SlotRec* out) {
     for (int s = 0; s < p->max_slots; ++s) {
         const SlotHost& h = p->slots[s];

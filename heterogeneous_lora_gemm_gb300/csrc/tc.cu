@@ -143,7 +143,8 @@ struct Tail {
     int tile_ra[MAX_N];               // shrink: slot id of each token of the token tile
     uint32_t slot_bits[MAX_SLOT_WORDS];   // projection: slots some row of the batch uses
     int ext_unit[EXT_CAP];            // projection: arena unit of each K-extension chunk, -1 = skip
-    int ext_slot[EXT_CAP];
+    int ext_slot[EXT_CAP];            // (then: the K-extension units with a chunk to multiply)
+    int n_ext, ext_first;             // projection: this split's share of that list
     unsigned long long t_start;       // profiling: globaltimer at the CTA's start
 };
 
@@ -385,9 +386,21 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     const int kb0 = (int)((long long)split * p.ksteps / p.splits);
     const int kb1 = (int)((long long)(split + 1) * p.ksteps / p.splits);
-    const int eu0 = SHRINK ? 0 : (int)((long long)split * p.ext_units / p.splits);
-    const int eu1 = SHRINK ? 0 : (int)((long long)(split + 1) * p.ext_units / p.splits);
-    const int n_steps = (kb1 - kb0) + (eu1 - eu0);
+    // K-extension units (EXT_SUB consecutive chunks of the table): the first LU are
+    // listed per row tile (those with a chunk this tile and token tile use, divided
+    // evenly over the K splits); the units past them are split by index, all kept
+    constexpr int LU_CAP = EXT_CAP / EXT_SUB;
+    const int LU = SHRINK ? 0 : min(p.ext_units, LU_CAP);
+    const int xu = SHRINK ? 0 : p.ext_units - LU;
+    const int eu0 = LU + (int)((long long)split * xu / p.splits);
+    const int eu1 = LU + (int)((long long)(split + 1) * xu / p.splits);
+    // pipeline steps: the din steps, with the K-extension steps inserted at `ins`; how
+    // many of those run is known once the CTA's chunk list is built (info_ready)
+    const int nw = kb1 - kb0;
+    const int ins = max(0, nw - p.ext_lead);
+    const int ne0 = LU + (eu1 - eu0);   // K-extension steps at most (exactly once listed)
+    auto ext_steps = [&]() { return tl.n_ext + (eu1 - eu0); };
+    auto ext_unit_at = [&](int e) { return e < tl.n_ext ? tl.ext_slot[tl.ext_first + e] : eu0 + (e - tl.n_ext); };
     const uint32_t ncols = p.N <= 32 ? 32 : (p.N <= 64 ? 64 : (p.N <= 128 ? 128 : 256));
 
     if (threadIdx.x == 0) {
@@ -441,7 +454,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         }
         ChunkRec cr{-2, 0, 0, 0.f, 0, 0};
         if (lane < CHUNKS_PER_TILE && cb + lane < p.n_chunks) cr = p.chunks[cb + lane];
-        // the table is in arena order: the window of the tile starts at its first chunk
+        // the table is in arena order within the tile (window mode): the window of the
+        // tile starts at its first chunk
         const int u0 = __shfl_sync(0xffffffffu, cr.unit, 0);
         uint32_t m = 0;
 #pragma unroll
@@ -494,21 +508,22 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         return;
     }
 
-    if (warp == 2 && !SHRINK && eu1 > eu0) {
-        // While the producer streams W: the slots the batch uses, then this CTA's
-        // K-extension chunks, the arena unit of each chunk whose slot is used and -1
-        // for the others (never loaded).  The producer waits for it at its first
-        // K-extension step.
+    if (warp == 2 && !SHRINK && LU > 0) {
+        // While the producer streams W: the slots the batch uses, then the listed
+        // K-extension chunks, the arena unit of each chunk whose slot is used and whose
+        // rows meet this tile, -1 for the others (never loaded).  The producer waits for
+        // it at its first K-extension step.
         int av[MAX_N / 32];
 #pragma unroll
         for (int i = 0; i < MAX_N / 32; ++i) {
             const int t = lane + 32 * i;
             av[i] = t < T ? p.row_adapter[tok0 + t] : -1;
         }
-        const int c0 = eu0 * EXT_SUB;
-        const int nx = min((eu1 - eu0) * EXT_SUB, EXT_CAP);
-        for (int k = lane; k < nx; k += 32) {
-            const int c = c0 + k;
+        const int nx = LU * EXT_SUB;
+#pragma unroll
+        for (int it = 0; it < EXT_CAP / 32; ++it) {   // (all records requested at once)
+            const int k = lane + 32 * it, c = k;
+            if (k >= nx) continue;
             int sl = -1, un = -1;
             if (c < p.n_chunks) {
                 const ChunkRec cr = p.chunks[c];
@@ -528,6 +543,27 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         for (int k = lane; k < nx; k += 32) {
             const int sl = tl.ext_slot[k];
             if (sl < 0 || !((tl.slot_bits[sl >> 5] >> (sl & 31)) & 1u)) tl.ext_unit[k] = -1;
+        }
+        __syncwarp();
+        // The tile's K-extension steps: only the listed units with a chunk to multiply
+        // (a step with nothing to load would still cost a pipeline round trip), in
+        // table order, this split taking its share of them.
+        int n_all = 0;
+        for (int u0 = 0; u0 < LU; u0 += 32) {
+            const int uu = u0 + lane;
+            bool any = false;
+            if (uu < LU)
+#pragma unroll
+                for (int j = 0; j < EXT_SUB; ++j) any |= tl.ext_unit[uu * EXT_SUB + j] >= 0;
+            const unsigned m = __ballot_sync(0xffffffffu, any);
+            __syncwarp();   // (the list overwrites the slot ids read above)
+            if (any) tl.ext_slot[n_all + __popc(m & ((1u << lane) - 1u))] = uu;
+            n_all += __popc(m);
+        }
+        if (lane == 0) {
+            const int f0 = (int)((long long)split * n_all / p.splits);
+            tl.ext_first = f0;
+            tl.n_ext = (int)((long long)(split + 1) * n_all / p.splits) - f0;
         }
         __syncwarp();
         if (lane == 0) mbar_expect_tx(&tl.info_ready, 0);
@@ -593,14 +629,19 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             s = pre % NS;
             ph = pre == NS ? 1u : 0u;
         }
-        for (; issued < n_steps; ++issued) {
+        int ne = ne0;   // K-extension steps (an upper bound until listed)
+        for (; issued < nw + ne; ++issued) {
             const int i = issued;
             if (!mbar_wait(&tl.empty[s], ph ^ 1, abort_flag, p.status)) break;
             uint8_t* a = smem + (size_t)s * SB;
             uint8_t* b = a + A_STAGE;
             // din steps, with the K-extension steps placed EXT_LEAD steps before the end
             // so that their Vt loads overlap the last W tiles
-            const int ne = eu1 - eu0, ins = max(0, (kb1 - kb0) - p.ext_lead);
+            if (i == ins && LU > 0) {
+                if (!mbar_wait(&tl.info_ready, 0, abort_flag, p.status)) break;
+                ne = ext_steps();
+                if (i == nw + ne) break;   // nothing left: no K-extension step, no din step after
+            }
             const bool ext = i >= ins && i < ins + ne;
             const int kb = kb0 + (i < ins ? i : i - ne);
             if (SHRINK) {
@@ -634,9 +675,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
                 }
             } else {
-                const int u = eu0 + (i - ins);
-                const int kx = (u - eu0) * EXT_SUB;
-                if (u == eu0 && !mbar_wait(&tl.info_ready, 0, abort_flag, p.status)) break;
+                const int u = ext_unit_at(i - ins);
+                const int kx = u * EXT_SUB;   // the unit's first chunk
                 int un[EXT_SUB];
                 uint32_t mask = 0;
 #pragma unroll
@@ -697,9 +737,14 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         uint32_t ph = 0;
         uint32_t acc = 0;
         uint32_t cph = 0;   // over codes: parity of each stage's next conversion
-        const int ne_m = eu1 - eu0, ins_m = max(0, (kb1 - kb0) - p.ext_lead);
-        for (int i = 0; i < n_steps; ++i) {
-            const bool din_step = !(i >= ins_m && i < ins_m + ne_m);
+        int ne_m = ne0;
+        for (int i = 0; i < nw + ne_m; ++i) {
+            if (i == ins && LU > 0) {   // as many K-extension steps as the producer issues
+                if (!mbar_wait(&tl.info_ready, 0, abort_flag, p.status)) break;
+                ne_m = ext_steps();
+                if (i == nw + ne_m) break;
+            }
+            const bool din_step = !(i >= ins && i < ins + ne_m);
             if (!SHRINK && p.qmode && din_step) {
                 // the epilogue warps saw the stage land and restored its W tile from the codes
                 if (!mbar_wait(&tl.conv[s], (cph >> s) & 1u, abort_flag, p.status)) break;
@@ -754,11 +799,16 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // thread) once its codes land, then release the stage to the MMA warp
             const int o = tile * BM + row;
             const float row_sc = (p.qmode == QMODE_INT8 && o < p.dout) ? __ldg(p.qscale + o) : 0.f;
-            const int ne_c = eu1 - eu0, ins_c = max(0, (kb1 - kb0) - p.ext_lead);
+            int ne_c = ne0;
             int s = 0;
             uint32_t ph = 0;
-            for (int i = 0; i < n_steps; ++i) {
-                if (!(i >= ins_c && i < ins_c + ne_c)) {
+            for (int i = 0; i < nw + ne_c; ++i) {
+                if (i == ins && LU > 0) {   // the stages the K-extension steps take
+                    if (!mbar_wait(&tl.info_ready, 0, abort_flag, p.status)) break;
+                    ne_c = ext_steps();
+                    if (i == nw + ne_c) break;
+                }
+                if (!(i >= ins && i < ins + ne_c)) {
                     // every din step is waited for in order (the MMA waits for this warp's
                     // release), so the parity never runs a phase ahead
                     const bool got = mbar_wait(&tl.full[s], ph, abort_flag, p.status);

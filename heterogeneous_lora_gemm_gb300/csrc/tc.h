@@ -42,7 +42,7 @@ struct TcForwardArgs {
     const void* arena_down;
     Workspace ws;
     PoolDims dims;
-    int n_chunks;           // chunks of the loaded slots (entries of ws.chunks, in arena order)
+    int n_chunks;           // chunks of the loaded slots (entries of ws.chunks: by module, then arena order)
     int tile_span;          // largest arena span of 8 consecutive chunks (first unit to last unit + 16)
     int units;              // rank units of the arena
     int n_loaded;           // loaded slots
