@@ -1192,6 +1192,10 @@ DecodeShape decode_shape(const PoolDims& d, int N, int budget1, int zt) {
         budget = PROJ_SMEM_BUDGET_2;
     } else if (tiles * splits < 3 * sm_count() / 4) {
         int s2 = 2 * sm_count() / tiles;
+        // clusters of s2 CTAs stay inside a GPC: filling more than nine tenths of the
+        // SMs' two CTA slots leaves a cluster or two without room until the first CTAs
+        // end (a second wave of a whole CTA lifetime), so take a split fewer there
+        while (s2 > 1 && 10 * tiles * s2 > 9 * 2 * sm_count()) --s2;
         s2 = s2 > kb_total ? kb_total : s2;
         s2 = s2 >= 8 ? 8 : (s2 >= 6 ? 6 : (s2 >= 4 ? 4 : s2));   // cluster sizes with a reducer
         if (s2 > splits) {
