@@ -156,15 +156,19 @@ def test_many_loaded_slots_few_used():
     check_forward_segments(layer, pool)
 
 
-@pytest.mark.parametrize("T,din,n_slots", [(200, 1000, 120), (100, 1000, 120), (128, 11008, 90)])
-def test_many_adapters_few_rows_each(T, din, n_slots):
+@pytest.mark.parametrize("T,din,n_slots,choices", [
+    (200, 1000, 120, (5, 16, 24, 8)), (100, 1000, 120, (5, 16, 24, 8)), (128, 11008, 90, (5, 16, 24, 8)),
+    (200, 1000, 120, (5, 16, 8)),     # every adapter one chunk (the second 8-column Up block unused at 5 and 8)
+    (128, 4096, 100, (16,)),
+])
+def test_many_adapters_few_rows_each(T, din, n_slots, choices):
     """Decode batches with at most two rows per loaded adapter on average take the
     CUDA-core shrink: ranks that are not multiples of 16 (partial chunks), one slot
     with more rows than one pass over its Down rows holds, rows without adapter,
     din not a multiple of 256 (and 11008, two rows per pass), with and without the
     L2 prefetch before the wait (T >= loaded slots or not)."""
     rng = np.random.default_rng(T + din)
-    ranks = list(rng.choice(np.array([5, 16, 24, 8]), size=n_slots))
+    ranks = list(rng.choice(np.array(choices), size=n_slots))
     ra = rng.integers(0, n_slots, size=T).astype(np.int32)
     ra[: 20] = 3                                  # slot 3: 20 rows (three passes of 8)
     ra[rng.random(T) < 0.1] = -1
@@ -180,7 +184,9 @@ def test_chained_forwards_read_the_previous_output():
     still run, and must read X only once it is written.  The kernels are
     deterministic (fixed split order), so the chain must equal, bit for bit, the same
     chain with a device synchronisation after every forward."""
-    for shape in ((1024, [16, 8]), (4096, [16, 16, 16]), (1024, [16, 8, 24] * 7)):   # the last: CUDA-core shrink
+    # the last two: CUDA-core shrink, with a rank-24 adapter spanning two chunks of the
+    # same rows, and with 24 adapters of one chunk each
+    for shape in ((1024, [16, 8]), (4096, [16, 16, 16]), (1024, [16, 8, 24] * 7), (1024, [16, 8] * 12)):
         chain_case(*shape)
 
 
