@@ -55,7 +55,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {"swapab_gemm_kernel": "heterogeneous_lora_gemm_gb300/csrc/tc.cu",
                   "prefill_gemm_kernel": "heterogeneous_lora_gemm_gb300/csrc/tc_prefill.cu"}
 STAMP_SHRINK, STAMP_PROJECTION, STAMP_PREFILL = 0, 1, 2
-KIND_NAMES = {STAMP_SHRINK: "swapab_gemm_kernel<true> (shrink)", STAMP_PROJECTION: "swapab_gemm_kernel<false>",
+KIND_NAMES = {STAMP_SHRINK: "shrink (swapab_gemm_kernel<true> or shrink_gemv_kernel)", STAMP_PROJECTION: "swapab_gemm_kernel<false>",
               STAMP_PREFILL: "prefill_gemm_kernel"}
 SUB_WORKLOADS = {"decode_step": (20480, 64), "fragmented_decode": (8192, 32), "prefill": (256, 8)}
 
