@@ -114,7 +114,8 @@ constexpr int MAX_SLOT_WORDS = 4096 / 32;
 constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
 constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
 constexpr int PROJ_KC = 2;         // projection: K chunks of 64 per pipeline step (one 3D box each for W and X)
-constexpr int PROJ_ZT_N = 128;     // projection: tokens per token tile of a decode batch above this size
+constexpr int PROJ_ZT_N = 128;
+constexpr int QUANT_KC = 2;        // projection over codes: K chunks of 64 per pipeline step     // projection: tokens per token tile of a decode batch above this size
 constexpr int QMODE_INT8 = 1, QMODE_NF4 = 2;
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
@@ -351,10 +352,10 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int NS = p.stages;
     const int B_SUB = b_bytes(p.N);                  // bytes of the B operand per K chunk
     const int A_STAGE = p.kc * p.a_sub;
-    const int Q_OFF = A_STAGE + p.kc * B_SUB;        // projection over codes: the code tile (kc == 1)
+    const int Q_OFF = A_STAGE + p.kc * B_SUB;        // projection over codes: the code tile [row][kc * q_x]
     // over 4-bit codes the stage also holds the K block's 128 fp32 scales
-    const int QS_OFF = Q_OFF + BM * p.q_x;
-    const int Q_BYTES = BM * p.q_x + (p.qmode == QMODE_NF4 ? BM * 4 : 0);   // bytes of the codes (+ scales)
+    const int QS_OFF = Q_OFF + BM * p.q_x * p.kc;    // 4-bit codes: the scales [kc][row]
+    const int Q_BYTES = (BM * p.q_x + (p.qmode == QMODE_NF4 ? BM * 4 : 0)) * p.kc;   // codes (+ scales)
     // (stages start on 1024-byte swizzle atoms)
     const int SB = (!SHRINK && p.qmode) ? (Q_OFF + Q_BYTES + 1023) & ~1023 : Q_OFF;
 
@@ -610,8 +611,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 tl.stage_kind[i] = -1;
                 if (p.qmode) {
                     mbar_expect_tx_only(&tl.full[i], (uint32_t)Q_BYTES);
-                    tma_2d(a + Q_OFF, &tmW, &tl.full[i], (kb0 + i) * p.q_x, tile * BM);
-                    if (p.qmode == QMODE_NF4) tma_2d(a + QS_OFF, &tmQs, &tl.full[i], tile * BM, kb0 + i);
+                    tma_2d(a + Q_OFF, &tmW, &tl.full[i], (kb0 + i) * p.kc * p.q_x, tile * BM);
+                    if (p.qmode == QMODE_NF4) tma_2d(a + QS_OFF, &tmQs, &tl.full[i], tile * BM, (kb0 + i) * p.kc);
                 } else {
                     mbar_expect_tx_only(&tl.full[i], (uint32_t)A_STAGE);
                     if (p.kc > 1) tma_3d(a, &tmW, &tl.full[i], 0, tile * BM, (kb0 + i) * p.kc);
@@ -660,10 +661,11 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             } else if (!ext && p.qmode) {
                 // the code tile and X; the epilogue warps restore the bf16 W tile from the codes
                 tl.stage_kind[s] = -1;
-                mbar_expect_tx(&tl.full[s], (uint32_t)(Q_BYTES + B_SUB));
-                tma_2d(a + Q_OFF, &tmW, &tl.full[s], kb * p.q_x, tile * BM);
-                if (p.qmode == QMODE_NF4) tma_2d(a + QS_OFF, &tmQs, &tl.full[s], tile * BM, kb);
-                tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
+                mbar_expect_tx(&tl.full[s], (uint32_t)(Q_BYTES + p.kc * B_SUB));
+                tma_2d(a + Q_OFF, &tmW, &tl.full[s], kb * p.kc * p.q_x, tile * BM);
+                if (p.qmode == QMODE_NF4) tma_2d(a + QS_OFF, &tmQs, &tl.full[s], tile * BM, kb * p.kc);
+                if (p.kc > 1) tma_3d(b, &tmX, &tl.full[s], 0, tok0, kb * p.kc);
+                else tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
             } else if (!ext) {
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)SB);
@@ -815,10 +817,13 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     __syncwarp();
                     if (!__all_sync(0xffffffffu, got)) break;
                     uint8_t* stg = smem + (size_t)s * SB;
-                    // (4-bit codes: the row's scale of this K block came with the codes)
-                    const float sc = p.qmode == QMODE_NF4 ? reinterpret_cast<const float*>(stg + QS_OFF)[row] : row_sc;
-                    restore_row(stg + Q_OFF + row * p.q_x, stg + row * 128, row, sc, p.qmode,
-                                reinterpret_cast<const float*>(smem + p.qtab_off));
+                    for (int j = 0; j < p.kc; ++j) {   // the stage's K chunks
+                        // (4-bit codes: the row's scale of this K block came with the codes)
+                        const float sc =
+                            p.qmode == QMODE_NF4 ? reinterpret_cast<const float*>(stg + QS_OFF)[j * BM + row] : row_sc;
+                        restore_row(stg + Q_OFF + (row * p.kc + j) * p.q_x, stg + j * p.a_sub + row * 128, row, sc,
+                                    p.qmode, reinterpret_cast<const float*>(smem + p.qtab_off));
+                    }
                     fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
                     __syncwarp();
                     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&tl.conv[s]))
@@ -1242,12 +1247,13 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     const int Np = zt > 1 ? PROJ_ZT_N : N;               // token rows per projection tile
     DecodeShape ds = decode_shape(d, decode ? Np : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE, zt);
     if (a.qmode) {
-        // over codes: one K chunk per stage (the code tile is one 2D box); a stage also
-        // holds the restored 16 KiB W tile, which comes from no load, so a deeper ring
-        // keeps as many code bytes in flight as the bf16 path keeps W bytes
-        ds.pkc = 1;
-        ds.ksteps = kb_total;
-        ds.splits = ds.splits < kb_total ? ds.splits : kb_total;
+        // over codes: QUANT_KC K chunks per stage (one 2D box of codes, one of scales);
+        // a stage also holds the restored 16 KiB W tile of each chunk, which comes from
+        // no load.  Each stage costs a round trip through the converting warps, so the
+        // steps carry two chunks, and the ring budget is the deep one.
+        ds.pkc = kb_total >= QUANT_KC ? QUANT_KC : 1;
+        ds.ksteps = (kb_total + ds.pkc - 1) / ds.pkc;
+        ds.splits = ds.splits < ds.ksteps ? ds.splits : ds.ksteps;
         if (ds.budget == PROJ_SMEM_BUDGET || ds.budget == PROJ_SMEM_BUDGET_SHARED) ds.budget = PROJ_SMEM_BUDGET_ALONE;
     }
     const int q_x = a.qmode == QMODE_INT8 ? BK : (a.qmode == QMODE_NF4 ? BK / 2 : 0);   // code bytes per row and K chunk
@@ -1366,16 +1372,16 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         // the block scales [din / 64][dout] fp32: boxes of 128 rows of one K block
         cuuint64_t dims[2] = {(cuuint64_t)d.dout, (cuuint64_t)(d.din / BK)};
         cuuint64_t strides[1] = {(cuuint64_t)d.dout * 4};
-        cuuint32_t box[2] = {(cuuint32_t)BM, 1};
+        cuuint32_t box[2] = {(cuuint32_t)BM, (cuuint32_t)ds.pkc};
         if (!tc_encode_typed(&tmQs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.qscale, 2, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
     if (a.qmode) {
-        // the codes as bytes {din / (8 / bits), dout}; boxes of one K chunk x 128 rows
+        // the codes as bytes {din / (8 / bits), dout}; boxes of a step's K chunks x 128 rows
         cuuint64_t dims[2] = {(cuuint64_t)d.din / (BK / q_x), (cuuint64_t)d.dout};
         cuuint64_t strides[1] = {(cuuint64_t)(d.din / (BK / q_x))};
-        cuuint32_t box[2] = {(cuuint32_t)q_x, (cuuint32_t)BM};
+        cuuint32_t box[2] = {(cuuint32_t)(q_x * ds.pkc), (cuuint32_t)BM};
         if (!tc_encode_typed(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, 2, dims, strides, box,
                              CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
@@ -1408,7 +1414,8 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         cuuint64_t wdims[3] = {(cuuint64_t)BK, (cuuint64_t)d.dout, (cuuint64_t)kb_total};
         cuuint64_t strides[2] = {(cuuint64_t)d.din * 2, (cuuint64_t)BK * 2};
         cuuint32_t wbox[3] = {BK, (cuuint32_t)BM, (cuuint32_t)pkc};
-        if (!tc_encode(&tmW, a.W, 3, wdims, strides, wbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+        if (!a.qmode && !tc_encode(&tmW, a.W, 3, wdims, strides, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
         cuuint64_t xdims[3] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)kb_total};
         cuuint32_t xbox[3] = {BK, (cuuint32_t)Np, (cuuint32_t)pkc};
         if (!tc_encode(&tmX, a.X, 3, xdims, strides, xbox, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
@@ -1433,7 +1440,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
     const int rx_bytes = p.push ? BM * Np * 4 : 0;
     // (over codes, the code tile too, and over 4-bit codes the K block's scales)
-    const int sbytes = (pkc * stage_bytes(Np) + BM * q_x + (a.qmode == QMODE_NF4 ? BM * 4 : 0) + 1023) & ~1023;
+    const int sbytes = (pkc * (stage_bytes(Np) + BM * q_x + (a.qmode == QMODE_NF4 ? BM * 4 : 0)) + 1023) & ~1023;
     const int qtab_bytes = a.qmode == QMODE_NF4 ? 64 : 0;
     p.stages = clamp_stages((budget - rx_bytes - qtab_bytes) / sbytes);
     p.a_sub = A_BYTES;

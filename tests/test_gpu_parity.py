@@ -408,6 +408,7 @@ def test_load_waits_for_last_reader_and_versions():
     (40, 256, 192, [16, 8]),          # decode: the projection reads the codes (push reduction)
     (200, 1024, 640, [16] * 120),     # decode, many adapters (CUDA-core shrink), staged reduction
     (128, 512, 7200, [16, 8]),        # decode, 57 row tiles (odd), two K splits
+    (40, 192, 256, [16, 8]),          # decode, 3 K chunks: the second step's second chunk past din
     (300, 256, 192, [16, 8]),         # prefill: restore pass into W_scratch, then the forward
     (40, 136, 192, [16, 8]),          # din not a multiple of 64: restore pass
 ])
