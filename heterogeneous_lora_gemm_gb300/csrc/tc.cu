@@ -189,6 +189,7 @@ struct GemmParams {
     const float* qscale;            // QMODE_INT8: [dout]; QMODE_NF4: [din / 64][dout]
     float qcb[16];                  // QMODE_NF4: the codebook
     int qtab_off;                   // QMODE_NF4: shared-memory offset of the codebook (16 floats)
+    int up_rows;                    // projection: output rows per row of the Up map (8 or 1)
 };
 
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
@@ -708,7 +709,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 #pragma unroll
                     for (int j = 0; j < EXT_SUB; ++j)
                         if ((mask >> j) & 1u)
-                            tma_3d(a + j * (BM * 32), &tmArena, &tl.full[s], 0, tile * BM, un[j] >> 3);
+                            tma_3d(a + j * (BM * 32), &tmArena, &tl.full[s], 0, tile * BM / p.up_rows, un[j] >> 3);
                     if (!waited) {
                         if (p.pdl) pdl_wait();   // Vt comes from the shrink
                         waited = true;
@@ -1157,8 +1158,23 @@ bool tc_encode_arena_maps(TcArenaMaps* m, void* arena_down, void* arena_up, int 
     cuuint64_t strides[2] = {16, (cuuint64_t)dout * 16};
     cuuint32_t box128[3] = {8, 128, 2};
     cuuint32_t box256[3] = {8, 256, 2};
-    return tc_encode(&m->up128, arena_up, 3, dims, strides, box128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           tc_encode(&m->up256, arena_up, 3, dims, strides, box256, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!tc_encode(&m->up128, arena_up, 3, dims, strides, box128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !tc_encode(&m->up256, arena_up, 3, dims, strides, box256, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    m->upw128 = m->up128;
+    m->upw256 = m->up256;
+    m->up_rows = 1;
+    if (dout % 8 == 0) {
+        cuuint64_t wdims[3] = {64, (cuuint64_t)dout / 8, (cuuint64_t)(units / 8)};
+        cuuint64_t wstrides[2] = {128, (cuuint64_t)dout * 16};
+        cuuint32_t wbox128[3] = {64, 16, 2};
+        cuuint32_t wbox256[3] = {64, 32, 2};
+        if (!tc_encode(&m->upw128, arena_up, 3, wdims, wstrides, wbox128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !tc_encode(&m->upw256, arena_up, 3, wdims, wstrides, wbox256, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+        m->up_rows = 8;
+    }
+    return true;
 }
 
 bool tc_quantized_fits(const PoolDims& d, int T, bool nf4) {
@@ -1463,9 +1479,10 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.qmode = a.qmode;
     p.q_x = q_x;
     p.qscale = a.qscale;
+    p.up_rows = a.maps.up_rows;
     for (int i = 0; i < 16; ++i) p.qcb[i] = a.qcb[i];
     return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, zt), dim3(NUM_THREADS), smem_bytes(p), st, true,
-                    p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.up128, tmQs, p);
+                    p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.upw128, tmQs, p);
 }
 
 cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din, int dout, void* Y,

@@ -19,8 +19,13 @@ TcWorkspaceNeeds tc_workspace_needs(bool bf16, const PoolDims& d);
 //   down   : 2D {din, units}, boxes of 64 din columns x 16 rank rows, 128-byte swizzle
 //   up128  : 3D {8, dout, units/8}, boxes of 8 rank columns x 128 rows x 2 blocks, no swizzle
 //   up256  : the same with 256 rows per box (prefill tiles)
+//   upw128, upw256: the same boxes seen as rows of 128 bytes (8 output rows x 8 rank
+//           columns: 3D {64, dout/8, units/8}): the same bytes in shared memory, in an
+//           eighth of the TMA rows; only when dout % 8 == 0 (up_rows == 8), else copies
+//           of up128 / up256 (up_rows == 1)
 struct TcArenaMaps {
-    CUtensorMap down, up128, up256;
+    CUtensorMap down, up128, up256, upw128, upw256;
+    int up_rows;   // output rows per row of the upw maps (8, or 1 for the plain maps)
 };
 bool tc_encode_arena_maps(TcArenaMaps* maps, void* arena_down, void* arena_up, int units, int din, int dout);
 

@@ -50,6 +50,7 @@ struct PrefillParams {
     int pdl;    // launched while the shrink may still run: wait before reading its outputs
     int group_m;   // token tiles per raster group
     unsigned long long* stamps;   // profiling records (NULL = off), see ptx::stamp_record
+    int up_rows;                  // output rows per row of the Up map (8 or 1)
     int stamp_cap;
 };
 
@@ -158,7 +159,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         tma_3d(a, &tmV, &full[s], 0, m * PM, c0);
 #pragma unroll
                         for (int j = 0; j < EXT_SUB; ++j)   // two blocks of 8 rank columns x 256 rows
-                            if ((mask >> j) & 1u) tma_3d(b + j * (PN * 32), &tmUp, &full[s], 0, n * PN, un[j] >> 3);
+                            if ((mask >> j) & 1u) tma_3d(b + j * (PN * 32), &tmUp, &full[s], 0, n * PN / p.up_rows, un[j] >> 3);
                     }
                 }
                 if (++s == PSTAGES) {
@@ -318,12 +319,13 @@ cudaError_t launch_prefill(const TcForwardArgs& a, const CUtensorMap& tmX, const
         if (p.group_m < 1) p.group_m = 1;
     }
     p.stamps = a.stamps;
+    p.up_rows = a.maps.up_rows;
     p.stamp_cap = a.stamp_cap;
     const int total = p.m_tiles * p.n_tiles;
     const int grid = total < num_sms ? total : num_sms;
     const size_t smem = 1024 + (size_t)PSTAGES * PSTAGE + (2 * PSTAGES + 5) * 8 + PSTAGES * 4 + 16;
     return launch_k(prefill_gemm_kernel, dim3(grid), dim3(P_THREADS), smem, st, after_shrink, 1, tmX,
-                    tmW, tmV, a.maps.up256, p);
+                    tmW, tmV, a.maps.upw256, p);
 }
 
 }  // namespace mlora
