@@ -80,6 +80,7 @@ struct MergeParams {
     const float* row_scale; // quantized base: the codes' scale per output row
     uint32_t* row_max;      // quantized base: max |w| per output row (fp32 bits)
     int dout;
+    int up_rows;            // output rows per row of the Up map (8: 128-byte rows, or 1)
 };
 
 
@@ -142,7 +143,7 @@ merge_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__
             const int u = rec.unit + issued * CHUNK;   // first arena unit of the chunk (a multiple of 8)
             mbar_expect_tx(&tl.full[s], (uint32_t)MG_STAGE);
             for (int j = 0; j < MG_BN / 64; ++j) tma_2d(dn + j * (CHUNK * 128), &tmDown, &tl.full[s], i0 + 64 * j, u);
-            tma_3d(up, &tmUp, &tl.full[s], 0, o0, u >> 3);
+            tma_3d(up, &tmUp, &tl.full[s], 0, o0 / p.up_rows, u >> 3);
             if (++s == MG_STAGES) {
                 s = 0;
                 ph ^= 1;
@@ -380,13 +381,13 @@ cudaError_t launch_merge_quant_tc(int8_t* Wq, float* row_scale, uint32_t* row_ma
     cuuint64_t strides[1] = {(cuuint64_t)d.din};
     cuuint32_t box[2] = {128, (cuuint32_t)MG_BM};
     if (!encode_u8(&tmQ, Wq, dims, strides, box)) return cudaErrorInvalidValue;
-    MergeParams p{slots, slot, 1.f, status, row_scale, row_max, d.dout};
+    MergeParams p{slots, slot, 1.f, status, row_scale, row_max, d.dout, maps.up_rows};
     const dim3 grid((d.din + MG_BN_USED - 1) / MG_BN_USED, (d.dout + MG_BM - 1) / MG_BM);
     cudaError_t e = launch_k(merge_tc_kernel<MG_BN_USED, MODE_QMAX>, grid, dim3(MG_THREADS),
-                             merge_smem<MG_BN_USED, MODE_QMAX>(), st, false, 1, tmQ, maps.down, maps.up128, p);
+                             merge_smem<MG_BN_USED, MODE_QMAX>(), st, false, 1, tmQ, maps.down, maps.upw128, p);
     if (e != cudaSuccess) return e;
     e = launch_k(merge_tc_kernel<MG_BN_USED, MODE_QCODES>, grid, dim3(MG_THREADS), merge_smem<MG_BN_USED, MODE_QCODES>(),
-                 st, false, 1, tmQ, maps.down, maps.up128, p);
+                 st, false, 1, tmQ, maps.down, maps.upw128, p);
     if (e != cudaSuccess) {   // the words hold this call's maxima: clear them for the next call
         cudaMemsetAsync(row_max, 0, sizeof(uint32_t) * (size_t)d.dout, st);
         return e;
@@ -402,10 +403,10 @@ cudaError_t launch_merge_tc(void* W, const SlotRec* slots, int slot, const TcAre
     cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)MG_BM};
     if (!tc_encode(&tmW, W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    MergeParams p{slots, slot, sign, status, nullptr, nullptr, d.dout};
+    MergeParams p{slots, slot, sign, status, nullptr, nullptr, d.dout, maps.up_rows};
     const dim3 grid((d.din + MG_BN_USED - 1) / MG_BN_USED, (d.dout + MG_BM - 1) / MG_BM);
     return launch_k(merge_tc_kernel<MG_BN_USED, MODE_BF16>, grid, dim3(MG_THREADS), merge_smem<MG_BN_USED, MODE_BF16>(),
-                    st, false, 1, tmW, maps.down, maps.up128, p);
+                    st, false, 1, tmW, maps.down, maps.upw128, p);
 }
 
 }  // namespace mlora
