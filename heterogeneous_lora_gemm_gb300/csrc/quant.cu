@@ -368,68 +368,102 @@ dequant_nf4_kernel(const uint8_t* __restrict__ q, const float* __restrict__ absm
 // (fp32, k ascending), take the block's new absmax, and give each w / absmax (fp32
 // division) the code of the nearest codebook value (fp32 distances, the first of equal
 // ones).
-constexpr int MN4_ROWS = 64;
+constexpr int MN4_ROWS = 256;   // output rows per CTA of the NF4 merge: one per thread
+
+// The nearest codebook entry to v (fp32 distances, the lower code on a tie), for an
+// ascending codebook: bisection to the two entries that bracket v, then their
+// distances.  (An entry further out is strictly further in fp32 as well: the gaps of
+// the codebook are far above the rounding of a difference of values in [-1, 1].)
+__device__ __forceinline__ uint32_t nf4_code_of(float v, const float* cb) {
+    int j = 0;   // entries below v, at most 15
+#pragma unroll
+    for (int step = 8; step > 0; step >>= 1)
+        if (cb[j + step - 1] < v) j += step;
+    if (j == 0) return 0u;
+    return fabsf(v - cb[j]) < fabsf(v - cb[j - 1]) ? (uint32_t)j : (uint32_t)(j - 1);
+}
 
 template <typename E>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(MN4_ROWS)
 merge_nf4_kernel(uint8_t* __restrict__ q, float* __restrict__ absmax, Codebook cb, const SlotRec* __restrict__ slots,
-                 int slot, const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout) {
-    extern __shared__ float mn4_s[];   // [rank][64] Down columns, then [64 rows][rank] Up
+                 int slot, const E* __restrict__ arena_down, const E* __restrict__ arena_up, int din, int dout,
+                 int aligned) {
+    extern __shared__ float4 mn4_s[];   // [rank][64] Down columns of the block, fp32
     __shared__ float cb_s[16];
     const SlotRec rec = slots[slot];
     const int rank = rec.rank;
-    const int blk = blockIdx.x, o0 = blockIdx.y * MN4_ROWS;
-    const int nr = min(MN4_ROWS, dout - o0);
-    float* down_s = mn4_s;
-    float* up_s = mn4_s + (size_t)rank * NF4_BLOCK;
+    const int blk = blockIdx.x;
+    const int o = blockIdx.y * MN4_ROWS + threadIdx.x;   // this thread's output row
+    float* down_s = reinterpret_cast<float*>(mn4_s);
     if (threadIdx.x < 16) cb_s[threadIdx.x] = cb.v[threadIdx.x];
     const E* down = arena_down + (size_t)rec.unit * din + blk * NF4_BLOCK;
     for (int idx = threadIdx.x; idx < rank * NF4_BLOCK; idx += blockDim.x) {
         const int k = idx / NF4_BLOCK, c = idx % NF4_BLOCK;
         down_s[idx] = as_f32(down[(size_t)k * din + c]);
     }
-    for (int idx = threadIdx.x; idx < MN4_ROWS * rank; idx += blockDim.x) {
-        const int r = idx / rank, k = idx % rank;
-        up_s[idx] = r < nr ? as_f32(arena_up[up_index(rec.unit, k, o0 + r, dout)]) : 0.f;
-    }
     __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r = warp; r < nr; r += blockDim.x / 32) {
-        const int o = o0 + r;
-        uint8_t* qb = q + (size_t)o * (din / 2) + blk * (NF4_BLOCK / 2) + lane;
-        float* am = absmax + (size_t)blk * dout + o;
-        const uint32_t byte = *qb;
-        const float old = *am;
-        float w0 = cb_s[byte & 15u] * old, w1 = cb_s[byte >> 4] * old;
-        float u0 = 0.f, u1 = 0.f;
-        const float* ur = up_s + (size_t)r * rank;
-        for (int k = 0; k < rank; ++k) {
-            const float up = ur[k];
-            const float2 dk = *reinterpret_cast<const float2*>(down_s + k * NF4_BLOCK + 2 * lane);
-            u0 = fmaf(up, dk.x, u0);
-            u1 = fmaf(up, dk.y, u1);
-        }
-        w0 = w0 + rec.scale * u0;
-        w1 = w1 + rec.scale * u1;
-        float m = fmaxf(fabsf(w0), fabsf(w1));
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-        auto code_of = [&](float w) {
-            const float v = m > 0.f ? w / m : 0.f;
-            int best = 0;
-            float bd = fabsf(v - cb_s[0]);
-            for (int j = 1; j < 16; ++j) {
-                const float dj = fabsf(v - cb_s[j]);
-                if (dj < bd) {
-                    bd = dj;
-                    best = j;
-                }
-            }
-            return (uint32_t)best;
-        };
-        *qb = (uint8_t)(code_of(w0) | (code_of(w1) << 4));
-        if (lane == 0) *am = m;
+    if (o >= dout) return;
+    // the row's 64 codes of the block (32 bytes) and its scale
+    uint8_t* qb = q + (size_t)o * (din / 2) + blk * (NF4_BLOCK / 2);
+    uint32_t cw[8];
+    if (aligned) {
+        const uint4 a = *reinterpret_cast<const uint4*>(qb), b = *reinterpret_cast<const uint4*>(qb + 16);
+        cw[0] = a.x; cw[1] = a.y; cw[2] = a.z; cw[3] = a.w; cw[4] = b.x; cw[5] = b.y; cw[6] = b.z; cw[7] = b.w;
+    } else {
+        for (int i = 0; i < 8; ++i)
+            cw[i] = qb[4 * i] | (qb[4 * i + 1] << 8) | (qb[4 * i + 2] << 16) | ((uint32_t)qb[4 * i + 3] << 24);
     }
+    float* am = absmax + (size_t)blk * dout + o;
+    const float old = *am;
+    // u = Up[o, :] Down[:, block] in fp32, k ascending
+    float u[NF4_BLOCK];
+#pragma unroll
+    for (int c = 0; c < NF4_BLOCK; ++c) u[c] = 0.f;
+    for (int k0 = 0; k0 < rank; k0 += 8) {
+        float upk[8];   // eight Up values requested at once
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            upk[kk] = k0 + kk < rank ? as_f32(arena_up[up_index(rec.unit, k0 + kk, o, dout)]) : 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            if (k0 + kk >= rank) break;
+            const float4* dk = mn4_s + (k0 + kk) * (NF4_BLOCK / 4);
+#pragma unroll
+            for (int c4 = 0; c4 < NF4_BLOCK / 4; ++c4) {
+                const float4 d = dk[c4];   // (the same address in every thread: a broadcast)
+                u[4 * c4] = fmaf(upk[kk], d.x, u[4 * c4]);
+                u[4 * c4 + 1] = fmaf(upk[kk], d.y, u[4 * c4 + 1]);
+                u[4 * c4 + 2] = fmaf(upk[kk], d.z, u[4 * c4 + 2]);
+                u[4 * c4 + 3] = fmaf(upk[kk], d.w, u[4 * c4 + 3]);
+            }
+        }
+    }
+    // merged values (restored + scale * u) and the block's new absmax
+    float m = 0.f;
+#pragma unroll
+    for (int c = 0; c < NF4_BLOCK; ++c) {
+        const uint32_t code = (cw[c >> 3] >> (4 * (c & 7))) & 15u;
+        u[c] = cb_s[code] * old + rec.scale * u[c];
+        m = fmaxf(m, fabsf(u[c]));
+    }
+    // the codes of w / absmax, two per byte (even column in the low nibble)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float v = m > 0.f ? u[8 * i + e] / m : 0.f;
+            word |= nf4_code_of(v, cb_s) << (4 * e);
+        }
+        cw[i] = word;
+    }
+    if (aligned) {
+        *reinterpret_cast<uint4*>(qb) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint4*>(qb + 16) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    } else {
+        for (int i = 0; i < 32; ++i) qb[i] = (uint8_t)(cw[i >> 2] >> (8 * (i & 3)));
+    }
+    *am = m;
 }
 
 }  // namespace
@@ -457,20 +491,22 @@ cudaError_t launch_merge_nf4(bool bf16, uint8_t* q, float* absmax, const float* 
     Codebook cb;
     for (int j = 0; j < 16; ++j) cb.v[j] = codebook[j];
     if (d.dout == 0 || d.din == 0) return cudaSuccess;
-    // shared memory for the largest rank the pool takes: Down [rank][64] and Up [64][rank], fp32
-    const size_t smem = sizeof(float) * (size_t)d.max_rank * (NF4_BLOCK + MN4_ROWS);
+    // shared memory for the largest rank the pool takes: Down [rank][64], fp32
+    const size_t smem = sizeof(float) * (size_t)d.max_rank * NF4_BLOCK;
     const dim3 grid((unsigned)(d.din / NF4_BLOCK), (unsigned)((d.dout + MN4_ROWS - 1) / MN4_ROWS));
+    const int aligned = ((uintptr_t)q & 15u) == 0 ? 1 : 0;   // rows of din / 2 bytes, din % 64 == 0
     cudaError_t e;
     if (bf16) {
         e = cudaFuncSetAttribute(merge_nf4_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        merge_nf4_kernel<__nv_bfloat16><<<grid, 256, smem, st>>>(
-            q, absmax, cb, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din, d.dout);
+        merge_nf4_kernel<__nv_bfloat16><<<grid, MN4_ROWS, smem, st>>>(
+            q, absmax, cb, slots, slot, (const __nv_bfloat16*)arena_down, (const __nv_bfloat16*)arena_up, d.din, d.dout,
+            aligned);
     } else {
         e = cudaFuncSetAttribute(merge_nf4_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        merge_nf4_kernel<float><<<grid, 256, smem, st>>>(q, absmax, cb, slots, slot, (const float*)arena_down,
-                                                       (const float*)arena_up, d.din, d.dout);
+        merge_nf4_kernel<float><<<grid, MN4_ROWS, smem, st>>>(q, absmax, cb, slots, slot, (const float*)arena_down,
+                                                            (const float*)arena_up, d.din, d.dout, aligned);
     }
     return cudaGetLastError();
 }
