@@ -1,11 +1,9 @@
 // Allocation-free base projection for decode-sized batches.
 //
 // Some callers cannot allocate device memory at the moment they need a
-// projection: code that runs inside a CUDA stream capture (cudaMalloc and
-// cudaFree cannot be captured and break the capture), plugins hosted by another
-// runtime that owns the whole device-memory budget and forbids allocations after
-// start-up, and latency-critical loops that cannot afford the device-wide
-// synchronisation an allocation may cause.  Such callers cannot create an adapter
+// projection: plugins hosted by another runtime that owns the whole device-memory
+// budget and forbids allocations after start-up, and latency-critical loops that
+// cannot afford the device-wide synchronisation an allocation may cause.  Such callers cannot create an adapter
 // pool, whose workspace comes from cudaMalloc.  This entry point runs the split-K
 // tensor-core projection of the decode path with its scratch -- the fp32 partial
 // tiles of the K splits, their arrival counters and a status word -- in one

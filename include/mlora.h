@@ -359,12 +359,11 @@ mlora_status mlora_profile_stamps(mlora_pool_t pool, void* records, int cap);
 /*
  * Base projection Y = X W^T for a decode-sized batch that allocates nothing.
  * The pages have no counterpart: this entry point exists for callers that cannot
- * allocate device memory when they need the projection -- code running inside a
- * CUDA stream capture (cudaMalloc/cudaFree cannot be captured), plugins whose
- * host runtime owns the device-memory budget and forbids allocations after
- * start-up, and latency-critical loops that cannot take the device-wide
- * synchronisation an allocation may cause.  Such callers cannot create a pool,
- * whose workspace comes from cudaMalloc.
+ * allocate device memory when they need the projection -- plugins whose host
+ * runtime owns the device-memory budget and forbids allocations after start-up,
+ * and latency-critical loops that cannot take the device-wide synchronisation an
+ * allocation may cause.  Such callers cannot create a pool, whose workspace comes
+ * from cudaMalloc.
  *
  *   X   device [T x din] bf16, W device [dout x din] bf16, Y device [T x dout] bf16,
  *       all 16-byte aligned, owned by the caller; Y is overwritten
@@ -377,8 +376,8 @@ mlora_status mlora_profile_stamps(mlora_pool_t pool, void* records, int cap);
  * this library holds until the process exits; larger shapes are rejected with
  * MLORA_ERR_UNSUPPORTED, never served from anywhere else.  No cudaMalloc, cudaFree
  * or allocating library routine is called.  The first call on a device looks up
- * the array's device address and raises the kernel's shared-memory cap; make
- * that first call outside any stream capture.  All calls share the one array
+ * the array's device address and raises the kernel's shared-memory cap (host
+ * calls that run once per device).  All calls share the one array
  * (it keeps what the last call left; the counters are cleared on every call), so
  * calls whose work overlaps on the GPU -- on different streams, or from several
  * host threads -- race and must be ordered by the caller.  A pipeline wait of
@@ -396,7 +395,7 @@ mlora_status mlora_project_noalloc(const void* X, const void* W, int T, int din,
  * scratch array (no allocation).  Returns MLORA_OK, MLORA_ERR_DEVICE_TIMEOUT (a
  * pipeline wait in one of those calls gave up after its bounded limit; that call's
  * Y is not valid) or MLORA_ERR_CUDA.  Like the calls it reports on, its first use
- * on a device sets up the array's address; make it outside any stream capture.
+ * on a device looks up the array's address.
  */
 mlora_status mlora_project_noalloc_status(mlora_stream_t stream);
 

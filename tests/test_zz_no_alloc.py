@@ -1,8 +1,8 @@
 """The allocation-free projection entry point, through the C ABI.
 
 mlora_project_noalloc serves callers that may not allocate device memory when
-they need a projection (inside a stream capture, inside a host runtime that owns
-the memory budget, in loops that cannot take an allocation's synchronisation).
+they need a projection (inside a host runtime that owns the memory budget, in
+loops that cannot take an allocation's synchronisation).
 Its output must match the fp64 oracle's projection X W^T, and what the
 pool-based entry point (mlora_forward with no row map) produces for the same X
 and W, call after call: the shared scratch array keeps the previous call's
