@@ -190,15 +190,20 @@ struct GemmParams {
     float qcb[16];                  // QMODE_NF4: the codebook
     int qtab_off;                   // QMODE_NF4: shared-memory offset of the codebook (16 floats)
     int up_rows;                    // projection: output rows per row of the Up map (8 or 1)
+    // projection: 128-row W tiles per CTA (1 or 2), sharing each X stage; with 2 the CTA
+    // owns 256 output rows, two MMAs per K slice into two accumulators (no K-extension,
+    // no codes, split-K through the staged cluster reduction, N <= 128)
+    int mt;
 };
 
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
-// rows x 1 token, gpt groups per token, group i of a token at staged row row_of(i),
+// rows x 1 token (rb staged rows per token), gpt groups per token, group i of a token
+// at staged row row_of(i),
 // loaded from the shared memory of all NSP CTAs of the cluster (or, NSP = 1, of this
 // CTA), 8 float4 loads in flight per thread, summed in split order.  A group that
 // need(token, i) rejects is not loaded: it is emitted as zeros.
 template <int NSP, typename RowOf, typename Need, typename Emit>
-__device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng, int gpt, int et, int nthr,
+__device__ __forceinline__ void staged_reduce(uint32_t part_a, int rb, int t_lo, int ng, int gpt, int et, int nthr,
                                               RowOf&& row_of, Need&& need, Emit&& emit) {
     constexpr int U = NSP >= 8 ? 1 : 8 / NSP;
     for (int g0 = et; g0 < ng; g0 += nthr * U) {
@@ -210,7 +215,7 @@ __device__ __forceinline__ void staged_reduce(uint32_t part_a, int t_lo, int ng,
             ok[u] = g < ng && need(t_lo + g / gpt, g % gpt);
             if (ok[u]) {
                 const int t = t_lo + g / gpt;
-                const uint32_t off = part_a + (uint32_t)((t * BM + row_of(g % gpt)) * 4);
+                const uint32_t off = part_a + (uint32_t)((t * rb + row_of(g % gpt)) * 4);
                 if (NSP == 1) {
                     q[u][0] = ld_shared_f4(off);
                 } else {
@@ -362,6 +367,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
+    const int MT = (!SHRINK && p.mt > 1) ? p.mt : 1;   // 128-row W tiles of this CTA
+    const int RB = MT * BM;                             // its output rows
     constexpr int kStampKind = SHRINK ? STAMP_SHRINK : STAMP_PROJECTION;
     const int tok0 = ztile * p.N;                    // first token of this token tile
     const int T = min(p.T - tok0, p.N);              // tokens in this tile
@@ -403,7 +410,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int ne0 = LU + (eu1 - eu0);   // K-extension steps at most (exactly once listed)
     auto ext_steps = [&]() { return tl.n_ext + (eu1 - eu0); };
     auto ext_unit_at = [&](int e) { return e < tl.n_ext ? tl.ext_slot[tl.ext_first + e] : eu0 + (e - tl.n_ext); };
-    const uint32_t ncols = p.N <= 32 ? 32 : (p.N <= 64 ? 64 : (p.N <= 128 ? 128 : 256));
+    const int acc_cols = MT * p.N;   // TMEM columns of the accumulators (MT of N columns)
+    const uint32_t ncols = acc_cols <= 32 ? 32 : (acc_cols <= 64 ? 64 : (acc_cols <= 128 ? 128 : (acc_cols <= 256 ? 256 : 512)));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -579,7 +587,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     bool have = false;
     // projection: final write of rows r0..r0+3 (a multiple of 4) of token t
     auto emit4 = [&](int t, int r0, const float4& v) {
-        const int o0 = tile * BM + r0;
+        const int o0 = tile * RB + r0;
         __nv_bfloat16* y = p.Y + (size_t)(tok0 + t) * p.dout + o0;
         if (p.dout % 4 == 0 && o0 + 4 <= p.dout) {
             __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
@@ -616,8 +624,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     if (p.qmode == QMODE_NF4) tma_2d(a + QS_OFF, &tmQs, &tl.full[i], tile * BM, (kb0 + i) * p.kc);
                 } else {
                     mbar_expect_tx_only(&tl.full[i], (uint32_t)A_STAGE);
-                    if (p.kc > 1) tma_3d(a, &tmW, &tl.full[i], 0, tile * BM, (kb0 + i) * p.kc);
-                    else tma_2d(a, &tmW, &tl.full[i], (kb0 + i) * BK, tile * BM);
+                    if (p.kc > 1) tma_3d(a, &tmW, &tl.full[i], 0, tile * RB, (kb0 + i) * p.kc);
+                    else tma_2d(a, &tmW, &tl.full[i], (kb0 + i) * BK, tile * RB);
                 }
             }
             pdl_wait();
@@ -671,10 +679,10 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 tl.stage_kind[s] = -1;
                 mbar_expect_tx(&tl.full[s], (uint32_t)SB);
                 if (p.kc > 1) {   // kc K chunks of W (128 rows) and of X (N tokens), one box each
-                    tma_3d(a, &tmW, &tl.full[s], 0, tile * BM, kb * p.kc);
+                    tma_3d(a, &tmW, &tl.full[s], 0, tile * RB, kb * p.kc);
                     tma_3d(b, &tmX, &tl.full[s], 0, tok0, kb * p.kc);
                 } else {
-                    tma_2d(a, &tmW, &tl.full[s], kb * BK, tile * BM);
+                    tma_2d(a, &tmW, &tl.full[s], kb * BK, tile * RB);
                     tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
                 }
             } else {
@@ -767,7 +775,11 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     const uint32_t ak = a + kc * p.a_sub, bk = b + kc * B_SUB;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        mma_bf16(tmem, sdesc(ak + k * 32, 1024, SW128), sdesc(bk + k * 32, 1024, SW128), idesc, acc);
+                        // tile u's rows follow tile u-1's in the W box (128-row blocks of
+                        // the 128-byte swizzle); each accumulator starts fresh on its first MMA
+                        for (int u = 0; u < MT; ++u)
+                            mma_bf16(tmem + (uint32_t)(u * p.N), sdesc(ak + u * A_BYTES + k * 32, 1024, SW128),
+                                     sdesc(bk + k * 32, 1024, SW128), idesc, acc);
                         acc = 1;
                     }
                 }
@@ -974,23 +986,24 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         float* part_s = reinterpret_cast<float*>(smem);
         const uint32_t part_a = smem_u32(part_s);
         const bool multi = p.splits > 1;
-        const int tp = min(p.N, (p.ring_bytes / (BM * 4)) & ~15);
+        const int tp = min(p.N, (p.ring_bytes / (RB * 4)) & ~15);
         const int rows = SHRINK ? (p.window ? p.win_rows : tile_chunks * CHUNK) : BM;
-        const int gpt = SHRINK ? tile_chunks * 4 : BM / 4;   // groups of 4 rows per token
+        const int gpt = SHRINK ? tile_chunks * 4 : RB / 4;   // groups of 4 rows per token
         const int et = multi ? (int)threadIdx.x : (int)threadIdx.x - 64;
         const int nthr = multi ? NUM_THREADS : 128;
         auto row_of = [&](int gi) { return SHRINK ? tl.my_off[gi >> 2] + (gi & 3) * 4 : gi * 4; };
         for (int p0 = 0; p0 < T; p0 += tp) {
             const int pt = min(tp, T - p0);
             if (warp >= 2 && q * 32 < rows)
-                for (int t0 = 0; t0 < pt; t0 += 16) {
-                    float v[16];
-                    if (have) tmem_ld16(tbase + p0 + t0, v);
-                    else
-                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                for (int u = 0; u < MT; ++u)   // accumulator u holds rows u * 128 + row
+                    for (int t0 = 0; t0 < pt; t0 += 16) {
+                        float v[16];
+                        if (have) tmem_ld16(tbase + (uint32_t)(u * p.N) + p0 + t0, v);
+                        else
+                            for (int j = 0; j < 16; ++j) v[j] = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) part_s[(t0 + j) * BM + row] = v[j];
-                }
+                        for (int j = 0; j < 16; ++j) part_s[(t0 + j) * RB + u * BM + row] = v[j];
+                    }
             __syncwarp();
             if (multi) cluster_sync();
             else epi_bar();
@@ -1018,12 +1031,12 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     emit4(p0 + t, gi * 4, v);
                 }
             };
-            if (p.splits == 1) staged_reduce<1>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
-            else if (p.splits == 2) staged_reduce<2>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
-            else if (p.splits == 3) staged_reduce<3>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
-            else if (p.splits == 4) staged_reduce<4>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
-            else if (p.splits == 6) staged_reduce<6>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
-            else staged_reduce<8>(part_a, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            if (p.splits == 1) staged_reduce<1>(part_a, RB, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 2) staged_reduce<2>(part_a, RB, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 3) staged_reduce<3>(part_a, RB, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 4) staged_reduce<4>(part_a, RB, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else if (p.splits == 6) staged_reduce<6>(part_a, RB, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
+            else staged_reduce<8>(part_a, RB, t_lo, ng, gpt, et, nthr, row_of, need, emit_g);
             __syncwarp();
             // no CTA refills or leaves while the others still read its shared memory
             if (multi) cluster_sync();
@@ -1198,8 +1211,9 @@ struct DecodeShape {
     int ksteps;   // pipeline steps over din
 };
 
-DecodeShape decode_shape(const PoolDims& d, int N, int budget1, int zt) {
-    const int tiles = proj_tiles(d) * zt;   // (row tile, token tile) pairs
+DecodeShape decode_shape(const PoolDims& d, int N, int budget1, int zt, int mt) {
+    const int tiles = (d.dout + mt * BM - 1) / (mt * BM) * zt;   // (row tile, token tile) pairs
+    auto stage_bytes = [&](int n) { return mt * A_BYTES + b_bytes(n); };
     const int kb_total = (d.din + BK - 1) / BK;
     // K splits of a tile: as many as fill the SMs with one CTA each (a power of two);
     // when that leaves a quarter of the SMs idle (few row tiles, long K), two CTAs per
@@ -1261,7 +1275,16 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     // whose slots its own tokens use, which its shrink tile wrote.
     const int zt = (decode && !a.qmode && N > PROJ_ZT_N) ? (T + PROJ_ZT_N - 1) / PROJ_ZT_N : 1;
     const int Np = zt > 1 ? PROJ_ZT_N : N;               // token rows per projection tile
-    DecodeShape ds = decode_shape(d, decode ? Np : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE, zt);
+    // More 128-row tiles than SMs and no adapters (the 7B layer's gate|up, 172 tiles):
+    // each CTA takes two row tiles that share its X stages, so that the K splits of half
+    // as many tiles fit the SMs' two CTA slots in one wave (instead of 1.7 waves), and
+    // each X tile is delivered to the SMs half as often.
+    int mt = (decode && !a.qmode && !shrink && Np > PUSH_MAX_N && Np <= 128 && proj_tiles(d) >= sm_count()) ? 2 : 1;
+    DecodeShape ds = decode_shape(d, decode ? Np : 16, shrink ? PROJ_SMEM_BUDGET : PROJ_SMEM_BUDGET_ALONE, zt, mt);
+    if (mt > 1 && ds.splits < 2) {   // (two tiles per CTA only through the staged split-K reduction)
+        mt = 1;
+        ds = decode_shape(d, Np, PROJ_SMEM_BUDGET_ALONE, zt, mt);
+    }
     if (a.qmode) {
         // over codes: QUANT_KC K chunks per stage (one 2D box of codes, one of scales);
         // a stage also holds the restored 16 KiB W tile of each chunk, which comes from
@@ -1290,7 +1313,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
             shrink_budget = SHRINK_SMEM_BUDGET_APART;
         } else {
             shrink_budget = SHRINK_SMEM_BUDGET_SHARED;
-            ds = decode_shape(d, Np, PROJ_SMEM_BUDGET_SHARED, zt);
+            ds = decode_shape(d, Np, PROJ_SMEM_BUDGET_SHARED, zt, mt);
         }
     }
 
@@ -1404,7 +1427,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     } else {
         cuuint64_t dims[2] = {(cuuint64_t)d.din, (cuuint64_t)d.dout};
         cuuint64_t strides[1] = {(cuuint64_t)d.din * 2};
-        cuuint32_t box[2] = {BK, decode ? (cuuint32_t)BM : 256u};
+        cuuint32_t box[2] = {BK, decode ? (cuuint32_t)(mt * BM) : 256u};
         if (!tc_encode(&tmW, a.W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
@@ -1424,12 +1447,12 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         return launch_prefill(a, tmX, tmW, tmV, sm_count(), shrink, st);
     }
 
-    const int tiles = proj_tiles(d);
+    const int tiles = (d.dout + mt * BM - 1) / (mt * BM);   // CTAs' row blocks
     const int budget = ds.budget, pkc = ds.pkc;
     if (pkc > 1) {
         cuuint64_t wdims[3] = {(cuuint64_t)BK, (cuuint64_t)d.dout, (cuuint64_t)kb_total};
         cuuint64_t strides[2] = {(cuuint64_t)d.din * 2, (cuuint64_t)BK * 2};
-        cuuint32_t wbox[3] = {BK, (cuuint32_t)BM, (cuuint32_t)pkc};
+        cuuint32_t wbox[3] = {BK, (cuuint32_t)(mt * BM), (cuuint32_t)pkc};
         if (!a.qmode && !tc_encode(&tmW, a.W, 3, wdims, strides, wbox, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
         cuuint64_t xdims[3] = {(cuuint64_t)BK, (cuuint64_t)T, (cuuint64_t)kb_total};
@@ -1456,10 +1479,11 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
     const int rx_bytes = p.push ? BM * Np * 4 : 0;
     // (over codes, the code tile too, and over 4-bit codes the K block's scales)
-    const int sbytes = (pkc * (stage_bytes(Np) + BM * q_x + (a.qmode == QMODE_NF4 ? BM * 4 : 0)) + 1023) & ~1023;
+    const int sbytes = (pkc * (stage_bytes(Np) + (mt - 1) * A_BYTES + BM * q_x + (a.qmode == QMODE_NF4 ? BM * 4 : 0)) +
+                        1023) & ~1023;
     const int qtab_bytes = a.qmode == QMODE_NF4 ? 64 : 0;
     p.stages = clamp_stages((budget - rx_bytes - qtab_bytes) / sbytes);
-    p.a_sub = A_BYTES;
+    p.a_sub = mt * A_BYTES;
     p.ring_bytes = p.stages * sbytes;
     p.rx_off = p.ring_bytes;
     p.qtab_off = p.ring_bytes + rx_bytes;
@@ -1480,6 +1504,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.q_x = q_x;
     p.qscale = a.qscale;
     p.up_rows = a.maps.up_rows;
+    p.mt = mt;
     for (int i = 0; i < 16; ++i) p.qcb[i] = a.qcb[i];
     return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, zt), dim3(NUM_THREADS), smem_bytes(p), st, true,
                     p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.upw128, tmQs, p);

@@ -144,6 +144,22 @@ def test_ragged_shapes(T, din, dout, ranks, dtype):
     assert_within(run_layer(layer, pool), want_of(layer), dtype, f"ragged {T}x{din}x{dout}")
 
 
+@pytest.mark.parametrize("T,din,dout,row_map", [
+    (100, 1024, 20000, False),   # 157 row tiles: two per CTA, the last 256-row block ragged (32 rows)
+    (128, 4096, 22016, True),    # the 7B layer's gate|up shape, row map of rows without adapter
+])
+def test_two_row_tiles_per_cta(T, din, dout, row_map):
+    """More 128-row W tiles than SMs and no adapters: each CTA takes two row tiles that
+    share its X stages (two accumulators, a 256-row partial tile in the split-K sums)."""
+    layer = wl.random_layer(T + dout, T=T, din=din, dout=dout, ranks=[])
+    pool = make_pool(layer)
+    X, W, ra, Y = upload(layer)
+    pool.forward(X, W, ra if row_map else None, Y)
+    torch.cuda.synchronize()
+    assert_within(to_f64(Y), want_of(layer), "bf16", f"two row tiles per CTA, {T}x{din}x{dout}")
+    assert pool.status() == mlora.MLORA_OK
+
+
 def test_many_loaded_slots_few_used():
     """300 loaded rank-16 slots, a batch that uses three of them: the shrink and the
     expand skip the unused chunks, and one projection CTA holds more chunks (300,
