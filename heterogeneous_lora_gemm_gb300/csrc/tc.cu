@@ -190,10 +190,6 @@ struct GemmParams {
     float qcb[16];                  // QMODE_NF4: the codebook
     int qtab_off;                   // QMODE_NF4: shared-memory offset of the codebook (16 floats)
     int up_rows;                    // projection: output rows per row of the Up map (8 or 1)
-    // projection: 128-row W tiles per CTA (1 or 2), sharing each X stage; with 2 the CTA
-    // owns 256 output rows, two MMAs per K slice into two accumulators (no K-extension,
-    // no codes, split-K through the staged cluster reduction, N <= 128)
-    int mt;
 };
 
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
@@ -346,7 +342,10 @@ __device__ __forceinline__ void restore_row(const uint8_t* codes, uint8_t* arow,
 
 // ---------------------------------------------------------------- the GEMM kernel
 // Two CTAs per SM: a shrink CTA and a projection CTA launched behind it share an SM.
-template <bool SHRINK>
+// MT: 128-row W tiles per projection CTA (1 or 2), sharing each X stage; with 2 the CTA
+// owns 256 output rows, two MMAs per K slice into two accumulators (no K-extension, no
+// codes, split-K through the staged cluster reduction, N <= 128).
+template <bool SHRINK, int MT = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 2)
 swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmArena,
@@ -367,8 +366,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tile = blockIdx.x, split = blockIdx.y, ztile = blockIdx.z;
-    const int MT = (!SHRINK && p.mt > 1) ? p.mt : 1;   // 128-row W tiles of this CTA
-    const int RB = MT * BM;                             // its output rows
+    static_assert(MT == 1 || (!SHRINK && MT == 2), "two row tiles only in the projection");
+    constexpr int RB = MT * BM;                         // output rows of this CTA
     constexpr int kStampKind = SHRINK ? STAMP_SHRINK : STAMP_PROJECTION;
     const int tok0 = ztile * p.N;                    // first token of this token tile
     const int T = min(p.T - tok0, p.N);              // tokens in this tile
@@ -777,6 +776,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     for (int k = 0; k < BK / 16; ++k) {
                         // tile u's rows follow tile u-1's in the W box (128-row blocks of
                         // the 128-byte swizzle); each accumulator starts fresh on its first MMA
+#pragma unroll
                         for (int u = 0; u < MT; ++u)
                             mma_bf16(tmem + (uint32_t)(u * p.N), sdesc(ak + u * A_BYTES + k * 32, 1024, SW128),
                                      sdesc(bk + k * 32, 1024, SW128), idesc, acc);
@@ -995,6 +995,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         for (int p0 = 0; p0 < T; p0 += tp) {
             const int pt = min(tp, T - p0);
             if (warp >= 2 && q * 32 < rows)
+#pragma unroll
                 for (int u = 0; u < MT; ++u)   // accumulator u holds rows u * 128 + row
                     for (int t0 = 0; t0 < pt; t0 += 16) {
                         float v[16];
@@ -1130,6 +1131,10 @@ cudaError_t tc_init() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(swapab_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin - (int)fa.sharedSizeBytes);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, swapab_gemm_kernel<false, 2>);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(swapab_gemm_kernel<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - (int)fa.sharedSizeBytes);
     if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, swapab_gemm_kernel<true>);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(swapab_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1138,6 +1143,8 @@ cudaError_t tc_init() {
     // consecutive kernels can share an SM without reconfiguring it
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(swapab_gemm_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(swapab_gemm_kernel<false, 2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(swapab_gemm_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess) e = prefill_init();
@@ -1504,9 +1511,9 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.q_x = q_x;
     p.qscale = a.qscale;
     p.up_rows = a.maps.up_rows;
-    p.mt = mt;
     for (int i = 0; i < 16; ++i) p.qcb[i] = a.qcb[i];
-    return launch_k(swapab_gemm_kernel<false>, dim3(tiles, p.splits, zt), dim3(NUM_THREADS), smem_bytes(p), st, true,
+    return launch_k(mt > 1 ? swapab_gemm_kernel<false, 2> : swapab_gemm_kernel<false, 1>, dim3(tiles, p.splits, zt),
+                    dim3(NUM_THREADS), smem_bytes(p), st, true,
                     p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.upw128, tmQs, p);
 }
 
