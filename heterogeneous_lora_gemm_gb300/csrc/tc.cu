@@ -114,8 +114,8 @@ constexpr int MAX_SLOT_WORDS = 4096 / 32;
 constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
 constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
 constexpr int PROJ_KC = 2;         // projection: K chunks of 64 per pipeline step (one 3D box each for W and X)
-constexpr int PROJ_ZT_N = 128;
-constexpr int QUANT_KC = 2;        // projection over codes: K chunks of 64 per pipeline step     // projection: tokens per token tile of a decode batch above this size
+constexpr int PROJ_ZT_N = 128;     // projection: tokens per token tile of a decode batch above this size
+constexpr int QUANT_KC = 2;        // projection over codes: K chunks of 64 per pipeline step
 constexpr int QMODE_INT8 = 1, QMODE_NF4 = 2;
 
 __host__ __device__ constexpr int b_bytes(int n) { return n * BK * 2; }
@@ -281,6 +281,19 @@ __device__ __forceinline__ uint32_t scaled_pair_bf16(float2 v, float sc) {
 // restored values bf16(codebook[i] * scale) are formed once per K block and kept as
 // byte tables in registers (low bytes, high bytes); byte permutations then look up
 // four codes at a time, no per-code arithmetic and no memory access.
+// 16 int8 codes -> 16 restored bf16 values (8 pairs, column order)
+__device__ __forceinline__ void int8_group_bf16(const uint4& raw, float sc, uint32_t (&w)[8]) {
+    const uint32_t wd[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
+                            raw.w ^ 0x80808080u};   // bytes c + 128
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t f0 = __byte_perm(wd[e], 0x4B000000u, 0x7540), f1 = __byte_perm(wd[e], 0x4B000000u, 0x7541);
+        const uint32_t f2 = __byte_perm(wd[e], 0x4B000000u, 0x7542), f3 = __byte_perm(wd[e], 0x4B000000u, 0x7543);
+        w[2 * e] = scaled_pair_bf16(f0, f1, -8388736.f, sc);
+        w[2 * e + 1] = scaled_pair_bf16(f2, f3, -8388736.f, sc);
+    }
+}
+
 __device__ __forceinline__ void restore_row(const uint8_t* codes, uint8_t* arow, int row, float sc, int qmode,
                                             const float* qcb) {
     const int sw = row & 7;
@@ -289,16 +302,8 @@ __device__ __forceinline__ void restore_row(const uint8_t* codes, uint8_t* arow,
         for (int jj = 0; jj < 4; ++jj) {
             const int j = (jj + row) & 3;   // codes of columns 16j .. 16j+15
             const uint4 raw = *reinterpret_cast<const uint4*>(codes + 16 * j);
-            const uint32_t wd[4] = {raw.x ^ 0x80808080u, raw.y ^ 0x80808080u, raw.z ^ 0x80808080u,
-                                    raw.w ^ 0x80808080u};   // bytes c + 128
             uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t f0 = __byte_perm(wd[e], 0x4B000000u, 0x7540), f1 = __byte_perm(wd[e], 0x4B000000u, 0x7541);
-                const uint32_t f2 = __byte_perm(wd[e], 0x4B000000u, 0x7542), f3 = __byte_perm(wd[e], 0x4B000000u, 0x7543);
-                w[2 * e] = scaled_pair_bf16(f0, f1, -8388736.f, sc);
-                w[2 * e + 1] = scaled_pair_bf16(f2, f3, -8388736.f, sc);
-            }
+            int8_group_bf16(raw, sc, w);
             *reinterpret_cast<uint4*>(arow + (((2 * j) ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(arow + (((2 * j + 1) ^ sw) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
@@ -337,6 +342,28 @@ __device__ __forceinline__ void restore_row(const uint8_t* codes, uint8_t* arow,
                                __byte_perm(t3, t4, 0x7632));
             }
         }
+    }
+}
+
+// The int8 codes of one row over a stage's two K chunks (128 bytes: chunk 0's 64 codes,
+// then chunk 1's) restored into both chunks' W rows as restore_row does, all eight
+// 16-byte reads issued first (starting at a row-dependent group: conflict-free across
+// 8 rows), so that one thread carries eight independent conversions.
+__device__ __forceinline__ void restore_row_int8x2(const uint8_t* codes, uint8_t* arow0, uint8_t* arow1, int row,
+                                                   float sc) {
+    const int sw = row & 7;
+    uint4 raw[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) raw[g] = *reinterpret_cast<const uint4*>(codes + 16 * ((g + row) & 7));
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const int gg = (g + row) & 7;   // chunk gg / 4, columns 16 (gg % 4) ..
+        uint8_t* arow = gg < 4 ? arow0 : arow1;
+        const int j = gg & 3;
+        uint32_t w[8];
+        int8_group_bf16(raw[g], sc, w);
+        *reinterpret_cast<uint4*>(arow + (((2 * j) ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(arow + (((2 * j + 1) ^ sw) * 16)) = make_uint4(w[4], w[5], w[6], w[7]);
     }
 }
 
@@ -830,12 +857,17 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     __syncwarp();
                     if (!__all_sync(0xffffffffu, got)) break;
                     uint8_t* stg = smem + (size_t)s * SB;
-                    for (int j = 0; j < p.kc; ++j) {   // the stage's K chunks
-                        // (4-bit codes: the row's scale of this K block came with the codes)
-                        const float sc =
-                            p.qmode == QMODE_NF4 ? reinterpret_cast<const float*>(stg + QS_OFF)[j * BM + row] : row_sc;
-                        restore_row(stg + Q_OFF + (row * p.kc + j) * p.q_x, stg + j * p.a_sub + row * 128, row, sc,
-                                    p.qmode, reinterpret_cast<const float*>(smem + p.qtab_off));
+                    if (p.qmode == QMODE_INT8 && p.kc == 2) {   // both K chunks of the stage at once
+                        restore_row_int8x2(stg + Q_OFF + row * 2 * p.q_x, stg + row * 128, stg + p.a_sub + row * 128, row,
+                                           row_sc);
+                    } else {
+                        for (int j = 0; j < p.kc; ++j) {   // the stage's K chunks
+                            // (4-bit codes: the row's scale of this K block came with the codes)
+                            const float sc =
+                                p.qmode == QMODE_NF4 ? reinterpret_cast<const float*>(stg + QS_OFF)[j * BM + row] : row_sc;
+                            restore_row(stg + Q_OFF + (row * p.kc + j) * p.q_x, stg + j * p.a_sub + row * 128, row, sc,
+                                        p.qmode, reinterpret_cast<const float*>(smem + p.qtab_off));
+                        }
                     }
                     fence_proxy_async_smem();   // the MMA (async proxy) reads what these threads wrote
                     __syncwarp();
