@@ -1515,7 +1515,10 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.splits = ds.splits;
     // small batches: the splits push their partial slices into a receive buffer
     p.push = (p.splits > 1 && Np <= PUSH_MAX_N && Np % p.splits == 0) ? 1 : 0;
-    p.ext_lead = (EXT_LEAD + pkc - 1) / pkc;
+    // K-extension steps: after the W steps, or, behind the CUDA-core shrink (done early
+    // in the W stream), a quarter of the way into them, where their Up tiles' DRAM
+    // latency overlaps the W stream
+    p.ext_lead = gemv ? 3 * (ds.ksteps / ds.splits) / 4 : (EXT_LEAD + pkc - 1) / pkc;
     const int rx_bytes = p.push ? BM * Np * 4 : 0;
     // (over codes, the code tile too, and over 4-bit codes the K block's scales)
     const int sbytes = (pkc * (stage_bytes(Np) + (mt - 1) * A_BYTES + BM * q_x + (a.qmode == QMODE_NF4 ? BM * 4 : 0)) +
