@@ -56,8 +56,10 @@ struct Workspace {
     int32_t* chunk_unit;   // [max_chunks] arena rank unit of the chunk's first rank column
     int32_t* chunk_kval;   // [max_chunks] valid rank columns of the chunk (<= CHUNK)
     float* v32;            // [max_tokens x max_rank] scale * Down x per row (SIMT path)
-    uint16_t* vt;          // [max_chunks x tcap x CHUNK] bf16 scale * Down x per loaded chunk (tensor path);
-                           // written for the (chunk, token tile) pairs tmask marks, read only there
+    uint16_t* vt;          // [max_chunks x 2 x tcap x 8] bf16 scale * Down x per loaded chunk (tensor path),
+                           // each chunk's 16 rank columns as two blocks of 8 (a block's 8 tokens
+                           // are one 128-byte row); written for the (chunk, token tile) pairs
+                           // tmask marks, read only there
     float* partials;       // split-K partial tiles
     int32_t* tile_ctr;     // split-K arrival counters (zero between forwards)
     const ChunkRec* chunks;   // [max_chunks] chunks of the loaded slots (pool state, not per forward)

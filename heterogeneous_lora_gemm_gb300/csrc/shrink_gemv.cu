@@ -197,9 +197,10 @@ __global__ void __launch_bounds__(G_THREADS, 1) shrink_gemv_kernel(const GemvPar
             __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
             w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.vt + ((size_t)c * p.tcap + t) * CHUNK);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        // Vt [chunk][block of 8 rank columns][tcap][8]
+        __nv_bfloat16* dst = p.vt + ((size_t)c * 2 * p.tcap + t) * 8;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + (size_t)p.tcap * 8) = make_uint4(w[4], w[5], w[6], w[7]);
     }
     if (threadIdx.x == 0) stamp_record(p.stamps, p.stamp_cap, t_start, STAMP_SHRINK);
 }

@@ -749,7 +749,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         waited = true;
                     }
                     mbar_expect_tx(&tl.full[s], (uint32_t)B_SUB);
-                    tma_3d(b, &tmV, &tl.full[s], 0, tok0, u * EXT_SUB);
+                    tma_3d(b, &tmV, &tl.full[s], 0, tok0 / 8, u * EXT_SUB * 2);
                 }
             }
             if (++s == NS) {
@@ -811,13 +811,14 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     }
                 }
             } else {
-                // Up chunk: [2 blocks of 8 columns][128 rows][16 B], no swizzle (K-direction core
-                // matrices BM*16 bytes apart, M-direction 128 bytes); Vt chunk: 32-byte swizzle
+                // Up chunk: [2 blocks of 8 columns][128 rows][16 B], Vt chunk: [2 blocks of 8
+                // columns][N tokens][16 B]; no swizzle (K-direction core matrices 128 or N rows
+                // x 16 bytes apart, M/N-direction 128 bytes)
 #pragma unroll
                 for (int j = 0; j < EXT_SUB; ++j)
                     if ((kind >> j) & 1) {
                         mma_bf16(tmem, sdesc_lbo(a + j * (BM * 32), BM * 16, 128, SW_NONE),
-                                 sdesc(b + j * (p.N * 32), 256, SW32), idesc, acc);
+                                 sdesc_lbo(b + j * (p.N * 32), p.N * 16, 128, SW_NONE), idesc, acc);
                         acc = 1;
                     }
             }
@@ -1059,7 +1060,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     uint2 w;
                     w.x = *reinterpret_cast<uint32_t*>(&lo);
                     w.y = *reinterpret_cast<uint32_t*>(&hi);
-                    *reinterpret_cast<uint2*>(p.vt + ((size_t)tl.my_c[k] * p.tcap + tok0 + p0 + t) * CHUNK + j0) = w;
+                    *reinterpret_cast<uint2*>(p.vt + (((size_t)tl.my_c[k] * 2 + (j0 >> 3)) * p.tcap + tok0 + p0 + t) * 8 +
+                                              (j0 & 7)) = w;
                 } else {
                     emit4(p0 + t, gi * 4, v);
                 }
@@ -1476,10 +1478,13 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         if (!tc_encode(&tmX, a.X, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     }
     {
-        cuuint64_t dims[3] = {(cuuint64_t)CHUNK, (cuuint64_t)d.tcap, (cuuint64_t)d.max_chunks};
-        cuuint64_t strides[2] = {(cuuint64_t)CHUNK * 2, (cuuint64_t)d.tcap * CHUNK * 2};
-        cuuint32_t box[3] = {CHUNK, (cuuint32_t)Np, EXT_SUB};
-        if (!tc_encode(&tmV, a.ws.vt, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_32B)) return cudaErrorInvalidValue;
+        // Vt [chunk][block of 8 rank columns][tcap][8] seen as rows of 128 bytes (8 tokens
+        // of one block): one box is a K-extension step's EXT_SUB chunks x 2 blocks x Np
+        // tokens, in the layout the MMA reads without swizzle, in Np / 8 rows per block
+        cuuint64_t dims[3] = {64, (cuuint64_t)d.tcap / 8, (cuuint64_t)d.max_chunks * 2};
+        cuuint64_t strides[2] = {128, (cuuint64_t)d.tcap * 16};
+        cuuint32_t box[3] = {64, (cuuint32_t)Np / 8, 2 * EXT_SUB};
+        if (!tc_encode(&tmV, a.ws.vt, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
     }
 
     if (!decode) {

@@ -156,7 +156,7 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         mbar_expect_tx(&full[s], 0);
                     } else {
                         mbar_expect_tx(&full[s], (uint32_t)(PA_BYTES + __popc(mask) * (PN * 32)));
-                        tma_3d(a, &tmV, &full[s], 0, m * PM, c0);
+                        tma_3d(a, &tmV, &full[s], 0, m * PM / 8, c0 * 2);
 #pragma unroll
                         for (int j = 0; j < EXT_SUB; ++j)   // two blocks of 8 rank columns x 256 rows
                             if ((mask >> j) & 1u) tma_3d(b + j * (PN * 32), &tmUp, &full[s], 0, n * PN / p.up_rows, un[j] >> 3);
@@ -202,12 +202,13 @@ prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_consta
                         acc = 1;
                     }
                 } else {
-                    // Vt chunk: 32-byte swizzle; Up chunk: [2 blocks of 8 columns][256 rows][16 B],
-                    // no swizzle (K-direction core matrices PN*16 bytes apart, N-direction 128)
+                    // Vt chunk: [2 blocks of 8 columns][128 tokens][16 B]; Up chunk: [2 blocks of 8
+                    // columns][256 rows][16 B]; no swizzle (K-direction core matrices PM*16 or
+                    // PN*16 bytes apart, M/N-direction 128)
 #pragma unroll
                     for (int j = 0; j < EXT_SUB; ++j)
                         if ((kind >> j) & 1) {
-                            mma_bf16(d, sdesc(a + j * (PM * 32), 256, SW32),
+                            mma_bf16(d, sdesc_lbo(a + j * (PM * 32), PM * 16, 128, SW_NONE),
                                      sdesc_lbo(b + j * (PN * 32), PN * 16, 128, SW_NONE), idesc, acc);
                             acc = 1;
                         }
