@@ -100,7 +100,7 @@ int sm_count() {
 // ---------------------------------------------------------------- constants
 constexpr int BM = 128;            // rows per tile (MMA M)
 constexpr int BK = 64;             // K per pipeline step (128 bytes of bf16)
-constexpr int EXT_SUB = 4;         // K-extension chunks per pipeline step
+constexpr int EXT_SUB = 4;         // K-extension chunks per pipeline step (one int4 of the step plan)
 constexpr int A_BYTES = BM * BK * 2;            // 16 KiB: W tile, 4 Up chunk tiles or 8 Down chunk tiles
 constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM, warps 2..5 epilogue
 constexpr int MAX_N = 256;
@@ -146,6 +146,8 @@ struct Tail {
     int ext_unit[EXT_CAP];            // projection: arena unit of each K-extension chunk, -1 = skip
     int ext_slot[EXT_CAP];            // (then: the K-extension units with a chunk to multiply)
     int n_ext, ext_first;             // projection: this split's share of that list
+    int4 ext_plan[EXT_CAP / EXT_SUB]; // projection: per listed step of this split, its chunks' arena
+    int ext_plan_u[EXT_CAP / EXT_SUB];   // units (-1 = not loaded), and the unit
     unsigned long long t_start;       // profiling: globaltimer at the CTA's start
 };
 
@@ -596,10 +598,21 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             if (any) tl.ext_slot[n_all + __popc(m & ((1u << lane) - 1u))] = uu;
             n_all += __popc(m);
         }
-        if (lane == 0) {
+        {
+            // this split's steps, each with its unit and its chunks' arena units in one
+            // 16-byte entry: the producer reads one entry per step instead of a chain
             const int f0 = (int)((long long)split * n_all / p.splits);
-            tl.ext_first = f0;
-            tl.n_ext = (int)((long long)(split + 1) * n_all / p.splits) - f0;
+            const int n_my = (int)((long long)(split + 1) * n_all / p.splits) - f0;
+            for (int e = lane; e < n_my; e += 32) {
+                const int uu = tl.ext_slot[f0 + e];
+                tl.ext_plan_u[e] = uu;
+                tl.ext_plan[e] = make_int4(tl.ext_unit[uu * EXT_SUB], tl.ext_unit[uu * EXT_SUB + 1],
+                                           tl.ext_unit[uu * EXT_SUB + 2], tl.ext_unit[uu * EXT_SUB + 3]);
+            }
+            if (lane == 0) {
+                tl.ext_first = f0;
+                tl.n_ext = n_my;
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_expect_tx(&tl.info_ready, 0);
@@ -712,27 +725,34 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     tma_2d(b, &tmX, &tl.full[s], kb * BK, tok0);
                 }
             } else {
-                const int u = ext_unit_at(i - ins);
-                const int kx = u * EXT_SUB;   // the unit's first chunk
-                int un[EXT_SUB];
+                const int e = i - ins;
+                int u, un[EXT_SUB];
                 uint32_t mask = 0;
+                if (e < tl.n_ext) {   // a listed step: its entry of the plan
+                    const int4 pl = tl.ext_plan[e];
+                    u = tl.ext_plan_u[e];
+                    un[0] = pl.x;
+                    un[1] = pl.y;
+                    un[2] = pl.z;
+                    un[3] = pl.w;
+                } else {              // a unit past the listed ones (split by index)
+                    u = ext_unit_at(e);
 #pragma unroll
-                for (int j = 0; j < EXT_SUB; ++j) {
-                    const int c = u * EXT_SUB + j;
-                    int v = -1;
-                    if (c < p.n_chunks) {
-                        if (kx + j < EXT_CAP) {
-                            v = tl.ext_unit[kx + j];
-                        } else {
+                    for (int j = 0; j < EXT_SUB; ++j) {
+                        const int c = u * EXT_SUB + j;
+                        int v = -1;
+                        if (c < p.n_chunks) {
                             const ChunkRec cr = p.chunks[c];
                             if (((tl.slot_bits[cr.slot >> 5] >> (cr.slot & 31)) & 1u) && cr.row0 < (tile + 1) * BM &&
                                 cr.row1 > tile * BM)
                                 v = cr.unit;
                         }
+                        un[j] = v;
                     }
-                    un[j] = v;
-                    if (v >= 0) mask |= 1u << j;
                 }
+#pragma unroll
+                for (int j = 0; j < EXT_SUB; ++j)
+                    if (un[j] >= 0) mask |= 1u << j;
                 tl.stage_kind[s] = (int)mask;
                 if (mask == 0) {
                     mbar_expect_tx(&tl.full[s], 0);
