@@ -119,6 +119,7 @@ struct mlora_pool {
     ChunkRec* d_chunks = nullptr;    // = set_chunks[cur]: chunks of the loaded slots, in arena order
     int n_chunks = 0;
     int tile_span = 0;               // largest arena span of 8 consecutive chunks of the table
+    int run_stride = 0;              // most common arena stride of 4-chunk K-extension units (0: none)
     TcArenaMaps maps{};              // TMA descriptors of the whole arena (bf16 pools)
     size_t table_bytes = 0;
     char* ws_base = nullptr;
@@ -226,6 +227,26 @@ mlora_status build_chunks(mlora_pool* p, std::vector<ChunkRec>& host) {
             if (host[c].unit < host[c - 1].unit) span = INT_MAX;
         if (span > p->tile_span) p->tile_span = span;
     }
+    // K-extension units (4 consecutive chunks of the table) whose chunks lie at one
+    // stride in the arena, within one module: the most common such stride lets a
+    // projection load a unit's Up tiles in one box (e.g. the q chunks of tenants whose
+    // slots each hold a q and a v adapter of one rank)
+    std::map<int, int> votes;
+    for (size_t u0 = 0; u0 + 4 <= host.size(); u0 += 4) {
+        const int d = host[u0 + 1].unit - host[u0].unit;
+        bool run = d >= CHUNK;
+        for (size_t j = 1; j < 4 && run; ++j)
+            run = host[u0 + j].unit - host[u0 + j - 1].unit == d && host[u0 + j].row0 == host[u0].row0 &&
+                  host[u0 + j].row1 == host[u0].row1;
+        if (run) ++votes[d];
+    }
+    p->run_stride = 0;
+    int best = 0;
+    for (const auto& v : votes)
+        if (v.second > best) {
+            best = v.second;
+            p->run_stride = v.first;
+        }
     return MLORA_OK;
 }
 
@@ -870,6 +891,8 @@ static mlora_status forward_impl(mlora_pool_t p, const void* X, const void* W, c
         a.dims = p->dims;
         a.n_chunks = p->n_chunks;
         a.tile_span = p->tile_span;
+        a.run_stride = p->run_stride;
+        a.arena_up = p->arena_up;
         a.units = p->units;
         a.n_loaded = p->loaded;
         a.stamps = p->prof_stamps;

@@ -79,7 +79,7 @@ bool tc_encode_typed(CUtensorMap* map, CUtensorMapDataType type, const void* bas
                      const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint32_t estr[3] = {1, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};   // (element strides, up to rank 5)
     CUresult r = fn(map, type, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -110,6 +110,9 @@ constexpr int MAX_SPLITS = 16;     // K splits per tile at most
 constexpr int MAX_CLUSTER = 8;     // K splits of a tile reduced inside one (portable) cluster
 constexpr int MAX_STAGES = 12;
 constexpr int EXT_CAP = 256;       // projection: K-extension chunks of a CTA kept in shared memory
+constexpr int UNUSED = 1 << 30;    // projection: flag of a listed chunk's arena unit the batch does not use
+// the arena unit of a listed chunk the batch uses, else -1
+__host__ __device__ constexpr int used_unit(int v) { return v >= 0 && !(v & UNUSED) ? v : -1; }
 constexpr int MAX_SLOT_WORDS = 4096 / 32;
 constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
 constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
@@ -143,11 +146,14 @@ struct Tail {
     float my_scale[CHUNKS_PER_TILE];
     int tile_ra[MAX_N];               // shrink: slot id of each token of the token tile
     uint32_t slot_bits[MAX_SLOT_WORDS];   // projection: slots some row of the batch uses
-    int ext_unit[EXT_CAP];            // projection: arena unit of each K-extension chunk, -1 = skip
+    int ext_unit[EXT_CAP];            // projection: arena unit of each K-extension chunk of this tile's
+                                      // module (| UNUSED when the batch does not use it), -1 = none
     int ext_slot[EXT_CAP];            // (then: the K-extension units with a chunk to multiply)
     int n_ext, ext_first;             // projection: this split's share of that list
     int4 ext_plan[EXT_CAP / EXT_SUB]; // projection: per listed step of this split, its chunks' arena
-    int ext_plan_u[EXT_CAP / EXT_SUB];   // units (-1 = not loaded), and the unit
+                                      // units (-1 = not loaded), and
+    int ext_plan_u[EXT_CAP / EXT_SUB];   // its unit (bits 0-7) | (arena unit of its first chunk + 1)
+                                         // << 8 when its 4 chunks form a run (else 0 there)
     unsigned long long t_start;       // profiling: globaltimer at the CTA's start
 };
 
@@ -192,6 +198,10 @@ struct GemmParams {
     float qcb[16];                  // QMODE_NF4: the codebook
     int qtab_off;                   // QMODE_NF4: shared-memory offset of the codebook (16 floats)
     int up_rows;                    // projection: output rows per row of the Up map (8 or 1)
+    // projection: a K-extension step whose 4 chunks lie at a stride of run_b blocks of
+    // 8 rank columns loads their Up tiles in one box of the runs map ({64, dout / 8,
+    // run_b, run_groups}); run_b = 0: never (always over codes)
+    int run_b, run_groups;
 };
 
 // Sum of one slice of the staged partial tiles: groups g in [et, ng) step nthr of 4
@@ -378,7 +388,10 @@ template <bool SHRINK, int MT = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 2)
 swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmArena,
-                   const __grid_constant__ CUtensorMap tmQs, GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmAux, GemmParams p) {
+    // tmAux: over 4-bit codes, the block scales; else, with adapters, the Up arena as runs
+    const CUtensorMap& tmQs = tmAux;
+    const CUtensorMap& tmRun = tmAux;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Tail& tl = *reinterpret_cast<Tail*>(smem + p.tail_off);
@@ -459,6 +472,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         if (!SHRINK && p.qmode == QMODE_NF4) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmQs) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
         if (SHRINK || p.ext_units > 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmArena) : "memory");
+        if (!SHRINK && p.run_b > 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmRun) : "memory");
     }
     if (!SHRINK && p.qmode == QMODE_NF4 && threadIdx.x < 16)   // the codebook of the 4-bit restore
         reinterpret_cast<float*>(smem + p.qtab_off)[threadIdx.x] = p.qcb[threadIdx.x];
@@ -580,7 +594,8 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         __syncwarp();
         for (int k = lane; k < nx; k += 32) {
             const int sl = tl.ext_slot[k];
-            if (sl < 0 || !((tl.slot_bits[sl >> 5] >> (sl & 31)) & 1u)) tl.ext_unit[k] = -1;
+            if (tl.ext_unit[k] >= 0 && (sl < 0 || !((tl.slot_bits[sl >> 5] >> (sl & 31)) & 1u)))
+                tl.ext_unit[k] |= UNUSED;
         }
         __syncwarp();
         // The tile's K-extension steps: only the listed units with a chunk to multiply
@@ -592,7 +607,7 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             bool any = false;
             if (uu < LU)
 #pragma unroll
-                for (int j = 0; j < EXT_SUB; ++j) any |= tl.ext_unit[uu * EXT_SUB + j] >= 0;
+                for (int j = 0; j < EXT_SUB; ++j) any |= used_unit(tl.ext_unit[uu * EXT_SUB + j]) >= 0;
             const unsigned m = __ballot_sync(0xffffffffu, any);
             __syncwarp();   // (the list overwrites the slot ids read above)
             if (any) tl.ext_slot[n_all + __popc(m & ((1u << lane) - 1u))] = uu;
@@ -605,9 +620,29 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             const int n_my = (int)((long long)(split + 1) * n_all / p.splits) - f0;
             for (int e = lane; e < n_my; e += 32) {
                 const int uu = tl.ext_slot[f0 + e];
-                tl.ext_plan_u[e] = uu;
-                tl.ext_plan[e] = make_int4(tl.ext_unit[uu * EXT_SUB], tl.ext_unit[uu * EXT_SUB + 1],
-                                           tl.ext_unit[uu * EXT_SUB + 2], tl.ext_unit[uu * EXT_SUB + 3]);
+                tl.ext_plan[e] = make_int4(used_unit(tl.ext_unit[uu * EXT_SUB]), used_unit(tl.ext_unit[uu * EXT_SUB + 1]),
+                                           used_unit(tl.ext_unit[uu * EXT_SUB + 2]),
+                                           used_unit(tl.ext_unit[uu * EXT_SUB + 3]));
+                // a run: all 4 chunks in the table and in this tile's module, at the stride
+                // of the run map, inside it (chunks the batch does not use are loaded too,
+                // and not multiplied)
+                int r0 = -1;
+                if (p.run_b > 0) {
+                    int cu[EXT_SUB];
+                    bool ok = true;
+#pragma unroll
+                    for (int j = 0; j < EXT_SUB; ++j) {
+                        const int v = tl.ext_unit[uu * EXT_SUB + j];
+                        cu[j] = v & ~UNUSED;
+                        ok = ok && v >= 0;
+                    }
+                    const int b0 = cu[0] >> 3;
+#pragma unroll
+                    for (int j = 1; j < EXT_SUB; ++j) ok = ok && cu[j] - cu[0] == j * 8 * p.run_b;
+                    ok = ok && (cu[0] & 7) == 0 && b0 % p.run_b + 2 <= p.run_b && b0 / p.run_b + EXT_SUB <= p.run_groups;
+                    if (ok) r0 = cu[0];
+                }
+                tl.ext_plan_u[e] = uu | ((r0 + 1) << 8);
             }
             if (lane == 0) {
                 tl.ext_first = f0;
@@ -726,11 +761,13 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                 }
             } else {
                 const int e = i - ins;
-                int u, un[EXT_SUB];
+                int u, un[EXT_SUB], run0 = -1;
                 uint32_t mask = 0;
                 if (e < tl.n_ext) {   // a listed step: its entry of the plan
                     const int4 pl = tl.ext_plan[e];
-                    u = tl.ext_plan_u[e];
+                    const int pu = tl.ext_plan_u[e];
+                    u = pu & 0xFF;
+                    run0 = (pu >> 8) - 1;
                     un[0] = pl.x;
                     un[1] = pl.y;
                     un[2] = pl.z;
@@ -758,12 +795,18 @@ swapab_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     mbar_expect_tx(&tl.full[s], 0);
                 } else {
                     // Up tiles (two blocks of 8 rank columns x 128 rows) are the pool's own
-                    // data: issue them before waiting for the shrink, then its Vt
-                    mbar_expect_tx_only(&tl.full[s], (uint32_t)(__popc(mask) * (BM * 32)));
+                    // data: issue them before waiting for the shrink, then its Vt.  A run's
+                    // 4 chunks are one box (the same layout: chunk j at j x 4 KiB)
+                    if (run0 >= 0) {
+                        mbar_expect_tx_only(&tl.full[s], (uint32_t)(EXT_SUB * (BM * 32)));
+                        tma_4d(a, &tmRun, &tl.full[s], 0, tile * BM / 8, (run0 >> 3) % p.run_b, (run0 >> 3) / p.run_b);
+                    } else {
+                        mbar_expect_tx_only(&tl.full[s], (uint32_t)(__popc(mask) * (BM * 32)));
 #pragma unroll
-                    for (int j = 0; j < EXT_SUB; ++j)
-                        if ((mask >> j) & 1u)
-                            tma_3d(a + j * (BM * 32), &tmArena, &tl.full[s], 0, tile * BM / p.up_rows, un[j] >> 3);
+                        for (int j = 0; j < EXT_SUB; ++j)
+                            if ((mask >> j) & 1u)
+                                tma_3d(a + j * (BM * 32), &tmArena, &tl.full[s], 0, tile * BM / p.up_rows, un[j] >> 3);
+                    }
                     if (!waited) {
                         if (p.pdl) pdl_wait();   // Vt comes from the shrink
                         waited = true;
@@ -1510,6 +1553,21 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     if (!decode) {
         return launch_prefill(a, tmX, tmW, tmV, sm_count(), shrink, st);
     }
+    // the Up arena seen as runs: {64 (8 rows x 8 columns), dout / 8, run_b blocks of 8
+    // rank columns, groups of run_b blocks}; a box is a K-extension step's 4 chunks of a
+    // run (2 blocks each) over 128 output rows
+    CUtensorMap tmRun;
+    std::memset(&tmRun, 0, sizeof tmRun);
+    int run_b = 0, run_groups = 0;
+    if (shrink && !a.qmode && a.run_stride >= CHUNK && a.run_stride % 8 == 0 && a.maps.up_rows == 8 && a.arena_up) {
+        run_b = a.run_stride / 8;
+        run_groups = a.units / a.run_stride;
+        cuuint64_t dims[4] = {64, (cuuint64_t)d.dout / 8, (cuuint64_t)run_b, (cuuint64_t)run_groups};
+        cuuint64_t strides[3] = {128, (cuuint64_t)d.dout * 16, (cuuint64_t)d.dout * 16 * run_b};
+        cuuint32_t box[4] = {64, BM / 8, 2, EXT_SUB};
+        if (run_groups < EXT_SUB || !tc_encode(&tmRun, a.arena_up, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+            run_b = run_groups = 0;
+    }
 
     const int tiles = (d.dout + mt * BM - 1) / (mt * BM);   // CTAs' row blocks
     const int budget = ds.budget, pkc = ds.pkc;
@@ -1571,10 +1629,12 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     p.q_x = q_x;
     p.qscale = a.qscale;
     p.up_rows = a.maps.up_rows;
+    p.run_b = run_b;
+    p.run_groups = run_groups;
     for (int i = 0; i < 16; ++i) p.qcb[i] = a.qcb[i];
     return launch_k(mt > 1 ? swapab_gemm_kernel<false, 2> : swapab_gemm_kernel<false, 1>, dim3(tiles, p.splits, zt),
                     dim3(NUM_THREADS), smem_bytes(p), st, true,
-                    p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.upw128, tmQs, p);
+                    p.cluster ? p.splits : 1, tmW, tmX, tmV, a.maps.upw128, a.qmode ? tmQs : tmRun, p);
 }
 
 cudaError_t tc_project_with_scratch(const void* X, const void* W, int T, int din, int dout, void* Y,

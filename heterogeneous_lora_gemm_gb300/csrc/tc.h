@@ -45,10 +45,12 @@ struct TcForwardArgs {
     const SlotRec* slots;
     TcArenaMaps maps;
     const void* arena_down;
+    const void* arena_up;   // the Up arena [units / 8][dout][8]
     Workspace ws;
     PoolDims dims;
     int n_chunks;           // chunks of the loaded slots (entries of ws.chunks: by module, then arena order)
     int tile_span;          // largest arena span of 8 consecutive chunks (first unit to last unit + 16)
+    int run_stride;         // most common arena stride (rank units) of 4-chunk units, 0 = none
     int units;              // rank units of the arena
     int n_loaded;           // loaded slots
     unsigned long long* stamps;   // profiling records of the kernels' CTAs (NULL = off)
