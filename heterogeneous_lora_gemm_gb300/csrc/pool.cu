@@ -1082,6 +1082,8 @@ mlora_status mlora_pool_info(mlora_pool_t p, mlora_pool_info_t* info) {
     info->arena_bytes = p->arena_bytes;
     info->table_bytes = p->table_bytes;
     info->workspace_bytes = p->ws_bytes;
+    info->ext_run_stride = p->run_stride;
+    info->reserved = 0;
     return MLORA_OK;
 }
 

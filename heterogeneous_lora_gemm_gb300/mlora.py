@@ -43,7 +43,8 @@ class PoolInfo(ctypes.Structure):
                 ("max_slots", ctypes.c_int32), ("max_rank", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("rank_units", ctypes.c_int32), ("rank_units_used", ctypes.c_int32), ("loaded", ctypes.c_int32),
                 ("device", ctypes.c_int32), ("arena_bytes", ctypes.c_uint64), ("table_bytes", ctypes.c_uint64),
-                ("workspace_bytes", ctypes.c_uint64)]
+                ("workspace_bytes", ctypes.c_uint64), ("ext_run_stride", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib = None

@@ -70,6 +70,11 @@ typedef struct mlora_pool_info_s {
     uint64_t arena_bytes;        /* device bytes of the adapter arena (Down and Up) */
     uint64_t table_bytes;        /* device bytes of the slot table and per-slot descriptors */
     uint64_t workspace_bytes;    /* device bytes of the per-forward workspace */
+    int32_t ext_run_stride;      /* bf16 pools: arena stride (rank units) at which the loaded
+                                    adapters' chunks most often lie in runs of 4 of one module;
+                                    the decode projection loads such a run's Up tiles in one
+                                    TMA box (0 = no run) */
+    int32_t reserved;
 } mlora_pool_info_t;
 
 /* Text for a status code (static storage). */

@@ -600,6 +600,50 @@ def test_fused_projection_with_per_module_adapters(T):
     assert e.value.status == mlora.MLORA_ERR_RANK
 
 
+@pytest.mark.parametrize("T,layout", [(128, "uniform"), (96, "mixed"), (48, "mixed")])
+def test_fused_projection_up_runs(T, layout):
+    """Tenants that each hold a q and a v adapter of rank 16 put consecutive tenants' q
+    (and v) chunks 32 rank columns apart in the arena: a K-extension step of 4 such
+    chunks loads their Up tiles in one box.  'mixed' breaks some of those runs with
+    tenants of other shapes (q alone, rank 8, rank 32, v alone) between them.  The v rows
+    start inside a 128-row tile, and the last tenants' chunks end the arena."""
+    from heterogeneous_lora_gemm_gb300 import Pool
+    rng = np.random.default_rng(61 + T)
+    din, modules = 512, [(0, 320), (320, 320)]   # q rows, v rows
+    dout = 640
+    n = 37
+    shapes = [(16, 16)] * n                      # (rank of q, rank of v) per tenant
+    if layout == "mixed":
+        shapes = list(shapes)
+        for s_, sh in ((5, (8, 0)), (13, (32, 16)), (14, (16, 0)), (29, (0, 24))):
+            shapes[s_] = sh
+    def rnd(shape, std):   # bf16 bit patterns
+        return wl.f32_to_bf16_bits(rng.standard_normal(shape) * std)
+    ads = [[(rnd((r, din), 1 / 16), rnd((modules[m][1], r), 0.05), 1.0 + 0.25 * m) if r else None
+            for m, r in enumerate(sh)] for sh in shapes]
+    budget = sum((r + 15) // 16 * 16 for sh in shapes for r in sh)   # a module takes whole chunks
+    pool = Pool(n, budget, 48, din, dout, "bf16", T)
+    for s_ in range(n):
+        mods = []
+        for m, (off, rows) in enumerate(modules):
+            a = ads[s_][m]
+            mods.append((off, rows, to_device(a[0], "bf16"), to_device(a[1], "bf16", "cpu"), a[2]) if a
+                        else (off, rows, None, None, 0.0))
+        pool.load_modules(s_, mods)
+    assert pool.info().ext_run_stride == 32
+    W = rnd((dout, din), 0.02)
+    X = rnd((T, din), 1.0)
+    ra = rng.choice(np.arange(-1, n, dtype=np.int32), size=T).astype(np.int32)
+    f64 = wl.bf16_bits_to_f64
+    tenants = [[oracle.OracleAdapter(f64(a[0]), f64(a[1]), a[2]) if a else None for a in row] for row in ads]
+    Y = torch.empty((T, dout), dtype=torch.bfloat16, device="cuda")
+    pool.forward(to_device(X, "bf16"), to_device(W, "bf16"), torch.from_numpy(ra).cuda(), Y)
+    torch.cuda.synchronize()
+    want = oracle.forward_modules(f64(X), f64(W), ra, modules, tenants)
+    assert_within(to_f64(Y), want, "bf16", f"fused projection with Up runs, T = {T}, {layout}")
+    assert pool.status() == mlora.MLORA_OK
+
+
 # --------------------------------------------------------------------------- #
 # host (cold) tier and asynchronous prefetch (M031 §06)
 def _host_tier_pool(layer, extra_budget=0, max_rank=None):
