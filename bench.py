@@ -262,7 +262,7 @@ def busy_union(rec: np.ndarray, kind: int) -> float:
 
 
 # --------------------------------------------------------------------------- #
-# algorithmic work (SURVEY-style accounting: what the method must move or compute)
+# algorithmic work: what the method must move or compute
 def call_work(din: int, dout: int, T: int, row_adapter, ranks_of_slot, up_rows_of_slot=None):
     """Bytes and FLOPs of one forward and of its projection kernel.  ranks_of_slot[s] is the
     list of (rank, rows its Up reaches) of slot s's adapters (one per adapted module)."""
