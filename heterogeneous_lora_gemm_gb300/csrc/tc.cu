@@ -111,6 +111,7 @@ constexpr int MAX_CLUSTER = 8;     // K splits of a tile reduced inside one (por
 constexpr int MAX_STAGES = 12;
 constexpr int EXT_CAP = 256;       // projection: K-extension chunks of a CTA kept in shared memory
 constexpr int UNUSED = 1 << 30;    // projection: flag of a listed chunk's arena unit the batch does not use
+constexpr int RUN_UNITS_MAX = (1 << 23) - 1;   // arenas read as runs: a step plan entry packs unit + 1 << 8
 // the arena unit of a listed chunk the batch uses, else -1
 __host__ __device__ constexpr int used_unit(int v) { return v >= 0 && !(v & UNUSED) ? v : -1; }
 constexpr int MAX_SLOT_WORDS = 4096 / 32;
@@ -1559,7 +1560,8 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     CUtensorMap tmRun;
     std::memset(&tmRun, 0, sizeof tmRun);
     int run_b = 0, run_groups = 0;
-    if (shrink && !a.qmode && a.run_stride >= CHUNK && a.run_stride % 8 == 0 && a.maps.up_rows == 8 && a.arena_up) {
+    if (shrink && !a.qmode && a.run_stride >= CHUNK && a.run_stride % 8 == 0 && a.maps.up_rows == 8 && a.arena_up &&
+        a.units <= RUN_UNITS_MAX) {
         run_b = a.run_stride / 8;
         run_groups = a.units / a.run_stride;
         cuuint64_t dims[4] = {64, (cuuint64_t)d.dout / 8, (cuuint64_t)run_b, (cuuint64_t)run_groups};
