@@ -58,6 +58,7 @@ STAMP_SHRINK, STAMP_PROJECTION, STAMP_PREFILL = 0, 1, 2
 KIND_NAMES = {STAMP_SHRINK: "shrink (swapab_gemm_kernel<true> or shrink_gemv_kernel)", STAMP_PROJECTION: "swapab_gemm_kernel<false>",
               STAMP_PREFILL: "prefill_gemm_kernel"}
 SUB_WORKLOADS = {"decode_step": (20480, 64), "fragmented_decode": (8192, 32), "prefill": (256, 8)}
+MAX_DECODE_T = 256   # the widest batch the decode kernels (swap-AB projection) take
 
 
 def parse_args(argv=None):
@@ -657,6 +658,27 @@ def run_extras(calls, L, stream, dev, peaks):
                         "merge_quantized_gbs": (2 * n_w + 8 * L.dout) / mq_us / 1e3,
                         "base": "int8 codes, fp32 scale per output row; the decode projection reads the codes",
                         "copies": qn}
+    # the same comparison at wider batches (the decode step's adapters, its row map
+    # repeated): the codes path moves half of W's bytes and restores W in every stage
+    qpool = Pool(L.max_slots, sum((a.rank + 7) // 8 * 8 for a in L.adapters), L.max_rank, L.din, L.dout, "bf16",
+                 MAX_DECODE_T)
+    for a in L.adapters:
+        qpool.load(a.slot, to_device(a.down, "bf16"), to_device(a.up, "bf16"), a.scale)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    by_t = {}
+    for T in (32, 128, 192, MAX_DECODE_T):
+        Xt = torch.randn((T, L.din), generator=gen, device=dev).to(torch.bfloat16)
+        rat = torch.from_numpy(np.resize(L.row_adapter, T).astype(np.int32)).to(dev)
+        Yt = torch.empty((T, L.dout), dtype=torch.bfloat16, device=dev)
+        q_us = t_us(lambda k: qpool.forward_quantized(Xt, Wqs[k % qn], scs[k % qn], scratch, rat, Yt, stream=stream),
+                    20 * qn)
+        b_us = t_us(lambda k: qpool.forward(Xt, calls[k % len(calls)].W, rat, Yt, stream=stream), 20 * len(calls))
+        by_t[str(T)] = {"forward_quantized_us": q_us, "forward_bf16_us": b_us}
+    qpool.close()
+    out["quantized"]["by_tokens"] = by_t
+    out["quantized"]["by_tokens_note"] = ("eager back-to-back forwards over 4096 x 4096, the decode step's three "
+                                          "rank-16 adapters with its row map repeated to T rows")
     del Wqs, scs, scratch
 
     # NF4 base (4-bit codes, fp32 absmax per row and 64 columns, the NormalFloat codebook)

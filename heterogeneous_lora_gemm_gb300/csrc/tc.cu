@@ -1378,6 +1378,16 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     // Over codes every token tile would restore the W tile again: one tile there.  Both
     // kernels tile alike: a token tile's projection reads the Vt of exactly the chunks
     // whose slots its own tokens use, which its shrink tile wrote.
+    const int q_x = a.qmode == QMODE_INT8 ? BK : (a.qmode == QMODE_NF4 ? BK / 2 : 0);   // code bytes per row and K chunk
+    // over codes: a stage of QUANT_KC K chunks (codes, restored W tiles, X), and whether
+    // a ring of two such stages fits shared memory at n tokens
+    auto qstage = [&](int n) {
+        return (QUANT_KC * (stage_bytes(n) + BM * q_x + (a.qmode == QMODE_NF4 ? BM * 4 : 0)) + 1023) & ~1023;
+    };
+    auto qfits = [&](int n) {
+        const int rest = (n <= PUSH_MAX_N ? BM * n * 4 : 0) + 64 + (int)sizeof(Tail) + 1024;   // receive buffer, codebook
+        return 2 * qstage(n) + rest <= max_dyn_smem();
+    };
     const int zt = (decode && !a.qmode && N > PROJ_ZT_N) ? (T + PROJ_ZT_N - 1) / PROJ_ZT_N : 1;
     const int Np = zt > 1 ? PROJ_ZT_N : N;               // token rows per projection tile
     // More 128-row tiles than SMs and no adapters (the 7B layer's gate|up, 172 tiles):
@@ -1394,13 +1404,14 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         // over codes: QUANT_KC K chunks per stage (one 2D box of codes, one of scales);
         // a stage also holds the restored 16 KiB W tile of each chunk, which comes from
         // no load.  Each stage costs a round trip through the converting warps, so the
-        // steps carry two chunks, and the ring budget is the deep one.
-        ds.pkc = kb_total >= QUANT_KC ? QUANT_KC : 1;
+        // steps carry two chunks, and the ring budget is the deep one.  Where two such
+        // stages do not fit (int8 above 224 tokens: 112 KiB a stage at 256), one chunk (two
+        // token tiles of two chunks were slower at 256 tokens: 28.9 against 26.0 us).
+        if (ds.budget == PROJ_SMEM_BUDGET || ds.budget == PROJ_SMEM_BUDGET_SHARED) ds.budget = PROJ_SMEM_BUDGET_ALONE;
+        ds.pkc = (kb_total >= QUANT_KC && qfits(Np)) ? QUANT_KC : 1;
         ds.ksteps = (kb_total + ds.pkc - 1) / ds.pkc;
         ds.splits = ds.splits < ds.ksteps ? ds.splits : ds.ksteps;
-        if (ds.budget == PROJ_SMEM_BUDGET || ds.budget == PROJ_SMEM_BUDGET_SHARED) ds.budget = PROJ_SMEM_BUDGET_ALONE;
     }
-    const int q_x = a.qmode == QMODE_INT8 ? BK : (a.qmode == QMODE_NF4 ? BK / 2 : 0);   // code bytes per row and K chunk
     // A decode batch with at most two rows per loaded adapter (on average) takes the
     // CUDA-core shrink: its adapters are read once each, with no split-K reduction.
     const bool gemv = decode && shrink && gemv_shrink_fits(d, T) && a.n_loaded > 0 && T <= 2 * a.n_loaded;

@@ -42,6 +42,7 @@ def test_nf4_restore_matches_oracle(dtype):
     (300, 256, 192, [16, 8]),         # prefill: restore pass into W_scratch, then the forward
     (40, 256, 198, [16, 8]),          # decode, dout not a multiple of 4: restore pass (scales not by TMA)
     (40, 192, 256, [16, 8]),          # decode, 3 K blocks: the second step's second block past din
+    (256, 512, 384, [16, 8, 16]),     # decode, 256 tokens: the widest token tile over codes
 ])
 def test_forward_over_an_nf4_base(T, din, dout, ranks):
     cb = wl.nf4_codebook()

@@ -427,6 +427,8 @@ def test_load_waits_for_last_reader_and_versions():
     (40, 192, 256, [16, 8]),          # decode, 3 K chunks: the second step's second chunk past din
     (300, 256, 192, [16, 8]),         # prefill: restore pass into W_scratch, then the forward
     (40, 136, 192, [16, 8]),          # din not a multiple of 64: restore pass
+    (256, 512, 384, [16, 8, 16]),     # decode, 256 tokens: one K chunk per stage (two do not fit)
+    (224, 320, 256, [16, 8]),         # decode, 224 tokens, 5 K chunks
 ])
 def test_forward_over_a_quantized_base(T, din, dout, ranks):
     """The dynamic branch over an int8 base (codes x row scale, one rounding of the
