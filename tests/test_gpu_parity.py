@@ -602,7 +602,8 @@ def test_fused_projection_with_per_module_adapters(T):
     assert e.value.status == mlora.MLORA_ERR_RANK
 
 
-@pytest.mark.parametrize("T,layout", [(128, "uniform"), (96, "mixed"), (48, "mixed")])
+@pytest.mark.parametrize("T,layout", [(128, "uniform"), (96, "mixed"), (48, "mixed"),
+                                      (200, "mixed"), (256, "uniform")])   # two token tiles
 def test_fused_projection_up_runs(T, layout):
     """Tenants that each hold a q and a v adapter of rank 16 put consecutive tenants' q
     (and v) chunks 32 rank columns apart in the arena: a K-extension step of 4 such
