@@ -671,9 +671,14 @@ def run_extras(calls, L, stream, dev, peaks):
         Xt = torch.randn((T, L.din), generator=gen, device=dev).to(torch.bfloat16)
         rat = torch.from_numpy(np.resize(L.row_adapter, T).astype(np.int32)).to(dev)
         Yt = torch.empty((T, L.dout), dtype=torch.bfloat16, device=dev)
+        # (NVTX ranges name these launches for a profiler: codes_T<T>, bf16_T<T>)
+        torch.cuda.nvtx.range_push(f"codes_T{T}")
         q_us = t_us(lambda k: qpool.forward_quantized(Xt, Wqs[k % qn], scs[k % qn], scratch, rat, Yt, stream=stream),
                     20 * qn)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.nvtx.range_push(f"bf16_T{T}")
         b_us = t_us(lambda k: qpool.forward(Xt, calls[k % len(calls)].W, rat, Yt, stream=stream), 20 * len(calls))
+        torch.cuda.nvtx.range_pop()
         by_t[str(T)] = {"forward_quantized_us": q_us, "forward_bf16_us": b_us}
     qpool.close()
     out["quantized"]["by_tokens"] = by_t
@@ -899,8 +904,6 @@ def run_ours(args, dist, rank, local):
         out["cpu_baseline"] = cpu_baseline(args, calls, host0, L_single)
     else:
         out["cpu_baseline"] = None
-    for c in calls:
-        pass
     del calls
     torch.cuda.synchronize(dev)
     torch.cuda.empty_cache()
