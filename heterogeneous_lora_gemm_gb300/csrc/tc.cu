@@ -118,7 +118,8 @@ constexpr int MAX_SLOT_WORDS = 4096 / 32;
 constexpr int EXT_LEAD = 0;        // projection: K-extension steps go this many K chunks of 64 before the end
 constexpr int PUSH_MAX_N = 64;     // projection: tokens up to which the splits push their partials
 constexpr int PROJ_KC = 2;         // projection: K chunks of 64 per pipeline step (one 3D box each for W and X)
-constexpr int PROJ_ZT_N = 128;     // projection: tokens per token tile of a decode batch above this size
+constexpr int PROJ_ZT_N = 128;     // projection: tokens per token tile of a wide decode batch
+constexpr int PROJ_ZT_MIN = 224;   // a decode batch of more tokens than this runs as token tiles
 constexpr int QUANT_KC = 2;        // projection over codes: K chunks of 64 per pipeline step
 constexpr int QMODE_INT8 = 1, QMODE_NF4 = 2;
 
@@ -1371,10 +1372,12 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
     cudaError_t e;
     const int N = decode ? (T + 15) / 16 * 16 : 128;     // token rows per tile
     if (a.qmode && !(decode && d.din % BK == 0)) return cudaErrorInvalidValue;
-    // A decode batch of more than 128 tokens runs its shrink and its projection as token
+    // A decode batch of more than 224 tokens runs its shrink and its projection as token
     // tiles of 128 (grid z): half the K splits per row tile, and a split's partial tile
     // half as large, for the same number of CTAs.  The token tiles of a row tile read
     // the same W slice at about the same time, so W is fetched from DRAM about once.
+    // Up to 224 tokens one tile is faster: the second tile would hold few tokens and
+    // take W into its SMs all the same.
     // Over codes every token tile would restore the W tile again: one tile there.  Both
     // kernels tile alike: a token tile's projection reads the Vt of exactly the chunks
     // whose slots its own tokens use, which its shrink tile wrote.
@@ -1388,7 +1391,7 @@ cudaError_t tc_forward(const TcForwardArgs& a, cudaStream_t st) {
         const int rest = (n <= PUSH_MAX_N ? BM * n * 4 : 0) + 64 + (int)sizeof(Tail) + 1024;   // receive buffer, codebook
         return 2 * qstage(n) + rest <= max_dyn_smem();
     };
-    const int zt = (decode && !a.qmode && N > PROJ_ZT_N) ? (T + PROJ_ZT_N - 1) / PROJ_ZT_N : 1;
+    const int zt = (decode && !a.qmode && N > PROJ_ZT_MIN) ? (T + PROJ_ZT_N - 1) / PROJ_ZT_N : 1;
     const int Np = zt > 1 ? PROJ_ZT_N : N;               // token rows per projection tile
     // More 128-row tiles than SMs and no adapters (the 7B layer's gate|up, 172 tiles):
     // each CTA takes two row tiles that share its X stages, so that the K splits of half
